@@ -1,0 +1,172 @@
+/*
+ * moe_decode.h -- C ABI of the GB300 (sm_103a) decode MoE expert block.
+ *
+ * The block (one token; M tokens are M independent copies of it):
+ *
+ *   w       = scale * q + bias                     per group of 64 codes along a row; q is an
+ *                                                  unsigned 4-, 6- or 8-bit code, scale and bias fp16
+ *   act_k   = silu(W_gate,k . x) * (W_up,k . x)    for each routed slot k and each shared expert
+ *   out     = resid + (sum_k score_k * W_down,k . act_k  +  scalar * sum_s W_down,s . act_s)
+ *   scalar  = sigmoid(x . g) with a gate vector g, else 1
+ *
+ * Sources: "two-kernel decode-MoE that beats gather_qmm" (What changed, step 2: kernel A computes
+ * gate/up + swiglu into act_g[K, Dff], kernel B computes down * score summed over K; Scope /
+ * flags: 4/8-bit affine codes; Next: 6-bit and mixed bits per projection) and "Red Lite dev39 --
+ * fused expert tail" (Change: one dispatch computes the weighted sum over the pool, then
+ * x = resid + (routed + shared * scalar), then writes the layer output).
+ *
+ * Conventions for every call:
+ *   - Pointers named "device" are CUDA device pointers of the current device; "host" pointers
+ *     are ordinary host memory.  Streams are cudaStream_t passed as void* (NULL = legacy stream).
+ *   - Weights are borrowed: the caller keeps them alive and unchanged until destroy.
+ *   - Host-detectable errors return a negative moe_status and enqueue nothing.  Errors the GPU
+ *     finds (an expert id outside [0, n_experts)) set a sticky device error word that
+ *     moe_decode_get_error / moe_stack_get_error read; the offending slot contributes zero.
+ *     No kernel traps or asserts.
+ *   - A handle is not thread-safe: calls on one handle must not run concurrently on the host, and
+ *     forwards enqueued on different streams must not overlap on the GPU (they share workspace).
+ */
+#ifndef MOE_DECODE_H
+#define MOE_DECODE_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum moe_status {
+  MOE_OK = 0,
+  MOE_ERR_INVALID_ARG = -1,  /* null pointer, bad size, misaligned pointer, bad enum */
+  MOE_ERR_UNSUPPORTED = -2,  /* valid but not built: bits not in {4,6,8}, gate bits != up bits,
+                                shared memory needs above the device limit, wrong GPU */
+  MOE_ERR_CUDA = -3,         /* a CUDA runtime call failed (launch, copy, graph) */
+  MOE_ERR_OOM = -4,          /* device or pinned allocation failed */
+  MOE_ERR_BAD_ID = -5,       /* device error word: an expert id was outside [0, n_experts) */
+  MOE_ERR_TIMEOUT = -6       /* reserved: no kernel here waits on another */
+} moe_status;
+
+enum { MOE_DTYPE_BF16 = 0, MOE_DTYPE_F32 = 1 };
+
+/* Shapes and formats of one layer, fixed at create time. */
+typedef struct moe_decode_config {
+  int32_t din;             /* hidden size; a multiple of 64 */
+  int32_t dff;             /* routed expert width; a multiple of 64 */
+  int32_t n_experts;       /* E >= 1 */
+  int32_t top_k;           /* K routed slots per token, 0 <= K (K + n_shared >= 1) */
+  int32_t max_tokens;      /* largest M a forward may pass, >= 1 */
+  int32_t bits_gate;       /* 4, 6 or 8; must equal bits_up */
+  int32_t bits_up;
+  int32_t bits_down;       /* 4, 6 or 8, independent of gate/up */
+  int32_t n_shared;        /* shared experts, 0..4 */
+  int32_t dff_shared;      /* shared expert width; a multiple of 64 when n_shared > 0 */
+  int32_t bits_shared;     /* 4, 6 or 8: gate, up and down of every shared expert */
+  int32_t shared_gate;     /* 0: scalar 1;  1: scalar = sigmoid(x . gate_vec) */
+  int32_t resid_dtype;     /* MOE_DTYPE_BF16 or MOE_DTYPE_F32 */
+  int32_t out_dtype;       /* MOE_DTYPE_F32 (default) or MOE_DTYPE_BF16 (rounded to nearest) */
+  int32_t warps_per_block; /* 0 = automatic */
+} moe_decode_config;
+
+/*
+ * One projection of every expert of a class, canonical packed layout, all device pointers:
+ *   codes  [experts][rows][cols*bits/8] bytes: per row a little-endian bit stream, code c at bits
+ *          [c*bits, c*bits + bits), LSB first (8 codes per uint32 at 4 bits, 4 at 8 bits,
+ *          16 per 3 uint32 at 6 bits); 16-byte aligned
+ *   scales [experts][rows][cols/64] fp16, biases likewise; 2-byte aligned
+ * gate and up have rows = dff, cols = din; down has rows = din, cols = dff.
+ */
+typedef struct moe_proj {
+  const void *codes;
+  const void *scales;
+  const void *biases;
+} moe_proj;
+
+typedef struct moe_layer_weights {
+  moe_proj gate, up, down;          /* routed experts, [n_experts] stacked */
+  moe_proj sh_gate, sh_up, sh_down; /* shared experts, [n_shared] stacked (ignored if none) */
+  const void *gate_vec;             /* bf16 [din] device, required when shared_gate == 1 */
+} moe_layer_weights;
+
+typedef struct moe_decode moe_decode_t;
+typedef struct moe_stack moe_stack_t;
+
+/* Prepares one layer: validates the config and weight pointers, picks the kernels, allocates the
+ * workspace (fp32 activations [max_tokens][K*dff + n_shared*dff_shared] and the error word).
+ * The prepared handle is the "prepared executor" form: nothing is set up per forward.
+ * Returns MOE_OK and *out, or an error and *out = NULL. */
+int moe_decode_create(const moe_decode_config *cfg, const moe_layer_weights *weights,
+                      moe_decode_t **out);
+
+/* Enqueues the block for m tokens on `stream` (asynchronous, allocation-free).
+ *   x      bf16 [m][din] device                 token activations
+ *   ids    int32 [m][top_k] device              routed expert ids, slot order as given
+ *   scores fp32 [m][top_k] device               router weights of the slots
+ *   resid  [m][din] device, cfg->resid_dtype    residual added in the tail
+ *   out    [m][din] device, cfg->out_dtype      result; may alias resid, must not alias x
+ * Kernel A (gate/up + SwiGLU, scaled by the slot's score or the shared scalar) writes the
+ * workspace; kernel B (down GEMV, summed over slots and shared experts, plus resid) writes out.
+ * Both launch with programmatic dependent launch so B streams its weights while A finishes. */
+int moe_decode_forward(moe_decode_t *h, const void *x, int32_t m, const int32_t *ids,
+                       const float *scores, const void *resid, void *out, void *stream);
+
+/* Synchronises the device, returns the sticky device error word in *device_error (0 or
+ * MOE_ERR_BAD_ID) and clears it. */
+int moe_decode_get_error(moe_decode_t *h, int32_t *device_error);
+
+void moe_decode_destroy(moe_decode_t *h);
+
+/* ---- a stack of layers replayed as one CUDA graph ------------------------------------------
+ * Layer l reads x_l = x + l*m*din, ids_l = ids + l*m*top_k, scores_l likewise; its residual is
+ * resid0 (cfg->resid_dtype) for l = 0 and the fp32 output of layer l-1 after that; the last
+ * layer writes `out` (fp32 [m][din]).  No layer reads its ids before the previous layer's output
+ * is complete: every kernel waits on its predecessor before touching token data, and only
+ * weight prefetch runs ahead.  cfg->out_dtype must be MOE_DTYPE_F32. */
+int moe_stack_create(const moe_decode_config *cfg, int32_t n_layers,
+                     const moe_layer_weights *layers, moe_stack_t **out);
+
+/* Enqueues one decode step of the whole stack on `stream` (device pointers as above).  The first
+ * call with a given (x, ids, scores, resid0, out, m) captures and instantiates a CUDA graph
+ * (not asynchronous, allocates); later calls with the same pointers only launch it. */
+int moe_stack_step(moe_stack_t *s, const void *x, int32_t m, const int32_t *ids,
+                   const float *scores, const void *resid0, void *out, void *stream);
+
+/* One decode step from HOST buffers: copies x, ids, scores and resid0 (best from pinned memory)
+ * into the stack's device staging buffers, replays the graph, copies out back, and synchronises
+ * the stream before returning. */
+int moe_stack_step_host(moe_stack_t *s, const void *x_host, int32_t m, const int32_t *ids_host,
+                        const float *scores_host, const void *resid0_host, float *out_host,
+                        void *stream);
+
+int moe_stack_get_error(moe_stack_t *s, int32_t *device_error);
+void moe_stack_destroy(moe_stack_t *s);
+
+/* ---- canonical packing (host) ---------------------------------------------------------------
+ * codes: uint8 [rows][cols], one code per byte, each < 2^bits; packed: [rows][cols*bits/8].
+ * cols must be a multiple of 64.  Returns MOE_ERR_INVALID_ARG on a code out of range. */
+int moe_pack_codes(const uint8_t *codes, int64_t rows, int64_t cols, int32_t bits, void *packed);
+int moe_unpack_codes(const void *packed, int64_t rows, int64_t cols, int32_t bits, uint8_t *codes);
+
+/* Debug: unpacks packed device codes on the GPU with the kernels' own window/mask decoding, one
+ * code per output byte (device [rows][cols]); for checking the decoding bit for bit. */
+int moe_unpack_codes_device(const void *packed, int64_t rows, int64_t cols, int32_t bits,
+                            uint8_t *codes, void *stream);
+
+/* ---- synthetic weights in HBM (input generation, not the block) ------------------------------
+ * Fill device buffers with the counter-based generator defined in the Python module
+ * quantized_moe_expert_dequant_gb300.synth, bit for bit: element i of expert e (e counted from
+ * expert0) is derived from mix64(key + G*(((e << 40) | i) + 1)).
+ *   codes : n_experts * words_per_expert uint64 words
+ *   scales: n_experts * per_expert fp16 values, about U(0.005, 0.02)
+ *   biases: fp16, about -2^(bits-1) * scale, from the scales already in `scales` */
+int moe_synth_codes(void *dst, uint64_t key, int32_t expert0, int32_t n_experts,
+                    int64_t words_per_expert, void *stream);
+int moe_synth_scales(void *dst, uint64_t key, int32_t expert0, int32_t n_experts,
+                     int64_t per_expert, void *stream);
+int moe_synth_biases(void *dst, const void *scales, uint64_t key, int32_t expert0,
+                     int32_t n_experts, int64_t per_expert, int32_t bits, void *stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MOE_DECODE_H */

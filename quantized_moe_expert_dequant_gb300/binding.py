@@ -1,0 +1,316 @@
+"""Thin Python binding of include/moe_decode.h (ctypes; argument marshalling only).
+
+Every step of the block runs in libmoe_decode.so.  PyTorch supplies device memory and streams.
+If the library is missing this module raises; there is no fallback path.
+"""
+from __future__ import annotations
+
+import ctypes
+import dataclasses
+import os
+import threading
+
+import numpy as np
+import torch
+
+from . import synth
+from .workloads import Shape
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libmoe_decode.so")
+
+MOE_OK, MOE_ERR_INVALID_ARG, MOE_ERR_UNSUPPORTED, MOE_ERR_CUDA, MOE_ERR_OOM, MOE_ERR_BAD_ID = (
+    0, -1, -2, -3, -4, -5)
+DTYPE_BF16, DTYPE_F32 = 0, 1
+_STATUS = {0: "MOE_OK", -1: "MOE_ERR_INVALID_ARG", -2: "MOE_ERR_UNSUPPORTED", -3: "MOE_ERR_CUDA",
+           -4: "MOE_ERR_OOM", -5: "MOE_ERR_BAD_ID", -6: "MOE_ERR_TIMEOUT"}
+
+EXPORTS = ["moe_decode_create", "moe_decode_forward", "moe_decode_get_error", "moe_decode_destroy",
+           "moe_stack_create", "moe_stack_step", "moe_stack_step_host", "moe_stack_get_error",
+           "moe_stack_destroy", "moe_pack_codes", "moe_unpack_codes", "moe_unpack_codes_device",
+           "moe_synth_codes", "moe_synth_scales", "moe_synth_biases"]
+
+
+class MoeError(RuntimeError):
+    def __init__(self, fn, rc):
+        super().__init__(f"{fn} returned {_STATUS.get(rc, rc)}")
+        self.rc = rc
+
+
+class Config(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_int32) for n in (
+        "din", "dff", "n_experts", "top_k", "max_tokens", "bits_gate", "bits_up", "bits_down",
+        "n_shared", "dff_shared", "bits_shared", "shared_gate", "resid_dtype", "out_dtype",
+        "warps_per_block")]
+
+
+class Proj(ctypes.Structure):
+    _fields_ = [("codes", ctypes.c_void_p), ("scales", ctypes.c_void_p), ("biases", ctypes.c_void_p)]
+
+
+class LayerWeights(ctypes.Structure):
+    _fields_ = [("gate", Proj), ("up", Proj), ("down", Proj), ("sh_gate", Proj), ("sh_up", Proj),
+                ("sh_down", Proj), ("gate_vec", ctypes.c_void_p)]
+
+
+_lock = threading.Lock()
+_lib = None
+
+
+def lib() -> ctypes.CDLL:
+    """The loaded library; raises if it was not built."""
+    global _lib
+    with _lock:
+        if _lib is None:
+            if not os.path.exists(LIB_PATH):
+                raise RuntimeError(f"{LIB_PATH} is missing: run __graft_entry__.build() or "
+                                   "python -m quantized_moe_expert_dequant_gb300.build")
+            L = ctypes.CDLL(LIB_PATH)
+            vp, i32, i64, u64 = ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64, ctypes.c_uint64
+            sig = {
+                "moe_decode_create": [ctypes.POINTER(Config), ctypes.POINTER(LayerWeights),
+                                      ctypes.POINTER(vp)],
+                "moe_decode_forward": [vp, vp, i32, vp, vp, vp, vp, vp],
+                "moe_decode_get_error": [vp, ctypes.POINTER(i32)],
+                "moe_decode_destroy": [vp],
+                "moe_stack_create": [ctypes.POINTER(Config), i32, ctypes.POINTER(LayerWeights),
+                                     ctypes.POINTER(vp)],
+                "moe_stack_step": [vp, vp, i32, vp, vp, vp, vp, vp],
+                "moe_stack_step_host": [vp, vp, i32, vp, vp, vp, vp, vp],
+                "moe_stack_get_error": [vp, ctypes.POINTER(i32)],
+                "moe_stack_destroy": [vp],
+                "moe_pack_codes": [vp, i64, i64, i32, vp],
+                "moe_unpack_codes": [vp, i64, i64, i32, vp],
+                "moe_unpack_codes_device": [vp, i64, i64, i32, vp, vp],
+                "moe_synth_codes": [vp, u64, i32, i32, i64, vp],
+                "moe_synth_scales": [vp, u64, i32, i32, i64, vp],
+                "moe_synth_biases": [vp, vp, u64, i32, i32, i64, i32, vp],
+            }
+            for name, args in sig.items():
+                f = getattr(L, name)
+                f.argtypes = args
+                f.restype = None if name.endswith("_destroy") else ctypes.c_int
+            _lib = L
+    return _lib
+
+
+def check(fn: str, rc: int) -> None:
+    if rc != MOE_OK:
+        raise MoeError(fn, rc)
+
+
+def _stream(stream) -> int | None:
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return stream.cuda_stream if isinstance(stream, torch.cuda.Stream) else int(stream)
+
+
+def _p(t) -> int | None:
+    return None if t is None else t.data_ptr()
+
+
+def config(shape: Shape, max_tokens: int = 1, resid_dtype: int = DTYPE_BF16,
+           out_dtype: int = DTYPE_F32, warps_per_block: int = 0) -> Config:
+    return Config(shape.din, shape.dff, shape.n_experts, shape.top_k, max_tokens, shape.bits_gate,
+                  shape.bits_up, shape.bits_down, shape.n_shared, shape.dff_shared,
+                  shape.bits_shared, shape.shared_gate, resid_dtype, out_dtype, warps_per_block)
+
+
+# ---------------------------------------------------------------- device weights
+
+@dataclasses.dataclass
+class DeviceProj:
+    codes: torch.Tensor   # uint8 [E, rows, rowbytes]
+    scales: torch.Tensor  # fp16 [E, rows, cols/64]
+    biases: torch.Tensor  # fp16 [E, rows, cols/64]
+
+    def struct(self) -> Proj:
+        return Proj(self.codes.data_ptr(), self.scales.data_ptr(), self.biases.data_ptr())
+
+    def nbytes(self) -> int:
+        return sum(t.numel() * t.element_size() for t in (self.codes, self.scales, self.biases))
+
+
+@dataclasses.dataclass
+class DeviceLayer:
+    shape: Shape
+    gate: DeviceProj | None
+    up: DeviceProj | None
+    down: DeviceProj | None
+    sh_gate: DeviceProj | None = None
+    sh_up: DeviceProj | None = None
+    sh_down: DeviceProj | None = None
+    gate_vec: torch.Tensor | None = None   # bf16 [din]
+
+    def struct(self) -> LayerWeights:
+        z = Proj(None, None, None)
+        f = lambda p: p.struct() if p is not None else z
+        return LayerWeights(f(self.gate), f(self.up), f(self.down), f(self.sh_gate),
+                            f(self.sh_up), f(self.sh_down), _p(self.gate_vec))
+
+
+def _empty_proj(n, rows, cols, bits, device) -> DeviceProj:
+    return DeviceProj(torch.empty((n, rows, cols * bits // 8), dtype=torch.uint8, device=device),
+                      torch.empty((n, rows, cols // 64), dtype=torch.float16, device=device),
+                      torch.empty((n, rows, cols // 64), dtype=torch.float16, device=device))
+
+
+def synth_proj_device(seed, layer, proj, n, rows, cols, bits, device="cuda", stream=None):
+    """All n experts of one projection drawn in HBM by the device generator."""
+    p = _empty_proj(n, rows, cols, bits, device)
+    L, st = lib(), _stream(stream)
+    words = rows * cols * bits // 8 // 8
+    groups = rows * (cols // 64)
+    check("moe_synth_codes", L.moe_synth_codes(
+        p.codes.data_ptr(), synth.tensor_key(seed, layer, proj, synth.CODES), 0, n, words, st))
+    check("moe_synth_scales", L.moe_synth_scales(
+        p.scales.data_ptr(), synth.tensor_key(seed, layer, proj, synth.SCALES), 0, n, groups, st))
+    check("moe_synth_biases", L.moe_synth_biases(
+        p.biases.data_ptr(), p.scales.data_ptr(), synth.tensor_key(seed, layer, proj, synth.BIASES),
+        0, n, groups, bits, st))
+    return p
+
+
+def synth_layer_device(shape: Shape, layer: int, device="cuda", stream=None) -> DeviceLayer:
+    s, E = shape.seed, shape.n_experts
+    mk = lambda proj, n, r, c, b: synth_proj_device(s, layer, proj, n, r, c, b, device, stream)
+    dl = DeviceLayer(shape, None, None, None)
+    if shape.top_k > 0:
+        dl.gate = mk(synth.GATE, E, shape.dff, shape.din, shape.bits_gate)
+        dl.up = mk(synth.UP, E, shape.dff, shape.din, shape.bits_up)
+        dl.down = mk(synth.DOWN, E, shape.din, shape.dff, shape.bits_down)
+    if shape.n_shared:
+        n, d, b = shape.n_shared, shape.dff_shared, shape.bits_shared
+        dl.sh_gate = mk(synth.SH_GATE, n, d, shape.din, b)
+        dl.sh_up = mk(synth.SH_UP, n, d, shape.din, b)
+        dl.sh_down = mk(synth.SH_DOWN, n, shape.din, d, b)
+        if shape.shared_gate:
+            dl.gate_vec = torch.from_numpy(
+                synth.gate_vector(s, layer, shape.din).view(np.int16)).view(torch.bfloat16).to(device)
+    return dl
+
+
+def proj_from_host(codes, scales, biases, device="cuda") -> DeviceProj:
+    """Stacked host arrays (uint8 codes, uint16 fp16 bits) copied to the device."""
+    t = lambda a, dt: torch.from_numpy(np.ascontiguousarray(a)).view(dt).to(device)
+    return DeviceProj(t(codes, torch.uint8), t(scales.view(np.int16), torch.float16),
+                      t(biases.view(np.int16), torch.float16))
+
+
+# ---------------------------------------------------------------- the block
+
+class MoeDecode:
+    """One prepared layer: moe_decode_create once, moe_decode_forward per token batch."""
+
+    def __init__(self, layer: DeviceLayer, max_tokens: int = 1, resid_dtype=DTYPE_BF16,
+                 out_dtype=DTYPE_F32, warps_per_block: int = 0):
+        self.layer = layer
+        self.cfg = config(layer.shape, max_tokens, resid_dtype, out_dtype, warps_per_block)
+        self._w = layer.struct()
+        h = ctypes.c_void_p()
+        check("moe_decode_create", lib().moe_decode_create(ctypes.byref(self.cfg),
+                                                           ctypes.byref(self._w), ctypes.byref(h)))
+        self.handle = h
+
+    def forward(self, x: torch.Tensor, ids: torch.Tensor | None, scores: torch.Tensor | None,
+                resid: torch.Tensor, out: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+        """x bf16 [m, din]; ids int32 [m, K]; scores fp32 [m, K]; resid [m, din]; out [m, din]."""
+        m = x.shape[0] if x.dim() == 2 else 1
+        if out is None:
+            dt = torch.float32 if self.cfg.out_dtype == DTYPE_F32 else torch.bfloat16
+            out = torch.empty((m, self.cfg.din), dtype=dt, device=x.device)
+        check("moe_decode_forward", lib().moe_decode_forward(
+            self.handle, _p(x), m, _p(ids), _p(scores), _p(resid), _p(out), _stream(stream)))
+        return out
+
+    def get_error(self) -> int:
+        v = ctypes.c_int32()
+        check("moe_decode_get_error", lib().moe_decode_get_error(self.handle, ctypes.byref(v)))
+        return v.value
+
+    def close(self):
+        if self.handle:
+            lib().moe_decode_destroy(self.handle)
+            self.handle = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+
+class MoeStack:
+    """A stack of layers replayed as one CUDA graph per decode step."""
+
+    def __init__(self, layers: list[DeviceLayer], max_tokens: int = 1, resid_dtype=DTYPE_BF16,
+                 warps_per_block: int = 0):
+        self.layers = layers
+        self.cfg = config(layers[0].shape, max_tokens, resid_dtype, DTYPE_F32, warps_per_block)
+        arr = (LayerWeights * len(layers))()
+        for i, l in enumerate(layers):
+            arr[i] = l.struct()
+        self._w = arr
+        h = ctypes.c_void_p()
+        check("moe_stack_create", lib().moe_stack_create(ctypes.byref(self.cfg), len(layers), arr,
+                                                         ctypes.byref(h)))
+        self.handle = h
+
+    def step(self, x, ids, scores, resid0, out, stream=None):
+        """x bf16 [L, m, din]; ids int32 [L, m, K]; scores fp32 [L, m, K]; resid0 [m, din];
+        out fp32 [m, din]; all on the device."""
+        m = resid0.shape[0]
+        check("moe_stack_step", lib().moe_stack_step(self.handle, _p(x), m, _p(ids), _p(scores),
+                                                     _p(resid0), _p(out), _stream(stream)))
+        return out
+
+    def step_host(self, x, ids, scores, resid0, out, stream=None):
+        """The same step from host (ideally pinned) tensors; returns after out is on the host."""
+        m = resid0.shape[0]
+        check("moe_stack_step_host", lib().moe_stack_step_host(
+            self.handle, _p(x), m, _p(ids), _p(scores), _p(resid0), _p(out), _stream(stream)))
+        return out
+
+    def get_error(self) -> int:
+        v = ctypes.c_int32()
+        check("moe_stack_get_error", lib().moe_stack_get_error(self.handle, ctypes.byref(v)))
+        return v.value
+
+    def close(self):
+        if self.handle:
+            lib().moe_stack_destroy(self.handle)
+            self.handle = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+
+# ---------------------------------------------------------------- packing
+
+def pack_codes(codes: np.ndarray, bits: int) -> np.ndarray:
+    codes = np.ascontiguousarray(codes, dtype=np.uint8)
+    rows, cols = codes.shape
+    out = np.empty((rows, cols * bits // 8), dtype=np.uint8)
+    check("moe_pack_codes", lib().moe_pack_codes(codes.ctypes.data, rows, cols, bits,
+                                                 out.ctypes.data))
+    return out
+
+
+def unpack_codes(packed: np.ndarray, cols: int, bits: int) -> np.ndarray:
+    packed = np.ascontiguousarray(packed, dtype=np.uint8)
+    rows = packed.shape[0]
+    out = np.empty((rows, cols), dtype=np.uint8)
+    check("moe_unpack_codes", lib().moe_unpack_codes(packed.ctypes.data, rows, cols, bits,
+                                                     out.ctypes.data))
+    return out
+
+
+def unpack_codes_device(packed: torch.Tensor, cols: int, bits: int, stream=None) -> torch.Tensor:
+    rows = packed.shape[0]
+    out = torch.empty((rows, cols), dtype=torch.uint8, device=packed.device)
+    check("moe_unpack_codes_device", lib().moe_unpack_codes_device(
+        packed.data_ptr(), rows, cols, bits, out.data_ptr(), _stream(stream)))
+    return out

@@ -1,0 +1,172 @@
+// moe_common.cuh -- device building blocks of the decode MoE kernels (sm_103a).
+//
+// Decoding packed codes without integer-to-float conversions
+// ----------------------------------------------------------
+// A 32-bit pattern below 2^24 read as an IEEE binary32 value is exactly  pattern * 2^-149
+// (a subnormal, or the smallest normal binade, whose value is linear in the bits).  So a code q
+// that sits at bit offset o of a word, with o + bits <= 24, becomes the exact float q * 2^(o-149)
+// with ONE bitwise AND, and one FMA multiplies it into the dot product if the activation it
+// meets was pre-scaled by 2^(149 - S - o).  The product is q * x * 2^-S; the step's sum is
+// rescaled by 2^S once, together with the group scale.  fp32 subnormals are kept (this code is
+// built without flush-to-zero), and S is chosen per vector from its largest magnitude so that no
+// pre-scaled activation overflows.
+//
+// Code windows per format (a "step" is the unit one lane decodes at a time):
+//   4-bit  step = 16 B  = 32 codes: nibbles 0..5 of a word masked in place (o = 0,4,..,20);
+//                                   nibbles 6, 7 from word >> 8 (o = 16, 20)
+//   8-bit  step = 16 B  = 16 codes: bytes 0..2 in place (o = 0, 8, 16); byte 3 from word >> 8
+//   6-bit  step = 48 B  = 64 codes: each 3-word triple (96 bits, 16 codes) is cut into four
+//                                   24-bit windows by funnel shifts; codes at o = 0, 6, 12, 18
+// Every step lies inside one group of 64 codes, so one (scale, bias) pair applies to it:
+//   sum_c (s q_c + b) x_c = s * sum_c q_c x_c + b * sum_c x_c.
+#pragma once
+
+#include <cstdint>
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+
+namespace moe {
+
+constexpr int kGroup = 64;
+
+// ------------------------------------------------------------------ programmatic dependent launch
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+// ------------------------------------------------------------------ small helpers
+__device__ __forceinline__ float bf16_to_float(uint16_t b) {
+  return __uint_as_float(static_cast<uint32_t>(b) << 16);
+}
+
+__device__ __forceinline__ uint16_t float_to_bf16_rn(float f) {
+  uint32_t u = __float_as_uint(f);
+  if ((u & 0x7fffffffu) > 0x7f800000u) return static_cast<uint16_t>((u >> 16) | 0x40);  // NaN
+  u += 0x7fffu + ((u >> 16) & 1u);
+  return static_cast<uint16_t>(u >> 16);
+}
+
+// 2^k as a float for k in [-126, 127]
+__device__ __forceinline__ float pow2f(int k) {
+  return __uint_as_float(static_cast<uint32_t>(k + 127) << 23);
+}
+
+// S for a vector whose largest magnitude is maxabs: pre-scaled values stay below 2^127.
+__device__ __forceinline__ int choose_shift(float maxabs) {
+  const int e = static_cast<int>((__float_as_uint(maxabs) >> 23) & 255u) - 127;
+  int s = e + 24;
+  s = s < 22 ? 22 : s;
+  return s > 127 ? 127 : s;
+}
+
+__device__ __forceinline__ float warp_sum(float v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+  return v;
+}
+
+__device__ __forceinline__ float warp_max(float v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+  return v;
+}
+
+// ------------------------------------------------------------------ packed formats
+template <int BITS>
+struct Fmt;
+template <>
+struct Fmt<4> {
+  static constexpr int kVecs = 1;   // uint4 vectors per step
+  static constexpr int kCodes = 32; // codes per step
+};
+template <>
+struct Fmt<8> {
+  static constexpr int kVecs = 1;
+  static constexpr int kCodes = 16;
+};
+template <>
+struct Fmt<6> {
+  static constexpr int kVecs = 3;
+  static constexpr int kCodes = 64;
+};
+
+// Bit offset o (inside its 24-bit window) of the code at column c of a row.
+template <int BITS>
+__host__ __device__ __forceinline__ int code_offset(int c) {
+  if (BITS == 4) {
+    const int n = c & 7;
+    return n < 6 ? 4 * n : (n == 6 ? 16 : 20);
+  } else if (BITS == 8) {
+    const int n = c & 3;
+    return n < 3 ? 8 * n : 16;
+  } else {
+    return 6 * (c & 3);
+  }
+}
+
+// Masked code words of one step, code j of the step in m[j]: each m[j] < 2^24, equal to
+// q_j << code_offset(j).
+template <int BITS>
+__device__ __forceinline__ void step_masks(const uint4 *v, uint32_t (&m)[Fmt<BITS>::kCodes]) {
+  if constexpr (BITS == 4) {
+    const uint32_t w[4] = {v[0].x, v[0].y, v[0].z, v[0].w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const uint32_t t = w[i] >> 8;
+      m[8 * i + 0] = w[i] & 0x0000000fu;
+      m[8 * i + 1] = w[i] & 0x000000f0u;
+      m[8 * i + 2] = w[i] & 0x00000f00u;
+      m[8 * i + 3] = w[i] & 0x0000f000u;
+      m[8 * i + 4] = w[i] & 0x000f0000u;
+      m[8 * i + 5] = w[i] & 0x00f00000u;
+      m[8 * i + 6] = t & 0x000f0000u;
+      m[8 * i + 7] = t & 0x00f00000u;
+    }
+  } else if constexpr (BITS == 8) {
+    const uint32_t w[4] = {v[0].x, v[0].y, v[0].z, v[0].w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      m[4 * i + 0] = w[i] & 0x000000ffu;
+      m[4 * i + 1] = w[i] & 0x0000ff00u;
+      m[4 * i + 2] = w[i] & 0x00ff0000u;
+      m[4 * i + 3] = (w[i] >> 8) & 0x00ff0000u;
+    }
+  } else {
+    const uint32_t w[12] = {v[0].x, v[0].y, v[0].z, v[0].w, v[1].x, v[1].y,
+                            v[1].z, v[1].w, v[2].x, v[2].y, v[2].z, v[2].w};
+#pragma unroll
+    for (int t = 0; t < 4; ++t) {
+      const uint32_t w0 = w[3 * t], w1 = w[3 * t + 1], w2 = w[3 * t + 2];
+      const uint32_t win[4] = {w0, __funnelshift_r(w0, w1, 24), __funnelshift_r(w1, w2, 16),
+                               w2 >> 8};
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        m[16 * t + 4 * q + 0] = win[q] & 0x0000003fu;
+        m[16 * t + 4 * q + 1] = win[q] & 0x00000fc0u;
+        m[16 * t + 4 * q + 2] = win[q] & 0x0003f000u;
+        m[16 * t + 4 * q + 3] = win[q] & 0x00fc0000u;
+      }
+    }
+  }
+}
+
+// sum_j q_j * x_j * 2^-S over one step; xs holds the step's pre-scaled activations (16-B aligned).
+template <int BITS>
+__device__ __forceinline__ float step_dot(const uint4 *v, const float *xs) {
+  constexpr int N = Fmt<BITS>::kCodes;
+  uint32_t m[N];
+  step_masks<BITS>(v, m);
+  float a0 = 0.f, a1 = 0.f, a2 = 0.f, a3 = 0.f;
+#pragma unroll
+  for (int j = 0; j < N; j += 4) {
+    const float4 x4 = *reinterpret_cast<const float4 *>(xs + j);
+    a0 = fmaf(__uint_as_float(m[j + 0]), x4.x, a0);
+    a1 = fmaf(__uint_as_float(m[j + 1]), x4.y, a1);
+    a2 = fmaf(__uint_as_float(m[j + 2]), x4.z, a2);
+    a3 = fmaf(__uint_as_float(m[j + 3]), x4.w, a3);
+  }
+  return (a0 + a1) + (a2 + a3);
+}
+
+}  // namespace moe

@@ -1,0 +1,107 @@
+"""Shared builders for the GPU tests: seeded problems, the oracle's expectation, and the parity bar.
+
+Parity bar (fp32-accumulated output): max|gpu - oracle| <= 1e-3 * rms(oracle) + 1e-6 and relative
+L2 error <= 1e-4.  A bf16 output is compared with the oracle rounded to bf16, within one bf16 ulp.
+"""
+from __future__ import annotations
+
+import numpy as np
+import torch
+
+from oracle import oracle as O
+from quantized_moe_expert_dequant_gb300 import binding as Bn
+from quantized_moe_expert_dequant_gb300 import synth
+from quantized_moe_expert_dequant_gb300.workloads import Shape
+
+ATOL_RMS, ATOL_ABS, REL_L2 = 1e-3, 1e-6, 1e-4
+
+
+def dev(a: np.ndarray, dtype: torch.dtype) -> torch.Tensor:
+    a = np.ascontiguousarray(a)
+    if dtype in (torch.bfloat16, torch.float16):
+        return torch.from_numpy(a.view(np.int16)).view(dtype).cuda()
+    return torch.from_numpy(a).cuda()
+
+
+def host_layer_device(shape: Shape, layer: int = 0) -> Bn.DeviceLayer:
+    """Every expert drawn on the host and copied: independent of the device generator."""
+    s, E = shape.seed, shape.n_experts
+    mk = lambda proj, n, r, c, b: Bn.proj_from_host(*synth.stacked_proj(s, layer, proj, n, r, c, b))
+    d = Bn.DeviceLayer(shape, None, None, None)
+    if shape.top_k > 0:
+        d.gate = mk(synth.GATE, E, shape.dff, shape.din, shape.bits_gate)
+        d.up = mk(synth.UP, E, shape.dff, shape.din, shape.bits_up)
+        d.down = mk(synth.DOWN, E, shape.din, shape.dff, shape.bits_down)
+    if shape.n_shared:
+        n, w, b = shape.n_shared, shape.dff_shared, shape.bits_shared
+        d.sh_gate = mk(synth.SH_GATE, n, w, shape.din, b)
+        d.sh_up = mk(synth.SH_UP, n, w, shape.din, b)
+        d.sh_down = mk(synth.SH_DOWN, n, shape.din, w, b)
+        if shape.shared_gate:
+            d.gate_vec = dev(synth.gate_vector(s, layer, shape.din), torch.bfloat16)
+    return d
+
+
+def token_inputs(shape: Shape, layer: int = 0, m: int = 1, step: int = 0):
+    """x, resid (bf16 bits) [m, din]; ids int32 and scores fp32 [m, K]."""
+    s = shape.seed
+    x = np.stack([synth.activations(s, layer, t + 1000 * step, shape.din) for t in range(m)])
+    r = np.stack([synth.residual(s, layer, t + 1000 * step, shape.din) for t in range(m)])
+    ids = np.stack([synth.topk_ids(s, layer, t, shape.n_experts, shape.top_k, step)
+                    for t in range(m)]).astype(np.int32).reshape(m, shape.top_k)
+    sc = np.stack([synth.scores(s, layer, t, shape.top_k, step)
+                   for t in range(m)]).astype(np.float32).reshape(m, shape.top_k)
+    return x, r, ids, sc
+
+
+class OracleLayer:
+    """The oracle's view of one synthetic layer: experts regenerated on the host on demand."""
+
+    def __init__(self, shape: Shape, layer: int = 0):
+        self.shape, self.layer = shape, layer
+        self._cache = {}
+
+    def packed(self, proj, e, rows, cols, bits):
+        key = (proj, e)
+        if key not in self._cache:
+            c, s, b = synth.expert_proj(self.shape.seed, self.layer, proj, e, rows, cols, bits)
+            self._cache[key] = O.Packed(c, s, b, bits)
+        return self._cache[key]
+
+    def token(self, x_bits, resid, ids, scores, rows=None):
+        sh = self.shape
+        valid = [(int(e), float(w)) for e, w in zip(ids, scores) if 0 <= int(e) < sh.n_experts]
+        g = [self.packed(synth.GATE, e, sh.dff, sh.din, sh.bits_gate) for e, _ in valid]
+        u = [self.packed(synth.UP, e, sh.dff, sh.din, sh.bits_up) for e, _ in valid]
+        d = [self.packed(synth.DOWN, e, sh.din, sh.dff, sh.bits_down) for e, _ in valid]
+        n, w, b = sh.n_shared, sh.dff_shared, sh.bits_shared
+        sg = [self.packed(synth.SH_GATE, i, w, sh.din, b) for i in range(n)]
+        su = [self.packed(synth.SH_UP, i, w, sh.din, b) for i in range(n)]
+        sd = [self.packed(synth.SH_DOWN, i, sh.din, w, b) for i in range(n)]
+        gv = synth.gate_vector(sh.seed, self.layer, sh.din) if (n and sh.shared_gate) else None
+        sc = np.array([w_ for _, w_ in valid], dtype=np.float32)
+        return O.moe_token(x_bits, resid, sc, g, u, d, sg, su, sd, gate_vec_bf16=gv, rows=rows)
+
+
+def parity(gpu, ref) -> tuple[float, float, float]:
+    gpu = np.asarray(gpu, dtype=np.float64).reshape(-1)
+    ref = np.asarray(ref, dtype=np.float64).reshape(-1)
+    err = float(np.abs(gpu - ref).max())
+    rms = float(np.sqrt(np.mean(ref ** 2)))
+    rel = float(np.linalg.norm(gpu - ref) / max(np.linalg.norm(ref), 1e-300))
+    return err, rms, rel
+
+
+def assert_parity(gpu, ref, what=""):
+    err, rms, rel = parity(gpu, ref)
+    assert np.all(np.isfinite(np.asarray(gpu, dtype=np.float64))), f"{what}: non-finite output"
+    assert err <= ATOL_RMS * rms + ATOL_ABS, f"{what}: max err {err:.3e} vs rms {rms:.3e}"
+    assert rel <= REL_L2, f"{what}: rel L2 {rel:.3e}"
+
+
+def assert_parity_bf16(gpu_bf16: torch.Tensor, ref: np.ndarray, what=""):
+    g = gpu_bf16.float().cpu().numpy().astype(np.float64).reshape(-1)
+    r = synth.bf16_bits_to_f32(synth.f32_to_bf16_bits(ref.astype(np.float32))).astype(np.float64)
+    _, e = np.frexp(r)
+    ulp = np.ldexp(1.0, e - 8)  # |r| in [2^(e-1), 2^e): bf16 spacing 2^(e-8)
+    assert np.all(np.abs(g - r) <= ulp), f"{what}: bf16 output beyond one ulp"
