@@ -1,0 +1,471 @@
+#!/usr/bin/env python
+"""Decode MoE expert block on GB300: throughput of the full layer stack, one JSON line.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--tokens M]
+    python bench.py --impl reference ...        # the fp64 CPU oracle on the host cores
+
+A step is one decode step through every layer of the stack (kernel A and kernel B per layer,
+replayed as one CUDA graph), on seeded synthetic weights drawn in HBM and token inputs already
+resident on the device.  Each step uses the next of several pre-drawn input sets, so expert ids
+change from step to step, and a step reads far more weight bytes than L2 holds.
+
+value      tokens per second through the whole stack (all ranks), timed with CUDA events
+e2e        the same through moe_stack_step_host: inputs copied from pinned host memory and the
+           output copied back inside the timed region
+roofline   kernel A (the gate/up GEMVs, the larger share of bytes): algorithmic bytes per launch
+           divided by its per-launch time, measured by replaying kernel A of every layer alone
+cpu_baseline  the oracle, as it stands, on a bounded sample of the same workload
+N > 1      independent replicas, one per GPU (the block has no exchange step); weak scaling
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from quantized_moe_expert_dequant_gb300 import synth  # noqa: E402
+from quantized_moe_expert_dequant_gb300.workloads import ALL, Shape  # noqa: E402
+
+METRIC = "MoE decode tok/s (full layer stack) and achieved HBM GB/s vs peak, 1 GB300"
+DEFAULT_WORKLOAD = "qwen3_stack_8bit"
+KERNEL_SOURCES = ["quantized_moe_expert_dequant_gb300/csrc/moe_kernels.cu",
+                  "quantized_moe_expert_dequant_gb300/csrc/moe_common.cuh"]
+
+
+# ---------------------------------------------------------------- algorithmic bytes
+
+def proj_bytes(rows, cols, bits):
+    return rows * cols * bits // 8 + (rows * cols // 64) * 4
+
+
+def layer_bytes(shape: Shape, m: int, unique_experts: int, first_layer: bool):
+    """(kernel A bytes, kernel B bytes) of one layer for m tokens whose slots name
+    `unique_experts` distinct experts: each selected weight byte is counted once."""
+    act = shape.top_k * shape.dff + shape.n_shared * shape.dff_shared
+    a = unique_experts * (proj_bytes(shape.dff, shape.din, shape.bits_gate)
+                          + proj_bytes(shape.dff, shape.din, shape.bits_up))
+    a += shape.n_shared * 2 * proj_bytes(shape.dff_shared, shape.din, shape.bits_shared)
+    a += m * (shape.din * 2 + act * 4 + shape.top_k * 8)
+    if shape.n_shared and shape.shared_gate:
+        a += shape.din * 2
+    b = unique_experts * proj_bytes(shape.din, shape.dff, shape.bits_down)
+    b += shape.n_shared * proj_bytes(shape.din, shape.dff_shared, shape.bits_shared)
+    b += m * (act * 4 + shape.din * (2 if first_layer else 4) + shape.din * 4 + shape.top_k * 4)
+    return a, b
+
+
+def per_token_layer_weight_bytes(shape: Shape):
+    return shape.top_k * shape.expert_bytes() + shape.shared_bytes()
+
+
+# ---------------------------------------------------------------- inputs
+
+def input_set(shape: Shape, m: int, step: int):
+    L = shape.layers
+    x = np.stack([np.stack([synth.activations(shape.seed, l, t + 1000 * step, shape.din)
+                            for t in range(m)]) for l in range(L)])
+    ids = np.stack([np.stack([synth.topk_ids(shape.seed, l, t, shape.n_experts, shape.top_k, step)
+                              for t in range(m)]) for l in range(L)]).astype(np.int32)
+    sc = np.stack([np.stack([synth.scores(shape.seed, l, t, shape.top_k, step)
+                             for t in range(m)]) for l in range(L)]).astype(np.float32)
+    resid0 = np.stack([synth.residual(shape.seed, 0, t + 1000 * step, shape.din) for t in range(m)])
+    return x, ids.reshape(L, m, shape.top_k), sc.reshape(L, m, shape.top_k), resid0
+
+
+def unique_per_layer(ids: np.ndarray):
+    return [len(set(ids[l].reshape(-1).tolist())) for l in range(ids.shape[0])]
+
+
+# ---------------------------------------------------------------- the oracle on the host
+
+def oracle_throughput(shape: Shape, target_s: float, max_units: int | None = None):
+    """Times the oracle, as it stands, on whole expert MLPs of input set 0 (each call one routed
+    slot or one shared expert of one layer for one token, all output rows), cycling over layers,
+    until target_s seconds of oracle time or max_units calls.  Returns (weight bytes per second,
+    units, seconds, description).  Only the oracle call is timed; drawing the packed experts on
+    the host is not."""
+    from oracle import oracle as O
+    x, ids, sc, resid0 = input_set(shape, 1, 0)
+    units, spent, nbytes = 0, 0.0, 0
+    layer = 0
+    while spent < target_s and (max_units is None or units < max_units):
+        l = layer % shape.layers
+        pk = lambda proj, e, r, c, b: O.Packed(*synth.expert_proj(shape.seed, l, proj, e, r, c, b), b)
+        xl = x[l][0]
+        resid = resid0[0] if l == 0 else synth.bf16_bits_to_f32(resid0[0])
+        calls = []
+        for k in range(shape.top_k):
+            e = int(ids[l][0][k])
+            g = pk(synth.GATE, e, shape.dff, shape.din, shape.bits_gate)
+            u = pk(synth.UP, e, shape.dff, shape.din, shape.bits_up)
+            d = pk(synth.DOWN, e, shape.din, shape.dff, shape.bits_down)
+            calls.append((dict(scores=sc[l][0][k:k + 1], gate=[g], up=[u], down=[d]),
+                          shape.expert_bytes()))
+        for s in range(shape.n_shared):
+            w, b = shape.dff_shared, shape.bits_shared
+            sh = dict(scores=np.zeros(0, np.float32), gate=[], up=[], down=[],
+                      sh_gate=[pk(synth.SH_GATE, s, w, shape.din, b)],
+                      sh_up=[pk(synth.SH_UP, s, w, shape.din, b)],
+                      sh_down=[pk(synth.SH_DOWN, s, shape.din, w, b)],
+                      gate_vec_bf16=synth.gate_vector(shape.seed, l, shape.din)
+                      if shape.shared_gate else None)
+            calls.append((sh, shape.shared_bytes() // shape.n_shared))
+        for kw, nb in calls:
+            t0 = time.perf_counter()
+            O.moe_token(xl, resid, **kw)
+            spent += time.perf_counter() - t0
+            nbytes += nb
+            units += 1
+            if spent >= target_s or (max_units is not None and units >= max_units):
+                break
+        layer += 1
+    desc = (f"{units} expert MLPs (one slot or shared expert of one token, all rows) from layers "
+            f"0..{min(layer, shape.layers) - 1}, single-threaded fp64 oracle")
+    return nbytes / spent, units, spent, desc
+
+
+def oracle_tok_per_s(shape: Shape, m: int, bps: float) -> float:
+    step_bytes = m * shape.layers * per_token_layer_weight_bytes(shape)
+    return m / (step_bytes / bps)
+
+
+# ---------------------------------------------------------------- clocks
+
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, bus_id: str | None):
+        self.proc = None
+        try:
+            cmd = ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                   "-lms", "100"]
+            if bus_id:
+                cmd += ["-i", bus_id]
+            self.proc = subprocess.Popen(cmd, stdout=subprocess.PIPE, stderr=subprocess.DEVNULL,
+                                         text=True)
+        except OSError:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        self.proc.terminate()
+        out, _ = self.proc.communicate(timeout=10)
+        rows = [r.split(", ") for r in out.strip().splitlines() if r.count(",") >= 8]
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for r in rows:
+            try:
+                sm.append(float(r[1]))
+                smax.append(float(r[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, r[5:9]):
+                if v.strip().lower() == "active":
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(smax) if smax else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ---------------------------------------------------------------- helpers
+
+def measured_peaks():
+    try:
+        return json.load(open(os.path.join(ROOT, "MEASURED_PEAKS.json")))
+    except (OSError, ValueError):
+        return None
+
+
+def kernel_source_hash() -> str:
+    h = hashlib.sha256()
+    for f in KERNEL_SOURCES:
+        h.update(open(os.path.join(ROOT, f), "rb").read())
+    return h.hexdigest()[:16]
+
+
+def profiled_traffic(kernel: str, workload: str):
+    """dram bytes per launch from the committed ncu summary, if taken on the current source."""
+    path = os.path.join(ROOT, "profiles", "traffic.txt")
+    if not os.path.exists(path):
+        return None
+    src = kernel_source_hash()
+    for line in open(path):
+        kv = dict(p.split("=", 1) for p in line.split() if "=" in p)
+        if kv.get("kernel") == kernel and kv.get("workload") == workload and kv.get("src") == src:
+            return float(kv["dram_bytes_per_launch"])
+    return None
+
+
+def dist_setup(backend):
+    import torch.distributed as dist
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1 and not dist.is_initialized():
+        dist.init_process_group(backend=backend)
+    return rank, world, local
+
+
+def max_over_ranks(v: float, device=None) -> float:
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return v
+    t = torch.tensor([v], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def barrier(device=None):
+    import torch.distributed as dist
+    if dist.is_available() and dist.is_initialized() and dist.get_world_size() > 1:
+        if device is not None:
+            dist.barrier(device_ids=[device.index])
+        else:
+            dist.barrier()
+
+
+# ---------------------------------------------------------------- the reference arm
+
+def run_reference(args, shape: Shape):
+    rank, world, _ = dist_setup("gloo")
+    if rank != 0:
+        return 0
+    # each step: one expert MLP of the stack through the oracle; the rate scales to the stack
+    for _ in range(args.warmup):
+        oracle_throughput(shape, 0.0, max_units=1)
+    nbytes, spent = 0.0, 0.0
+    units = 0
+    for _ in range(args.steps):
+        bps, u, s, desc = oracle_throughput(shape, 0.0, max_units=1)
+        nbytes += bps * s
+        spent += s
+        units += u
+    bps = nbytes / spent
+    tok = oracle_tok_per_s(shape, args.tokens, bps)
+    step_s = args.tokens / tok
+    line = {
+        "impl": "reference", "metric": METRIC, "value": tok, "unit": "tok/s", "n_gpus": 0,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": step_s * 1e3,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic",
+        "config": {"workload": shape.name, "layers": shape.layers, "tokens_per_step": args.tokens},
+        "cpu_baseline": {"value": tok, "unit": "tok/s", "cores": 1, "kind": "oracle",
+                         "sample": f"each step one expert MLP (one slot of one token of one "
+                                   f"layer, all rows) through the fp64 oracle; {units} timed in "
+                                   f"{spent:.1f} s, scaled by weight bytes to the full stack"},
+        "e2e": {"value": tok, "unit": "tok/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+# ---------------------------------------------------------------- our arm
+
+def run_ours(args, shape: Shape):
+    import torch
+
+    from quantized_moe_expert_dequant_gb300 import binding as Bn
+
+    rank, world, local = dist_setup("nccl")
+    torch.cuda.set_device(local)
+    device = torch.device("cuda", local)
+    m, L, S = args.tokens, shape.layers, args.input_sets
+
+    free, _ = torch.cuda.mem_get_info()
+    need = shape.layer_weight_bytes() * L
+    if free < need * 1.05:
+        raise SystemExit(f"workload needs {need / 1e9:.1f} GB, {free / 1e9:.1f} GB free")
+    layers = [Bn.synth_layer_device(shape, l) for l in range(L)]
+    stack = Bn.MoeStack(layers, max_tokens=m)
+
+    def dev(a, dt):
+        a = np.ascontiguousarray(a)
+        if dt == torch.bfloat16:
+            return torch.from_numpy(a.view(np.int16)).view(dt).to(device)
+        return torch.from_numpy(a).to(device)
+
+    sets, uniq = [], []
+    for s in range(S):
+        x, ids, sc, r0 = input_set(shape, m, s)
+        uniq.append(unique_per_layer(ids))
+        sets.append((dev(x, torch.bfloat16), dev(ids, torch.int32), dev(sc, torch.float32),
+                     dev(r0, torch.bfloat16), torch.empty((m, shape.din), dtype=torch.float32,
+                                                          device=device), (x, ids, sc, r0)))
+    bytes_a = [sum(layer_bytes(shape, m, u[l], l == 0)[0] for l in range(L)) for u in uniq]
+    bytes_b = [sum(layer_bytes(shape, m, u[l], l == 0)[1] for l in range(L)) for u in uniq]
+
+    stream = torch.cuda.current_stream(device)
+
+    def step(i, parts=3):
+        x, ids, sc, r0, out, _ = sets[i % S]
+        if parts == 3:
+            stack.step(x, ids, sc, r0, out, stream)
+        else:
+            stack.step_parts(parts, x, ids, sc, r0, out, stream)
+
+    bus = None
+    try:
+        bus = torch.cuda.get_device_properties(device).pci_bus_id
+    except AttributeError:
+        bus = None
+    sampler = ClockSampler(bus if bus else str(local))
+
+    # warm-up: captures every graph, then W untimed steps
+    for i in range(S):
+        step(i)
+        step(i, Bn.PART_GATE_UP)
+        step(i, Bn.PART_DOWN)
+    torch.cuda.synchronize(device)
+    for i in range(args.warmup):
+        step(i)
+    torch.cuda.synchronize(device)
+    assert stack.get_error() == 0
+
+    # timed region: exactly K steps
+    barrier(device)
+    torch.cuda.synchronize(device)
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for i in range(args.steps):
+        step(i)
+    e1.record(stream)
+    torch.cuda.synchronize(device)
+    barrier(device)
+    ms_local = e0.elapsed_time(e1)
+    ms = max_over_ranks(ms_local, device)
+    ms_per_step = ms / args.steps
+    tokens_all = world * m * args.steps
+    value = tokens_all / (ms / 1e3)
+    step_bytes = sum(bytes_a[i % S] + bytes_b[i % S] for i in range(args.steps)) / args.steps
+
+    # dominant kernel: kernel A of every layer replayed alone (same launch configuration)
+    reps = max(args.steps, 20)
+
+    def time_part(parts):
+        torch.cuda.synchronize(device)
+        a0 = torch.cuda.Event(enable_timing=True)
+        a1 = torch.cuda.Event(enable_timing=True)
+        a0.record(stream)
+        for i in range(reps):
+            step(i, parts)
+        a1.record(stream)
+        torch.cuda.synchronize(device)
+        return a0.elapsed_time(a1) / (reps * L * m)   # ms per launch
+
+    ms_a = time_part(Bn.PART_GATE_UP)
+    ms_b = time_part(Bn.PART_DOWN)
+    mean_a = sum(bytes_a[i % S] for i in range(reps)) / reps / (L * m)
+    mean_b = sum(bytes_b[i % S] for i in range(reps)) / reps / (L * m)
+
+    # end to end through the public host-buffer call
+    pinned = []
+    for (_, _, _, _, _, host) in sets:
+        x, ids, sc, r0 = host
+        pin = lambda a, dt: (torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).view(dt)
+                             if dt == torch.bfloat16 else torch.from_numpy(np.ascontiguousarray(a))
+                             ).pin_memory()
+        pinned.append((pin(x, torch.bfloat16), pin(ids, torch.int32), pin(sc, torch.float32),
+                       pin(r0, torch.bfloat16),
+                       torch.empty((m, shape.din), dtype=torch.float32).pin_memory()))
+    for i in range(min(3, len(pinned))):
+        stack.step_host(*pinned[i], stream=stream)
+    e2e_steps = max(args.steps // 4, 10)
+    barrier(device)
+    t0 = time.perf_counter()
+    for i in range(e2e_steps):
+        stack.step_host(*pinned[i % S], stream=stream)
+    t1 = time.perf_counter()
+    barrier(device)
+    e2e_s = max_over_ranks(t1 - t0, device)
+    h2d = sum(t.numel() * t.element_size() for t in pinned[0][:4])
+    d2h = pinned[0][4].numel() * 4
+    clocks = sampler.stop()
+    assert stack.get_error() == 0
+
+    peaks = measured_peaks()
+    peak = peaks["hbm_gbs"] if peaks else 6800.0
+    peak_note = "of measured" if peaks else "of fallback"
+    ach_a = mean_a / (ms_a * 1e-3) / 1e9
+    ach_b = mean_b / (ms_b * 1e-3) / 1e9
+    traffic = profiled_traffic("gate_up_kernel", args.workload)
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        bps, units, spent, desc = oracle_throughput(shape, args.cpu_seconds)
+        cpu = {"value": oracle_tok_per_s(shape, m, bps), "unit": "tok/s", "cores": 1,
+               "kind": "oracle", "sample": f"{desc}; {spent:.1f} s of oracle time, scaled by "
+                                           f"weight bytes to one step of the full stack"}
+
+    line = {
+        "metric": METRIC, "value": value, "unit": "tok/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_per_step,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+        "data": "synthetic (seeded weights drawn in HBM, seeded token inputs)",
+        "config": {"workload": shape.name, "din": shape.din, "dff": shape.dff,
+                   "experts": shape.n_experts, "top_k": shape.top_k,
+                   "bits": [shape.bits_gate, shape.bits_up, shape.bits_down],
+                   "shared": [shape.n_shared, shape.dff_shared, shape.bits_shared],
+                   "layers": L, "tokens_per_step": m, "input_sets": S,
+                   "parallelism": f"replicas x{world}",
+                   "l2": f"inputs larger than L2: {step_bytes / 1e9:.3f} GB of selected weights "
+                         f"per step, ids re-drawn per step"},
+        "hbm": {"step_bytes": step_bytes, "step_gbs": step_bytes / (ms_per_step * 1e-3) / 1e9,
+                "peak_gbs": peak, "frac": step_bytes / (ms_per_step * 1e-3) / 1e9 / peak,
+                "note": peak_note},
+        "roofline": {"kernel": "gate_up_kernel", "bound": "hbm", "achieved": ach_a, "peak": peak,
+                     "unit": "GB/s", "frac": ach_a / peak, "traffic": traffic,
+                     "bytes_per_launch": mean_a, "us_per_launch": ms_a * 1e3,
+                     "note": peak_note + " (copy peak)"},
+        "kernel_b": {"kernel": "down_kernel", "achieved": ach_b, "frac": ach_b / peak,
+                     "bytes_per_launch": mean_b, "us_per_launch": ms_b * 1e3},
+        "cpu_baseline": cpu,
+        "e2e": {"value": world * m * e2e_steps / e2e_s, "unit": "tok/s",
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+        "gpu_launches": args.steps * L * m * 2,
+        "clocks": clocks,
+    }
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    stack.close()
+    return 0
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__.splitlines()[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", choices=sorted(ALL), default=DEFAULT_WORKLOAD)
+    ap.add_argument("--tokens", type=int, default=1)
+    ap.add_argument("--input-sets", type=int, default=4)
+    ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args(argv)
+    if args.warmup < 3:
+        ap.error("--warmup must be at least 3")
+    shape = ALL[args.workload]
+    if shape.layers == 1:
+        ap.error("bench workloads are the layer stacks")
+    if args.impl == "reference":
+        return run_reference(args, shape)
+    return run_ours(args, shape)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

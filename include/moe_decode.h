@@ -130,6 +130,15 @@ int moe_stack_create(const moe_decode_config *cfg, int32_t n_layers,
 int moe_stack_step(moe_stack_t *s, const void *x, int32_t m, const int32_t *ids,
                    const float *scores, const void *resid0, void *out, void *stream);
 
+/* Measurement aid: the same step with only some kernels of every layer in the graph.
+ * parts = MOE_PART_GATE_UP (kernel A of each layer), MOE_PART_DOWN (kernel B of each layer, reading
+ * whatever activations the workspace holds) or both (identical to moe_stack_step).  Replaying one
+ * part times that kernel's launches back to back with the same launch configuration. */
+enum { MOE_PART_GATE_UP = 1, MOE_PART_DOWN = 2 };
+int moe_stack_step_parts(moe_stack_t *s, int32_t parts, const void *x, int32_t m,
+                         const int32_t *ids, const float *scores, const void *resid0, void *out,
+                         void *stream);
+
 /* One decode step from HOST buffers: copies x, ids, scores and resid0 (best from pinned memory)
  * into the stack's device staging buffers, replays the graph, copies out back, and synchronises
  * the stream before returning. */

@@ -22,11 +22,13 @@ LIB_PATH = os.path.join(_HERE, "libmoe_decode.so")
 MOE_OK, MOE_ERR_INVALID_ARG, MOE_ERR_UNSUPPORTED, MOE_ERR_CUDA, MOE_ERR_OOM, MOE_ERR_BAD_ID = (
     0, -1, -2, -3, -4, -5)
 DTYPE_BF16, DTYPE_F32 = 0, 1
+PART_GATE_UP, PART_DOWN = 1, 2
 _STATUS = {0: "MOE_OK", -1: "MOE_ERR_INVALID_ARG", -2: "MOE_ERR_UNSUPPORTED", -3: "MOE_ERR_CUDA",
            -4: "MOE_ERR_OOM", -5: "MOE_ERR_BAD_ID", -6: "MOE_ERR_TIMEOUT"}
 
 EXPORTS = ["moe_decode_create", "moe_decode_forward", "moe_decode_get_error", "moe_decode_destroy",
-           "moe_stack_create", "moe_stack_step", "moe_stack_step_host", "moe_stack_get_error",
+           "moe_stack_create", "moe_stack_step", "moe_stack_step_parts", "moe_stack_step_host",
+           "moe_stack_get_error",
            "moe_stack_destroy", "moe_pack_codes", "moe_unpack_codes", "moe_unpack_codes_device",
            "moe_synth_codes", "moe_synth_scales", "moe_synth_biases"]
 
@@ -76,6 +78,7 @@ def lib() -> ctypes.CDLL:
                 "moe_stack_create": [ctypes.POINTER(Config), i32, ctypes.POINTER(LayerWeights),
                                      ctypes.POINTER(vp)],
                 "moe_stack_step": [vp, vp, i32, vp, vp, vp, vp, vp],
+                "moe_stack_step_parts": [vp, i32, vp, i32, vp, vp, vp, vp, vp],
                 "moe_stack_step_host": [vp, vp, i32, vp, vp, vp, vp, vp],
                 "moe_stack_get_error": [vp, ctypes.POINTER(i32)],
                 "moe_stack_destroy": [vp],
@@ -262,6 +265,14 @@ class MoeStack:
         m = resid0.shape[0]
         check("moe_stack_step", lib().moe_stack_step(self.handle, _p(x), m, _p(ids), _p(scores),
                                                      _p(resid0), _p(out), _stream(stream)))
+        return out
+
+    def step_parts(self, parts, x, ids, scores, resid0, out, stream=None):
+        """Only kernel A (parts=1) or only kernel B (parts=2) of every layer: a timing aid."""
+        m = resid0.shape[0]
+        check("moe_stack_step_parts", lib().moe_stack_step_parts(
+            self.handle, parts, _p(x), m, _p(ids), _p(scores), _p(resid0), _p(out),
+            _stream(stream)))
         return out
 
     def step_host(self, x, ids, scores, resid0, out, stream=None):

@@ -113,7 +113,7 @@ size_t dtype_bytes(int dt) { return dt == MOE_DTYPE_F32 ? 4 : 2; }
 cudaError_t enqueue_layer(const Layer &L, float *act, int32_t *err, const void *x, int m,
                           const int32_t *ids, const float *scores, const void *resid,
                           int resid_dtype, void *out, int out_dtype, cudaStream_t stream,
-                          bool pdl) {
+                          bool pdl, int parts = MOE_PART_GATE_UP | MOE_PART_DOWN) {
   const moe_decode_config &c = L.cfg;
   for (int t = 0; t < m; ++t) {
     GateUpParams a;
@@ -135,8 +135,9 @@ cudaError_t enqueue_layer(const Layer &L, float *act, int32_t *err, const void *
     a.n_experts = c.n_experts;
     a.n_shared = c.n_shared;
     a.dff_shared = c.dff_shared;
-    cudaError_t e =
-        moe::launch_gate_up(a, c.bits_gate, L.bits_s, L.grid_a, L.smem_a, stream, pdl);
+    cudaError_t e = cudaSuccess;
+    if (parts & MOE_PART_GATE_UP)
+      e = moe::launch_gate_up(a, c.bits_gate, L.bits_s, L.grid_a, L.smem_a, stream, pdl);
     if (e != cudaSuccess) return e;
 
     DownParams b;
@@ -155,7 +156,8 @@ cudaError_t enqueue_layer(const Layer &L, float *act, int32_t *err, const void *
     b.n_experts = c.n_experts;
     b.n_shared = c.n_shared;
     b.dff_shared = c.dff_shared;
-    e = moe::launch_down(b, c.bits_down, L.bits_sd, L.grid_b, L.smem_b, stream, pdl);
+    if (parts & MOE_PART_DOWN)
+      e = moe::launch_down(b, c.bits_down, L.bits_sd, L.grid_b, L.smem_b, stream, pdl);
     if (e != cudaSuccess) return e;
   }
   return cudaSuccess;
@@ -238,7 +240,7 @@ extern "C" void moe_decode_destroy(moe_decode_t *h) {
 namespace {
 struct GraphEntry {
   const void *x, *ids, *scores, *resid0, *out;
-  int m;
+  int m, parts;
   cudaGraphExec_t exec;
   uint64_t last_use;
 };
@@ -326,7 +328,7 @@ namespace {
 
 cudaError_t enqueue_stack(moe_stack *s, const void *x, int m, const int32_t *ids,
                           const float *scores, const void *resid0, void *out, cudaStream_t st,
-                          bool pdl) {
+                          bool pdl, int parts) {
   const int L = (int)s->layers.size();
   const size_t din = s->cfg.din, K = s->cfg.top_k;
   for (int l = 0; l < L; ++l) {
@@ -337,18 +339,18 @@ cudaError_t enqueue_stack(moe_stack *s, const void *x, int m, const int32_t *ids
     const int rdt = l == 0 ? s->cfg.resid_dtype : MOE_DTYPE_F32;
     void *ol = l == L - 1 ? out : s->ping[l & 1];
     cudaError_t e = enqueue_layer(s->layers[l], s->act, s->err, xl, m, il, sl, rl, rdt, ol,
-                                  MOE_DTYPE_F32, st, pdl);
+                                  MOE_DTYPE_F32, st, pdl, parts);
     if (e != cudaSuccess) return e;
   }
   return cudaSuccess;
 }
 
 int capture(moe_stack *s, const void *x, int m, const int32_t *ids, const float *scores,
-            const void *resid0, void *out, bool pdl, cudaGraphExec_t *exec) {
+            const void *resid0, void *out, bool pdl, int parts, cudaGraphExec_t *exec) {
   cudaGraph_t graph = nullptr;
   if (cudaStreamBeginCapture(s->cap, cudaStreamCaptureModeThreadLocal) != cudaSuccess)
     return MOE_ERR_CUDA;
-  cudaError_t e = enqueue_stack(s, x, m, ids, scores, resid0, out, s->cap, pdl);
+  cudaError_t e = enqueue_stack(s, x, m, ids, scores, resid0, out, s->cap, pdl, parts);
   cudaError_t e2 = cudaStreamEndCapture(s->cap, &graph);
   if (e != cudaSuccess || e2 != cudaSuccess || !graph) {
     if (graph) cudaGraphDestroy(graph);
@@ -366,9 +368,11 @@ int capture(moe_stack *s, const void *x, int m, const int32_t *ids, const float 
 
 }  // namespace
 
-extern "C" int moe_stack_step(moe_stack_t *s, const void *x, int32_t m, const int32_t *ids,
-                              const float *scores, const void *resid0, void *out, void *stream) {
+extern "C" int moe_stack_step_parts(moe_stack_t *s, int32_t parts, const void *x, int32_t m,
+                                    const int32_t *ids, const float *scores, const void *resid0,
+                                    void *out, void *stream) {
   if (!s || !x || !resid0 || !out) return MOE_ERR_INVALID_ARG;
+  if (parts < 1 || parts > (MOE_PART_GATE_UP | MOE_PART_DOWN)) return MOE_ERR_INVALID_ARG;
   if (m < 1 || m > s->cfg.max_tokens) return MOE_ERR_INVALID_ARG;
   if (s->cfg.top_k > 0 && (!ids || !scores)) return MOE_ERR_INVALID_ARG;
   if (!aligned(out, 4) || !aligned(x, 2) || !aligned(resid0, dtype_bytes(s->cfg.resid_dtype)))
@@ -376,14 +380,14 @@ extern "C" int moe_stack_step(moe_stack_t *s, const void *x, int32_t m, const in
   GraphEntry *hit = nullptr;
   for (auto &g : s->graphs)
     if (g.x == x && g.ids == ids && g.scores == scores && g.resid0 == resid0 && g.out == out &&
-        g.m == m)
+        g.m == m && g.parts == parts)
       hit = &g;
   if (!hit) {
     cudaGraphExec_t exec = nullptr;
-    int rc = capture(s, x, m, ids, scores, resid0, out, s->pdl, &exec);
+    int rc = capture(s, x, m, ids, scores, resid0, out, s->pdl, parts, &exec);
     if (rc != MOE_OK && s->pdl) {  // a driver without programmatic edges in graphs
       s->pdl = false;
-      rc = capture(s, x, m, ids, scores, resid0, out, false, &exec);
+      rc = capture(s, x, m, ids, scores, resid0, out, false, parts, &exec);
     }
     if (rc != MOE_OK) return rc;
     if (s->graphs.size() >= kMaxGraphs) {
@@ -393,13 +397,19 @@ extern "C" int moe_stack_step(moe_stack_t *s, const void *x, int32_t m, const in
       cudaGraphExecDestroy(s->graphs[lru].exec);
       s->graphs.erase(s->graphs.begin() + lru);
     }
-    s->graphs.push_back(GraphEntry{x, ids, scores, resid0, out, m, exec, 0});
+    s->graphs.push_back(GraphEntry{x, ids, scores, resid0, out, m, parts, exec, 0});
     hit = &s->graphs.back();
   }
   hit->last_use = ++s->clock;
   return cudaGraphLaunch(hit->exec, static_cast<cudaStream_t>(stream)) == cudaSuccess
              ? MOE_OK
              : MOE_ERR_CUDA;
+}
+
+extern "C" int moe_stack_step(moe_stack_t *s, const void *x, int32_t m, const int32_t *ids,
+                              const float *scores, const void *resid0, void *out, void *stream) {
+  return moe_stack_step_parts(s, MOE_PART_GATE_UP | MOE_PART_DOWN, x, m, ids, scores, resid0, out,
+                              stream);
 }
 
 extern "C" int moe_stack_step_host(moe_stack_t *s, const void *x_host, int32_t m,

@@ -174,6 +174,8 @@ def topk_ids(seed, layer, token, n_experts, top_k, step=0) -> np.ndarray:
 
 
 def scores(seed, layer, token, top_k, step=0) -> np.ndarray:
+    if top_k == 0:
+        return np.zeros(0, dtype=np.float32)
     logits = normals_f64(key(seed, layer, ROLE_LOGITS, token, step), top_k)
     e = np.exp(logits - logits.max())
     return (e / e.sum()).astype(np.float32)
