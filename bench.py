@@ -88,50 +88,49 @@ def unique_per_layer(ids: np.ndarray):
 
 # ---------------------------------------------------------------- the oracle on the host
 
-def oracle_throughput(shape: Shape, target_s: float, max_units: int | None = None):
-    """Times the oracle, as it stands, on whole expert MLPs of input set 0 (each call one routed
-    slot or one shared expert of one layer for one token, all output rows), cycling over layers,
-    until target_s seconds of oracle time or max_units calls.  Returns (weight bytes per second,
-    units, seconds, description).  Only the oracle call is timed; drawing the packed experts on
-    the host is not."""
+def oracle_units(shape: Shape):
+    """Endless sequence of (oracle call, weight bytes): whole expert MLPs of input set 0, each one
+    routed slot or one shared expert of one layer for one token with all output rows, cycling
+    over the layers.  Drawing the packed experts on the host happens here, outside any timing."""
     from oracle import oracle as O
     x, ids, sc, resid0 = input_set(shape, 1, 0)
-    units, spent, nbytes = 0, 0.0, 0
     layer = 0
-    while spent < target_s and (max_units is None or units < max_units):
+    while True:
         l = layer % shape.layers
         pk = lambda proj, e, r, c, b: O.Packed(*synth.expert_proj(shape.seed, l, proj, e, r, c, b), b)
         xl = x[l][0]
-        resid = resid0[0] if l == 0 else synth.bf16_bits_to_f32(resid0[0])
-        calls = []
+        resid = resid0[0]
         for k in range(shape.top_k):
             e = int(ids[l][0][k])
-            g = pk(synth.GATE, e, shape.dff, shape.din, shape.bits_gate)
-            u = pk(synth.UP, e, shape.dff, shape.din, shape.bits_up)
-            d = pk(synth.DOWN, e, shape.din, shape.dff, shape.bits_down)
-            calls.append((dict(scores=sc[l][0][k:k + 1], gate=[g], up=[u], down=[d]),
-                          shape.expert_bytes()))
+            kw = dict(scores=sc[l][0][k:k + 1],
+                      gate=[pk(synth.GATE, e, shape.dff, shape.din, shape.bits_gate)],
+                      up=[pk(synth.UP, e, shape.dff, shape.din, shape.bits_up)],
+                      down=[pk(synth.DOWN, e, shape.din, shape.dff, shape.bits_down)])
+            yield (lambda kw=kw: O.moe_token(xl, resid, **kw)), shape.expert_bytes()
         for s in range(shape.n_shared):
             w, b = shape.dff_shared, shape.bits_shared
-            sh = dict(scores=np.zeros(0, np.float32), gate=[], up=[], down=[],
+            kw = dict(scores=np.zeros(0, np.float32), gate=[], up=[], down=[],
                       sh_gate=[pk(synth.SH_GATE, s, w, shape.din, b)],
                       sh_up=[pk(synth.SH_UP, s, w, shape.din, b)],
                       sh_down=[pk(synth.SH_DOWN, s, shape.din, w, b)],
                       gate_vec_bf16=synth.gate_vector(shape.seed, l, shape.din)
                       if shape.shared_gate else None)
-            calls.append((sh, shape.shared_bytes() // shape.n_shared))
-        for kw, nb in calls:
-            t0 = time.perf_counter()
-            O.moe_token(xl, resid, **kw)
-            spent += time.perf_counter() - t0
-            nbytes += nb
-            units += 1
-            if spent >= target_s or (max_units is not None and units >= max_units):
-                break
+            yield (lambda kw=kw: O.moe_token(xl, resid, **kw)), shape.shared_bytes() // shape.n_shared
         layer += 1
-    desc = (f"{units} expert MLPs (one slot or shared expert of one token, all rows) from layers "
-            f"0..{min(layer, shape.layers) - 1}, single-threaded fp64 oracle")
-    return nbytes / spent, units, spent, desc
+
+
+def time_units(units, n: int | None = None, target_s: float | None = None):
+    """Times the oracle, as it stands, on the next units until n calls or target_s seconds of
+    oracle time.  Returns (weight bytes, seconds, calls); only the oracle calls are timed."""
+    nbytes, spent, calls = 0, 0.0, 0
+    while (n is None or calls < n) and (target_s is None or spent < target_s or calls == 0):
+        call, nb = next(units)
+        t0 = time.perf_counter()
+        call()
+        spent += time.perf_counter() - t0
+        nbytes += nb
+        calls += 1
+    return nbytes, spent, calls
 
 
 def oracle_tok_per_s(shape: Shape, m: int, bps: float) -> float:
@@ -245,15 +244,9 @@ def run_reference(args, shape: Shape):
     if rank != 0:
         return 0
     # each step: one expert MLP of the stack through the oracle; the rate scales to the stack
-    for _ in range(args.warmup):
-        oracle_throughput(shape, 0.0, max_units=1)
-    nbytes, spent = 0.0, 0.0
-    units = 0
-    for _ in range(args.steps):
-        bps, u, s, desc = oracle_throughput(shape, 0.0, max_units=1)
-        nbytes += bps * s
-        spent += s
-        units += u
+    units = oracle_units(shape)
+    time_units(units, n=args.warmup)
+    nbytes, spent, calls = time_units(units, n=args.steps)
     bps = nbytes / spent
     tok = oracle_tok_per_s(shape, args.tokens, bps)
     step_s = args.tokens / tok
@@ -265,7 +258,7 @@ def run_reference(args, shape: Shape):
         "config": {"workload": shape.name, "layers": shape.layers, "tokens_per_step": args.tokens},
         "cpu_baseline": {"value": tok, "unit": "tok/s", "cores": 1, "kind": "oracle",
                          "sample": f"each step one expert MLP (one slot of one token of one "
-                                   f"layer, all rows) through the fp64 oracle; {units} timed in "
+                                   f"layer, all rows) through the fp64 oracle; {calls} timed in "
                                    f"{spent:.1f} s, scaled by weight bytes to the full stack"},
         "e2e": {"value": tok, "unit": "tok/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
@@ -406,10 +399,13 @@ def run_ours(args, shape: Shape):
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        bps, units, spent, desc = oracle_throughput(shape, args.cpu_seconds)
-        cpu = {"value": oracle_tok_per_s(shape, m, bps), "unit": "tok/s", "cores": 1,
-               "kind": "oracle", "sample": f"{desc}; {spent:.1f} s of oracle time, scaled by "
-                                           f"weight bytes to one step of the full stack"}
+        nbytes, spent, calls = time_units(oracle_units(shape), target_s=args.cpu_seconds)
+        cpu = {"value": oracle_tok_per_s(shape, m, nbytes / spent), "unit": "tok/s", "cores": 1,
+               "kind": "oracle",
+               "sample": f"{calls} expert MLPs (one routed slot or shared expert of one token of "
+                         f"one layer, all rows) through the single-threaded fp64 oracle, "
+                         f"{spent:.1f} s of oracle time, scaled by weight bytes to one step of "
+                         f"the full stack"}
 
     line = {
         "metric": METRIC, "value": value, "unit": "tok/s", "n_gpus": world,
@@ -456,11 +452,15 @@ def main(argv=None):
     ap.add_argument("--input-sets", type=int, default=4)
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--layers", type=int, default=0,
+                    help="run only the first N layers of the workload (profiling runs)")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")
     shape = ALL[args.workload]
-    if shape.layers == 1:
+    if args.layers:
+        shape = shape.with_(layers=args.layers, name=f"{shape.name} (first {args.layers} layers)")
+    if shape.layers == 1 and not args.layers:
         ap.error("bench workloads are the layer stacks")
     if args.impl == "reference":
         return run_reference(args, shape)

@@ -43,7 +43,8 @@ typedef enum moe_status {
   MOE_ERR_CUDA = -3,         /* a CUDA runtime call failed (launch, copy, graph) */
   MOE_ERR_OOM = -4,          /* device or pinned allocation failed */
   MOE_ERR_BAD_ID = -5,       /* device error word: an expert id was outside [0, n_experts) */
-  MOE_ERR_TIMEOUT = -6       /* reserved: no kernel here waits on another */
+  MOE_ERR_TIMEOUT = -6       /* device error word: a pipeline wait gave up after about two seconds
+                                (a bug, never expected); the kernel returned without its result */
 } moe_status;
 
 enum { MOE_DTYPE_BF16 = 0, MOE_DTYPE_F32 = 1 };
@@ -64,15 +65,21 @@ typedef struct moe_decode_config {
   int32_t shared_gate;     /* 0: scalar 1;  1: scalar = sigmoid(x . gate_vec) */
   int32_t resid_dtype;     /* MOE_DTYPE_BF16 or MOE_DTYPE_F32 */
   int32_t out_dtype;       /* MOE_DTYPE_F32 (default) or MOE_DTYPE_BF16 (rounded to nearest) */
-  int32_t warps_per_block; /* 0 = automatic */
+  int32_t kernel_mode;     /* MOE_KERNELS_FUSED (default) or MOE_KERNELS_SEPARATE */
 } moe_decode_config;
+
+/* How a layer is launched.  FUSED: one cooperative persistent kernel per forward (or per stack
+ * step) runs the gate/up phase, a device-wide barrier, then the down phase, streaming the down
+ * weights into shared memory while the gate/up phase computes.  SEPARATE: kernel A then kernel B
+ * per layer with programmatic dependent launch (the unfused form, kept for comparison). */
+enum { MOE_KERNELS_FUSED = 0, MOE_KERNELS_SEPARATE = 1 };
 
 /*
  * One projection of every expert of a class, canonical packed layout, all device pointers:
  *   codes  [experts][rows][cols*bits/8] bytes: per row a little-endian bit stream, code c at bits
  *          [c*bits, c*bits + bits), LSB first (8 codes per uint32 at 4 bits, 4 at 8 bits,
  *          16 per 3 uint32 at 6 bits); 16-byte aligned
- *   scales [experts][rows][cols/64] fp16, biases likewise; 2-byte aligned
+ *   scales [experts][rows][cols/64] fp16, biases likewise; 16-byte aligned
  * gate and up have rows = dff, cols = din; down has rows = din, cols = dff.
  */
 typedef struct moe_proj {
@@ -98,7 +105,7 @@ int moe_decode_create(const moe_decode_config *cfg, const moe_layer_weights *wei
                       moe_decode_t **out);
 
 /* Enqueues the block for m tokens on `stream` (asynchronous, allocation-free).
- *   x      bf16 [m][din] device                 token activations
+ *   x      bf16 [m][din] device, 16-byte aligned token activations
  *   ids    int32 [m][top_k] device              routed expert ids, slot order as given
  *   scores fp32 [m][top_k] device               router weights of the slots
  *   resid  [m][din] device, cfg->resid_dtype    residual added in the tail
@@ -109,8 +116,8 @@ int moe_decode_create(const moe_decode_config *cfg, const moe_layer_weights *wei
 int moe_decode_forward(moe_decode_t *h, const void *x, int32_t m, const int32_t *ids,
                        const float *scores, const void *resid, void *out, void *stream);
 
-/* Synchronises the device, returns the sticky device error word in *device_error (0 or
- * MOE_ERR_BAD_ID) and clears it. */
+/* Synchronises the device, returns the sticky device error word in *device_error (MOE_OK,
+ * MOE_ERR_BAD_ID or MOE_ERR_TIMEOUT) and clears it. */
 int moe_decode_get_error(moe_decode_t *h, int32_t *device_error);
 
 void moe_decode_destroy(moe_decode_t *h);

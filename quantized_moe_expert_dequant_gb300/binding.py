@@ -23,6 +23,7 @@ MOE_OK, MOE_ERR_INVALID_ARG, MOE_ERR_UNSUPPORTED, MOE_ERR_CUDA, MOE_ERR_OOM, MOE
     0, -1, -2, -3, -4, -5)
 DTYPE_BF16, DTYPE_F32 = 0, 1
 PART_GATE_UP, PART_DOWN = 1, 2
+KERNELS_FUSED, KERNELS_SEPARATE = 0, 1
 _STATUS = {0: "MOE_OK", -1: "MOE_ERR_INVALID_ARG", -2: "MOE_ERR_UNSUPPORTED", -3: "MOE_ERR_CUDA",
            -4: "MOE_ERR_OOM", -5: "MOE_ERR_BAD_ID", -6: "MOE_ERR_TIMEOUT"}
 
@@ -43,7 +44,7 @@ class Config(ctypes.Structure):
     _fields_ = [(n, ctypes.c_int32) for n in (
         "din", "dff", "n_experts", "top_k", "max_tokens", "bits_gate", "bits_up", "bits_down",
         "n_shared", "dff_shared", "bits_shared", "shared_gate", "resid_dtype", "out_dtype",
-        "warps_per_block")]
+        "kernel_mode")]
 
 
 class Proj(ctypes.Structure):
@@ -113,10 +114,10 @@ def _p(t) -> int | None:
 
 
 def config(shape: Shape, max_tokens: int = 1, resid_dtype: int = DTYPE_BF16,
-           out_dtype: int = DTYPE_F32, warps_per_block: int = 0) -> Config:
+           out_dtype: int = DTYPE_F32, kernel_mode: int = KERNELS_FUSED) -> Config:
     return Config(shape.din, shape.dff, shape.n_experts, shape.top_k, max_tokens, shape.bits_gate,
                   shape.bits_up, shape.bits_down, shape.n_shared, shape.dff_shared,
-                  shape.bits_shared, shape.shared_gate, resid_dtype, out_dtype, warps_per_block)
+                  shape.bits_shared, shape.shared_gate, resid_dtype, out_dtype, kernel_mode)
 
 
 # ---------------------------------------------------------------- device weights
@@ -206,9 +207,9 @@ class MoeDecode:
     """One prepared layer: moe_decode_create once, moe_decode_forward per token batch."""
 
     def __init__(self, layer: DeviceLayer, max_tokens: int = 1, resid_dtype=DTYPE_BF16,
-                 out_dtype=DTYPE_F32, warps_per_block: int = 0):
+                 out_dtype=DTYPE_F32, kernel_mode: int = KERNELS_FUSED):
         self.layer = layer
-        self.cfg = config(layer.shape, max_tokens, resid_dtype, out_dtype, warps_per_block)
+        self.cfg = config(layer.shape, max_tokens, resid_dtype, out_dtype, kernel_mode)
         self._w = layer.struct()
         h = ctypes.c_void_p()
         check("moe_decode_create", lib().moe_decode_create(ctypes.byref(self.cfg),
@@ -247,9 +248,9 @@ class MoeStack:
     """A stack of layers replayed as one CUDA graph per decode step."""
 
     def __init__(self, layers: list[DeviceLayer], max_tokens: int = 1, resid_dtype=DTYPE_BF16,
-                 warps_per_block: int = 0):
+                 kernel_mode: int = KERNELS_FUSED):
         self.layers = layers
-        self.cfg = config(layers[0].shape, max_tokens, resid_dtype, DTYPE_F32, warps_per_block)
+        self.cfg = config(layers[0].shape, max_tokens, resid_dtype, DTYPE_F32, kernel_mode)
         arr = (LayerWeights * len(layers))()
         for i, l in enumerate(layers):
             arr[i] = l.struct()

@@ -10,16 +10,12 @@
 
 namespace {
 
-using moe::DownParams;
-using moe::GateUpParams;
-using moe::ProjDev;
-
 bool bits_ok(int b) { return b == 4 || b == 6 || b == 8; }
 bool aligned(const void *p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 
 bool proj_ok(const moe_proj &p) {
-  return p.codes && p.scales && p.biases && aligned(p.codes, 16) && aligned(p.scales, 2) &&
-         aligned(p.biases, 2);
+  return p.codes && p.scales && p.biases && aligned(p.codes, 16) && aligned(p.scales, 16) &&
+         aligned(p.biases, 16);
 }
 
 int validate_config(const moe_decode_config *c) {
@@ -39,7 +35,8 @@ int validate_config(const moe_decode_config *c) {
   if (c->resid_dtype != MOE_DTYPE_BF16 && c->resid_dtype != MOE_DTYPE_F32)
     return MOE_ERR_INVALID_ARG;
   if (c->out_dtype != MOE_DTYPE_BF16 && c->out_dtype != MOE_DTYPE_F32) return MOE_ERR_INVALID_ARG;
-  if (c->warps_per_block < 0) return MOE_ERR_INVALID_ARG;
+  if (c->kernel_mode != MOE_KERNELS_FUSED && c->kernel_mode != MOE_KERNELS_SEPARATE)
+    return MOE_ERR_INVALID_ARG;
   // int32 indexing of the activation vector and of one expert's rows
   const int64_t act = (int64_t)c->top_k * c->dff + (int64_t)c->n_shared * c->dff_shared;
   if (act > (1 << 24) || (int64_t)c->din * c->dff > (int64_t)1 << 30) return MOE_ERR_UNSUPPORTED;
@@ -57,32 +54,42 @@ int validate_weights(const moe_decode_config *c, const moe_layer_weights *w) {
   return MOE_OK;
 }
 
-ProjDev dev(const moe_proj &p) {
-  return ProjDev{static_cast<const uint8_t *>(p.codes), static_cast<const __half *>(p.scales),
-                 static_cast<const __half *>(p.biases)};
+moe::ProjDev dev(const moe_proj &p) {
+  return moe::ProjDev{static_cast<const uint8_t *>(p.codes),
+                      static_cast<const __half *>(p.scales), static_cast<const __half *>(p.biases)};
 }
 
-// Everything a layer launch needs, resolved once.
-struct Layer {
+moe::LayerPtrs layer_ptrs(const moe_decode_config &c, const moe_layer_weights &w) {
+  moe::LayerPtrs p;
+  p.gate = dev(w.gate);
+  p.up = dev(w.up);
+  p.down = dev(w.down);
+  p.sh_gate = dev(w.sh_gate);
+  p.sh_up = dev(w.sh_up);
+  p.sh_down = dev(w.sh_down);
+  p.gate_vec = (c.n_shared > 0 && c.shared_gate == 1) ? static_cast<const uint16_t *>(w.gate_vec)
+                                                      : nullptr;
+  return p;
+}
+
+// What every launch of a given shape needs, resolved once at create time.
+struct Prepared {
   moe_decode_config cfg;
-  moe_layer_weights w;
-  int bits_s, bits_sd;      // shared-class bits (routed bits when there is no shared expert)
-  size_t smem_a, smem_b;
-  int grid_a, grid_b;
+  moe::LayerShape shape;
+  moe::Plan plan;
+  int bits_sh;       // shared-expert code width as the kernels see it
+  int grid_sep;      // CTAs of the separate kernels
+  int grid_fused;    // CTAs of the fused kernel (all resident)
 };
 
-int prepare_layer(const moe_decode_config *c, const moe_layer_weights *w, Layer &L) {
+int prepare(const moe_decode_config *c, Prepared &P) {
   int rc = validate_config(c);
   if (rc != MOE_OK) return rc;
-  rc = validate_weights(c, w);
-  if (rc != MOE_OK) return rc;
-  L.cfg = *c;
-  L.w = *w;
-  L.bits_s = c->n_shared > 0 ? c->bits_shared : c->bits_gate;
-  L.bits_sd = c->n_shared > 0 ? c->bits_shared : c->bits_down;
-  L.smem_a = moe::gate_up_smem_bytes(c->din, c->bits_gate, L.bits_s, c->n_shared);
-  L.smem_b = moe::down_smem_bytes(c->dff, c->top_k, c->n_shared, c->dff_shared, c->bits_down,
-                                  L.bits_sd);
+  P.cfg = *c;
+  P.shape = moe::LayerShape{c->din, c->dff, c->top_k, c->n_experts, c->n_shared, c->dff_shared};
+  P.bits_sh = c->n_shared > 0 ? c->bits_shared : c->bits_down;
+  if (!moe::make_plan(P.shape, c->bits_gate, c->bits_down, P.bits_sh, &P.plan))
+    return MOE_ERR_UNSUPPORTED;
   int device = 0, sms = 0, smem_optin = 0, major = 0, minor = 0;
   if (cudaGetDevice(&device) != cudaSuccess) return MOE_ERR_CUDA;
   if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, device) != cudaSuccess ||
@@ -92,14 +99,17 @@ int prepare_layer(const moe_decode_config *c, const moe_layer_weights *w, Layer 
       cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, device) != cudaSuccess)
     return MOE_ERR_CUDA;
   if (major != 10 || minor != 3) return MOE_ERR_UNSUPPORTED;  // built for sm_103a only
-  const size_t static_reserve = 2048;  // the kernels' static shared memory
-  if (L.smem_a + static_reserve > (size_t)smem_optin || L.smem_b + static_reserve > (size_t)smem_optin)
-    return MOE_ERR_UNSUPPORTED;
-  if (moe::prepare_kernels(smem_optin - (int)static_reserve, c->bits_gate, L.bits_s, c->bits_down,
-                           L.bits_sd) != cudaSuccess)
+  const size_t static_reserve = 4096;  // the kernels' static shared memory
+  if (P.plan.smem + static_reserve > (size_t)smem_optin) return MOE_ERR_UNSUPPORTED;
+  if (moe::prepare_kernels(smem_optin - (int)static_reserve, c->bits_gate, c->bits_down,
+                           P.bits_sh) != cudaSuccess)
     return MOE_ERR_CUDA;
-  L.grid_a = sms;
-  L.grid_b = sms;
+  P.grid_sep = sms;
+  const int lim = moe::fused_grid_limit(P.plan, c->bits_gate, c->bits_down, P.bits_sh);
+  P.grid_fused = lim < sms ? lim : sms;
+  if (c->kernel_mode == MOE_KERNELS_FUSED && P.grid_fused < 1) return MOE_ERR_UNSUPPORTED;
+  const int grid = c->kernel_mode == MOE_KERNELS_FUSED ? P.grid_fused : P.grid_sep;
+  if ((c->din + grid - 1) / grid > moe::kMaxRowsB) return MOE_ERR_UNSUPPORTED;
   return MOE_OK;
 }
 
@@ -109,58 +119,69 @@ size_t act_floats(const moe_decode_config &c) {
 
 size_t dtype_bytes(int dt) { return dt == MOE_DTYPE_F32 ? 4 : 2; }
 
-// Enqueues one layer for m tokens (kernel A then kernel B per token).
-cudaError_t enqueue_layer(const Layer &L, float *act, int32_t *err, const void *x, int m,
-                          const int32_t *ids, const float *scores, const void *resid,
-                          int resid_dtype, void *out, int out_dtype, cudaStream_t stream,
-                          bool pdl, int parts = MOE_PART_GATE_UP | MOE_PART_DOWN) {
-  const moe_decode_config &c = L.cfg;
+// Separate kernels: kernel A then kernel B for each token of one layer.
+cudaError_t enqueue_separate(const Prepared &P, const moe::LayerPtrs &w, float *act,
+                             int32_t *err, const void *x, int m, const int32_t *ids,
+                             const float *scores, const void *resid, int resid_dtype, void *out,
+                             int out_dtype, cudaStream_t stream, int parts) {
+  const moe_decode_config &c = P.cfg;
   for (int t = 0; t < m; ++t) {
-    GateUpParams a;
-    a.gate = dev(L.w.gate);
-    a.up = dev(L.w.up);
-    a.sh_gate = dev(L.w.sh_gate);
-    a.sh_up = dev(L.w.sh_up);
+    const int32_t *it = ids ? ids + (size_t)t * c.top_k : nullptr;
+    moe::GateUpParams a;
+    a.s = P.shape;
+    a.w = w;
+    a.plan = P.plan;
     a.x = static_cast<const uint16_t *>(x) + (size_t)t * c.din;
-    a.ids = ids ? ids + (size_t)t * c.top_k : nullptr;
+    a.ids = it;
     a.scores = scores ? scores + (size_t)t * c.top_k : nullptr;
-    a.gate_vec = (c.n_shared > 0 && c.shared_gate == 1)
-                     ? static_cast<const uint16_t *>(L.w.gate_vec)
-                     : nullptr;
     a.act = act;
     a.err = err;
-    a.din = c.din;
-    a.dff = c.dff;
-    a.top_k = c.top_k;
-    a.n_experts = c.n_experts;
-    a.n_shared = c.n_shared;
-    a.dff_shared = c.dff_shared;
     cudaError_t e = cudaSuccess;
-    if (parts & MOE_PART_GATE_UP)
-      e = moe::launch_gate_up(a, c.bits_gate, L.bits_s, L.grid_a, L.smem_a, stream, pdl);
+    if (parts & MOE_PART_GATE_UP) e = moe::launch_gate_up(a, P.grid_sep, stream, true);
     if (e != cudaSuccess) return e;
-
-    DownParams b;
-    b.down = dev(L.w.down);
-    b.sh_down = dev(L.w.sh_down);
-    b.ids = a.ids;
+    moe::DownParams b;
+    b.s = P.shape;
+    b.w = w;
+    b.plan = P.plan;
+    b.ids = it;
     b.act = act;
     b.resid = static_cast<const char *>(resid) + (size_t)t * c.din * dtype_bytes(resid_dtype);
     b.out = static_cast<char *>(out) + (size_t)t * c.din * dtype_bytes(out_dtype);
-    b.err = err;
     b.resid_f32 = resid_dtype == MOE_DTYPE_F32;
     b.out_f32 = out_dtype == MOE_DTYPE_F32;
-    b.din = c.din;
-    b.dff = c.dff;
-    b.top_k = c.top_k;
-    b.n_experts = c.n_experts;
-    b.n_shared = c.n_shared;
-    b.dff_shared = c.dff_shared;
-    if (parts & MOE_PART_DOWN)
-      e = moe::launch_down(b, c.bits_down, L.bits_sd, L.grid_b, L.smem_b, stream, pdl);
+    b.err = err;
+    if (parts & MOE_PART_DOWN) e = moe::launch_down(b, P.grid_sep, stream, true);
     if (e != cudaSuccess) return e;
   }
   return cudaSuccess;
+}
+
+// Fused kernel over L layers (device array `layers`) and m tokens.
+cudaError_t enqueue_fused(const Prepared &P, const moe::LayerPtrs *layers, int L, float *act,
+                          int32_t *err, uint32_t *bar, float *ping0, float *ping1, const void *x,
+                          int m, const int32_t *ids, const float *scores, const void *resid0,
+                          int resid_dtype, void *out, int out_dtype, cudaStream_t stream) {
+  cudaError_t e = cudaMemsetAsync(bar, 0, sizeof(uint32_t), stream);
+  if (e != cudaSuccess) return e;
+  moe::StackParams p;
+  p.s = P.shape;
+  p.plan = P.plan;
+  p.layers = layers;
+  p.L = L;
+  p.m = m;
+  p.x = static_cast<const uint16_t *>(x);
+  p.ids = ids;
+  p.scores = scores;
+  p.resid0 = resid0;
+  p.resid0_f32 = resid_dtype == MOE_DTYPE_F32;
+  p.ping0 = ping0;
+  p.ping1 = ping1;
+  p.out = out;
+  p.out_f32 = out_dtype == MOE_DTYPE_F32;
+  p.act = act;
+  p.err = err;
+  p.bar = bar;
+  return moe::launch_fused(p, P.grid_fused, stream);
 }
 
 int read_and_clear_error(int32_t *err, int32_t *out) {
@@ -169,39 +190,69 @@ int read_and_clear_error(int32_t *err, int32_t *out) {
   int32_t v = 0;
   if (cudaMemcpy(&v, err, sizeof v, cudaMemcpyDeviceToHost) != cudaSuccess) return MOE_ERR_CUDA;
   if (cudaMemset(err, 0, sizeof v) != cudaSuccess) return MOE_ERR_CUDA;
-  *out = v ? MOE_ERR_BAD_ID : MOE_OK;
+  *out = (v & 2) ? MOE_ERR_TIMEOUT : (v & 1) ? MOE_ERR_BAD_ID : MOE_OK;
   return MOE_OK;
 }
+
+// Device workspace of a handle or a stack.
+struct Workspace {
+  float *act = nullptr;
+  int32_t *err = nullptr;
+  uint32_t *bar = nullptr;
+  moe::LayerPtrs *layers = nullptr;
+
+  bool alloc(const moe_decode_config &c, int n_layers) {
+    const size_t na = act_floats(c);
+    bool ok = cudaMalloc(&act, (na > 0 ? na : 1) * sizeof(float)) == cudaSuccess &&
+              cudaMalloc(&err, sizeof(int32_t)) == cudaSuccess &&
+              cudaMemset(err, 0, sizeof(int32_t)) == cudaSuccess &&
+              cudaMalloc(&bar, sizeof(uint32_t)) == cudaSuccess &&
+              cudaMalloc(&layers, sizeof(moe::LayerPtrs) * n_layers) == cudaSuccess;
+    if (!ok) cudaGetLastError();
+    return ok;
+  }
+  void release() {
+    cudaFree(act);
+    cudaFree(err);
+    cudaFree(bar);
+    cudaFree(layers);
+  }
+};
 
 }  // namespace
 
 // ====================================================================== single layer
 struct moe_decode {
-  Layer layer;
-  float *act = nullptr;
-  int32_t *err = nullptr;
+  Prepared P;
+  moe::LayerPtrs w;
+  Workspace ws;
 };
 
 extern "C" int moe_decode_create(const moe_decode_config *cfg, const moe_layer_weights *weights,
                                  moe_decode_t **out) {
   if (!out) return MOE_ERR_INVALID_ARG;
   *out = nullptr;
+  int rc = validate_config(cfg);
+  if (rc != MOE_OK) return rc;
+  rc = validate_weights(cfg, weights);
+  if (rc != MOE_OK) return rc;
   moe_decode *h = new (std::nothrow) moe_decode();
   if (!h) return MOE_ERR_OOM;
-  int rc = prepare_layer(cfg, weights, h->layer);
+  rc = prepare(cfg, h->P);
   if (rc != MOE_OK) {
     delete h;
     return rc;
   }
-  const size_t n = act_floats(*cfg) * cfg->max_tokens;
-  if (cudaMalloc(&h->act, (n > 0 ? n : 1) * sizeof(float)) != cudaSuccess ||
-      cudaMalloc(&h->err, sizeof(int32_t)) != cudaSuccess ||
-      cudaMemset(h->err, 0, sizeof(int32_t)) != cudaSuccess) {
-    cudaFree(h->act);
-    cudaFree(h->err);
+  h->w = layer_ptrs(*cfg, *weights);
+  if (!h->ws.alloc(*cfg, 1)) {
+    h->ws.release();
     delete h;
-    cudaGetLastError();
     return MOE_ERR_OOM;
+  }
+  if (cudaMemcpy(h->ws.layers, &h->w, sizeof h->w, cudaMemcpyHostToDevice) != cudaSuccess) {
+    h->ws.release();
+    delete h;
+    return MOE_ERR_CUDA;
   }
   *out = h;
   return MOE_OK;
@@ -211,28 +262,34 @@ extern "C" int moe_decode_forward(moe_decode_t *h, const void *x, int32_t m, con
                                   const float *scores, const void *resid, void *out,
                                   void *stream) {
   if (!h || !x || !resid || !out) return MOE_ERR_INVALID_ARG;
-  const moe_decode_config &c = h->layer.cfg;
+  const moe_decode_config &c = h->P.cfg;
   if (m < 1 || m > c.max_tokens) return MOE_ERR_INVALID_ARG;
   if (c.top_k > 0 && (!ids || !scores)) return MOE_ERR_INVALID_ARG;
-  if (!aligned(x, 2) || !aligned(resid, dtype_bytes(c.resid_dtype)) ||
+  if (!aligned(x, 16) || !aligned(resid, dtype_bytes(c.resid_dtype)) ||
       !aligned(out, dtype_bytes(c.out_dtype)) || (ids && !aligned(ids, 4)) ||
       (scores && !aligned(scores, 4)))
     return MOE_ERR_INVALID_ARG;
   if (x == out) return MOE_ERR_INVALID_ARG;
-  cudaError_t e = enqueue_layer(h->layer, h->act, h->err, x, m, ids, scores, resid, c.resid_dtype,
-                                out, c.out_dtype, static_cast<cudaStream_t>(stream), true);
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  cudaError_t e;
+  if (c.kernel_mode == MOE_KERNELS_FUSED)
+    e = enqueue_fused(h->P, h->ws.layers, 1, h->ws.act, h->ws.err, h->ws.bar, nullptr, nullptr, x,
+                      m, ids, scores, resid, c.resid_dtype, out, c.out_dtype, st);
+  else
+    e = enqueue_separate(h->P, h->w, h->ws.act, h->ws.err, x, m, ids, scores, resid,
+                         c.resid_dtype, out, c.out_dtype, st,
+                         MOE_PART_GATE_UP | MOE_PART_DOWN);
   return e == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
 }
 
 extern "C" int moe_decode_get_error(moe_decode_t *h, int32_t *device_error) {
   if (!h) return MOE_ERR_INVALID_ARG;
-  return read_and_clear_error(h->err, device_error);
+  return read_and_clear_error(h->ws.err, device_error);
 }
 
 extern "C" void moe_decode_destroy(moe_decode_t *h) {
   if (!h) return;
-  cudaFree(h->act);
-  cudaFree(h->err);
+  h->ws.release();
   delete h;
 }
 
@@ -248,15 +305,13 @@ constexpr size_t kMaxGraphs = 16;
 }  // namespace
 
 struct moe_stack {
-  std::vector<Layer> layers;       // layers[0] reads resid0 in cfg.resid_dtype, the rest fp32
-  moe_decode_config cfg;
-  float *act = nullptr;
-  int32_t *err = nullptr;
+  Prepared P;
+  std::vector<moe::LayerPtrs> layers;
+  Workspace ws;
   float *ping[2] = {nullptr, nullptr};
   cudaStream_t cap = nullptr;
   std::vector<GraphEntry> graphs;
   uint64_t clock = 0;
-  bool pdl = true;
   // device staging for moe_stack_step_host
   void *x_dev = nullptr, *resid_dev = nullptr;
   int32_t *ids_dev = nullptr;
@@ -267,8 +322,7 @@ extern "C" void moe_stack_destroy(moe_stack_t *s) {
   if (!s) return;
   for (auto &g : s->graphs) cudaGraphExecDestroy(g.exec);
   if (s->cap) cudaStreamDestroy(s->cap);
-  cudaFree(s->act);
-  cudaFree(s->err);
+  s->ws.release();
   cudaFree(s->ping[0]);
   cudaFree(s->ping[1]);
   cudaFree(s->x_dev);
@@ -284,25 +338,24 @@ extern "C" int moe_stack_create(const moe_decode_config *cfg, int32_t n_layers,
   if (!out) return MOE_ERR_INVALID_ARG;
   *out = nullptr;
   if (!cfg || !layers || n_layers < 1) return MOE_ERR_INVALID_ARG;
+  int rc = validate_config(cfg);
+  if (rc != MOE_OK) return rc;
   if (cfg->out_dtype != MOE_DTYPE_F32) return MOE_ERR_INVALID_ARG;
+  for (int l = 0; l < n_layers; ++l) {
+    rc = validate_weights(cfg, &layers[l]);
+    if (rc != MOE_OK) return rc;
+  }
   moe_stack *s = new (std::nothrow) moe_stack();
   if (!s) return MOE_ERR_OOM;
-  s->cfg = *cfg;
-  s->layers.resize(n_layers);
-  for (int l = 0; l < n_layers; ++l) {
-    moe_decode_config c = *cfg;
-    if (l > 0) c.resid_dtype = MOE_DTYPE_F32;
-    int rc = prepare_layer(&c, &layers[l], s->layers[l]);
-    if (rc != MOE_OK) {
-      moe_stack_destroy(s);
-      return rc;
-    }
+  rc = prepare(cfg, s->P);
+  if (rc != MOE_OK) {
+    delete s;
+    return rc;
   }
+  s->layers.resize(n_layers);
+  for (int l = 0; l < n_layers; ++l) s->layers[l] = layer_ptrs(*cfg, layers[l]);
   const size_t M = cfg->max_tokens, din = cfg->din, K = cfg->top_k;
-  const size_t na = act_floats(*cfg);
-  bool ok = cudaMalloc(&s->act, (na > 0 ? na : 1) * sizeof(float)) == cudaSuccess &&
-            cudaMalloc(&s->err, sizeof(int32_t)) == cudaSuccess &&
-            cudaMemset(s->err, 0, sizeof(int32_t)) == cudaSuccess &&
+  bool ok = s->ws.alloc(*cfg, n_layers) &&
             cudaMalloc(&s->ping[0], M * din * sizeof(float)) == cudaSuccess &&
             cudaMalloc(&s->ping[1], M * din * sizeof(float)) == cudaSuccess &&
             cudaMalloc(&s->x_dev, (size_t)n_layers * M * din * 2) == cudaSuccess &&
@@ -316,7 +369,9 @@ extern "C" int moe_stack_create(const moe_decode_config *cfg, int32_t n_layers,
     moe_stack_destroy(s);
     return MOE_ERR_OOM;
   }
-  if (cudaStreamCreateWithFlags(&s->cap, cudaStreamNonBlocking) != cudaSuccess) {
+  if (cudaMemcpy(s->ws.layers, s->layers.data(), sizeof(moe::LayerPtrs) * n_layers,
+                 cudaMemcpyHostToDevice) != cudaSuccess ||
+      cudaStreamCreateWithFlags(&s->cap, cudaStreamNonBlocking) != cudaSuccess) {
     moe_stack_destroy(s);
     return MOE_ERR_CUDA;
   }
@@ -328,29 +383,34 @@ namespace {
 
 cudaError_t enqueue_stack(moe_stack *s, const void *x, int m, const int32_t *ids,
                           const float *scores, const void *resid0, void *out, cudaStream_t st,
-                          bool pdl, int parts) {
+                          int parts) {
   const int L = (int)s->layers.size();
-  const size_t din = s->cfg.din, K = s->cfg.top_k;
+  const moe_decode_config &c = s->P.cfg;
+  if (c.kernel_mode == MOE_KERNELS_FUSED && parts == (MOE_PART_GATE_UP | MOE_PART_DOWN))
+    return enqueue_fused(s->P, s->ws.layers, L, s->ws.act, s->ws.err, s->ws.bar, s->ping[0],
+                         s->ping[1], x, m, ids, scores, resid0, c.resid_dtype, out, MOE_DTYPE_F32,
+                         st);
+  const size_t din = c.din, K = c.top_k;
   for (int l = 0; l < L; ++l) {
     const void *xl = static_cast<const uint16_t *>(x) + (size_t)l * m * din;
     const int32_t *il = ids ? ids + (size_t)l * m * K : nullptr;
     const float *sl = scores ? scores + (size_t)l * m * K : nullptr;
     const void *rl = l == 0 ? resid0 : s->ping[(l - 1) & 1];
-    const int rdt = l == 0 ? s->cfg.resid_dtype : MOE_DTYPE_F32;
+    const int rdt = l == 0 ? c.resid_dtype : MOE_DTYPE_F32;
     void *ol = l == L - 1 ? out : s->ping[l & 1];
-    cudaError_t e = enqueue_layer(s->layers[l], s->act, s->err, xl, m, il, sl, rl, rdt, ol,
-                                  MOE_DTYPE_F32, st, pdl, parts);
+    cudaError_t e = enqueue_separate(s->P, s->layers[l], s->ws.act, s->ws.err, xl, m, il, sl, rl,
+                                     rdt, ol, MOE_DTYPE_F32, st, parts);
     if (e != cudaSuccess) return e;
   }
   return cudaSuccess;
 }
 
 int capture(moe_stack *s, const void *x, int m, const int32_t *ids, const float *scores,
-            const void *resid0, void *out, bool pdl, int parts, cudaGraphExec_t *exec) {
+            const void *resid0, void *out, int parts, cudaGraphExec_t *exec) {
   cudaGraph_t graph = nullptr;
   if (cudaStreamBeginCapture(s->cap, cudaStreamCaptureModeThreadLocal) != cudaSuccess)
     return MOE_ERR_CUDA;
-  cudaError_t e = enqueue_stack(s, x, m, ids, scores, resid0, out, s->cap, pdl, parts);
+  cudaError_t e = enqueue_stack(s, x, m, ids, scores, resid0, out, s->cap, parts);
   cudaError_t e2 = cudaStreamEndCapture(s->cap, &graph);
   if (e != cudaSuccess || e2 != cudaSuccess || !graph) {
     if (graph) cudaGraphDestroy(graph);
@@ -373,9 +433,9 @@ extern "C" int moe_stack_step_parts(moe_stack_t *s, int32_t parts, const void *x
                                     void *out, void *stream) {
   if (!s || !x || !resid0 || !out) return MOE_ERR_INVALID_ARG;
   if (parts < 1 || parts > (MOE_PART_GATE_UP | MOE_PART_DOWN)) return MOE_ERR_INVALID_ARG;
-  if (m < 1 || m > s->cfg.max_tokens) return MOE_ERR_INVALID_ARG;
-  if (s->cfg.top_k > 0 && (!ids || !scores)) return MOE_ERR_INVALID_ARG;
-  if (!aligned(out, 4) || !aligned(x, 2) || !aligned(resid0, dtype_bytes(s->cfg.resid_dtype)))
+  if (m < 1 || m > s->P.cfg.max_tokens) return MOE_ERR_INVALID_ARG;
+  if (s->P.cfg.top_k > 0 && (!ids || !scores)) return MOE_ERR_INVALID_ARG;
+  if (!aligned(out, 4) || !aligned(x, 16) || !aligned(resid0, dtype_bytes(s->P.cfg.resid_dtype)))
     return MOE_ERR_INVALID_ARG;
   GraphEntry *hit = nullptr;
   for (auto &g : s->graphs)
@@ -384,11 +444,7 @@ extern "C" int moe_stack_step_parts(moe_stack_t *s, int32_t parts, const void *x
       hit = &g;
   if (!hit) {
     cudaGraphExec_t exec = nullptr;
-    int rc = capture(s, x, m, ids, scores, resid0, out, s->pdl, parts, &exec);
-    if (rc != MOE_OK && s->pdl) {  // a driver without programmatic edges in graphs
-      s->pdl = false;
-      rc = capture(s, x, m, ids, scores, resid0, out, false, parts, &exec);
-    }
+    int rc = capture(s, x, m, ids, scores, resid0, out, parts, &exec);
     if (rc != MOE_OK) return rc;
     if (s->graphs.size() >= kMaxGraphs) {
       size_t lru = 0;
@@ -416,14 +472,14 @@ extern "C" int moe_stack_step_host(moe_stack_t *s, const void *x_host, int32_t m
                                    const int32_t *ids_host, const float *scores_host,
                                    const void *resid0_host, float *out_host, void *stream) {
   if (!s || !x_host || !resid0_host || !out_host) return MOE_ERR_INVALID_ARG;
-  if (m < 1 || m > s->cfg.max_tokens) return MOE_ERR_INVALID_ARG;
-  const size_t L = s->layers.size(), din = s->cfg.din, K = s->cfg.top_k;
+  if (m < 1 || m > s->P.cfg.max_tokens) return MOE_ERR_INVALID_ARG;
+  const size_t L = s->layers.size(), din = s->P.cfg.din, K = s->P.cfg.top_k;
   if (K > 0 && (!ids_host || !scores_host)) return MOE_ERR_INVALID_ARG;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   bool ok =
       cudaMemcpyAsync(s->x_dev, x_host, L * m * din * 2, cudaMemcpyHostToDevice, st) ==
           cudaSuccess &&
-      cudaMemcpyAsync(s->resid_dev, resid0_host, m * din * dtype_bytes(s->cfg.resid_dtype),
+      cudaMemcpyAsync(s->resid_dev, resid0_host, m * din * dtype_bytes(s->P.cfg.resid_dtype),
                       cudaMemcpyHostToDevice, st) == cudaSuccess;
   if (ok && K > 0)
     ok = cudaMemcpyAsync(s->ids_dev, ids_host, L * m * K * 4, cudaMemcpyHostToDevice, st) ==
@@ -443,7 +499,7 @@ extern "C" int moe_stack_step_host(moe_stack_t *s, const void *x_host, int32_t m
 
 extern "C" int moe_stack_get_error(moe_stack_t *s, int32_t *device_error) {
   if (!s) return MOE_ERR_INVALID_ARG;
-  return read_and_clear_error(s->err, device_error);
+  return read_and_clear_error(s->ws.err, device_error);
 }
 
 // ====================================================================== debug unpack

@@ -130,7 +130,7 @@ __device__ __forceinline__ void step_masks(const uint4 *v, uint32_t (&m)[Fmt<BIT
       m[4 * i + 0] = w[i] & 0x000000ffu;
       m[4 * i + 1] = w[i] & 0x0000ff00u;
       m[4 * i + 2] = w[i] & 0x00ff0000u;
-      m[4 * i + 3] = (w[i] >> 8) & 0x00ff0000u;
+      m[4 * i + 3] = __byte_perm(w[i], 0u, 0x4344u);  // byte 3 moved to byte 2, rest zero
     }
   } else {
     const uint32_t w[12] = {v[0].x, v[0].y, v[0].z, v[0].w, v[1].x, v[1].y,

@@ -1,4 +1,4 @@
-// moe_kernels.cuh -- parameters and launchers of the decode MoE kernels (host-visible).
+// moe_kernels.cuh -- parameters, stage plans and launchers of the decode MoE kernels.
 #pragma once
 
 #include <cstdint>
@@ -8,50 +8,116 @@
 namespace moe {
 
 struct ProjDev {
-  const uint8_t *codes;   // [experts][rows][cols*bits/8]
-  const __half *scales;   // [experts][rows][cols/64]
-  const __half *biases;   // [experts][rows][cols/64]
+  const uint8_t *codes;   // [experts][rows][cols*bits/8], 16-byte aligned
+  const __half *scales;   // [experts][rows][cols/64], 16-byte aligned
+  const __half *biases;   // [experts][rows][cols/64], 16-byte aligned
 };
 
-// Kernel A: act[u] = coef_u * silu(gate_u . x) * (up_u . x) for every row pair u of the routed
-// slots (coef = the slot's score) and of the shared experts (coef = the shared scalar).
-struct GateUpParams {
-  ProjDev gate, up, sh_gate, sh_up;
-  const uint16_t *x;         // bf16 [din]
-  const int32_t *ids;        // [top_k]
-  const float *scores;       // [top_k]
+struct LayerShape {
+  int din, dff, top_k, n_experts, n_shared, dff_shared;
+};
+
+struct LayerPtrs {
+  ProjDev gate, up, down, sh_gate, sh_up, sh_down;
   const uint16_t *gate_vec;  // bf16 [din] or nullptr (shared scalar 1)
-  float *act;                // [top_k*dff + n_shared*dff_shared]
-  int32_t *err;              // sticky error word
-  int din, dff, top_k, n_experts, n_shared, dff_shared;
-};
-
-// Kernel B: out[i] = resid[i] + sum over slots and shared experts of W_down[i, :] . act_segment.
-struct DownParams {
-  ProjDev down, sh_down;
-  const int32_t *ids;        // [top_k]
-  const float *act;          // [top_k*dff + n_shared*dff_shared], from kernel A
-  const void *resid;         // [din] bf16 or fp32
-  void *out;                 // [din] fp32 or bf16
-  int32_t *err;
-  int resid_f32, out_f32;
-  int din, dff, top_k, n_experts, n_shared, dff_shared;
 };
 
 constexpr int kMaxTopK = 64;
-constexpr int kAThreads = 512;
-constexpr int kBThreads = 256;
-constexpr int kBRows = 2;  // output rows per warp item in kernel B
+constexpr int kConsumerWarps = 16;
+constexpr int kConsumers = kConsumerWarps * 32;
+constexpr int kProducerWarps = 1;           // issues the weight stream (bulk copies)
+constexpr int kProducers = kProducerWarps * 32;
+constexpr int kThreads = kConsumers + kProducers;
+constexpr int kRingBytes = 208 * 1024;      // shared-memory ring of one CTA
+constexpr int kMaxStages = 8;
+constexpr int kMaxRowsB = 128;              // phase B: output rows one CTA owns, at most
+constexpr int kMaxActRegs = 32;             // phase B: activation registers per thread (6-bit: 64)
 
-size_t gate_up_smem_bytes(int din, int bits_r, int bits_s, int n_shared);
-size_t down_smem_bytes(int dff, int top_k, int n_shared, int dff_shared, int bits_d, int bits_sd);
+// Phase A geometry of one class (routed or shared) of gate/up rows.
+struct GateUpGeom {
+  int bits;     // code width
+  int rb;       // bytes per row
+  int T;        // 16-B (6-bit: 48-B) steps per row
+  int tpr;      // consumer threads per row group: T rounded up to 32, at most kConsumers
+  int groups;   // row groups = kConsumers / tpr
+  int R;        // rows per chunk = rows per thread * groups
+  int sw;       // bytes reserved per scale/bias window in a stage
+};
 
-// Both return a cudaError_t; `pdl` launches with programmatic stream serialisation.
-cudaError_t launch_gate_up(const GateUpParams &p, int bits_r, int bits_s, int grid, size_t smem,
-                           cudaStream_t stream, bool pdl);
-cudaError_t launch_down(const DownParams &p, int bits_d, int bits_sd, int grid, size_t smem,
-                        cudaStream_t stream, bool pdl);
-cudaError_t prepare_kernels(int smem_optin, int bits_r, int bits_s, int bits_d, int bits_sd);
+// Phase B geometry.
+struct DownGeom {
+  int bits_r, bits_s;  // code widths of routed / shared down rows
+  int rb_r, rb_s;      // row bytes
+  int G_r, G_s;        // groups per row
+  int spr_r, spr_s;    // steps per row
+  int T_r, T_s;        // steps over the concatenated contraction
+  int tpr, groups;     // consumer threads per row group, row groups
+  int spt;             // steps per consumer thread
+  int R;               // rows per chunk (rows per thread * groups)
+  int sw_r, sw_s;      // bytes reserved per scale/bias window
+  int codes_bytes;     // code bytes of one stage
+};
+
+struct Plan {
+  GateUpGeom geo_r, geo_s;
+  DownGeom geo_b;
+  int nst, stage_bytes;
+  size_t smem;
+};
+
+// Kernel A alone.
+struct GateUpParams {
+  LayerShape s;
+  LayerPtrs w;
+  Plan plan;
+  const uint16_t *x;        // bf16 [din]
+  const int32_t *ids;       // [top_k]
+  const float *scores;      // [top_k]
+  float *act;               // [top_k*dff + n_shared*dff_shared]
+  int32_t *err;             // sticky error word
+};
+
+// Kernel B alone.
+struct DownParams {
+  LayerShape s;
+  LayerPtrs w;
+  Plan plan;
+  const int32_t *ids;       // [top_k]
+  const float *act;         // from kernel A
+  const void *resid;        // [din] bf16 or fp32
+  void *out;                // [din] fp32 or bf16
+  int resid_f32, out_f32;
+  int32_t *err;
+};
+
+// The fused persistent kernel over layers [0, L) and tokens [0, m): phase A, grid barrier,
+// phase B, grid barrier, for each (layer, token).
+struct StackParams {
+  LayerShape s;
+  Plan plan;
+  const LayerPtrs *layers;  // device array [L]
+  int L, m;
+  const uint16_t *x;        // bf16 [L][m][din]
+  const int32_t *ids;       // [L][m][top_k]
+  const float *scores;      // [L][m][top_k]
+  const void *resid0;       // [m][din], bf16 or fp32: residual of layer 0
+  int resid0_f32;
+  float *ping0, *ping1;     // fp32 [m][din] outputs of the layers before the last
+  void *out;                // [m][din] output of the last layer
+  int out_f32;
+  float *act;
+  int32_t *err;
+  uint32_t *bar;            // grid-barrier counter, zero at launch
+};
+
+// Host-side plan; false when the shape is outside what the kernels support.
+bool make_plan(const LayerShape &s, int bits_gu, int bits_d, int bits_sh, Plan *plan);
+
+cudaError_t launch_gate_up(const GateUpParams &p, int grid, cudaStream_t stream, bool pdl);
+cudaError_t launch_down(const DownParams &p, int grid, cudaStream_t stream, bool pdl);
+cudaError_t launch_fused(const StackParams &p, int grid, cudaStream_t stream);
+cudaError_t prepare_kernels(int smem_optin, int bits_gu, int bits_d, int bits_sh);
+int fused_grid_limit(const Plan &plan, int bits_gu, int bits_d, int bits_sh);
 cudaError_t launch_unpack(const uint8_t *packed, int64_t rows, int64_t cols, int bits,
                           uint8_t *codes, cudaStream_t stream);
 

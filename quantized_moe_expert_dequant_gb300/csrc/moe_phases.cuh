@@ -1,0 +1,766 @@
+// moe_phases.cuh -- the two phases of the decode MoE block as device functions, shared by the
+// separate kernels (kernel A, kernel B) and the fused persistent kernel.
+//
+// Phase A ("two-kernel decode-MoE that beats gather_qmm", What changed, step 2, kernel A):
+//   act[u] = coef_u * silu(gate_u . x) * (up_u . x) for every gate/up row pair u of the routed slots
+//   (coef = the slot's score) and of the shared experts (coef = the shared scalar).
+// Phase B (same step, kernel B, fused with the tail of "Red Lite dev39 -- fused expert tail"):
+//   out[i] = resid[i] + sum over slots and shared experts of W_down[i, :] . act_segment.
+//
+// Both phases run on one CTA per SM: 16 consumer warps and one producer warp.
+//  * Each CTA owns a contiguous, balanced range of rows.  The producer streams those rows' packed
+//    codes, scales and biases into a ring of shared-memory stages with bulk asynchronous copies
+//    (TMA, 1-D form) completing on mbarriers; consumers release a stage on its "empty" barrier.
+//  * Each consumer thread owns fixed 16-byte code steps (48 bytes at 6 bits) of a row and keeps
+//    the matching activations, pre-scaled for the decoding of moe_common.cuh, in registers, so
+//    shared memory carries codes only and each code costs one bitwise op and half a packed FMA.
+//  * Per-row partial sums leave a warp through a transpose-reduction and are summed across warps
+//    in a fixed order, so results are bitwise reproducible.
+#pragma once
+
+#include "moe_common.cuh"
+#include "moe_kernels.cuh"
+#include "moe_tma.cuh"
+
+namespace moe {
+
+// ------------------------------------------------------------------ helpers
+template <int BITS>
+__host__ __device__ constexpr int rows_per_thread_a() {
+  return BITS == 6 ? 1 : 2;
+}
+
+template <int V>
+struct Log2 {
+  static constexpr int v = V == 1 ? 0 : V == 2 ? 1 : V == 4 ? 2 : V == 8 ? 3 : -1;
+};
+
+// Sums V values over the 32 lanes of a warp: log2(V) exchange steps that halve the values a lane
+// holds, then a butterfly over the rest.  Lane l returns the warp sum of value
+// (l >> (5 - log2 V)) & (V - 1).
+template <int V>
+__device__ __forceinline__ float warp_transpose_reduce(float (&v)[V], int lane) {
+#pragma unroll
+  for (int k = V / 2, off = 16; k >= 1; k >>= 1, off >>= 1) {
+    const bool upper = (lane & off) != 0;
+#pragma unroll
+    for (int j = 0; j < k; ++j) {
+      const float send = upper ? v[j] : v[j + k];
+      const float keep = upper ? v[j + k] : v[j];
+      v[j] = keep + __shfl_xor_sync(0xffffffffu, send, off);
+    }
+  }
+#pragma unroll
+  for (int off = 16 / V; off >= 1; off >>= 1) v[0] += __shfl_xor_sync(0xffffffffu, v[0], off);
+  return v[0];
+}
+
+// Deterministic reductions over the consumer threads (red holds kConsumerWarps floats).
+__device__ __forceinline__ float consumers_max(float v, float *red, int warp, int lane) {
+  v = warp_max(v);
+  if (lane == 0) red[warp] = v;
+  consumer_sync(kConsumers);
+  float m = 0.f;
+#pragma unroll
+  for (int w = 0; w < kConsumerWarps; ++w) m = fmaxf(m, red[w]);
+  consumer_sync(kConsumers);
+  return m;
+}
+
+__device__ __forceinline__ float consumers_sum(float v, float *red, int warp, int lane) {
+  v = warp_sum(v);
+  if (lane == 0) red[warp] = v;
+  consumer_sync(kConsumers);
+  float s = 0.f;
+#pragma unroll
+  for (int w = 0; w < kConsumerWarps; ++w) s += red[w];
+  consumer_sync(kConsumers);
+  return s;
+}
+
+// 16-B aligned window around a contiguous fp16 run [p, p + n): start, length, offset of p.
+struct Window {
+  const uint8_t *src;
+  uint32_t bytes;
+  uint32_t delta;
+};
+
+__device__ __forceinline__ Window window_of(const __half *p, int64_t n) {
+  const uintptr_t a = reinterpret_cast<uintptr_t>(p);
+  const uintptr_t lo = a & ~uintptr_t(15);
+  const uintptr_t hi = (a + uintptr_t(n) * 2 + 15) & ~uintptr_t(15);
+  return Window{reinterpret_cast<const uint8_t *>(lo), static_cast<uint32_t>(hi - lo),
+                static_cast<uint32_t>(a - lo)};
+}
+
+__device__ __forceinline__ float lds_half(const uint8_t *p) {
+  return __half2float(*reinterpret_cast<const __half *>(p));
+}
+
+__device__ __forceinline__ uint4 lds_u4(const uint8_t *p) {
+  return *reinterpret_cast<const uint4 *>(p);
+}
+
+// One step's dot product (units 2^-S) against pre-scaled activations held in registers, with
+// packed fp32x2 FMAs (two lanes of arithmetic per instruction, subnormals kept).
+template <int BITS>
+__device__ __forceinline__ float step_dot_regs(const uint4 *v, const float *xs) {
+  constexpr int N = Fmt<BITS>::kCodes;
+  uint32_t m[N];
+  step_masks<BITS>(v, m);
+  float2 a0 = make_float2(0.f, 0.f), a1 = make_float2(0.f, 0.f);
+#pragma unroll
+  for (int j = 0; j < N; j += 4) {
+    a0 = __ffma2_rn(make_float2(__uint_as_float(m[j + 0]), __uint_as_float(m[j + 1])),
+                    make_float2(xs[j + 0], xs[j + 1]), a0);
+    a1 = __ffma2_rn(make_float2(__uint_as_float(m[j + 2]), __uint_as_float(m[j + 3])),
+                    make_float2(xs[j + 2], xs[j + 3]), a1);
+  }
+  return (a0.x + a0.y) + (a1.x + a1.y);
+}
+
+// C bf16 values of x from column c0 into registers, pre-scaled for BITS-bit decoding with a
+// shift S chosen from these values alone (each thread rescales its own partial sums, so threads
+// need not agree on S), plus their plain sum.  x + c0 is 16-byte aligned.
+template <int BITS>
+__device__ __forceinline__ void load_x_regs(const uint16_t *x, int c0, bool active,
+                                            float (&xs)[Fmt<BITS>::kCodes], float &xsum, int &S) {
+  constexpr int C = Fmt<BITS>::kCodes;
+  xsum = 0.f;
+  float mx = 0.f;
+#pragma unroll
+  for (int v = 0; v < C / 8; ++v) {
+    const uint4 w =
+        active ? *reinterpret_cast<const uint4 *>(x + c0 + 8 * v) : make_uint4(0, 0, 0, 0);
+    const uint32_t ww[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+    for (int h = 0; h < 4; ++h) {
+      const int c = 8 * v + 2 * h;
+      xs[c] = __uint_as_float(ww[h] << 16);
+      xs[c + 1] = __uint_as_float(ww[h] & 0xffff0000u);
+      xsum += xs[c];
+      xsum += xs[c + 1];
+      mx = fmaxf(mx, fmaxf(fabsf(xs[c]), fabsf(xs[c + 1])));
+    }
+  }
+  S = choose_shift(mx);
+#pragma unroll
+  for (int c = 0; c < C; ++c) xs[c] *= pow2f(149 - S - code_offset<BITS>(c));
+}
+
+__device__ __forceinline__ float silu_f(float z) { return z / (1.0f + expf(-z)); }
+
+// ------------------------------------------------------------------ ring and grid barrier
+struct Ring {
+  uint64_t *full;
+  uint64_t *empty;
+  uint8_t *base;
+  int nst, stage_bytes;
+  int i;            // chunks this role has handed out (producer) or taken (consumers)
+  int *abort;       // shared flag: a wait timed out, stop waiting
+  int32_t *err;
+};
+
+__device__ __forceinline__ bool flag_abort(int *abort) {
+  return *reinterpret_cast<volatile int *>(abort) != 0;
+}
+
+__device__ __forceinline__ void set_timeout(int *abort, int32_t *err) {
+  atomicOr(err, kDevErrTimeout);
+  *reinterpret_cast<volatile int *>(abort) = 1;
+}
+
+__device__ __forceinline__ bool ring_wait(uint64_t *bar, uint32_t parity, int *abort,
+                                          int32_t *err) {
+  if (flag_abort(abort)) return false;
+  if (mbar_try_wait(bar, parity)) return true;
+  const long long t0 = clock64();
+  while (!mbar_try_wait(bar, parity)) {
+    if (flag_abort(abort)) return false;
+    if (clock64() - t0 > kWaitCycles) {
+      set_timeout(abort, err);
+      return false;
+    }
+    __nanosleep(64);  // leave the issue slots to the warps that have work
+  }
+  return true;
+}
+
+// Consumer side: lane 0 of each warp waits for the stage and the warp follows it.  One waiter
+// per warp instead of 32 keeps the barrier word free for the arrivals that complete the phase.
+__device__ __forceinline__ bool warp_wait_full(Ring &r, int st, int lane) {
+  int ok = 1;
+  if (lane == 0) ok = ring_wait(&r.full[st], (r.i / r.nst) & 1, r.abort, r.err);
+  ok = __shfl_sync(0xffffffffu, ok, 0);
+  __syncwarp();
+  return ok != 0;
+}
+
+
+// Producer side: claims the next stage (waits until its previous use was released).
+__device__ __forceinline__ uint32_t warp_sum_u32(uint32_t v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+  return v;
+}
+
+__device__ __forceinline__ uint8_t *ring_claim(Ring &r, int lane, int &st, bool &ok) {
+  st = r.i % r.nst;
+  int good = 1;
+  if (r.i >= r.nst && lane == 0) good = ring_wait(&r.empty[st], ((r.i / r.nst) - 1) & 1, r.abort, r.err);
+  ok = __shfl_sync(0xffffffffu, good, 0) != 0;
+  return r.base + static_cast<size_t>(st) * r.stage_bytes;
+}
+
+// Producer side, at exit: the copies into the last use of every stage have landed.
+__device__ __forceinline__ void ring_drain(Ring &r, int lane) {
+  if (lane != 0) return;
+  for (int s = r.i - r.nst < 0 ? 0 : r.i - r.nst; s < r.i; ++s)
+    mbar_wait(&r.full[s % r.nst], (s / r.nst) & 1);
+}
+
+__device__ __forceinline__ uint32_t ld_acquire(const uint32_t *p) {
+  uint32_t v;
+  asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+
+__device__ __forceinline__ void red_release_add(uint32_t *p, uint32_t v) {
+  asm volatile("red.release.gpu.global.add.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+
+// Waits until *cnt >= target (bounded).  Only meaningful when every CTA of the grid is resident.
+__device__ __forceinline__ bool wait_count(const uint32_t *cnt, uint32_t target, int *abort,
+                                           int32_t *err) {
+  if (ld_acquire(cnt) >= target) return true;
+  const long long t0 = clock64();
+  while (ld_acquire(cnt) < target) {
+    if (flag_abort(abort)) return false;
+    if (clock64() - t0 > kWaitCycles) {
+      set_timeout(abort, err);
+      return false;
+    }
+    __nanosleep(64);
+  }
+  return true;
+}
+
+// Grid barrier among the consumer threads of all CTAs: every CTA's consumers finished their writes.
+__device__ __forceinline__ void consumers_grid_barrier(uint32_t *cnt, uint32_t target, int tid,
+                                                       int *abort, int32_t *err) {
+  consumer_sync(kConsumers);
+  if (tid == 0) {
+    // bar.sync orders the CTA's writes before this thread's release, which is cumulative
+    red_release_add(cnt, 1u);
+    wait_count(cnt, target, abort, err);
+  }
+  consumer_sync(kConsumers);
+}
+
+// ================================================================== phase A
+struct ChunkA {
+  int k;   // slot (routed) or shared expert index
+  int j;   // first row inside the expert
+  int n;   // rows in the chunk
+  int u;   // flattened index of the first row (= its act index)
+};
+
+// Walks the chunks of a CTA's row range [a, b) of one class: at most R rows each, never crossing
+// an expert's block of rows_pe rows.  One division per range, 32-bit arithmetic (the flattened
+// row space is below 2^24 rows).
+struct ChunkIterA {
+  int u, b, k, j, rows_pe, R;
+  __device__ __forceinline__ ChunkIterA(int64_t a, int64_t b_, int64_t base_u, int rows_pe_, int R_)
+      : u(static_cast<int>(a)), b(static_cast<int>(b_)), rows_pe(rows_pe_), R(R_) {
+    const int v = static_cast<int>(a - base_u);
+    k = rows_pe_ > 0 ? v / rows_pe_ : 0;
+    j = v - k * rows_pe_;
+  }
+  __device__ __forceinline__ bool next(ChunkA &c) {
+    if (u >= b) return false;
+    int n = b - u;
+    if (n > R) n = R;
+    if (n > rows_pe - j) n = rows_pe - j;
+    c.k = k;
+    c.j = j;
+    c.n = n;
+    c.u = u;
+    u += n;
+    j += n;
+    if (j == rows_pe) {
+      j = 0;
+      ++k;
+    }
+    return true;
+  }
+};
+
+// The rows a CTA owns in phase A: [u0, u1) of the flattened routed-then-shared row space.
+struct RangeA {
+  int64_t ra, rb;   // routed rows
+  int64_t sa, sb;   // shared rows
+  int64_t Ur;       // routed row count
+};
+
+__device__ __forceinline__ RangeA range_a(const LayerShape &s) {
+  const int64_t Ur = static_cast<int64_t>(s.top_k) * s.dff;
+  const int64_t U = Ur + static_cast<int64_t>(s.n_shared) * s.dff_shared;
+  const int64_t u0 = U * blockIdx.x / gridDim.x, u1 = U * (blockIdx.x + 1) / gridDim.x;
+  RangeA r;
+  r.ra = u0;
+  r.rb = u1 < Ur ? u1 : Ur;
+  r.sa = u0 > Ur ? u0 : Ur;
+  r.sb = u1;
+  r.Ur = Ur;
+  return r;
+}
+
+template <int BITS>
+__device__ void produce_a_class(const LayerShape &s, const GateUpGeom &g, const ProjDev &gate,
+                                const ProjDev &up, bool shared_class, int64_t a, int64_t b,
+                                int64_t base_u, int rows_pe, const int32_t *ids, Ring &r, int lane,
+                                uint64_t pol) {
+  const int G = s.din / kGroup;
+  ChunkIterA it(a, b, base_u, rows_pe, g.R);
+  ChunkA c;
+  while (it.next(c)) {
+    const int e = shared_class ? c.k : ids[c.k];
+    if (!shared_class && (e < 0 || e >= s.n_experts)) continue;
+    int st;
+    bool ok;
+    uint8_t *sb = ring_claim(r, lane, st, ok);
+    if (!ok) return;
+    const int64_t row = static_cast<int64_t>(e) * rows_pe + c.j;
+    const uint32_t code_bytes = static_cast<uint32_t>(c.n) * g.rb;
+    const int64_t ng = static_cast<int64_t>(c.n) * G;
+    const Window w0 = window_of(gate.scales + row * G, ng);
+    const Window w1 = window_of(gate.biases + row * G, ng);
+    const Window w2 = window_of(up.scales + row * G, ng);
+    const Window w3 = window_of(up.biases + row * G, ng);
+    uint8_t *wb = sb + 2 * g.R * g.rb;
+    if (lane == 0)
+      mbar_arrive_expect_tx(&r.full[st], 2 * code_bytes + w0.bytes + w1.bytes + w2.bytes + w3.bytes);
+    __syncwarp();
+    if (lane == 0) bulk_g2s(sb, gate.codes + row * g.rb, code_bytes, &r.full[st], pol);
+    if (lane == 1) bulk_g2s(sb + g.R * g.rb, up.codes + row * g.rb, code_bytes, &r.full[st], pol);
+    if (lane == 2) bulk_g2s(wb + 0 * g.sw, w0.src, w0.bytes, &r.full[st], pol);
+    if (lane == 3) bulk_g2s(wb + 1 * g.sw, w1.src, w1.bytes, &r.full[st], pol);
+    if (lane == 4) bulk_g2s(wb + 2 * g.sw, w2.src, w2.bytes, &r.full[st], pol);
+    if (lane == 5) bulk_g2s(wb + 3 * g.sw, w3.src, w3.bytes, &r.full[st], pol);
+    ++r.i;
+  }
+}
+
+template <int BR, int BS>
+__device__ void produce_a(const LayerShape &s, const LayerPtrs &w, const GateUpGeom &gr,
+                          const GateUpGeom &gs, const int32_t *ids, Ring &r, int lane,
+                          uint64_t pol) {
+  const RangeA ra = range_a(s);
+  produce_a_class<BR>(s, gr, w.gate, w.up, false, ra.ra, ra.rb, 0, s.dff, ids, r, lane, pol);
+  if (!flag_abort(r.abort))
+    produce_a_class<BS>(s, gs, w.sh_gate, w.sh_up, true, ra.sa, ra.sb, ra.Ur, s.dff_shared, ids, r,
+                        lane, pol);
+}
+
+// Stages per reduction: consumers accumulate the partial sums of kPair consecutive stages and
+// reduce them together, so the reduction, the barrier and the finalize run once per pair.
+constexpr int kPair = 2;
+
+// Scratch of the consumer side of phase A.
+struct SmemA {
+  float red[2][kPair][2][32];  // [buffer][stage in pair][gate/up][row * warps-per-group + slot]
+  float stat[kConsumerWarps];
+  int ids[kMaxTopK];
+  float coef[kMaxTopK];
+};
+
+template <int BITS>
+__device__ void consume_a_class(const LayerShape &s, const GateUpGeom &g, const ProjDev &gate,
+                                const ProjDev &up, bool shared_class, int64_t a, int64_t b,
+                                int64_t base_u, int rows_pe, const uint16_t *x, float *act,
+                                float shared_scalar, Ring &r, int &buf, SmemA &sm, int tid) {
+  constexpr int C = Fmt<BITS>::kCodes, VEC = Fmt<BITS>::kVecs;
+  constexpr int RPT = rows_per_thread_a<BITS>();
+  constexpr int VS = 2 * RPT;        // values per stage: gate and up of RPT rows
+  constexpr int V = kPair * VS;
+  const int warp = tid >> 5, lane = tid & 31;
+  const int G = s.din / kGroup;
+  const int my_group = tid / g.tpr, my_step = tid % g.tpr;
+  const bool grp_ok = my_group < g.groups;
+  const bool active = grp_ok && my_step < g.T;
+  const int wpg = g.tpr / 32;
+  const int wslot = warp - my_group * wpg;
+  float xs[C], xsum;
+  int S;
+  load_x_regs<BITS>(x, my_step * C, active, xs, xsum, S);
+  const float twoS = pow2f(S);
+  const int grp = (my_step * C) / kGroup;
+
+  ChunkIterA it(a, b, base_u, rows_pe, g.R);
+  ChunkA c, cs[kPair];
+  bool more = it.next(c);
+  while (more) {
+    float v[V];
+#pragma unroll
+    for (int q = 0; q < V; ++q) v[q] = 0.f;
+    int np = 0;
+    while (more && np < kPair) {
+      const int e = shared_class ? c.k : sm.ids[c.k];
+      if (!shared_class && (e < 0 || e >= s.n_experts)) {   // the slot contributes nothing
+        for (int t = tid; t < c.n; t += kConsumers) act[c.u + t] = 0.f;
+        more = it.next(c);
+        continue;
+      }
+      const int st = r.i % r.nst;
+      const bool ok = warp_wait_full(r, st, lane);
+      const uint8_t *sb = r.base + static_cast<size_t>(st) * r.stage_bytes;
+      const int64_t row = static_cast<int64_t>(e) * rows_pe + c.j;
+      const uint8_t *wb = sb + 2 * g.R * g.rb;
+      if (active && ok) {
+        const int off0 = grp * 2;
+        const uint8_t *ps0 = wb + 0 * g.sw + window_of(gate.scales + row * G, 0).delta + off0;
+        const uint8_t *pb0 = wb + 1 * g.sw + window_of(gate.biases + row * G, 0).delta + off0;
+        const uint8_t *ps1 = wb + 2 * g.sw + window_of(up.scales + row * G, 0).delta + off0;
+        const uint8_t *pb1 = wb + 3 * g.sw + window_of(up.biases + row * G, 0).delta + off0;
+#pragma unroll
+        for (int q = 0; q < RPT; ++q) {
+          const int rr = q * g.groups + my_group;
+          if (rr < c.n) {
+            uint4 cg[VEC], cu[VEC];
+            const uint8_t *pg = sb + rr * g.rb + my_step * 16 * VEC;
+            const uint8_t *pu = pg + g.R * g.rb;
+#pragma unroll
+            for (int w = 0; w < VEC; ++w) {
+              cg[w] = lds_u4(pg + 16 * w);
+              cu[w] = lds_u4(pu + 16 * w);
+            }
+            const float dg = step_dot_regs<BITS>(cg, xs);
+            const float du = step_dot_regs<BITS>(cu, xs);
+            const int off = rr * G * 2;
+            // np is 0 or 1: select the slot with a compile-time index
+            const float vg = fmaf(lds_half(ps0 + off), dg * twoS, lds_half(pb0 + off) * xsum);
+            const float vu = fmaf(lds_half(ps1 + off), du * twoS, lds_half(pb1 + off) * xsum);
+            if (np == 0) {
+              v[q] = vg;
+              v[RPT + q] = vu;
+            } else {
+              v[VS + q] = vg;
+              v[VS + RPT + q] = vu;
+            }
+          }
+        }
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&r.empty[st]);
+      cs[np++] = c;
+      ++r.i;
+      more = it.next(c);
+    }
+    if (np == 0) break;   // only slots with invalid ids were left
+    const float val = warp_transpose_reduce<V>(v, lane);
+    const int idx = (lane >> (5 - Log2<V>::v)) & (V - 1);
+    if (grp_ok && (lane & ((32 / V) - 1)) == 0) {
+      const int pp = idx / VS, kind = (idx % VS) / RPT, q = idx % RPT;
+      const int rr = q * g.groups + my_group;
+      if (pp < np && rr < cs[pp].n) sm.red[buf][pp][kind][rr * wpg + wslot] = val;
+    }
+    consumer_sync(kConsumers);
+    const int n0 = cs[0].n, nt = n0 + (np > 1 ? cs[1].n : 0);
+    if (tid < nt) {
+      const int pp = tid < n0 ? 0 : 1, rr = tid - (pp ? n0 : 0);
+      float gsum = 0.f, usum = 0.f;
+      for (int w = 0; w < wpg; ++w) {
+        gsum += sm.red[buf][pp][0][rr * wpg + w];
+        usum += sm.red[buf][pp][1][rr * wpg + w];
+      }
+      const float coef = shared_class ? shared_scalar : sm.coef[cs[pp].k];
+      act[cs[pp].u + rr] = coef * (silu_f(gsum) * usum);
+    }
+    buf ^= 1;
+  }
+}
+
+// Consumers of phase A for one token of one layer.  ids/scores/x are read here (after whatever
+// wait made them complete).  Leaves a consumer_sync-free tail: callers synchronise as needed.
+template <int BR, int BS>
+__device__ void consume_a(const LayerShape &s, const LayerPtrs &w, const GateUpGeom &gr,
+                          const GateUpGeom &gs, const uint16_t *x, const int32_t *ids,
+                          const float *scores, float *act, int32_t *err, Ring &r, int &buf,
+                          SmemA &sm, int tid) {
+  const int warp = tid >> 5, lane = tid & 31;
+  for (int k = tid; k < s.top_k; k += kConsumers) {
+    sm.ids[k] = ids[k];
+    sm.coef[k] = scores[k];
+  }
+  float shared_scalar = 1.0f;
+  if (w.gate_vec != nullptr && s.n_shared > 0) {
+    float dot = 0.f;
+    for (int c = tid; c < s.din; c += kConsumers)
+      dot = fmaf(bf16_to_float(x[c]), bf16_to_float(w.gate_vec[c]), dot);
+    dot = consumers_sum(dot, sm.stat, warp, lane);   // also publishes sm.ids / sm.coef
+    shared_scalar = 1.0f / (1.0f + expf(-dot));
+  } else {
+    consumer_sync(kConsumers);                       // publishes sm.ids / sm.coef
+  }
+  if (tid == 0)
+    for (int k = 0; k < s.top_k; ++k)
+      if (sm.ids[k] < 0 || sm.ids[k] >= s.n_experts) atomicOr(err, kDevErrBadId);
+  const RangeA ra = range_a(s);
+  consume_a_class<BR>(s, gr, w.gate, w.up, false, ra.ra, ra.rb, 0, s.dff, x, act, 1.f, r, buf,
+                      sm, tid);
+  consume_a_class<BS>(s, gs, w.sh_gate, w.sh_up, true, ra.sa, ra.sb, ra.Ur, s.dff_shared, x, act,
+                      shared_scalar, r, buf, sm, tid);
+}
+
+// ================================================================== phase B
+struct SegB {
+  const ProjDev *pr;
+  int64_t expert;   // -1 when the slot's id is invalid
+  int rb, G, sw;
+  int code_off, win_off;
+};
+
+__device__ __forceinline__ SegB seg_b(const LayerShape &s, const LayerPtrs &w, const DownGeom &g,
+                                      int expert_id, int q) {
+  SegB sg;
+  if (q < s.top_k) {
+    sg.pr = &w.down;
+    sg.expert = (expert_id >= 0 && expert_id < s.n_experts) ? expert_id : -1;
+    sg.rb = g.rb_r;
+    sg.G = g.G_r;
+    sg.sw = g.sw_r;
+    sg.code_off = q * g.R * g.rb_r;
+    sg.win_off = q * g.sw_r;
+  } else {
+    const int t = q - s.top_k;
+    sg.pr = &w.sh_down;
+    sg.expert = t;
+    sg.rb = g.rb_s;
+    sg.G = g.G_s;
+    sg.sw = g.sw_s;
+    sg.code_off = s.top_k * g.R * g.rb_r + t * g.R * g.rb_s;
+    sg.win_off = s.top_k * g.sw_r + t * g.sw_s;
+  }
+  return sg;
+}
+
+__device__ __forceinline__ void range_b(const LayerShape &s, int &i0, int &i1) {
+  i0 = static_cast<int>(static_cast<int64_t>(s.din) * blockIdx.x / gridDim.x);
+  i1 = static_cast<int>(static_cast<int64_t>(s.din) * (blockIdx.x + 1) / gridDim.x);
+}
+
+__device__ void produce_b(const LayerShape &s, const LayerPtrs &w, const DownGeom &g,
+                          const int32_t *ids, Ring &r, int lane, uint64_t pol) {
+  int i0, i1;
+  range_b(s, i0, i1);
+  const int nseg = s.top_k + s.n_shared;
+  const int wins = s.top_k * g.sw_r + s.n_shared * g.sw_s;
+  for (int r0 = i0; r0 < i1; r0 += g.R) {
+    const int n = (i1 - r0) < g.R ? (i1 - r0) : g.R;
+    int st;
+    bool ok;
+    uint8_t *sb = ring_claim(r, lane, st, ok);
+    if (!ok) return;
+    uint8_t *wb = sb + g.codes_bytes;
+    // lane q handles segment q (and q + 32, ...): its codes, scale window and bias window
+    uint32_t tx = 0;
+    for (int q = lane; q < nseg; q += 32) {
+      const SegB sg = seg_b(s, w, g, q < s.top_k ? ids[q] : 0, q);
+      if (sg.expert < 0) continue;
+      const int64_t row = sg.expert * s.din + r0;
+      const int64_t ng = static_cast<int64_t>(n) * sg.G;
+      tx += static_cast<uint32_t>(n) * sg.rb + window_of(sg.pr->scales + row * sg.G, ng).bytes +
+            window_of(sg.pr->biases + row * sg.G, ng).bytes;
+    }
+    tx = warp_sum_u32(tx);
+    if (lane == 0) mbar_arrive_expect_tx(&r.full[st], tx);
+    __syncwarp();
+    for (int q = lane; q < nseg; q += 32) {
+      const SegB sg = seg_b(s, w, g, q < s.top_k ? ids[q] : 0, q);
+      if (sg.expert < 0) continue;
+      const int64_t row = sg.expert * s.din + r0;
+      const int64_t ng = static_cast<int64_t>(n) * sg.G;
+      const Window ws = window_of(sg.pr->scales + row * sg.G, ng);
+      const Window wbi = window_of(sg.pr->biases + row * sg.G, ng);
+      bulk_g2s(sb + sg.code_off, sg.pr->codes + row * sg.rb, static_cast<uint32_t>(n) * sg.rb,
+               &r.full[st], pol);
+      bulk_g2s(wb + sg.win_off, ws.src, ws.bytes, &r.full[st], pol);
+      bulk_g2s(wb + wins + sg.win_off, wbi.src, wbi.bytes, &r.full[st], pol);
+    }
+    ++r.i;
+  }
+}
+
+struct SmemB {
+  float red[2][kPair][64];  // [buffer][stage in pair][row * warps-per-group + warp slot]
+  int ids[kMaxTopK];
+  float resid[kMaxRowsB];   // the CTA's residual rows, loaded once per phase
+};
+
+template <int BITS, int CMAX>
+__device__ __forceinline__ float down_step(const uint8_t *codes, const float (&as)[CMAX]) {
+  constexpr int VEC = Fmt<BITS>::kVecs;
+  uint4 cv[VEC];
+#pragma unroll
+  for (int w = 0; w < VEC; ++w) cv[w] = lds_u4(codes + 16 * w);
+  return step_dot_regs<BITS>(cv, as);
+}
+
+// Consumers of phase B for one token: act must be complete (the caller waited for phase A).
+template <int BD, int BSD>
+__device__ void consume_b(const LayerShape &s, const LayerPtrs &w, const DownGeom &g,
+                          const int32_t *ids, const float *act, const void *resid, int resid_f32,
+                          void *out, int out_f32, int32_t *err, Ring &r, int &buf, SmemB &sm,
+                          int tid) {
+  constexpr int CR = Fmt<BD>::kCodes, CS = Fmt<BSD>::kCodes;
+  constexpr int CMAX = CR > CS ? CR : CS;
+  constexpr int SPTMAX = kMaxActRegs / CMAX > 0 ? kMaxActRegs / CMAX : 1;
+  constexpr int VS = 4;             // rows per thread per stage, at most
+  constexpr int V = kPair * VS;
+  const int warp = tid >> 5, lane = tid & 31;
+  for (int k = tid; k < s.top_k; k += kConsumers) sm.ids[k] = ids[k];
+  int i0, i1;
+  range_b(s, i0, i1);
+  for (int t = tid; t < i1 - i0; t += kConsumers)
+    sm.resid[t] = resid_f32 ? static_cast<const float *>(resid)[i0 + t]
+                            : bf16_to_float(static_cast<const uint16_t *>(resid)[i0 + t]);
+  const int my_group = tid / g.tpr, my_step = tid % g.tpr;
+  const bool grp_ok = my_group < g.groups;
+  const int wpg = g.tpr / 32;
+  const int wslot = warp - my_group * wpg;
+  const int Lr = s.top_k * s.dff;
+
+  // this thread's steps of the concatenated contraction and their activations, with a decoding
+  // shift of its own (each thread rescales its own partial sums)
+  float as[SPTMAX][CMAX];
+  float asum[SPTMAX], twoS[SPTMAX];
+  int seg[SPTMAX], jst[SPTMAX];
+  bool own[SPTMAX], shr[SPTMAX];
+#pragma unroll
+  for (int i = 0; i < SPTMAX; ++i) {
+    const int t = my_step + g.tpr * i;
+    own[i] = grp_ok && i < g.spt && t < g.T_r + g.T_s;
+    shr[i] = t >= g.T_r;
+    int base;
+    if (!shr[i]) {
+      seg[i] = t / g.spr_r;
+      jst[i] = t - seg[i] * g.spr_r;
+      base = t * CR;
+    } else {
+      const int ts = t - g.T_r;
+      const int si = ts / (g.spr_s > 0 ? g.spr_s : 1);
+      seg[i] = s.top_k + si;
+      jst[i] = ts - si * g.spr_s;
+      base = Lr + ts * CS;
+    }
+    const int C = shr[i] ? CS : CR;
+    const float4 *ap = reinterpret_cast<const float4 *>(act + base);
+    float mx = 0.f;
+    asum[i] = 0.f;
+#pragma unroll
+    for (int c = 0; c < CMAX; c += 4) {
+      const float4 a4 = (own[i] && c < C) ? ap[c / 4] : make_float4(0.f, 0.f, 0.f, 0.f);
+      as[i][c] = a4.x;
+      as[i][c + 1] = a4.y;
+      as[i][c + 2] = a4.z;
+      as[i][c + 3] = a4.w;
+      asum[i] += (a4.x + a4.y) + (a4.z + a4.w);
+      mx = fmaxf(mx, fmaxf(fmaxf(fabsf(a4.x), fabsf(a4.y)), fmaxf(fabsf(a4.z), fabsf(a4.w))));
+    }
+    const int S = choose_shift(mx);
+    twoS[i] = pow2f(S);
+#pragma unroll
+    for (int c = 0; c < CMAX; ++c) {
+      const int o = shr[i] ? code_offset<BSD>(c) : code_offset<BD>(c);
+      as[i][c] *= pow2f(149 - S - o);
+    }
+  }
+  consumer_sync(kConsumers);   // publishes sm.ids and sm.resid
+  int grp[SPTMAX];
+  bool seg_ok[SPTMAX];
+#pragma unroll
+  for (int i = 0; i < SPTMAX; ++i) {
+    grp[i] = (jst[i] * (shr[i] ? CS : CR)) / kGroup;
+    seg_ok[i] =
+        own[i] && (seg[i] >= s.top_k || (sm.ids[seg[i]] >= 0 && sm.ids[seg[i]] < s.n_experts));
+  }
+  if (tid == 0)
+    for (int k = 0; k < s.top_k; ++k)
+      if (sm.ids[k] < 0 || sm.ids[k] >= s.n_experts) atomicOr(err, kDevErrBadId);
+  const int wins = s.top_k * g.sw_r + s.n_shared * g.sw_s;
+  const int rpt = g.R / g.groups;
+
+  int r0 = i0;
+  while (r0 < i1) {
+    float acc[V];
+#pragma unroll
+    for (int q = 0; q < V; ++q) acc[q] = 0.f;
+    int np = 0, rows0 = 0, nrows[kPair] = {0, 0}, base_row[kPair] = {0, 0};
+    while (r0 < i1 && np < kPair) {
+      const int n = (i1 - r0) < g.R ? (i1 - r0) : g.R;
+      const int st = r.i % r.nst;
+      const bool ok = warp_wait_full(r, st, lane);
+      const uint8_t *sb = r.base + static_cast<size_t>(st) * r.stage_bytes;
+      const uint8_t *wb = sb + g.codes_bytes;
+      if (ok) {
+#pragma unroll
+        for (int i = 0; i < SPTMAX; ++i) {
+          if (!seg_ok[i]) continue;
+          const SegB sg = seg_b(s, w, g, seg[i] < s.top_k ? sm.ids[seg[i]] : 0, seg[i]);
+          const int64_t row0 = sg.expert * s.din + r0;
+          const uint8_t *cp =
+              sb + sg.code_off + jst[i] * 16 * (shr[i] ? Fmt<BSD>::kVecs : Fmt<BD>::kVecs);
+          const uint8_t *sp =
+              wb + sg.win_off + window_of(sg.pr->scales + row0 * sg.G, 0).delta + grp[i] * 2;
+          const uint8_t *bp = wb + wins + sg.win_off +
+                              window_of(sg.pr->biases + row0 * sg.G, 0).delta + grp[i] * 2;
+#pragma unroll
+          for (int q = 0; q < VS; ++q) {
+            const int rr = q * g.groups + my_group;
+            if (q < rpt && rr < n) {
+              const float d = shr[i] ? down_step<BSD, CMAX>(cp + rr * sg.rb, as[i])
+                                     : down_step<BD, CMAX>(cp + rr * sg.rb, as[i]);
+              const int off = rr * sg.G * 2;
+              const float t = fmaf(lds_half(sp + off), d * twoS[i], lds_half(bp + off) * asum[i]);
+              if (np == 0)
+                acc[q] += t;
+              else
+                acc[VS + q] += t;
+            }
+          }
+        }
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&r.empty[st]);
+      nrows[np] = n;
+      base_row[np] = rows0;
+      rows0 += n;
+      ++np;
+      ++r.i;
+      r0 += n;
+    }
+    const float val = warp_transpose_reduce<V>(acc, lane);
+    const int idx = (lane >> (5 - Log2<V>::v)) & (V - 1);
+    if (grp_ok && (lane & ((32 / V) - 1)) == 0) {
+      const int pp = idx / VS, q = idx % VS;
+      const int rr = q * g.groups + my_group;
+      if (pp < np && q < rpt && rr < nrows[pp]) sm.red[buf][pp][rr * wpg + wslot] = val;
+    }
+    consumer_sync(kConsumers);
+    if (tid < rows0) {
+      const int pp = tid < nrows[0] ? 0 : 1, rr = tid - (pp ? nrows[0] : 0);
+      float sum = 0.f;
+      for (int ww = 0; ww < wpg; ++ww) sum += sm.red[buf][pp][rr * wpg + ww];
+      const int i = r0 - rows0 + tid;   // first row of the pair + tid
+      const float o = sm.resid[i - i0] + sum;
+      if (out_f32)
+        static_cast<float *>(out)[i] = o;
+      else
+        static_cast<uint16_t *>(out)[i] = float_to_bf16_rn(o);
+    }
+    (void)base_row;
+    buf ^= 1;
+  }
+}
+
+}  // namespace moe

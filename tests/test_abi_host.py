@@ -61,7 +61,7 @@ def test_host_pack_rejects_bad_input(L):
 def _cfg(**kw):
     base = dict(din=256, dff=128, n_experts=8, top_k=2, max_tokens=1, bits_gate=4, bits_up=4,
                 bits_down=4, n_shared=0, dff_shared=0, bits_shared=4, shared_gate=0,
-                resid_dtype=0, out_dtype=1, warps_per_block=0)
+                resid_dtype=0, out_dtype=1, kernel_mode=0)
     base.update(kw)
     return Bn.Config(**base)
 
@@ -88,6 +88,7 @@ def _weights(n_proj=6, gate_vec=True, misalign=False):
     (dict(shared_gate=2), Bn.MOE_ERR_INVALID_ARG),
     (dict(resid_dtype=7), Bn.MOE_ERR_INVALID_ARG),
     (dict(out_dtype=-1), Bn.MOE_ERR_INVALID_ARG),
+    (dict(kernel_mode=2), Bn.MOE_ERR_INVALID_ARG),
 ])
 def test_create_rejects_invalid_config(L, kw, rc):
     h = ctypes.c_void_p()

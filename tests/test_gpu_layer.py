@@ -180,3 +180,23 @@ def test_forward_rejects_bad_arguments():
         blk.forward(xd, C.dev(ids[:1], torch.int32), C.dev(sc[:1], torch.float32),
                     C.dev(r[:1], torch.bfloat16), out=xd)   # out may not alias x
     blk.close()
+
+
+@pytest.mark.parametrize("name", ["ragged 192x320 E6 K3 6/6/8 gated shared",
+                                  "4096x1408 E12 K6 4/4/6 two shared",
+                                  "qwen3-30b-a3b layer (full size)"])
+def test_separate_kernels_match_fused_kernel_bit_for_bit(name):
+    shape = SHAPES[name]
+    layer = C.host_layer_device(shape)
+    x, r, ids, sc = C.token_inputs(shape)
+    outs = []
+    for mode in (Bn.KERNELS_FUSED, Bn.KERNELS_SEPARATE):
+        blk = Bn.MoeDecode(layer, kernel_mode=mode)
+        o = blk.forward(C.dev(x, torch.bfloat16), C.dev(ids, torch.int32),
+                        C.dev(sc, torch.float32), C.dev(r, torch.bfloat16))
+        torch.cuda.synchronize()
+        assert blk.get_error() == 0
+        blk.close()
+        outs.append(o)
+    assert torch.equal(outs[0].view(torch.int32), outs[1].view(torch.int32))
+    C.assert_parity(outs[1].cpu().numpy(), C.OracleLayer(shape).token(x[0], r[0], ids[0], sc[0]))

@@ -85,12 +85,13 @@ def test_small_stack_graph_equals_chain_and_oracle():
     stack.close()
 
 
-def test_small_stack_several_tokens():
+@pytest.mark.parametrize("mode", [Bn.KERNELS_FUSED, Bn.KERNELS_SEPARATE])
+def test_small_stack_several_tokens(mode):
     shape = Shape("small stack m3", 384, 192, 10, 3, 6, 6, 4, layers=3, seed=32)
     layers = [C.host_layer_device(shape, l) for l in range(shape.layers)]
     m = 3
     x, ids, sc, resid0 = stack_inputs(shape, m=m)
-    stack = Bn.MoeStack(layers, max_tokens=m)
+    stack = Bn.MoeStack(layers, max_tokens=m, kernel_mode=mode)
     out = torch.empty((m, shape.din), dtype=torch.float32, device="cuda")
     stack.step(C.dev(x, torch.bfloat16), C.dev(ids, torch.int32), C.dev(sc, torch.float32),
                C.dev(resid0, torch.bfloat16), out)
