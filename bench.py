@@ -4,16 +4,19 @@
     python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--tokens M]
     python bench.py --impl reference ...        # the fp64 CPU oracle on the host cores
 
-A step is one decode step through every layer of the stack (kernel A and kernel B per layer,
-replayed as one CUDA graph), on seeded synthetic weights drawn in HBM and token inputs already
-resident on the device.  Each step uses the next of several pre-drawn input sets, so expert ids
-change from step to step, and a step reads far more weight bytes than L2 holds.
+A step is one decode step through every layer of the stack (both phases of every layer in one
+persistent cooperative kernel launch, replayed as a CUDA graph), on seeded synthetic weights drawn
+in HBM and token inputs already resident on the device.  Each step uses the next of several
+pre-drawn input sets, so expert ids change from step to step, and a step reads far more weight
+bytes than L2 holds.
 
 value      tokens per second through the whole stack (all ranks), timed with CUDA events
 e2e        the same through moe_stack_step_host: inputs copied from pinned host memory and the
            output copied back inside the timed region
-roofline   kernel A (the gate/up GEMVs, the larger share of bytes): algorithmic bytes per launch
-           divided by its per-launch time, measured by replaying kernel A of every layer alone
+roofline   the fused stack kernel (the only kernel of a step): algorithmic bytes of one step
+           divided by the step's device time
+separate_kernels  the same layers through the two-kernel mode (kernel A then kernel B per layer),
+           each phase replayed alone: per-launch bytes and time, for comparison
 cpu_baseline  the oracle, as it stands, on a bounded sample of the same workload
 N > 1      independent replicas, one per GPU (the block has no exchange step); weak scaling
 """
@@ -39,6 +42,9 @@ from quantized_moe_expert_dequant_gb300.workloads import ALL, Shape  # noqa: E40
 METRIC = "MoE decode tok/s (full layer stack) and achieved HBM GB/s vs peak, 1 GB300"
 DEFAULT_WORKLOAD = "qwen3_stack_8bit"
 KERNEL_SOURCES = ["quantized_moe_expert_dequant_gb300/csrc/moe_kernels.cu",
+                  "quantized_moe_expert_dequant_gb300/csrc/moe_kernels.cuh",
+                  "quantized_moe_expert_dequant_gb300/csrc/moe_phases.cuh",
+                  "quantized_moe_expert_dequant_gb300/csrc/moe_tma.cuh",
                   "quantized_moe_expert_dequant_gb300/csrc/moe_common.cuh"]
 
 
@@ -228,6 +234,15 @@ def max_over_ranks(v: float, device=None) -> float:
     return float(t.item())
 
 
+def job_rate(units_per_rank: float, ms_local: float, device=None):
+    """Whole-job rate: the units every rank processed over the slowest rank's time.
+    Returns (units per second, the max-over-ranks milliseconds)."""
+    import torch.distributed as dist
+    world = dist.get_world_size() if dist.is_available() and dist.is_initialized() else 1
+    ms = max_over_ranks(ms_local, device)
+    return world * units_per_rank / (ms / 1e3), ms
+
+
 def barrier(device=None):
     import torch.distributed as dist
     if dist.is_available() and dist.is_initialized() and dist.get_world_size() > 1:
@@ -283,7 +298,9 @@ def run_ours(args, shape: Shape):
     if free < need * 1.05:
         raise SystemExit(f"workload needs {need / 1e9:.1f} GB, {free / 1e9:.1f} GB free")
     layers = [Bn.synth_layer_device(shape, l) for l in range(L)]
-    stack = Bn.MoeStack(layers, max_tokens=m)
+    mode = Bn.KERNELS_FUSED if args.kernels == "fused" else Bn.KERNELS_SEPARATE
+    stack = Bn.MoeStack(layers, max_tokens=m, kernel_mode=mode)
+    parts_stack = Bn.MoeStack(layers, max_tokens=m, kernel_mode=Bn.KERNELS_SEPARATE)
 
     def dev(a, dt):
         a = np.ascontiguousarray(a)
@@ -308,7 +325,7 @@ def run_ours(args, shape: Shape):
         if parts == 3:
             stack.step(x, ids, sc, r0, out, stream)
         else:
-            stack.step_parts(parts, x, ids, sc, r0, out, stream)
+            parts_stack.step_parts(parts, x, ids, sc, r0, out, stream)
 
     bus = None
     try:
@@ -340,14 +357,12 @@ def run_ours(args, shape: Shape):
     torch.cuda.synchronize(device)
     barrier(device)
     ms_local = e0.elapsed_time(e1)
-    ms = max_over_ranks(ms_local, device)
+    value, ms = job_rate(m * args.steps, ms_local, device)
     ms_per_step = ms / args.steps
-    tokens_all = world * m * args.steps
-    value = tokens_all / (ms / 1e3)
     step_bytes = sum(bytes_a[i % S] + bytes_b[i % S] for i in range(args.steps)) / args.steps
 
-    # dominant kernel: kernel A of every layer replayed alone (same launch configuration)
-    reps = max(args.steps, 20)
+    # the two-kernel mode, each phase of every layer replayed alone (for comparison)
+    reps = max(args.steps // 4, 20)
 
     def time_part(parts):
         torch.cuda.synchronize(device)
@@ -388,14 +403,21 @@ def run_ours(args, shape: Shape):
     h2d = sum(t.numel() * t.element_size() for t in pinned[0][:4])
     d2h = pinned[0][4].numel() * 4
     clocks = sampler.stop()
-    assert stack.get_error() == 0
+    assert stack.get_error() == 0 and parts_stack.get_error() == 0
 
     peaks = measured_peaks()
     peak = peaks["hbm_gbs"] if peaks else 6800.0
     peak_note = "of measured" if peaks else "of fallback"
     ach_a = mean_a / (ms_a * 1e-3) / 1e9
     ach_b = mean_b / (ms_b * 1e-3) / 1e9
-    traffic = profiled_traffic("gate_up_kernel", args.workload)
+    dominant = "fused_kernel" if mode == Bn.KERNELS_FUSED else "gate_up_kernel"
+    if mode == Bn.KERNELS_FUSED:
+        # one launch per step: the step's bytes over the step's device time
+        ach, per_launch_bytes, per_launch_us = (step_bytes / (ms_per_step * 1e-3) / 1e9,
+                                                step_bytes, ms_per_step * 1e3)
+    else:
+        ach, per_launch_bytes, per_launch_us = ach_a, mean_a, ms_a * 1e3
+    traffic = profiled_traffic(dominant, args.workload)
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
@@ -423,21 +445,25 @@ def run_ours(args, shape: Shape):
         "hbm": {"step_bytes": step_bytes, "step_gbs": step_bytes / (ms_per_step * 1e-3) / 1e9,
                 "peak_gbs": peak, "frac": step_bytes / (ms_per_step * 1e-3) / 1e9 / peak,
                 "note": peak_note},
-        "roofline": {"kernel": "gate_up_kernel", "bound": "hbm", "achieved": ach_a, "peak": peak,
-                     "unit": "GB/s", "frac": ach_a / peak, "traffic": traffic,
-                     "bytes_per_launch": mean_a, "us_per_launch": ms_a * 1e3,
+        "roofline": {"kernel": dominant, "bound": "hbm", "achieved": ach, "peak": peak,
+                     "unit": "GB/s", "frac": ach / peak, "traffic": traffic,
+                     "bytes_per_launch": per_launch_bytes, "us_per_launch": per_launch_us,
                      "note": peak_note + " (copy peak)"},
-        "kernel_b": {"kernel": "down_kernel", "achieved": ach_b, "frac": ach_b / peak,
-                     "bytes_per_launch": mean_b, "us_per_launch": ms_b * 1e3},
+        "separate_kernels": {
+            "gate_up_kernel": {"achieved": ach_a, "frac": ach_a / peak,
+                               "bytes_per_launch": mean_a, "us_per_launch": ms_a * 1e3},
+            "down_kernel": {"achieved": ach_b, "frac": ach_b / peak,
+                            "bytes_per_launch": mean_b, "us_per_launch": ms_b * 1e3}},
         "cpu_baseline": cpu,
         "e2e": {"value": world * m * e2e_steps / e2e_s, "unit": "tok/s",
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
-        "gpu_launches": args.steps * L * m * 2,
+        "gpu_launches": args.steps if mode == Bn.KERNELS_FUSED else args.steps * L * m * 2,
         "clocks": clocks,
     }
     if rank == 0:
         print(json.dumps(line), flush=True)
     stack.close()
+    parts_stack.close()
     return 0
 
 
@@ -449,6 +475,8 @@ def main(argv=None):
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", choices=sorted(ALL), default=DEFAULT_WORKLOAD)
     ap.add_argument("--tokens", type=int, default=1)
+    ap.add_argument("--kernels", choices=["fused", "separate"], default="fused",
+                    help="one persistent kernel per step, or kernel A and kernel B per layer")
     ap.add_argument("--input-sets", type=int, default=4)
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
