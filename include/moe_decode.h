@@ -122,6 +122,40 @@ int moe_decode_get_error(moe_decode_t *h, int32_t *device_error);
 
 void moe_decode_destroy(moe_decode_t *h);
 
+/* ---- one layer without a handle and without device allocation -------------------------------
+ * The pages have no counterpart of this call: their kernels always run inside an engine that owns
+ * its buffers.  It exists for callers that may not allocate device memory at all (an allocator
+ * that is frozen while graphs are captured, a memory pool with a hard budget): it runs the same
+ * two kernels as MOE_KERNELS_SEPARATE, kernel A then kernel B per token, with the activation vector
+ * kept in a fixed scratch array of the library instead of a handle's workspace.
+ *
+ *   cfg, weights   as for moe_decode_create; cfg->kernel_mode must be MOE_KERNELS_SEPARATE and
+ *                  K*dff + n_shared*dff_shared must not exceed MOE_NOALLOC_MAX_ACT_FLOATS
+ *                  (else MOE_ERR_UNSUPPORTED); weights are borrowed for the call
+ *   x, ids, scores, resid, out, m, stream   as for moe_decode_forward (m <= cfg->max_tokens)
+ *   device_error   int32 device word the kernels OR error bits into (bit 0: an expert id outside
+ *                  [0, n_experts), that slot contributed zero; bit 1: a wait gave up).  It must
+ *                  hold 0 before the first call and is never cleared by the library.  NULL sends
+ *                  the bits to a library word that no call reads.
+ *
+ * Scratch: a file-scope device array of MOE_NOALLOC_MAX_ACT_FLOATS floats (256 KiB) per device,
+ * whose address is looked up once per device (with the lookup's return code checked).  Nothing is
+ * allocated, freed or zeroed by the call; the scratch needs no initial value because kernel A
+ * writes every activation before kernel B reads it.
+ * Races: every call on a device shares that one array.  Calls on one device must be ordered on
+ * the GPU (one stream, or streams joined by events); two calls that overlap on the GPU corrupt
+ * each other's activations.
+ * Capture: the first call on a device looks the scratch up, and the first call with a given config
+ * sets the kernels' shared-memory limits (the last 8 configs per device are remembered); make those
+ * calls outside stream capture.  Later calls with a remembered config only enqueue two kernels per
+ * token and may be captured into a CUDA graph.
+ * Returns MOE_OK, or a negative status with nothing enqueued. */
+#define MOE_NOALLOC_MAX_ACT_FLOATS 65536
+int moe_decode_forward_noalloc(const moe_decode_config *cfg, const moe_layer_weights *weights,
+                               const void *x, int32_t m, const int32_t *ids, const float *scores,
+                               const void *resid, void *out, int32_t *device_error,
+                               void *stream);
+
 /* ---- a stack of layers replayed as one CUDA graph ------------------------------------------
  * Layer l reads x_l = x + l*m*din, ids_l = ids + l*m*top_k, scores_l likewise; its residual is
  * resid0 (cfg->resid_dtype) for l = 0 and the fp32 output of layer l-1 after that; the last

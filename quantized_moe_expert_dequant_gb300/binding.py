@@ -24,10 +24,12 @@ MOE_OK, MOE_ERR_INVALID_ARG, MOE_ERR_UNSUPPORTED, MOE_ERR_CUDA, MOE_ERR_OOM, MOE
 DTYPE_BF16, DTYPE_F32 = 0, 1
 PART_GATE_UP, PART_DOWN = 1, 2
 KERNELS_FUSED, KERNELS_SEPARATE = 0, 1
+NOALLOC_MAX_ACT_FLOATS = 65536
 _STATUS = {0: "MOE_OK", -1: "MOE_ERR_INVALID_ARG", -2: "MOE_ERR_UNSUPPORTED", -3: "MOE_ERR_CUDA",
            -4: "MOE_ERR_OOM", -5: "MOE_ERR_BAD_ID", -6: "MOE_ERR_TIMEOUT"}
 
 EXPORTS = ["moe_decode_create", "moe_decode_forward", "moe_decode_get_error", "moe_decode_destroy",
+           "moe_decode_forward_noalloc",
            "moe_stack_create", "moe_stack_step", "moe_stack_step_parts", "moe_stack_step_host",
            "moe_stack_get_error",
            "moe_stack_destroy", "moe_pack_codes", "moe_unpack_codes", "moe_unpack_codes_device",
@@ -76,6 +78,8 @@ def lib() -> ctypes.CDLL:
                 "moe_decode_forward": [vp, vp, i32, vp, vp, vp, vp, vp],
                 "moe_decode_get_error": [vp, ctypes.POINTER(i32)],
                 "moe_decode_destroy": [vp],
+                "moe_decode_forward_noalloc": [ctypes.POINTER(Config), ctypes.POINTER(LayerWeights),
+                                               vp, i32, vp, vp, vp, vp, vp, vp],
                 "moe_stack_create": [ctypes.POINTER(Config), i32, ctypes.POINTER(LayerWeights),
                                      ctypes.POINTER(vp)],
                 "moe_stack_step": [vp, vp, i32, vp, vp, vp, vp, vp],
@@ -242,6 +246,22 @@ class MoeDecode:
             self.close()
         except Exception:
             pass
+
+
+def forward_noalloc(layer: "DeviceLayer", x: torch.Tensor, ids: torch.Tensor | None,
+                    scores: torch.Tensor | None, resid: torch.Tensor, out: torch.Tensor,
+                    device_error: torch.Tensor | None = None, max_tokens: int | None = None,
+                    resid_dtype=DTYPE_BF16, out_dtype=DTYPE_F32, stream=None) -> torch.Tensor:
+    """moe_decode_forward_noalloc: one layer without a handle, activations in the library's
+    fixed scratch array (two-kernel mode).  `out` must be given; `device_error` is an int32
+    device tensor of one element that must start at 0."""
+    m = x.shape[0] if x.dim() == 2 else 1
+    cfg = config(layer.shape, max_tokens or m, resid_dtype, out_dtype, KERNELS_SEPARATE)
+    w = layer.struct()
+    check("moe_decode_forward_noalloc", lib().moe_decode_forward_noalloc(
+        ctypes.byref(cfg), ctypes.byref(w), _p(x), m, _p(ids), _p(scores), _p(resid), _p(out),
+        _p(device_error), _stream(stream)))
+    return out
 
 
 class MoeStack:

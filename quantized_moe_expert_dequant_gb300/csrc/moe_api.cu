@@ -2,6 +2,7 @@
 // CUDA-graph driver and the host-buffer step.
 #include <cstdint>
 #include <cstring>
+#include <mutex>
 #include <new>
 #include <vector>
 
@@ -291,6 +292,105 @@ extern "C" void moe_decode_destroy(moe_decode_t *h) {
   if (!h) return;
   h->ws.release();
   delete h;
+}
+
+// ====================================================================== one layer, no allocation
+namespace {
+
+// The activations between kernel A and kernel B of moe_decode_forward_noalloc, and the error word
+// of calls that pass none.  Static storage: zero at module load, never allocated or freed.
+static __device__ __align__(256) float g_noalloc_act[MOE_NOALLOC_MAX_ACT_FLOATS];
+static __device__ __align__(256) int32_t g_noalloc_err[64];
+
+constexpr int kNoallocDevices = 64;
+
+constexpr int kNoallocPlans = 8;
+
+struct NoallocPlan {
+  bool valid = false;
+  moe_decode_config cfg{};  // the config `prep` was made for
+  Prepared prep{};
+};
+
+struct NoallocDevice {
+  bool ready = false;
+  float *act = nullptr;
+  int32_t *err = nullptr;
+  NoallocPlan plans[kNoallocPlans];  // the last configs seen on this device
+  int next = 0;                      // the entry the next new config replaces
+};
+
+NoallocDevice g_noalloc[kNoallocDevices];
+std::mutex g_noalloc_mu;
+
+// Scratch addresses and the prepared launch plan of the current device: the addresses are looked
+// up once per device, a plan once per config (the last kNoallocPlans configs are kept).
+int noalloc_setup(const moe_decode_config *cfg, float **act, int32_t **err, Prepared *P) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return MOE_ERR_CUDA;
+  if (dev < 0 || dev >= kNoallocDevices) return MOE_ERR_UNSUPPORTED;
+  std::lock_guard<std::mutex> lock(g_noalloc_mu);
+  NoallocDevice &d = g_noalloc[dev];
+  if (!d.ready) {
+    void *a = nullptr, *e = nullptr;
+    if (cudaGetSymbolAddress(&a, g_noalloc_act) != cudaSuccess ||
+        cudaGetSymbolAddress(&e, g_noalloc_err) != cudaSuccess) {
+      cudaGetLastError();
+      return MOE_ERR_CUDA;
+    }
+    d.act = static_cast<float *>(a);
+    d.err = static_cast<int32_t *>(e);
+    d.ready = true;
+  }
+  NoallocPlan *hit = nullptr;
+  for (NoallocPlan &p : d.plans)
+    if (p.valid && std::memcmp(&p.cfg, cfg, sizeof *cfg) == 0) hit = &p;
+  if (!hit) {
+    hit = &d.plans[d.next];
+    d.next = (d.next + 1) % kNoallocPlans;
+    hit->valid = false;
+    const int rc = prepare(cfg, hit->prep);
+    if (rc != MOE_OK) return rc;
+    hit->cfg = *cfg;
+    hit->valid = true;
+  }
+  *act = d.act;
+  *err = d.err;
+  *P = hit->prep;
+  return MOE_OK;
+}
+
+}  // namespace
+
+extern "C" int moe_decode_forward_noalloc(const moe_decode_config *cfg,
+                                          const moe_layer_weights *weights, const void *x,
+                                          int32_t m, const int32_t *ids, const float *scores,
+                                          const void *resid, void *out, int32_t *device_error,
+                                          void *stream) {
+  int rc = validate_config(cfg);
+  if (rc != MOE_OK) return rc;
+  if (cfg->kernel_mode != MOE_KERNELS_SEPARATE) return MOE_ERR_UNSUPPORTED;
+  if (act_floats(*cfg) > (size_t)MOE_NOALLOC_MAX_ACT_FLOATS) return MOE_ERR_UNSUPPORTED;
+  rc = validate_weights(cfg, weights);
+  if (rc != MOE_OK) return rc;
+  if (!x || !resid || !out) return MOE_ERR_INVALID_ARG;
+  if (m < 1 || m > cfg->max_tokens) return MOE_ERR_INVALID_ARG;
+  if (cfg->top_k > 0 && (!ids || !scores)) return MOE_ERR_INVALID_ARG;
+  if (!aligned(x, 16) || !aligned(resid, dtype_bytes(cfg->resid_dtype)) ||
+      !aligned(out, dtype_bytes(cfg->out_dtype)) || (ids && !aligned(ids, 4)) ||
+      (scores && !aligned(scores, 4)) || (device_error && !aligned(device_error, 4)))
+    return MOE_ERR_INVALID_ARG;
+  if (x == out) return MOE_ERR_INVALID_ARG;
+  float *act = nullptr;
+  int32_t *err = nullptr;
+  Prepared P;
+  rc = noalloc_setup(cfg, &act, &err, &P);
+  if (rc != MOE_OK) return rc;
+  const cudaError_t e = enqueue_separate(
+      P, layer_ptrs(*cfg, *weights), act, device_error ? device_error : err, x, m, ids, scores,
+      resid, cfg->resid_dtype, out, cfg->out_dtype, static_cast<cudaStream_t>(stream),
+      MOE_PART_GATE_UP | MOE_PART_DOWN);
+  return e == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
 }
 
 // ====================================================================== stack of layers
