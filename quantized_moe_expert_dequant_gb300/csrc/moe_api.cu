@@ -100,11 +100,13 @@ int prepare(const moe_decode_config *c, Prepared &P) {
       cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, device) != cudaSuccess)
     return MOE_ERR_CUDA;
   if (major != 10 || minor != 3) return MOE_ERR_UNSUPPORTED;  // built for sm_103a only
-  const size_t static_reserve = 4096;  // the kernels' static shared memory
-  if (P.plan.smem + static_reserve > (size_t)smem_optin) return MOE_ERR_UNSUPPORTED;
-  if (moe::prepare_kernels(smem_optin - (int)static_reserve, c->bits_gate, c->bits_down,
-                           P.bits_sh) != cudaSuccess)
+  int dyn_limit = 0;
+  if (moe::prepare_kernels(smem_optin, c->bits_gate, c->bits_down, P.bits_sh, &dyn_limit) !=
+      cudaSuccess) {
+    cudaGetLastError();
     return MOE_ERR_CUDA;
+  }
+  if (P.plan.smem > (size_t)dyn_limit) return MOE_ERR_UNSUPPORTED;
   P.grid_sep = sms;
   const int lim = moe::fused_grid_limit(P.plan, c->bits_gate, c->bits_down, P.bits_sh);
   P.grid_fused = lim < sms ? lim : sms;

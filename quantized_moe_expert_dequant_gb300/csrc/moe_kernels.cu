@@ -44,16 +44,15 @@ __global__ void __launch_bounds__(kThreads, 1) gate_up_kernel(const GateUpParams
   pdl_launch_dependents();
   __syncthreads();
   Ring r{full, empty, ring, p.plan.nst, p.plan.stage_bytes, 0, &abort_s, p.err};
-  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int tid = threadIdx.x, warp = tid >> 5;
   if (warp >= kConsumerWarps) {
     produce_a<BR, BS>(p.s, p.w, p.plan.geo_r, p.plan.geo_s, p.ids, r, tid - kConsumers,
                       policy_evict_first());
     ring_drain(r, tid - kConsumers);
     return;
   }
-  int buf = 0;
   consume_a<BR, BS>(p.s, p.w, p.plan.geo_r, p.plan.geo_s, p.x, p.ids, p.scores, p.act, p.err, r,
-                    buf, sm, tid);
+                    sm, tid);
 }
 
 template <int BD, int BSD>
@@ -62,12 +61,13 @@ __global__ void __launch_bounds__(kThreads, 1) down_kernel(const DownParams p) {
   __shared__ __align__(8) uint64_t full[kMaxStages];
   __shared__ __align__(8) uint64_t empty[kMaxStages];
   __shared__ SmemB sm;
+  __shared__ float resid_s[kMaxRowsB];
   __shared__ int abort_s;
   init_ring(full, empty, p.plan.nst, &abort_s);
   pdl_launch_dependents();
   __syncthreads();
   Ring r{full, empty, ring, p.plan.nst, p.plan.stage_bytes, 0, &abort_s, p.err};
-  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int tid = threadIdx.x, warp = tid >> 5;
   if (warp >= kConsumerWarps) {
     // The ids were complete before kernel A started (A waits on its predecessor before it lets
     // this kernel launch), so the weight stream may start before the activations are ready.
@@ -75,10 +75,11 @@ __global__ void __launch_bounds__(kThreads, 1) down_kernel(const DownParams p) {
     ring_drain(r, tid - kConsumers);
     return;
   }
-  pdl_wait();  // the activations come from kernel A
-  int buf = 0;
-  consume_b<BD, BSD>(p.s, p.w, p.plan.geo_b, p.ids, p.act, p.resid, p.resid_f32, p.out,
-                     p.out_f32, p.err, r, buf, sm, tid);
+  pdl_wait();  // the activations come from kernel A (and, in a stack, resid from the kernel
+               // before it)
+  load_resid_rows(p.s, p.resid, p.resid_f32, resid_s, tid);
+  consume_b<BD, BSD>(p.s, p.plan.geo_b, p.ids, p.act, resid_s, p.out, p.out_f32, p.err, r, sm,
+                     tid);
 }
 
 template <int BR, int BD, int BSH>
@@ -86,8 +87,8 @@ __global__ void __launch_bounds__(kThreads, 1) fused_kernel(const StackParams p)
   extern __shared__ __align__(128) uint8_t ring[];
   __shared__ __align__(8) uint64_t full[kMaxStages];
   __shared__ __align__(8) uint64_t empty[kMaxStages];
-  __shared__ SmemA sma;
-  __shared__ SmemB smb;
+  __shared__ SmemAB sm;
+  __shared__ float resid_s[kMaxRowsB];
   __shared__ LayerPtrs wl;   // the consumers' copy of the current layer's pointers
   __shared__ LayerPtrs wpr;  // the producers' copy
   __shared__ int ids_pr[kMaxTopK];
@@ -96,7 +97,7 @@ __global__ void __launch_bounds__(kThreads, 1) fused_kernel(const StackParams p)
   init_ring(full, empty, p.plan.nst, &abort_s);
   __syncthreads();
   Ring r{full, empty, ring, p.plan.nst, p.plan.stage_bytes, 0, &abort_s, p.err};
-  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int tid = threadIdx.x, warp = tid >> 5;
   const LayerShape &s = p.s;
   const uint32_t n = gridDim.x;
   const int64_t xs = static_cast<int64_t>(s.din), ks = s.top_k;
@@ -110,15 +111,18 @@ __global__ void __launch_bounds__(kThreads, 1) fused_kernel(const StackParams p)
       for (int t = 0; t < p.m; ++t, ++pass) {
         producer_sync();  // every producer is done with the previous pass's copies
         if (pl == 0) {
+          wpr = p.layers[l];  // weight addresses do not depend on the ids: fetch them early
           // the previous (layer, token) output is complete before these ids are read
           if (pass > 0) wait_count(p.bar, 2u * pass * n, &abort_s, p.err);
-          wpr = p.layers[l];
-          const int32_t *ids = p.ids + (static_cast<int64_t>(l) * p.m + t) * ks;
-          for (int k = 0; k < s.top_k; ++k) ids_pr[k] = ids[k];
           stop_pr = flag_abort(&abort_s);
         }
-        producer_sync();
+        producer_sync();      // orders every lane's id loads after lane 0's acquire
         if (stop_pr) break;
+        {
+          const int32_t *ids = p.ids + (static_cast<int64_t>(l) * p.m + t) * ks;
+          for (int k = pl; k < s.top_k; k += kProducers) ids_pr[k] = ids[k];
+        }
+        producer_sync();
         produce_a<BR, BSH>(s, wpr, p.plan.geo_r, p.plan.geo_s, ids_pr, r, pl, pol);
         produce_b(s, wpr, p.plan.geo_b, ids_pr, r, pl, pol);
       }
@@ -128,7 +132,7 @@ __global__ void __launch_bounds__(kThreads, 1) fused_kernel(const StackParams p)
     return;
   }
 
-  int bufa = 0, bufb = 0, pass = 0;
+  int pass = 0;
   for (int l = 0; l < p.L; ++l) {
     if (tid == 0) wl = p.layers[l];
     consumer_sync(kConsumers);
@@ -136,18 +140,16 @@ __global__ void __launch_bounds__(kThreads, 1) fused_kernel(const StackParams p)
     for (int t = 0; t < p.m; ++t, ++pass) {
       const int64_t tok = static_cast<int64_t>(l) * p.m + t;
       const int32_t *ids = p.ids + tok * ks;
+      // The residual is an input (layer 0) or the previous layer's output, complete since the
+      // last grid barrier: fetch it now, off the path between the two phases.
+      if (l == 0)
+        load_resid_rows(s, static_cast<const char *>(p.resid0) + t * xs * (p.resid0_f32 ? 4 : 2),
+                        p.resid0_f32, resid_s, tid);
+      else
+        load_resid_rows(s, ((l - 1) & 1 ? p.ping1 : p.ping0) + t * xs, 1, resid_s, tid);
       consume_a<BR, BSH>(s, w, p.plan.geo_r, p.plan.geo_s, p.x + tok * xs, ids, p.scores + tok * ks,
-                         p.act, p.err, r, bufa, sma, tid);
+                         p.act, p.err, r, sm.a, tid);
       consumers_grid_barrier(p.bar, (2u * pass + 1u) * n, tid, &abort_s, p.err);
-      const void *resid;
-      int resid_f32;
-      if (l == 0) {
-        resid = static_cast<const char *>(p.resid0) + t * xs * (p.resid0_f32 ? 4 : 2);
-        resid_f32 = p.resid0_f32;
-      } else {
-        resid = ((l - 1) & 1 ? p.ping1 : p.ping0) + t * xs;
-        resid_f32 = 1;
-      }
       void *out;
       int out_f32;
       if (l == p.L - 1) {
@@ -157,8 +159,7 @@ __global__ void __launch_bounds__(kThreads, 1) fused_kernel(const StackParams p)
         out = (l & 1 ? p.ping1 : p.ping0) + t * xs;
         out_f32 = 1;
       }
-      consume_b<BD, BSH>(s, w, p.plan.geo_b, ids, p.act, resid, resid_f32, out, out_f32, p.err, r,
-                         bufb, smb, tid);
+      consume_b<BD, BSH>(s, p.plan.geo_b, ids, p.act, resid_s, out, out_f32, p.err, r, sm.b, tid);
       if (!(l == p.L - 1 && t == p.m - 1))
         consumers_grid_barrier(p.bar, (2u * pass + 2u) * n, tid, &abort_s, p.err);
     }
@@ -312,19 +313,30 @@ cudaError_t launch_fused(const StackParams &p, int grid, cudaStream_t stream) {
   return cudaErrorInvalidValue;
 }
 
-cudaError_t prepare_kernels(int smem_optin, int bits_gu, int bits_d, int bits_sh) {
-  // The attribute is global to a kernel instance: set it to the device's opt-in maximum so one
-  // handle can never lower it below what another handle launches with.
+cudaError_t prepare_kernels(int smem_optin, int bits_gu, int bits_d, int bits_sh,
+                            int *dyn_limit) {
+  // The attribute is global to a kernel instance: set it to the most the device allows next to
+  // the kernel's static shared memory, so one handle can never lower it below what another
+  // handle launches with.  *dyn_limit is the smallest of the three kernels' limits.
   cudaError_t e = cudaSuccess;
-  const auto attr = cudaFuncAttributeMaxDynamicSharedMemorySize;
+  int lim = smem_optin;
+  auto set = [&](const void *fn) {
+    cudaFuncAttributes fa;
+    e = cudaFuncGetAttributes(&fa, fn);
+    if (e != cudaSuccess) return;
+    const int dyn = smem_optin - static_cast<int>(fa.sharedSizeBytes);
+    if (dyn < lim) lim = dyn;
+    e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, dyn);
+  };
   MOE_BITS_SWITCH(bits_gu, BR, MOE_BITS_SWITCH(bits_sh, BS,
-      e = cudaFuncSetAttribute(gate_up_kernel<BR, BS>, attr, smem_optin)));
+      set(reinterpret_cast<const void *>(gate_up_kernel<BR, BS>))));
   if (e != cudaSuccess) return e;
   MOE_BITS_SWITCH(bits_d, BD, MOE_BITS_SWITCH(bits_sh, BSD,
-      e = cudaFuncSetAttribute(down_kernel<BD, BSD>, attr, smem_optin)));
+      set(reinterpret_cast<const void *>(down_kernel<BD, BSD>))));
   if (e != cudaSuccess) return e;
   MOE_BITS_SWITCH(bits_gu, BR, MOE_BITS_SWITCH(bits_d, BD, MOE_BITS_SWITCH(bits_sh, BSH,
-      e = cudaFuncSetAttribute(fused_kernel<BR, BD, BSH>, attr, smem_optin))));
+      set(reinterpret_cast<const void *>(fused_kernel<BR, BD, BSH>)))));
+  *dyn_limit = lim;
   return e;
 }
 

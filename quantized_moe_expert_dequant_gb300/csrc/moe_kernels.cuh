@@ -116,7 +116,8 @@ bool make_plan(const LayerShape &s, int bits_gu, int bits_d, int bits_sh, Plan *
 cudaError_t launch_gate_up(const GateUpParams &p, int grid, cudaStream_t stream, bool pdl);
 cudaError_t launch_down(const DownParams &p, int grid, cudaStream_t stream, bool pdl);
 cudaError_t launch_fused(const StackParams &p, int grid, cudaStream_t stream);
-cudaError_t prepare_kernels(int smem_optin, int bits_gu, int bits_d, int bits_sh);
+// Sets the kernels' dynamic shared-memory limits; *dyn_limit = the dynamic bytes all three allow.
+cudaError_t prepare_kernels(int smem_optin, int bits_gu, int bits_d, int bits_sh, int *dyn_limit);
 int fused_grid_limit(const Plan &plan, int bits_gu, int bits_d, int bits_sh);
 cudaError_t launch_unpack(const uint8_t *packed, int64_t rows, int64_t cols, int bits,
                           uint8_t *codes, cudaStream_t stream);

@@ -362,27 +362,63 @@ __device__ void produce_a(const LayerShape &s, const LayerPtrs &w, const GateUpG
                         lane, pol);
 }
 
-// Stages per reduction: consumers accumulate the partial sums of kPair consecutive stages and
-// reduce them together, so the reduction, the barrier and the finalize run once per pair.
-constexpr int kPair = 2;
+// Scratch of the consumer side of both phases.  Per-row partial sums are reduced within a warp as
+// soon as a stage is consumed, parked in shared memory (one slot per row and warp), and summed
+// across warps once per batch of rows, so warps run through the stages independently and the
+// only block-wide synchronisation in a phase is the final one.
+constexpr int kRedA = 1024;   // phase A: parked partial sums per kind (gate, up)
+constexpr int kBatchA = 256;  // phase A: rows parked before a flush, at most
 
-// Scratch of the consumer side of phase A.
 struct SmemA {
-  float red[2][kPair][2][32];  // [buffer][stage in pair][gate/up][row * warps-per-group + slot]
+  float red[2][kRedA];        // [gate/up][held row * warps-per-group + warp slot]
+  int row_u[kBatchA];         // act index of each held row
+  float coef[kBatchA];        // its coefficient: the slot's score or the shared scalar
   float stat[kConsumerWarps];
   int ids[kMaxTopK];
-  float coef[kMaxTopK];
+  float scoef[kMaxTopK];
 };
 
+struct SmemB {
+  float red[kMaxRowsB * kConsumerWarps];  // [row - first row][warp slot]
+  int ids[kMaxTopK];
+};
+
+// Phase A and phase B never hold scratch at the same time (a grid barrier or a kernel boundary
+// separates them), so they share it.
+union SmemAB {
+  SmemA a;
+  SmemB b;
+};
+
+// Sums the parked partials of the held rows across warps (fixed order) and writes the
+// activations.  `trailing` adds the barrier that frees the buffer for reuse.
+__device__ __forceinline__ void flush_a(SmemA &sm, int held, int wpg, float *act, int tid,
+                                        bool trailing) {
+  consumer_sync(kConsumers);
+  for (int t = tid; t < held; t += kConsumers) {
+    float gs = 0.f, us = 0.f;
+    for (int w = 0; w < wpg; ++w) {
+      gs += sm.red[0][t * wpg + w];
+      us += sm.red[1][t * wpg + w];
+    }
+    act[sm.row_u[t]] = sm.coef[t] * (silu_f(gs) * us);
+  }
+  if (trailing) consumer_sync(kConsumers);
+}
+
+// Consumes the chunks of one class (routed slots or shared experts) of a CTA's phase A rows.
+// Returns the number of rows still parked, which the caller flushes (the two classes may have
+// different warps per row, so a batch never mixes them).
 template <int BITS>
-__device__ void consume_a_class(const LayerShape &s, const GateUpGeom &g, const ProjDev &gate,
-                                const ProjDev &up, bool shared_class, int64_t a, int64_t b,
-                                int64_t base_u, int rows_pe, const uint16_t *x, float *act,
-                                float shared_scalar, Ring &r, int &buf, SmemA &sm, int tid) {
+__device__ int consume_a_class(const LayerShape &s, const GateUpGeom &g, bool shared_class,
+                               int64_t a, int64_t b, int64_t base_u, int rows_pe,
+                               const uint16_t *x, float *act, float shared_scalar, Ring &r,
+                               SmemA &sm, int tid) {
   constexpr int C = Fmt<BITS>::kCodes, VEC = Fmt<BITS>::kVecs;
   constexpr int RPT = rows_per_thread_a<BITS>();
-  constexpr int VS = 2 * RPT;        // values per stage: gate and up of RPT rows
-  constexpr int V = kPair * VS;
+  constexpr int V = 2 * RPT;        // values per stage: gate and up of RPT rows
+  int held = 0;
+  if (a >= b) return held;
   const int warp = tid >> 5, lane = tid & 31;
   const int G = s.din / kGroup;
   const int my_group = tid / g.tpr, my_step = tid % g.tpr;
@@ -394,122 +430,103 @@ __device__ void consume_a_class(const LayerShape &s, const GateUpGeom &g, const 
   int S;
   load_x_regs<BITS>(x, my_step * C, active, xs, xsum, S);
   const float twoS = pow2f(S);
-  const int grp = (my_step * C) / kGroup;
+  const int code_off = my_step * 16 * VEC;          // the thread's step inside a row
+  const int win_off = ((my_step * C) / kGroup) * 2;  // its group's scale inside a row's run
+  // after the transpose-reduction, lane l holds value idx of the stage
+  const int idx = (lane >> (5 - Log2<V>::v)) & (V - 1);
+  const bool writer = grp_ok && (lane & ((32 / V) - 1)) == 0;
+  const int w_kind = idx / RPT, w_row = (idx % RPT) * g.groups + my_group;
+  const int cap = kRedA / wpg < kBatchA ? kRedA / wpg : kBatchA;
 
   ChunkIterA it(a, b, base_u, rows_pe, g.R);
-  ChunkA c, cs[kPair];
-  bool more = it.next(c);
-  while (more) {
+  ChunkA c;
+  while (it.next(c)) {
+    const int e = shared_class ? c.k : sm.ids[c.k];
+    if (!shared_class && (e < 0 || e >= s.n_experts)) {   // the slot contributes nothing
+      for (int t = tid; t < c.n; t += kConsumers) act[c.u + t] = 0.f;
+      continue;
+    }
+    if (held + c.n > cap) {
+      flush_a(sm, held, wpg, act, tid, true);
+      held = 0;
+    }
+    if (tid < c.n) {
+      sm.row_u[held + tid] = c.u + tid;
+      sm.coef[held + tid] = shared_class ? shared_scalar : sm.scoef[c.k];
+    }
+    const int st = r.i % r.nst;
+    const bool ok = warp_wait_full(r, st, lane);
+    const uint8_t *sb = r.base + static_cast<size_t>(st) * r.stage_bytes;
+    // The four scale/bias windows start at the 16-B boundary below the chunk's first group; the
+    // arrays are 16-B aligned, so the offset of that group is (row * G mod 8) halves.
+    const uint32_t delta = ((static_cast<uint32_t>(e) * rows_pe + c.j) * G & 7u) * 2u;
+    const uint8_t *ws = sb + 2 * g.R * g.rb + delta + win_off;
     float v[V];
 #pragma unroll
     for (int q = 0; q < V; ++q) v[q] = 0.f;
-    int np = 0;
-    while (more && np < kPair) {
-      const int e = shared_class ? c.k : sm.ids[c.k];
-      if (!shared_class && (e < 0 || e >= s.n_experts)) {   // the slot contributes nothing
-        for (int t = tid; t < c.n; t += kConsumers) act[c.u + t] = 0.f;
-        more = it.next(c);
-        continue;
-      }
-      const int st = r.i % r.nst;
-      const bool ok = warp_wait_full(r, st, lane);
-      const uint8_t *sb = r.base + static_cast<size_t>(st) * r.stage_bytes;
-      const int64_t row = static_cast<int64_t>(e) * rows_pe + c.j;
-      const uint8_t *wb = sb + 2 * g.R * g.rb;
-      if (active && ok) {
-        const int off0 = grp * 2;
-        const uint8_t *ps0 = wb + 0 * g.sw + window_of(gate.scales + row * G, 0).delta + off0;
-        const uint8_t *pb0 = wb + 1 * g.sw + window_of(gate.biases + row * G, 0).delta + off0;
-        const uint8_t *ps1 = wb + 2 * g.sw + window_of(up.scales + row * G, 0).delta + off0;
-        const uint8_t *pb1 = wb + 3 * g.sw + window_of(up.biases + row * G, 0).delta + off0;
+    if (active && ok) {
 #pragma unroll
-        for (int q = 0; q < RPT; ++q) {
-          const int rr = q * g.groups + my_group;
-          if (rr < c.n) {
-            uint4 cg[VEC], cu[VEC];
-            const uint8_t *pg = sb + rr * g.rb + my_step * 16 * VEC;
-            const uint8_t *pu = pg + g.R * g.rb;
+      for (int q = 0; q < RPT; ++q) {
+        const int rr = q * g.groups + my_group;
+        if (rr < c.n) {
+          uint4 cg[VEC], cu[VEC];
+          const uint8_t *pg = sb + rr * g.rb + code_off;
+          const uint8_t *pu = pg + g.R * g.rb;
 #pragma unroll
-            for (int w = 0; w < VEC; ++w) {
-              cg[w] = lds_u4(pg + 16 * w);
-              cu[w] = lds_u4(pu + 16 * w);
-            }
-            const float dg = step_dot_regs<BITS>(cg, xs);
-            const float du = step_dot_regs<BITS>(cu, xs);
-            const int off = rr * G * 2;
-            // np is 0 or 1: select the slot with a compile-time index
-            const float vg = fmaf(lds_half(ps0 + off), dg * twoS, lds_half(pb0 + off) * xsum);
-            const float vu = fmaf(lds_half(ps1 + off), du * twoS, lds_half(pb1 + off) * xsum);
-            if (np == 0) {
-              v[q] = vg;
-              v[RPT + q] = vu;
-            } else {
-              v[VS + q] = vg;
-              v[VS + RPT + q] = vu;
-            }
+          for (int w = 0; w < VEC; ++w) {
+            cg[w] = lds_u4(pg + 16 * w);
+            cu[w] = lds_u4(pu + 16 * w);
           }
+          const float dg = step_dot_regs<BITS>(cg, xs);
+          const float du = step_dot_regs<BITS>(cu, xs);
+          const uint8_t *wr = ws + rr * G * 2;
+          v[q] = fmaf(lds_half(wr), dg * twoS, lds_half(wr + g.sw) * xsum);
+          v[RPT + q] = fmaf(lds_half(wr + 2 * g.sw), du * twoS, lds_half(wr + 3 * g.sw) * xsum);
         }
       }
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&r.empty[st]);
-      cs[np++] = c;
-      ++r.i;
-      more = it.next(c);
     }
-    if (np == 0) break;   // only slots with invalid ids were left
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&r.empty[st]);
+    ++r.i;
     const float val = warp_transpose_reduce<V>(v, lane);
-    const int idx = (lane >> (5 - Log2<V>::v)) & (V - 1);
-    if (grp_ok && (lane & ((32 / V) - 1)) == 0) {
-      const int pp = idx / VS, kind = (idx % VS) / RPT, q = idx % RPT;
-      const int rr = q * g.groups + my_group;
-      if (pp < np && rr < cs[pp].n) sm.red[buf][pp][kind][rr * wpg + wslot] = val;
-    }
-    consumer_sync(kConsumers);
-    const int n0 = cs[0].n, nt = n0 + (np > 1 ? cs[1].n : 0);
-    if (tid < nt) {
-      const int pp = tid < n0 ? 0 : 1, rr = tid - (pp ? n0 : 0);
-      float gsum = 0.f, usum = 0.f;
-      for (int w = 0; w < wpg; ++w) {
-        gsum += sm.red[buf][pp][0][rr * wpg + w];
-        usum += sm.red[buf][pp][1][rr * wpg + w];
-      }
-      const float coef = shared_class ? shared_scalar : sm.coef[cs[pp].k];
-      act[cs[pp].u + rr] = coef * (silu_f(gsum) * usum);
-    }
-    buf ^= 1;
+    if (writer && w_row < c.n) sm.red[w_kind][(held + w_row) * wpg + wslot] = val;
+    held += c.n;
   }
+  return held;
 }
 
 // Consumers of phase A for one token of one layer.  ids/scores/x are read here (after whatever
-// wait made them complete).  Leaves a consumer_sync-free tail: callers synchronise as needed.
+// wait made them complete).  Ends with the activations written and a consumer_sync-free tail:
+// callers synchronise as needed.
 template <int BR, int BS>
 __device__ void consume_a(const LayerShape &s, const LayerPtrs &w, const GateUpGeom &gr,
                           const GateUpGeom &gs, const uint16_t *x, const int32_t *ids,
-                          const float *scores, float *act, int32_t *err, Ring &r, int &buf,
-                          SmemA &sm, int tid) {
+                          const float *scores, float *act, int32_t *err, Ring &r, SmemA &sm,
+                          int tid) {
   const int warp = tid >> 5, lane = tid & 31;
   for (int k = tid; k < s.top_k; k += kConsumers) {
     sm.ids[k] = ids[k];
-    sm.coef[k] = scores[k];
+    sm.scoef[k] = scores[k];
   }
   float shared_scalar = 1.0f;
   if (w.gate_vec != nullptr && s.n_shared > 0) {
     float dot = 0.f;
     for (int c = tid; c < s.din; c += kConsumers)
       dot = fmaf(bf16_to_float(x[c]), bf16_to_float(w.gate_vec[c]), dot);
-    dot = consumers_sum(dot, sm.stat, warp, lane);   // also publishes sm.ids / sm.coef
+    dot = consumers_sum(dot, sm.stat, warp, lane);   // also publishes sm.ids / sm.scoef
     shared_scalar = 1.0f / (1.0f + expf(-dot));
   } else {
-    consumer_sync(kConsumers);                       // publishes sm.ids / sm.coef
+    consumer_sync(kConsumers);                       // publishes sm.ids / sm.scoef
   }
   if (tid == 0)
     for (int k = 0; k < s.top_k; ++k)
       if (sm.ids[k] < 0 || sm.ids[k] >= s.n_experts) atomicOr(err, kDevErrBadId);
   const RangeA ra = range_a(s);
-  consume_a_class<BR>(s, gr, w.gate, w.up, false, ra.ra, ra.rb, 0, s.dff, x, act, 1.f, r, buf,
-                      sm, tid);
-  consume_a_class<BS>(s, gs, w.sh_gate, w.sh_up, true, ra.sa, ra.sb, ra.Ur, s.dff_shared, x, act,
-                      shared_scalar, r, buf, sm, tid);
+  int held = consume_a_class<BR>(s, gr, false, ra.ra, ra.rb, 0, s.dff, x, act, 1.f, r, sm, tid);
+  if (held > 0) flush_a(sm, held, gr.tpr / 32, act, tid, ra.sa < ra.sb);
+  held = consume_a_class<BS>(s, gs, true, ra.sa, ra.sb, ra.Ur, s.dff_shared, x, act,
+                             shared_scalar, r, sm, tid);
+  if (held > 0) flush_a(sm, held, gs.tpr / 32, act, tid, false);
 }
 
 // ================================================================== phase B
@@ -591,12 +608,6 @@ __device__ void produce_b(const LayerShape &s, const LayerPtrs &w, const DownGeo
   }
 }
 
-struct SmemB {
-  float red[2][kPair][64];  // [buffer][stage in pair][row * warps-per-group + warp slot]
-  int ids[kMaxTopK];
-  float resid[kMaxRowsB];   // the CTA's residual rows, loaded once per phase
-};
-
 template <int BITS, int CMAX>
 __device__ __forceinline__ float down_step(const uint8_t *codes, const float (&as)[CMAX]) {
   constexpr int VEC = Fmt<BITS>::kVecs;
@@ -606,24 +617,31 @@ __device__ __forceinline__ float down_step(const uint8_t *codes, const float (&a
   return step_dot_regs<BITS>(cv, as);
 }
 
-// Consumers of phase B for one token: act must be complete (the caller waited for phase A).
+// The CTA's residual rows of phase B into shared memory (the tail adds them).  The residual may
+// be read at any time during the layer: it is an input or the previous layer's complete output.
+__device__ __forceinline__ void load_resid_rows(const LayerShape &s, const void *resid,
+                                                int resid_f32, float *dst, int tid) {
+  int i0, i1;
+  range_b(s, i0, i1);
+  for (int t = tid; t < i1 - i0; t += kConsumers)
+    dst[t] = resid_f32 ? static_cast<const float *>(resid)[i0 + t]
+                       : bf16_to_float(static_cast<const uint16_t *>(resid)[i0 + t]);
+}
+
+// Consumers of phase B for one token: act must be complete (the caller waited for phase A) and
+// resid_s must hold the CTA's residual rows (load_resid_rows, before a consumer_sync).
 template <int BD, int BSD>
-__device__ void consume_b(const LayerShape &s, const LayerPtrs &w, const DownGeom &g,
-                          const int32_t *ids, const float *act, const void *resid, int resid_f32,
-                          void *out, int out_f32, int32_t *err, Ring &r, int &buf, SmemB &sm,
-                          int tid) {
+__device__ void consume_b(const LayerShape &s, const DownGeom &g, const int32_t *ids,
+                          const float *act, const float *resid_s, void *out, int out_f32,
+                          int32_t *err, Ring &r, SmemB &sm, int tid) {
   constexpr int CR = Fmt<BD>::kCodes, CS = Fmt<BSD>::kCodes;
   constexpr int CMAX = CR > CS ? CR : CS;
   constexpr int SPTMAX = kMaxActRegs / CMAX > 0 ? kMaxActRegs / CMAX : 1;
   constexpr int VS = 4;             // rows per thread per stage, at most
-  constexpr int V = kPair * VS;
   const int warp = tid >> 5, lane = tid & 31;
   for (int k = tid; k < s.top_k; k += kConsumers) sm.ids[k] = ids[k];
   int i0, i1;
   range_b(s, i0, i1);
-  for (int t = tid; t < i1 - i0; t += kConsumers)
-    sm.resid[t] = resid_f32 ? static_cast<const float *>(resid)[i0 + t]
-                            : bf16_to_float(static_cast<const uint16_t *>(resid)[i0 + t]);
   const int my_group = tid / g.tpr, my_step = tid % g.tpr;
   const bool grp_ok = my_group < g.groups;
   const int wpg = g.tpr / 32;
@@ -675,91 +693,83 @@ __device__ void consume_b(const LayerShape &s, const LayerPtrs &w, const DownGeo
       as[i][c] *= pow2f(149 - S - o);
     }
   }
-  consumer_sync(kConsumers);   // publishes sm.ids and sm.resid
-  int grp[SPTMAX];
-  bool seg_ok[SPTMAX];
-#pragma unroll
-  for (int i = 0; i < SPTMAX; ++i) {
-    grp[i] = (jst[i] * (shr[i] ? CS : CR)) / kGroup;
-    seg_ok[i] =
-        own[i] && (seg[i] >= s.top_k || (sm.ids[seg[i]] >= 0 && sm.ids[seg[i]] < s.n_experts));
-  }
+  consumer_sync(kConsumers);   // publishes sm.ids
   if (tid == 0)
     for (int k = 0; k < s.top_k; ++k)
       if (sm.ids[k] < 0 || sm.ids[k] >= s.n_experts) atomicOr(err, kDevErrBadId);
-  const int wins = s.top_k * g.sw_r + s.n_shared * g.sw_s;
-  const int rpt = g.R / g.groups;
 
-  int r0 = i0;
-  while (r0 < i1) {
-    float acc[V];
+  // Per-thread constants of each owned step: where its codes and its group's scale/bias sit in
+  // a stage, and the low bits of its expert's first row (for the window offset).
+  const int wins = s.top_k * g.sw_r + s.n_shared * g.sw_s;
+  bool seg_ok[SPTMAX];
+  int cbase[SPTMAX], sbase[SPTMAX], rbs[SPTMAX], Gs[SPTMAX];
+  uint32_t rowbase[SPTMAX];
 #pragma unroll
-    for (int q = 0; q < V; ++q) acc[q] = 0.f;
-    int np = 0, rows0 = 0, nrows[kPair] = {0, 0}, base_row[kPair] = {0, 0};
-    while (r0 < i1 && np < kPair) {
-      const int n = (i1 - r0) < g.R ? (i1 - r0) : g.R;
-      const int st = r.i % r.nst;
-      const bool ok = warp_wait_full(r, st, lane);
-      const uint8_t *sb = r.base + static_cast<size_t>(st) * r.stage_bytes;
-      const uint8_t *wb = sb + g.codes_bytes;
-      if (ok) {
+  for (int i = 0; i < SPTMAX; ++i) {
+    const bool routed = seg[i] < s.top_k;
+    const int e = routed ? sm.ids[seg[i]] : seg[i] - s.top_k;
+    seg_ok[i] = own[i] && (!routed || (e >= 0 && e < s.n_experts));
+    const int t = seg[i] - s.top_k;
+    const int code_off = routed ? seg[i] * g.R * g.rb_r : s.top_k * g.R * g.rb_r + t * g.R * g.rb_s;
+    const int win_off = routed ? seg[i] * g.sw_r : s.top_k * g.sw_r + t * g.sw_s;
+    const int C = shr[i] ? CS : CR;
+    cbase[i] = code_off + jst[i] * 16 * (shr[i] ? Fmt<BSD>::kVecs : Fmt<BD>::kVecs);
+    sbase[i] = win_off + ((jst[i] * C) / kGroup) * 2;
+    rbs[i] = routed ? g.rb_r : g.rb_s;
+    Gs[i] = routed ? g.G_r : g.G_s;
+    rowbase[i] = static_cast<uint32_t>(e) * static_cast<uint32_t>(s.din);
+  }
+  const int rpt = g.R / g.groups;
+  // after the transpose-reduction, lane l holds the sum of row slot q_w
+  const int q_w = (lane >> (5 - Log2<VS>::v)) & (VS - 1);
+  const bool writer = grp_ok && (lane & ((32 / VS) - 1)) == 0;
+  const int w_row = q_w * g.groups + my_group;
+
+  for (int r0 = i0; r0 < i1; r0 += g.R) {
+    const int n = (i1 - r0) < g.R ? (i1 - r0) : g.R;
+    const int st = r.i % r.nst;
+    const bool ok = warp_wait_full(r, st, lane);
+    const uint8_t *sb = r.base + static_cast<size_t>(st) * r.stage_bytes;
+    const uint8_t *wb = sb + g.codes_bytes;
+    float acc[VS];
 #pragma unroll
-        for (int i = 0; i < SPTMAX; ++i) {
-          if (!seg_ok[i]) continue;
-          const SegB sg = seg_b(s, w, g, seg[i] < s.top_k ? sm.ids[seg[i]] : 0, seg[i]);
-          const int64_t row0 = sg.expert * s.din + r0;
-          const uint8_t *cp =
-              sb + sg.code_off + jst[i] * 16 * (shr[i] ? Fmt<BSD>::kVecs : Fmt<BD>::kVecs);
-          const uint8_t *sp =
-              wb + sg.win_off + window_of(sg.pr->scales + row0 * sg.G, 0).delta + grp[i] * 2;
-          const uint8_t *bp = wb + wins + sg.win_off +
-                              window_of(sg.pr->biases + row0 * sg.G, 0).delta + grp[i] * 2;
+    for (int q = 0; q < VS; ++q) acc[q] = 0.f;
+    if (ok) {
 #pragma unroll
-          for (int q = 0; q < VS; ++q) {
-            const int rr = q * g.groups + my_group;
-            if (q < rpt && rr < n) {
-              const float d = shr[i] ? down_step<BSD, CMAX>(cp + rr * sg.rb, as[i])
-                                     : down_step<BD, CMAX>(cp + rr * sg.rb, as[i]);
-              const int off = rr * sg.G * 2;
-              const float t = fmaf(lds_half(sp + off), d * twoS[i], lds_half(bp + off) * asum[i]);
-              if (np == 0)
-                acc[q] += t;
-              else
-                acc[VS + q] += t;
-            }
+      for (int i = 0; i < SPTMAX; ++i) {
+        if (!seg_ok[i]) continue;
+        // windows start at the 16-B boundary below the first group of row r0 (arrays 16-B
+        // aligned), so the group sits (row * G mod 8) halves in
+        const uint32_t delta = (((rowbase[i] + r0) * static_cast<uint32_t>(Gs[i])) & 7u) * 2u;
+        const uint8_t *cp = sb + cbase[i];
+        const uint8_t *sp = wb + sbase[i] + delta;
+#pragma unroll
+        for (int q = 0; q < VS; ++q) {
+          const int rr = q * g.groups + my_group;
+          if (q < rpt && rr < n) {
+            const float d = shr[i] ? down_step<BSD, CMAX>(cp + rr * rbs[i], as[i])
+                                   : down_step<BD, CMAX>(cp + rr * rbs[i], as[i]);
+            const uint8_t *wr = sp + rr * Gs[i] * 2;
+            acc[q] += fmaf(lds_half(wr), d * twoS[i], lds_half(wr + wins) * asum[i]);
           }
         }
       }
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&r.empty[st]);
-      nrows[np] = n;
-      base_row[np] = rows0;
-      rows0 += n;
-      ++np;
-      ++r.i;
-      r0 += n;
     }
-    const float val = warp_transpose_reduce<V>(acc, lane);
-    const int idx = (lane >> (5 - Log2<V>::v)) & (V - 1);
-    if (grp_ok && (lane & ((32 / V) - 1)) == 0) {
-      const int pp = idx / VS, q = idx % VS;
-      const int rr = q * g.groups + my_group;
-      if (pp < np && q < rpt && rr < nrows[pp]) sm.red[buf][pp][rr * wpg + wslot] = val;
-    }
-    consumer_sync(kConsumers);
-    if (tid < rows0) {
-      const int pp = tid < nrows[0] ? 0 : 1, rr = tid - (pp ? nrows[0] : 0);
-      float sum = 0.f;
-      for (int ww = 0; ww < wpg; ++ww) sum += sm.red[buf][pp][rr * wpg + ww];
-      const int i = r0 - rows0 + tid;   // first row of the pair + tid
-      const float o = sm.resid[i - i0] + sum;
-      if (out_f32)
-        static_cast<float *>(out)[i] = o;
-      else
-        static_cast<uint16_t *>(out)[i] = float_to_bf16_rn(o);
-    }
-    (void)base_row;
-    buf ^= 1;
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&r.empty[st]);
+    ++r.i;
+    const float val = warp_transpose_reduce<VS>(acc, lane);
+    if (writer && q_w < rpt && w_row < n) sm.red[(r0 - i0 + w_row) * wpg + wslot] = val;
+  }
+  consumer_sync(kConsumers);
+  for (int t = tid; t < i1 - i0; t += kConsumers) {
+    float sum = 0.f;
+    for (int ww = 0; ww < wpg; ++ww) sum += sm.red[t * wpg + ww];
+    const float o = resid_s[t] + sum;
+    if (out_f32)
+      static_cast<float *>(out)[i0 + t] = o;
+    else
+      static_cast<uint16_t *>(out)[i0 + t] = float_to_bf16_rn(o);
   }
 }
 
