@@ -31,72 +31,79 @@ __device__ __forceinline__ void init_ring(uint64_t *full, uint64_t *empty, int n
   }
 }
 
+// Shared state of the stage ring besides the stages themselves.
+struct RingSmem {
+  uint64_t full[kMaxStages];
+  uint64_t empty[kMaxStages];
+  StageDesc desc[kMaxStages];
+  int cnt[2];              // phase A chunks of the current token: routed, shared
+  int ids[kMaxTopK];       // the producer's copy of the current token's expert ids
+  float scores[kMaxTopK];  // and scores
+  int abort;
+};
+
 template <int BR, int BS>
 __global__ void __launch_bounds__(kThreads, 1) gate_up_kernel(const GateUpParams p) {
   extern __shared__ __align__(128) uint8_t ring[];
-  __shared__ __align__(8) uint64_t full[kMaxStages];
-  __shared__ __align__(8) uint64_t empty[kMaxStages];
+  __shared__ __align__(16) RingSmem rs;
   __shared__ SmemA sm;
-  __shared__ int abort_s;
-  init_ring(full, empty, p.plan.nst, &abort_s);
+  init_ring(rs.full, rs.empty, p.plan.nst, &rs.abort);
   // Token data (x, ids, scores) may come from the previous kernel on the stream.
   pdl_wait();
   pdl_launch_dependents();
   __syncthreads();
-  Ring r{full, empty, ring, p.plan.nst, p.plan.stage_bytes, 0, &abort_s, p.err};
+  Ring r = make_ring(rs.full, rs.empty, ring, rs.desc, p.plan, &rs.abort, p.err);
   const int tid = threadIdx.x, warp = tid >> 5;
   if (warp >= kConsumerWarps) {
-    produce_a<BR, BS>(p.s, p.w, p.plan.geo_r, p.plan.geo_s, p.ids, r, tid - kConsumers,
+    const int pl = tid - kConsumers;
+    producer_load_token(p.s, p.ids, p.scores, rs.ids, rs.scores, p.err, pl);
+    produce_a<BR, BS>(p.s, p.w, p.plan.geo_r, p.plan.geo_s, rs.ids, rs.scores, rs.cnt, r, pl,
                       policy_evict_first());
-    ring_drain(r, tid - kConsumers);
+    ring_drain(r, pl);
     return;
   }
-  consume_a<BR, BS>(p.s, p.w, p.plan.geo_r, p.plan.geo_s, p.x, p.ids, p.scores, p.act, p.err, r,
-                    sm, tid);
+  consume_a<BR, BS>(p.s, p.w, p.plan.geo_r, p.plan.geo_s, p.x, rs.cnt, p.act, r, sm, tid);
 }
 
 template <int BD, int BSD>
 __global__ void __launch_bounds__(kThreads, 1) down_kernel(const DownParams p) {
   extern __shared__ __align__(128) uint8_t ring[];
-  __shared__ __align__(8) uint64_t full[kMaxStages];
-  __shared__ __align__(8) uint64_t empty[kMaxStages];
+  __shared__ __align__(16) RingSmem rs;
   __shared__ SmemB sm;
   __shared__ float resid_s[kMaxRowsB];
-  __shared__ int abort_s;
-  init_ring(full, empty, p.plan.nst, &abort_s);
+  init_ring(rs.full, rs.empty, p.plan.nst, &rs.abort);
   pdl_launch_dependents();
   __syncthreads();
-  Ring r{full, empty, ring, p.plan.nst, p.plan.stage_bytes, 0, &abort_s, p.err};
+  Ring r = make_ring(rs.full, rs.empty, ring, rs.desc, p.plan, &rs.abort, p.err);
   const int tid = threadIdx.x, warp = tid >> 5;
   if (warp >= kConsumerWarps) {
     // The ids were complete before kernel A started (A waits on its predecessor before it lets
     // this kernel launch), so the weight stream may start before the activations are ready.
-    produce_b(p.s, p.w, p.plan.geo_b, p.ids, r, tid - kConsumers, policy_evict_first());
-    ring_drain(r, tid - kConsumers);
+    const int pl = tid - kConsumers;
+    producer_load_token(p.s, p.ids, nullptr, rs.ids, rs.scores, p.err, pl);
+    produce_b(p.s, p.w, p.plan.geo_b, rs.ids, r, pl, policy_evict_first());
+    ring_drain(r, pl);
     return;
   }
   pdl_wait();  // the activations come from kernel A (and, in a stack, resid from the kernel
                // before it)
   load_resid_rows(p.s, p.resid, p.resid_f32, resid_s, tid);
-  consume_b<BD, BSD>(p.s, p.plan.geo_b, p.ids, p.act, resid_s, p.out, p.out_f32, p.err, r, sm,
-                     tid);
+  consumer_sync(kConsumers);  // publishes resid_s
+  consume_b<BD, BSD>(p.s, p.plan.geo_b, rs.ids, p.act, resid_s, p.out, p.out_f32, r, sm, tid);
 }
 
 template <int BR, int BD, int BSH>
 __global__ void __launch_bounds__(kThreads, 1) fused_kernel(const StackParams p) {
   extern __shared__ __align__(128) uint8_t ring[];
-  __shared__ __align__(8) uint64_t full[kMaxStages];
-  __shared__ __align__(8) uint64_t empty[kMaxStages];
+  __shared__ __align__(16) RingSmem rs;
   __shared__ SmemAB sm;
   __shared__ float resid_s[kMaxRowsB];
   __shared__ LayerPtrs wl;   // the consumers' copy of the current layer's pointers
   __shared__ LayerPtrs wpr;  // the producers' copy
-  __shared__ int ids_pr[kMaxTopK];
   __shared__ int stop_pr;
-  __shared__ int abort_s;
-  init_ring(full, empty, p.plan.nst, &abort_s);
+  init_ring(rs.full, rs.empty, p.plan.nst, &rs.abort);
   __syncthreads();
-  Ring r{full, empty, ring, p.plan.nst, p.plan.stage_bytes, 0, &abort_s, p.err};
+  Ring r = make_ring(rs.full, rs.empty, ring, rs.desc, p.plan, &rs.abort, p.err);
   const int tid = threadIdx.x, warp = tid >> 5;
   const LayerShape &s = p.s;
   const uint32_t n = gridDim.x;
@@ -113,18 +120,17 @@ __global__ void __launch_bounds__(kThreads, 1) fused_kernel(const StackParams p)
         if (pl == 0) {
           wpr = p.layers[l];  // weight addresses do not depend on the ids: fetch them early
           // the previous (layer, token) output is complete before these ids are read
-          if (pass > 0) wait_count(p.bar, 2u * pass * n, &abort_s, p.err);
-          stop_pr = flag_abort(&abort_s);
+          if (pass > 0) wait_count(p.bar, 2u * pass * n, &rs.abort, p.err);
+          stop_pr = flag_abort(&rs.abort);
         }
         producer_sync();      // orders every lane's id loads after lane 0's acquire
         if (stop_pr) break;
-        {
-          const int32_t *ids = p.ids + (static_cast<int64_t>(l) * p.m + t) * ks;
-          for (int k = pl; k < s.top_k; k += kProducers) ids_pr[k] = ids[k];
-        }
-        producer_sync();
-        produce_a<BR, BSH>(s, wpr, p.plan.geo_r, p.plan.geo_s, ids_pr, r, pl, pol);
-        produce_b(s, wpr, p.plan.geo_b, ids_pr, r, pl, pol);
+        const int64_t tok = static_cast<int64_t>(l) * p.m + t;
+        producer_load_token(s, p.ids + tok * ks, p.scores + tok * ks, rs.ids, rs.scores, p.err,
+                            pl);
+        produce_a<BR, BSH>(s, wpr, p.plan.geo_r, p.plan.geo_s, rs.ids, rs.scores, rs.cnt, r, pl,
+                           pol);
+        produce_b(s, wpr, p.plan.geo_b, rs.ids, r, pl, pol);
       }
       if (stop_pr) break;
     }
@@ -139,7 +145,6 @@ __global__ void __launch_bounds__(kThreads, 1) fused_kernel(const StackParams p)
     const LayerPtrs &w = wl;
     for (int t = 0; t < p.m; ++t, ++pass) {
       const int64_t tok = static_cast<int64_t>(l) * p.m + t;
-      const int32_t *ids = p.ids + tok * ks;
       // The residual is an input (layer 0) or the previous layer's output, complete since the
       // last grid barrier: fetch it now, off the path between the two phases.
       if (l == 0)
@@ -147,9 +152,9 @@ __global__ void __launch_bounds__(kThreads, 1) fused_kernel(const StackParams p)
                         p.resid0_f32, resid_s, tid);
       else
         load_resid_rows(s, ((l - 1) & 1 ? p.ping1 : p.ping0) + t * xs, 1, resid_s, tid);
-      consume_a<BR, BSH>(s, w, p.plan.geo_r, p.plan.geo_s, p.x + tok * xs, ids, p.scores + tok * ks,
-                         p.act, p.err, r, sm.a, tid);
-      consumers_grid_barrier(p.bar, (2u * pass + 1u) * n, tid, &abort_s, p.err);
+      consume_a<BR, BSH>(s, w, p.plan.geo_r, p.plan.geo_s, p.x + tok * xs, rs.cnt, p.act, r, sm.a,
+                         tid);
+      consumers_grid_barrier(p.bar, (2u * pass + 1u) * n, tid, &rs.abort, p.err);
       void *out;
       int out_f32;
       if (l == p.L - 1) {
@@ -159,9 +164,9 @@ __global__ void __launch_bounds__(kThreads, 1) fused_kernel(const StackParams p)
         out = (l & 1 ? p.ping1 : p.ping0) + t * xs;
         out_f32 = 1;
       }
-      consume_b<BD, BSH>(s, p.plan.geo_b, ids, p.act, resid_s, out, out_f32, p.err, r, sm.b, tid);
+      consume_b<BD, BSH>(s, p.plan.geo_b, rs.ids, p.act, resid_s, out, out_f32, r, sm.b, tid);
       if (!(l == p.L - 1 && t == p.m - 1))
-        consumers_grid_barrier(p.bar, (2u * pass + 2u) * n, tid, &abort_s, p.err);
+        consumers_grid_barrier(p.bar, (2u * pass + 2u) * n, tid, &rs.abort, p.err);
     }
   }
 }

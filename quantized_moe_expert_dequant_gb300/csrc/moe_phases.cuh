@@ -151,15 +151,55 @@ __device__ __forceinline__ void load_x_regs(const uint16_t *x, int c0, bool acti
 __device__ __forceinline__ float silu_f(float z) { return z / (1.0f + expf(-z)); }
 
 // ------------------------------------------------------------------ ring and grid barrier
+// What the producer tells the consumers about a phase-A stage (written before the stage's
+// arrive.expect_tx, whose release makes it visible to every consumer that waited on the stage).
+struct StageDesc {
+  int u;        // act index of the stage's first row
+  int n;        // rows in the stage (0: an empty stage that only carries the phase's counts)
+  float coef;   // the routed slot's score (unused for shared experts)
+  int delta;    // byte offset of the first row's first group inside each scale/bias window
+};
+
 struct Ring {
   uint64_t *full;
   uint64_t *empty;
   uint8_t *base;
+  StageDesc *desc;  // [kMaxStages]
   int nst, stage_bytes;
-  int i;            // chunks this role has handed out (producer) or taken (consumers)
+  int st;           // the next stage this role hands out (producer) or takes (consumers)
+  uint32_t ph;      // the parity of that stage's current use
+  int used;         // stages handed out or taken so far
   int *abort;       // shared flag: a wait timed out, stop waiting
   int32_t *err;
+  __device__ __forceinline__ void advance() {
+    if (++st == nst) {
+      st = 0;
+      ph ^= 1u;
+    }
+    ++used;
+  }
+  __device__ __forceinline__ uint8_t *stage() const {
+    return base + static_cast<size_t>(st) * stage_bytes;
+  }
 };
+
+__device__ __forceinline__ Ring make_ring(uint64_t *full, uint64_t *empty, uint8_t *base,
+                                          StageDesc *desc, const Plan &plan, int *abort,
+                                          int32_t *err) {
+  Ring r;
+  r.full = full;
+  r.empty = empty;
+  r.base = base;
+  r.desc = desc;
+  r.nst = plan.nst;
+  r.stage_bytes = plan.stage_bytes;
+  r.st = 0;
+  r.ph = 0;
+  r.used = 0;
+  r.abort = abort;
+  r.err = err;
+  return r;
+}
 
 __device__ __forceinline__ bool flag_abort(int *abort) {
   return *reinterpret_cast<volatile int *>(abort) != 0;
@@ -186,36 +226,40 @@ __device__ __forceinline__ bool ring_wait(uint64_t *bar, uint32_t parity, int *a
   return true;
 }
 
-// Consumer side: lane 0 of each warp waits for the stage and the warp follows it.  One waiter
-// per warp instead of 32 keeps the barrier word free for the arrivals that complete the phase.
-__device__ __forceinline__ bool warp_wait_full(Ring &r, int st, int lane) {
+// Consumer side: lane 0 of each warp waits for the current stage and the warp follows it.  One
+// waiter per warp instead of 32 keeps the barrier word free for the arrivals that complete it.
+__device__ __forceinline__ bool warp_wait_full(Ring &r, int lane) {
   int ok = 1;
-  if (lane == 0) ok = ring_wait(&r.full[st], (r.i / r.nst) & 1, r.abort, r.err);
+  if (lane == 0) ok = ring_wait(&r.full[r.st], r.ph, r.abort, r.err);
   ok = __shfl_sync(0xffffffffu, ok, 0);
   __syncwarp();
   return ok != 0;
 }
 
+// Consumer side: the warp is done reading the current stage.
+__device__ __forceinline__ void warp_release(Ring &r, int lane) {
+  __syncwarp();
+  if (lane == 0) mbar_arrive(&r.empty[r.st]);
+  r.advance();
+}
 
-// Producer side: claims the next stage (waits until its previous use was released).
 __device__ __forceinline__ uint32_t warp_sum_u32(uint32_t v) {
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
   return v;
 }
 
-__device__ __forceinline__ uint8_t *ring_claim(Ring &r, int lane, int &st, bool &ok) {
-  st = r.i % r.nst;
+// Producer side: claims the current stage (waits until its previous use was released).
+__device__ __forceinline__ bool ring_claim(Ring &r, int lane) {
   int good = 1;
-  if (r.i >= r.nst && lane == 0) good = ring_wait(&r.empty[st], ((r.i / r.nst) - 1) & 1, r.abort, r.err);
-  ok = __shfl_sync(0xffffffffu, good, 0) != 0;
-  return r.base + static_cast<size_t>(st) * r.stage_bytes;
+  if (r.used >= r.nst && lane == 0) good = ring_wait(&r.empty[r.st], r.ph ^ 1u, r.abort, r.err);
+  return __shfl_sync(0xffffffffu, good, 0) != 0;
 }
 
 // Producer side, at exit: the copies into the last use of every stage have landed.
 __device__ __forceinline__ void ring_drain(Ring &r, int lane) {
   if (lane != 0) return;
-  for (int s = r.i - r.nst < 0 ? 0 : r.i - r.nst; s < r.i; ++s)
+  for (int s = r.used - r.nst < 0 ? 0 : r.used - r.nst; s < r.used; ++s)
     mbar_wait(&r.full[s % r.nst], (s / r.nst) & 1);
 }
 
@@ -255,6 +299,22 @@ __device__ __forceinline__ void consumers_grid_barrier(uint32_t *cnt, uint32_t t
     wait_count(cnt, target, abort, err);
   }
   consumer_sync(kConsumers);
+}
+
+// Producer side, at the start of a (layer, token): the expert ids and scores into shared memory
+// (lanes in parallel) and the error bit for ids outside [0, n_experts).  The caller has already
+// waited for whatever makes them complete; the producer_sync after the loads orders them before
+// the producer's first arrive on a stage, which publishes them to the consumers.
+__device__ __forceinline__ void producer_load_token(const LayerShape &s, const int32_t *ids,
+                                                    const float *scores, int *ids_s,
+                                                    float *scores_s, int32_t *err, int lane) {
+  for (int k = lane; k < s.top_k; k += kProducers) {
+    const int e = ids[k];
+    ids_s[k] = e;
+    scores_s[k] = scores != nullptr ? scores[k] : 0.f;
+    if (e < 0 || e >= s.n_experts) atomicOr(err, kDevErrBadId);
+  }
+  producer_sync();
 }
 
 // ================================================================== phase A
@@ -315,21 +375,33 @@ __device__ __forceinline__ RangeA range_a(const LayerShape &s) {
   return r;
 }
 
+// Chunks of one class that carry data (routed chunks of a slot with an invalid id are skipped).
+__device__ __forceinline__ int count_a_class(const LayerShape &s, int R, bool shared_class,
+                                             int64_t a, int64_t b, int64_t base_u, int rows_pe,
+                                             const int *ids) {
+  ChunkIterA it(a, b, base_u, rows_pe, R);
+  ChunkA c;
+  int n = 0;
+  while (it.next(c)) {
+    const int e = shared_class ? c.k : ids[c.k];
+    n += shared_class || (e >= 0 && e < s.n_experts);
+  }
+  return n;
+}
+
 template <int BITS>
 __device__ void produce_a_class(const LayerShape &s, const GateUpGeom &g, const ProjDev &gate,
                                 const ProjDev &up, bool shared_class, int64_t a, int64_t b,
-                                int64_t base_u, int rows_pe, const int32_t *ids, Ring &r, int lane,
-                                uint64_t pol) {
+                                int64_t base_u, int rows_pe, const int *ids, const float *scores,
+                                Ring &r, int lane, uint64_t pol) {
   const int G = s.din / kGroup;
   ChunkIterA it(a, b, base_u, rows_pe, g.R);
   ChunkA c;
   while (it.next(c)) {
     const int e = shared_class ? c.k : ids[c.k];
     if (!shared_class && (e < 0 || e >= s.n_experts)) continue;
-    int st;
-    bool ok;
-    uint8_t *sb = ring_claim(r, lane, st, ok);
-    if (!ok) return;
+    if (!ring_claim(r, lane)) return;
+    uint8_t *sb = r.stage();
     const int64_t row = static_cast<int64_t>(e) * rows_pe + c.j;
     const uint32_t code_bytes = static_cast<uint32_t>(c.n) * g.rb;
     const int64_t ng = static_cast<int64_t>(c.n) * G;
@@ -338,28 +410,51 @@ __device__ void produce_a_class(const LayerShape &s, const GateUpGeom &g, const 
     const Window w2 = window_of(up.scales + row * G, ng);
     const Window w3 = window_of(up.biases + row * G, ng);
     uint8_t *wb = sb + 2 * g.R * g.rb;
-    if (lane == 0)
-      mbar_arrive_expect_tx(&r.full[st], 2 * code_bytes + w0.bytes + w1.bytes + w2.bytes + w3.bytes);
+    if (lane == 0) {
+      r.desc[r.st] = StageDesc{c.u, c.n, shared_class ? 0.f : scores[c.k],
+                               static_cast<int>(w0.delta)};
+      mbar_arrive_expect_tx(&r.full[r.st],
+                            2 * code_bytes + w0.bytes + w1.bytes + w2.bytes + w3.bytes);
+    }
     __syncwarp();
-    if (lane == 0) bulk_g2s(sb, gate.codes + row * g.rb, code_bytes, &r.full[st], pol);
-    if (lane == 1) bulk_g2s(sb + g.R * g.rb, up.codes + row * g.rb, code_bytes, &r.full[st], pol);
-    if (lane == 2) bulk_g2s(wb + 0 * g.sw, w0.src, w0.bytes, &r.full[st], pol);
-    if (lane == 3) bulk_g2s(wb + 1 * g.sw, w1.src, w1.bytes, &r.full[st], pol);
-    if (lane == 4) bulk_g2s(wb + 2 * g.sw, w2.src, w2.bytes, &r.full[st], pol);
-    if (lane == 5) bulk_g2s(wb + 3 * g.sw, w3.src, w3.bytes, &r.full[st], pol);
-    ++r.i;
+    if (lane == 0) bulk_g2s(sb, gate.codes + row * g.rb, code_bytes, &r.full[r.st], pol);
+    if (lane == 1) bulk_g2s(sb + g.R * g.rb, up.codes + row * g.rb, code_bytes, &r.full[r.st], pol);
+    if (lane == 2) bulk_g2s(wb + 0 * g.sw, w0.src, w0.bytes, &r.full[r.st], pol);
+    if (lane == 3) bulk_g2s(wb + 1 * g.sw, w1.src, w1.bytes, &r.full[r.st], pol);
+    if (lane == 4) bulk_g2s(wb + 2 * g.sw, w2.src, w2.bytes, &r.full[r.st], pol);
+    if (lane == 5) bulk_g2s(wb + 3 * g.sw, w3.src, w3.bytes, &r.full[r.st], pol);
+    r.advance();
   }
 }
 
+// Producer of phase A for one token: counts the CTA's chunks per class (the consumers learn them
+// from the phase's first stage), then streams them.  A CTA without any phase-A chunk still hands
+// out one empty stage, so the consumers always have a first stage to wait on.
 template <int BR, int BS>
 __device__ void produce_a(const LayerShape &s, const LayerPtrs &w, const GateUpGeom &gr,
-                          const GateUpGeom &gs, const int32_t *ids, Ring &r, int lane,
-                          uint64_t pol) {
+                          const GateUpGeom &gs, const int *ids, const float *scores, int *cnt,
+                          Ring &r, int lane, uint64_t pol) {
   const RangeA ra = range_a(s);
-  produce_a_class<BR>(s, gr, w.gate, w.up, false, ra.ra, ra.rb, 0, s.dff, ids, r, lane, pol);
-  if (!flag_abort(r.abort))
-    produce_a_class<BS>(s, gs, w.sh_gate, w.sh_up, true, ra.sa, ra.sb, ra.Ur, s.dff_shared, ids, r,
-                        lane, pol);
+  const int nr = count_a_class(s, gr.R, false, ra.ra, ra.rb, 0, s.dff, ids);
+  const int ns = count_a_class(s, gs.R, true, ra.sa, ra.sb, ra.Ur, s.dff_shared, ids);
+  if (lane == 0) {
+    cnt[0] = nr;
+    cnt[1] = ns;
+  }
+  __syncwarp();
+  produce_a_class<BR>(s, gr, w.gate, w.up, false, ra.ra, ra.rb, 0, s.dff, ids, scores, r, lane,
+                      pol);
+  if (flag_abort(r.abort)) return;
+  produce_a_class<BS>(s, gs, w.sh_gate, w.sh_up, true, ra.sa, ra.sb, ra.Ur, s.dff_shared, ids,
+                      scores, r, lane, pol);
+  if (nr + ns == 0 && !flag_abort(r.abort)) {
+    if (!ring_claim(r, lane)) return;
+    if (lane == 0) {
+      r.desc[r.st] = StageDesc{0, 0, 0.f, 0};
+      mbar_arrive_expect_tx(&r.full[r.st], 0);
+    }
+    r.advance();
+  }
 }
 
 // Scratch of the consumer side of both phases.  Per-row partial sums are reduced within a warp as
@@ -374,13 +469,10 @@ struct SmemA {
   int row_u[kBatchA];         // act index of each held row
   float coef[kBatchA];        // its coefficient: the slot's score or the shared scalar
   float stat[kConsumerWarps];
-  int ids[kMaxTopK];
-  float scoef[kMaxTopK];
 };
 
 struct SmemB {
   float red[kMaxRowsB * kConsumerWarps];  // [row - first row][warp slot]
-  int ids[kMaxTopK];
 };
 
 // Phase A and phase B never hold scratch at the same time (a grid barrier or a kernel boundary
@@ -406,19 +498,32 @@ __device__ __forceinline__ void flush_a(SmemA &sm, int held, int wpg, float *act
   if (trailing) consumer_sync(kConsumers);
 }
 
-// Consumes the chunks of one class (routed slots or shared experts) of a CTA's phase A rows.
-// Returns the number of rows still parked, which the caller flushes (the two classes may have
-// different warps per row, so a batch never mixes them).
+// Consumes the `count` stages of one class (routed slots or shared experts) of a CTA's phase A
+// rows.  `waited`: the current stage has already been waited on (the phase's first stage is
+// waited before the counts are read).  Returns the rows still parked, which the caller flushes
+// (the two classes may have different warps per row, so a batch never mixes them).
+// The thread's x values for one class's geometry, pre-scaled for decoding (see load_x_regs).
+template <int BITS>
+struct XRegs {
+  float xs[Fmt<BITS>::kCodes];
+  float xsum;
+  int S;
+  __device__ __forceinline__ void load(const GateUpGeom &g, const uint16_t *x, int tid) {
+    const int my_group = tid / g.tpr, my_step = tid % g.tpr;
+    load_x_regs<BITS>(x, my_step * Fmt<BITS>::kCodes, my_group < g.groups && my_step < g.T, xs,
+                      xsum, S);
+  }
+};
+
 template <int BITS>
 __device__ int consume_a_class(const LayerShape &s, const GateUpGeom &g, bool shared_class,
-                               int64_t a, int64_t b, int64_t base_u, int rows_pe,
-                               const uint16_t *x, float *act, float shared_scalar, Ring &r,
-                               SmemA &sm, int tid) {
+                               int count, const XRegs<BITS> &xr, float *act, float shared_scalar,
+                               Ring &r, SmemA &sm, bool &waited, bool &ok, int tid) {
   constexpr int C = Fmt<BITS>::kCodes, VEC = Fmt<BITS>::kVecs;
   constexpr int RPT = rows_per_thread_a<BITS>();
   constexpr int V = 2 * RPT;        // values per stage: gate and up of RPT rows
   int held = 0;
-  if (a >= b) return held;
+  if (count == 0) return held;
   const int warp = tid >> 5, lane = tid & 31;
   const int G = s.din / kGroup;
   const int my_group = tid / g.tpr, my_step = tid % g.tpr;
@@ -426,10 +531,9 @@ __device__ int consume_a_class(const LayerShape &s, const GateUpGeom &g, bool sh
   const bool active = grp_ok && my_step < g.T;
   const int wpg = g.tpr / 32;
   const int wslot = warp - my_group * wpg;
-  float xs[C], xsum;
-  int S;
-  load_x_regs<BITS>(x, my_step * C, active, xs, xsum, S);
-  const float twoS = pow2f(S);
+  const float(&xs)[C] = xr.xs;
+  const float xsum = xr.xsum;
+  const float twoS = pow2f(xr.S);
   const int code_off = my_step * 16 * VEC;          // the thread's step inside a row
   const int win_off = ((my_step * C) / kGroup) * 2;  // its group's scale inside a row's run
   // after the transpose-reduction, lane l holds value idx of the stage
@@ -437,30 +541,22 @@ __device__ int consume_a_class(const LayerShape &s, const GateUpGeom &g, bool sh
   const bool writer = grp_ok && (lane & ((32 / V) - 1)) == 0;
   const int w_kind = idx / RPT, w_row = (idx % RPT) * g.groups + my_group;
   const int cap = kRedA / wpg < kBatchA ? kRedA / wpg : kBatchA;
+  const int wbase = 2 * g.R * g.rb + win_off;
 
-  ChunkIterA it(a, b, base_u, rows_pe, g.R);
-  ChunkA c;
-  while (it.next(c)) {
-    const int e = shared_class ? c.k : sm.ids[c.k];
-    if (!shared_class && (e < 0 || e >= s.n_experts)) {   // the slot contributes nothing
-      for (int t = tid; t < c.n; t += kConsumers) act[c.u + t] = 0.f;
-      continue;
-    }
-    if (held + c.n > cap) {
+  for (int i = 0; i < count; ++i) {
+    if (!waited) ok = warp_wait_full(r, lane);
+    waited = false;
+    const StageDesc d = r.desc[r.st];
+    if (held + d.n > cap) {
       flush_a(sm, held, wpg, act, tid, true);
       held = 0;
     }
-    if (tid < c.n) {
-      sm.row_u[held + tid] = c.u + tid;
-      sm.coef[held + tid] = shared_class ? shared_scalar : sm.scoef[c.k];
+    if (tid < d.n) {
+      sm.row_u[held + tid] = d.u + tid;
+      sm.coef[held + tid] = shared_class ? shared_scalar : d.coef;
     }
-    const int st = r.i % r.nst;
-    const bool ok = warp_wait_full(r, st, lane);
-    const uint8_t *sb = r.base + static_cast<size_t>(st) * r.stage_bytes;
-    // The four scale/bias windows start at the 16-B boundary below the chunk's first group; the
-    // arrays are 16-B aligned, so the offset of that group is (row * G mod 8) halves.
-    const uint32_t delta = ((static_cast<uint32_t>(e) * rows_pe + c.j) * G & 7u) * 2u;
-    const uint8_t *ws = sb + 2 * g.R * g.rb + delta + win_off;
+    const uint8_t *sb = r.stage();
+    const uint8_t *ws = sb + wbase + d.delta;
     float v[V];
 #pragma unroll
     for (int q = 0; q < V; ++q) v[q] = 0.f;
@@ -468,7 +564,7 @@ __device__ int consume_a_class(const LayerShape &s, const GateUpGeom &g, bool sh
 #pragma unroll
       for (int q = 0; q < RPT; ++q) {
         const int rr = q * g.groups + my_group;
-        if (rr < c.n) {
+        if (rr < d.n) {
           uint4 cg[VEC], cu[VEC];
           const uint8_t *pg = sb + rr * g.rb + code_off;
           const uint8_t *pu = pg + g.R * g.rb;
@@ -485,48 +581,47 @@ __device__ int consume_a_class(const LayerShape &s, const GateUpGeom &g, bool sh
         }
       }
     }
-    __syncwarp();
-    if (lane == 0) mbar_arrive(&r.empty[st]);
-    ++r.i;
+    warp_release(r, lane);
     const float val = warp_transpose_reduce<V>(v, lane);
-    if (writer && w_row < c.n) sm.red[w_kind][(held + w_row) * wpg + wslot] = val;
-    held += c.n;
+    if (writer && w_row < d.n) sm.red[w_kind][(held + w_row) * wpg + wslot] = val;
+    held += d.n;
   }
   return held;
 }
 
-// Consumers of phase A for one token of one layer.  ids/scores/x are read here (after whatever
-// wait made them complete).  Ends with the activations written and a consumer_sync-free tail:
-// callers synchronise as needed.
+// Consumers of phase A for one token of one layer: x is read here; the stages' descriptors carry
+// the rest.  Ends with the activations written and a consumer_sync-free tail: callers
+// synchronise as needed.
 template <int BR, int BS>
 __device__ void consume_a(const LayerShape &s, const LayerPtrs &w, const GateUpGeom &gr,
-                          const GateUpGeom &gs, const uint16_t *x, const int32_t *ids,
-                          const float *scores, float *act, int32_t *err, Ring &r, SmemA &sm,
-                          int tid) {
+                          const GateUpGeom &gs, const uint16_t *x, const int *cnt, float *act,
+                          Ring &r, SmemA &sm, int tid) {
   const int warp = tid >> 5, lane = tid & 31;
-  for (int k = tid; k < s.top_k; k += kConsumers) {
-    sm.ids[k] = ids[k];
-    sm.scoef[k] = scores[k];
-  }
   float shared_scalar = 1.0f;
   if (w.gate_vec != nullptr && s.n_shared > 0) {
     float dot = 0.f;
     for (int c = tid; c < s.din; c += kConsumers)
       dot = fmaf(bf16_to_float(x[c]), bf16_to_float(w.gate_vec[c]), dot);
-    dot = consumers_sum(dot, sm.stat, warp, lane);   // also publishes sm.ids / sm.scoef
+    dot = consumers_sum(dot, sm.stat, warp, lane);
     shared_scalar = 1.0f / (1.0f + expf(-dot));
-  } else {
-    consumer_sync(kConsumers);                       // publishes sm.ids / sm.scoef
   }
-  if (tid == 0)
-    for (int k = 0; k < s.top_k; ++k)
-      if (sm.ids[k] < 0 || sm.ids[k] >= s.n_experts) atomicOr(err, kDevErrBadId);
-  const RangeA ra = range_a(s);
-  int held = consume_a_class<BR>(s, gr, false, ra.ra, ra.rb, 0, s.dff, x, act, 1.f, r, sm, tid);
-  if (held > 0) flush_a(sm, held, gr.tpr / 32, act, tid, ra.sa < ra.sb);
-  held = consume_a_class<BS>(s, gs, true, ra.sa, ra.sb, ra.Ur, s.dff_shared, x, act,
-                             shared_scalar, r, sm, tid);
-  if (held > 0) flush_a(sm, held, gs.tpr / 32, act, tid, false);
+  XRegs<BR> xr;   // x for the routed rows, loaded while the first stage is in flight
+  xr.load(gr, x, tid);
+  // the phase's first stage publishes the counts
+  bool ok = warp_wait_full(r, lane), waited = true;
+  const int nr = cnt[0], ns = cnt[1];
+  if (nr + ns == 0) {   // an empty stage
+    warp_release(r, lane);
+    return;
+  }
+  int held = consume_a_class<BR>(s, gr, false, nr, xr, act, 1.f, r, sm, waited, ok, tid);
+  if (held > 0) flush_a(sm, held, gr.tpr / 32, act, tid, ns > 0);
+  if (ns > 0) {
+    XRegs<BS> xs;
+    xs.load(gs, x, tid);
+    held = consume_a_class<BS>(s, gs, true, ns, xs, act, shared_scalar, r, sm, waited, ok, tid);
+    if (held > 0) flush_a(sm, held, gs.tpr / 32, act, tid, false);
+  }
 }
 
 // ================================================================== phase B
@@ -566,20 +661,20 @@ __device__ __forceinline__ void range_b(const LayerShape &s, int &i0, int &i1) {
   i1 = static_cast<int>(static_cast<int64_t>(s.din) * (blockIdx.x + 1) / gridDim.x);
 }
 
+// Producer of phase B: per stage, lane q handles segment q (and q + 32, ...): the codes of R
+// output rows of that slot's (or shared expert's) down projection plus their scale and bias
+// windows.  `ids` is the producer's shared copy.
 __device__ void produce_b(const LayerShape &s, const LayerPtrs &w, const DownGeom &g,
-                          const int32_t *ids, Ring &r, int lane, uint64_t pol) {
+                          const int *ids, Ring &r, int lane, uint64_t pol) {
   int i0, i1;
   range_b(s, i0, i1);
   const int nseg = s.top_k + s.n_shared;
   const int wins = s.top_k * g.sw_r + s.n_shared * g.sw_s;
   for (int r0 = i0; r0 < i1; r0 += g.R) {
     const int n = (i1 - r0) < g.R ? (i1 - r0) : g.R;
-    int st;
-    bool ok;
-    uint8_t *sb = ring_claim(r, lane, st, ok);
-    if (!ok) return;
+    if (!ring_claim(r, lane)) return;
+    uint8_t *sb = r.stage();
     uint8_t *wb = sb + g.codes_bytes;
-    // lane q handles segment q (and q + 32, ...): its codes, scale window and bias window
     uint32_t tx = 0;
     for (int q = lane; q < nseg; q += 32) {
       const SegB sg = seg_b(s, w, g, q < s.top_k ? ids[q] : 0, q);
@@ -590,7 +685,7 @@ __device__ void produce_b(const LayerShape &s, const LayerPtrs &w, const DownGeo
             window_of(sg.pr->biases + row * sg.G, ng).bytes;
     }
     tx = warp_sum_u32(tx);
-    if (lane == 0) mbar_arrive_expect_tx(&r.full[st], tx);
+    if (lane == 0) mbar_arrive_expect_tx(&r.full[r.st], tx);
     __syncwarp();
     for (int q = lane; q < nseg; q += 32) {
       const SegB sg = seg_b(s, w, g, q < s.top_k ? ids[q] : 0, q);
@@ -600,11 +695,11 @@ __device__ void produce_b(const LayerShape &s, const LayerPtrs &w, const DownGeo
       const Window ws = window_of(sg.pr->scales + row * sg.G, ng);
       const Window wbi = window_of(sg.pr->biases + row * sg.G, ng);
       bulk_g2s(sb + sg.code_off, sg.pr->codes + row * sg.rb, static_cast<uint32_t>(n) * sg.rb,
-               &r.full[st], pol);
-      bulk_g2s(wb + sg.win_off, ws.src, ws.bytes, &r.full[st], pol);
-      bulk_g2s(wb + wins + sg.win_off, wbi.src, wbi.bytes, &r.full[st], pol);
+               &r.full[r.st], pol);
+      bulk_g2s(wb + sg.win_off, ws.src, ws.bytes, &r.full[r.st], pol);
+      bulk_g2s(wb + wins + sg.win_off, wbi.src, wbi.bytes, &r.full[r.st], pol);
     }
-    ++r.i;
+    r.advance();
   }
 }
 
@@ -628,20 +723,21 @@ __device__ __forceinline__ void load_resid_rows(const LayerShape &s, const void 
                        : bf16_to_float(static_cast<const uint16_t *>(resid)[i0 + t]);
 }
 
-// Consumers of phase B for one token: act must be complete (the caller waited for phase A) and
-// resid_s must hold the CTA's residual rows (load_resid_rows, before a consumer_sync).
+// Consumers of phase B for one token.  act must be complete (the caller waited for phase A);
+// resid_s holds the CTA's residual rows (load_resid_rows, before a consumer_sync); ids_s is the
+// producer's shared copy of the expert ids, published by the first stage the consumers wait on.
 template <int BD, int BSD>
-__device__ void consume_b(const LayerShape &s, const DownGeom &g, const int32_t *ids,
+__device__ void consume_b(const LayerShape &s, const DownGeom &g, const int *ids_s,
                           const float *act, const float *resid_s, void *out, int out_f32,
-                          int32_t *err, Ring &r, SmemB &sm, int tid) {
+                          Ring &r, SmemB &sm, int tid) {
   constexpr int CR = Fmt<BD>::kCodes, CS = Fmt<BSD>::kCodes;
   constexpr int CMAX = CR > CS ? CR : CS;
   constexpr int SPTMAX = kMaxActRegs / CMAX > 0 ? kMaxActRegs / CMAX : 1;
   constexpr int VS = 4;             // rows per thread per stage, at most
   const int warp = tid >> 5, lane = tid & 31;
-  for (int k = tid; k < s.top_k; k += kConsumers) sm.ids[k] = ids[k];
   int i0, i1;
   range_b(s, i0, i1);
+  if (i1 <= i0) return;
   const int my_group = tid / g.tpr, my_step = tid % g.tpr;
   const bool grp_ok = my_group < g.groups;
   const int wpg = g.tpr / 32;
@@ -693,13 +789,11 @@ __device__ void consume_b(const LayerShape &s, const DownGeom &g, const int32_t 
       as[i][c] *= pow2f(149 - S - o);
     }
   }
-  consumer_sync(kConsumers);   // publishes sm.ids
-  if (tid == 0)
-    for (int k = 0; k < s.top_k; ++k)
-      if (sm.ids[k] < 0 || sm.ids[k] >= s.n_experts) atomicOr(err, kDevErrBadId);
 
+  // the first stage publishes the ids
+  bool ok = warp_wait_full(r, lane);
   // Per-thread constants of each owned step: where its codes and its group's scale/bias sit in
-  // a stage, and the low bits of its expert's first row (for the window offset).
+  // a stage, and its expert's first row (for the window offset).
   const int wins = s.top_k * g.sw_r + s.n_shared * g.sw_s;
   bool seg_ok[SPTMAX];
   int cbase[SPTMAX], sbase[SPTMAX], rbs[SPTMAX], Gs[SPTMAX];
@@ -707,7 +801,7 @@ __device__ void consume_b(const LayerShape &s, const DownGeom &g, const int32_t 
 #pragma unroll
   for (int i = 0; i < SPTMAX; ++i) {
     const bool routed = seg[i] < s.top_k;
-    const int e = routed ? sm.ids[seg[i]] : seg[i] - s.top_k;
+    const int e = routed ? ids_s[seg[i]] : seg[i] - s.top_k;
     seg_ok[i] = own[i] && (!routed || (e >= 0 && e < s.n_experts));
     const int t = seg[i] - s.top_k;
     const int code_off = routed ? seg[i] * g.R * g.rb_r : s.top_k * g.R * g.rb_r + t * g.R * g.rb_s;
@@ -726,10 +820,9 @@ __device__ void consume_b(const LayerShape &s, const DownGeom &g, const int32_t 
   const int w_row = q_w * g.groups + my_group;
 
   for (int r0 = i0; r0 < i1; r0 += g.R) {
+    if (r0 != i0) ok = warp_wait_full(r, lane);
     const int n = (i1 - r0) < g.R ? (i1 - r0) : g.R;
-    const int st = r.i % r.nst;
-    const bool ok = warp_wait_full(r, st, lane);
-    const uint8_t *sb = r.base + static_cast<size_t>(st) * r.stage_bytes;
+    const uint8_t *sb = r.stage();
     const uint8_t *wb = sb + g.codes_bytes;
     float acc[VS];
 #pragma unroll
@@ -755,9 +848,7 @@ __device__ void consume_b(const LayerShape &s, const DownGeom &g, const int32_t 
         }
       }
     }
-    __syncwarp();
-    if (lane == 0) mbar_arrive(&r.empty[st]);
-    ++r.i;
+    warp_release(r, lane);
     const float val = warp_transpose_reduce<VS>(acc, lane);
     if (writer && q_w < rpt && w_row < n) sm.red[(r0 - i0 + w_row) * wpg + wslot] = val;
   }
