@@ -101,51 +101,25 @@ __device__ __forceinline__ uint4 lds_u4(const uint8_t *p) {
   return *reinterpret_cast<const uint4 *>(p);
 }
 
-// One step's dot product (units 2^-S) against pre-scaled activations held in registers, with
-// packed fp32x2 FMAs (two lanes of arithmetic per instruction, subnormals kept).
+// The Operand of C bf16 values of x from column c0 (x + c0 16-byte aligned); zeros when the
+// thread has no step.
 template <int BITS>
-__device__ __forceinline__ float step_dot_regs(const uint4 *v, const float *xs) {
-  constexpr int N = Fmt<BITS>::kCodes;
-  uint32_t m[N];
-  step_masks<BITS>(v, m);
-  float2 a0 = make_float2(0.f, 0.f), a1 = make_float2(0.f, 0.f);
+__device__ __forceinline__ void load_x_operand(Operand<BITS> &op, const uint16_t *x, int c0,
+                                               bool active) {
+  constexpr int C = Operand<BITS>::C;
+  float v[C];
 #pragma unroll
-  for (int j = 0; j < N; j += 4) {
-    a0 = __ffma2_rn(make_float2(__uint_as_float(m[j + 0]), __uint_as_float(m[j + 1])),
-                    make_float2(xs[j + 0], xs[j + 1]), a0);
-    a1 = __ffma2_rn(make_float2(__uint_as_float(m[j + 2]), __uint_as_float(m[j + 3])),
-                    make_float2(xs[j + 2], xs[j + 3]), a1);
-  }
-  return (a0.x + a0.y) + (a1.x + a1.y);
-}
-
-// C bf16 values of x from column c0 into registers, pre-scaled for BITS-bit decoding with a
-// shift S chosen from these values alone (each thread rescales its own partial sums, so threads
-// need not agree on S), plus their plain sum.  x + c0 is 16-byte aligned.
-template <int BITS>
-__device__ __forceinline__ void load_x_regs(const uint16_t *x, int c0, bool active,
-                                            float (&xs)[Fmt<BITS>::kCodes], float &xsum, int &S) {
-  constexpr int C = Fmt<BITS>::kCodes;
-  xsum = 0.f;
-  float mx = 0.f;
-#pragma unroll
-  for (int v = 0; v < C / 8; ++v) {
+  for (int q = 0; q < C / 8; ++q) {
     const uint4 w =
-        active ? *reinterpret_cast<const uint4 *>(x + c0 + 8 * v) : make_uint4(0, 0, 0, 0);
+        active ? *reinterpret_cast<const uint4 *>(x + c0 + 8 * q) : make_uint4(0, 0, 0, 0);
     const uint32_t ww[4] = {w.x, w.y, w.z, w.w};
 #pragma unroll
     for (int h = 0; h < 4; ++h) {
-      const int c = 8 * v + 2 * h;
-      xs[c] = __uint_as_float(ww[h] << 16);
-      xs[c + 1] = __uint_as_float(ww[h] & 0xffff0000u);
-      xsum += xs[c];
-      xsum += xs[c + 1];
-      mx = fmaxf(mx, fmaxf(fabsf(xs[c]), fabsf(xs[c + 1])));
+      v[8 * q + 2 * h] = __uint_as_float(ww[h] << 16);
+      v[8 * q + 2 * h + 1] = __uint_as_float(ww[h] & 0xffff0000u);
     }
   }
-  S = choose_shift(mx);
-#pragma unroll
-  for (int c = 0; c < C; ++c) xs[c] *= pow2f(149 - S - code_offset<BITS>(c));
+  op.set(v);
 }
 
 __device__ __forceinline__ float silu_f(float z) { return z / (1.0f + expf(-z)); }
@@ -502,22 +476,17 @@ __device__ __forceinline__ void flush_a(SmemA &sm, int held, int wpg, float *act
 // rows.  `waited`: the current stage has already been waited on (the phase's first stage is
 // waited before the counts are read).  Returns the rows still parked, which the caller flushes
 // (the two classes may have different warps per row, so a batch never mixes them).
-// The thread's x values for one class's geometry, pre-scaled for decoding (see load_x_regs).
+// The thread's x operand for one class's geometry.
 template <int BITS>
-struct XRegs {
-  float xs[Fmt<BITS>::kCodes];
-  float xsum;
-  int S;
-  __device__ __forceinline__ void load(const GateUpGeom &g, const uint16_t *x, int tid) {
-    const int my_group = tid / g.tpr, my_step = tid % g.tpr;
-    load_x_regs<BITS>(x, my_step * Fmt<BITS>::kCodes, my_group < g.groups && my_step < g.T, xs,
-                      xsum, S);
-  }
-};
+__device__ __forceinline__ void load_x_class(Operand<BITS> &op, const GateUpGeom &g,
+                                             const uint16_t *x, int tid) {
+  const int my_group = tid / g.tpr, my_step = tid % g.tpr;
+  load_x_operand<BITS>(op, x, my_step * Operand<BITS>::C, my_group < g.groups && my_step < g.T);
+}
 
 template <int BITS>
 __device__ int consume_a_class(const LayerShape &s, const GateUpGeom &g, bool shared_class,
-                               int count, const XRegs<BITS> &xr, float *act, float shared_scalar,
+                               int count, const Operand<BITS> &xo, float *act, float shared_scalar,
                                Ring &r, SmemA &sm, bool &waited, bool &ok, int tid) {
   constexpr int C = Fmt<BITS>::kCodes, VEC = Fmt<BITS>::kVecs;
   constexpr int RPT = rows_per_thread_a<BITS>();
@@ -531,9 +500,7 @@ __device__ int consume_a_class(const LayerShape &s, const GateUpGeom &g, bool sh
   const bool active = grp_ok && my_step < g.T;
   const int wpg = g.tpr / 32;
   const int wslot = warp - my_group * wpg;
-  const float(&xs)[C] = xr.xs;
-  const float xsum = xr.xsum;
-  const float twoS = pow2f(xr.S);
+  const float xunit = xo.unit, xsum = xo.sum;
   const int code_off = my_step * 16 * VEC;          // the thread's step inside a row
   const int win_off = ((my_step * C) / kGroup) * 2;  // its group's scale inside a row's run
   // after the transpose-reduction, lane l holds value idx of the stage
@@ -573,11 +540,11 @@ __device__ int consume_a_class(const LayerShape &s, const GateUpGeom &g, bool sh
             cg[w] = lds_u4(pg + 16 * w);
             cu[w] = lds_u4(pu + 16 * w);
           }
-          const float dg = step_dot_regs<BITS>(cg, xs);
-          const float du = step_dot_regs<BITS>(cu, xs);
+          const float dg = xo.dot(cg);
+          const float du = xo.dot(cu);
           const uint8_t *wr = ws + rr * G * 2;
-          v[q] = fmaf(lds_half(wr), dg * twoS, lds_half(wr + g.sw) * xsum);
-          v[RPT + q] = fmaf(lds_half(wr + 2 * g.sw), du * twoS, lds_half(wr + 3 * g.sw) * xsum);
+          v[q] = fmaf(lds_half(wr), dg * xunit, lds_half(wr + g.sw) * xsum);
+          v[RPT + q] = fmaf(lds_half(wr + 2 * g.sw), du * xunit, lds_half(wr + 3 * g.sw) * xsum);
         }
       }
     }
@@ -605,8 +572,8 @@ __device__ void consume_a(const LayerShape &s, const LayerPtrs &w, const GateUpG
     dot = consumers_sum(dot, sm.stat, warp, lane);
     shared_scalar = 1.0f / (1.0f + expf(-dot));
   }
-  XRegs<BR> xr;   // x for the routed rows, loaded while the first stage is in flight
-  xr.load(gr, x, tid);
+  Operand<BR> xr;   // x for the routed rows, loaded while the first stage is in flight
+  load_x_class<BR>(xr, gr, x, tid);
   // the phase's first stage publishes the counts
   bool ok = warp_wait_full(r, lane), waited = true;
   const int nr = cnt[0], ns = cnt[1];
@@ -617,9 +584,9 @@ __device__ void consume_a(const LayerShape &s, const LayerPtrs &w, const GateUpG
   int held = consume_a_class<BR>(s, gr, false, nr, xr, act, 1.f, r, sm, waited, ok, tid);
   if (held > 0) flush_a(sm, held, gr.tpr / 32, act, tid, ns > 0);
   if (ns > 0) {
-    XRegs<BS> xs;
-    xs.load(gs, x, tid);
-    held = consume_a_class<BS>(s, gs, true, ns, xs, act, shared_scalar, r, sm, waited, ok, tid);
+    Operand<BS> xsh;
+    load_x_class<BS>(xsh, gs, x, tid);
+    held = consume_a_class<BS>(s, gs, true, ns, xsh, act, shared_scalar, r, sm, waited, ok, tid);
     if (held > 0) flush_a(sm, held, gs.tpr / 32, act, tid, false);
   }
 }
@@ -703,13 +670,40 @@ __device__ void produce_b(const LayerShape &s, const LayerPtrs &w, const DownGeo
   }
 }
 
-template <int BITS, int CMAX>
-__device__ __forceinline__ float down_step(const uint8_t *codes, const float (&as)[CMAX]) {
+// A thread's step of the down contraction: routed (BD-bit codes) or shared (BSD-bit codes).
+template <int BD, int BSD>
+struct DownOperand {
+  union {
+    Operand<BD> r;
+    Operand<BSD> s;
+  };
+};
+
+template <int BITS>
+__device__ __forceinline__ float down_dot(const uint8_t *codes, const Operand<BITS> &op) {
   constexpr int VEC = Fmt<BITS>::kVecs;
   uint4 cv[VEC];
 #pragma unroll
   for (int w = 0; w < VEC; ++w) cv[w] = lds_u4(codes + 16 * w);
-  return step_dot_regs<BITS>(cv, as);
+  return op.dot(cv) * op.unit;
+}
+
+// The Operand of C activations from act + base (16-byte aligned); zeros when not owned.
+template <int BITS>
+__device__ __forceinline__ void load_act_operand(Operand<BITS> &op, const float *act, int base,
+                                                 bool own) {
+  constexpr int C = Operand<BITS>::C;
+  float v[C];
+  const float4 *ap = reinterpret_cast<const float4 *>(act + base);
+#pragma unroll
+  for (int c = 0; c < C; c += 4) {
+    const float4 a4 = own ? ap[c / 4] : make_float4(0.f, 0.f, 0.f, 0.f);
+    v[c] = a4.x;
+    v[c + 1] = a4.y;
+    v[c + 2] = a4.z;
+    v[c + 3] = a4.w;
+  }
+  op.set(v);
 }
 
 // The CTA's residual rows of phase B into shared memory (the tail adds them).  The residual may
@@ -723,16 +717,16 @@ __device__ __forceinline__ void load_resid_rows(const LayerShape &s, const void 
                        : bf16_to_float(static_cast<const uint16_t *>(resid)[i0 + t]);
 }
 
-// Consumers of phase B for one token.  act must be complete (the caller waited for phase A);
+// Consumers of phase B for one token, each thread owning at most SPTMAX steps of the
+// concatenated contraction.  act must be complete (the caller waited for phase A);
 // resid_s holds the CTA's residual rows (load_resid_rows, before a consumer_sync); ids_s is the
 // producer's shared copy of the expert ids, published by the first stage the consumers wait on.
-template <int BD, int BSD>
-__device__ void consume_b(const LayerShape &s, const DownGeom &g, const int *ids_s,
-                          const float *act, const float *resid_s, void *out, int out_f32,
-                          Ring &r, SmemB &sm, int tid) {
+template <int BD, int BSD, int SPTMAX>
+__device__ void consume_b_spt(const LayerShape &s, const DownGeom &g, const int *ids_s,
+                              const float *act, const float *resid_s, void *out, int out_f32,
+                              Ring &r, SmemB &sm, int tid) {
   constexpr int CR = Fmt<BD>::kCodes, CS = Fmt<BSD>::kCodes;
   constexpr int CMAX = CR > CS ? CR : CS;
-  constexpr int SPTMAX = kMaxActRegs / CMAX > 0 ? kMaxActRegs / CMAX : 1;
   constexpr int VS = 4;             // rows per thread per stage, at most
   const int warp = tid >> 5, lane = tid & 31;
   int i0, i1;
@@ -744,10 +738,9 @@ __device__ void consume_b(const LayerShape &s, const DownGeom &g, const int *ids
   const int wslot = warp - my_group * wpg;
   const int Lr = s.top_k * s.dff;
 
-  // this thread's steps of the concatenated contraction and their activations, with a decoding
-  // shift of its own (each thread rescales its own partial sums)
-  float as[SPTMAX][CMAX];
-  float asum[SPTMAX], twoS[SPTMAX];
+  // this thread's steps of the concatenated contraction and their activations (each thread
+  // scales its own operands)
+  DownOperand<BD, BSD> op[SPTMAX];
   int seg[SPTMAX], jst[SPTMAX];
   bool own[SPTMAX], shr[SPTMAX];
 #pragma unroll
@@ -755,38 +748,16 @@ __device__ void consume_b(const LayerShape &s, const DownGeom &g, const int *ids
     const int t = my_step + g.tpr * i;
     own[i] = grp_ok && i < g.spt && t < g.T_r + g.T_s;
     shr[i] = t >= g.T_r;
-    int base;
     if (!shr[i]) {
       seg[i] = t / g.spr_r;
       jst[i] = t - seg[i] * g.spr_r;
-      base = t * CR;
+      load_act_operand<BD>(op[i].r, act, t * CR, own[i]);
     } else {
       const int ts = t - g.T_r;
       const int si = ts / (g.spr_s > 0 ? g.spr_s : 1);
       seg[i] = s.top_k + si;
       jst[i] = ts - si * g.spr_s;
-      base = Lr + ts * CS;
-    }
-    const int C = shr[i] ? CS : CR;
-    const float4 *ap = reinterpret_cast<const float4 *>(act + base);
-    float mx = 0.f;
-    asum[i] = 0.f;
-#pragma unroll
-    for (int c = 0; c < CMAX; c += 4) {
-      const float4 a4 = (own[i] && c < C) ? ap[c / 4] : make_float4(0.f, 0.f, 0.f, 0.f);
-      as[i][c] = a4.x;
-      as[i][c + 1] = a4.y;
-      as[i][c + 2] = a4.z;
-      as[i][c + 3] = a4.w;
-      asum[i] += (a4.x + a4.y) + (a4.z + a4.w);
-      mx = fmaxf(mx, fmaxf(fmaxf(fabsf(a4.x), fabsf(a4.y)), fmaxf(fabsf(a4.z), fabsf(a4.w))));
-    }
-    const int S = choose_shift(mx);
-    twoS[i] = pow2f(S);
-#pragma unroll
-    for (int c = 0; c < CMAX; ++c) {
-      const int o = shr[i] ? code_offset<BSD>(c) : code_offset<BD>(c);
-      as[i][c] *= pow2f(149 - S - o);
+      load_act_operand<BSD>(op[i].s, act, Lr + ts * CS, own[i]);
     }
   }
 
@@ -840,10 +811,11 @@ __device__ void consume_b(const LayerShape &s, const DownGeom &g, const int *ids
         for (int q = 0; q < VS; ++q) {
           const int rr = q * g.groups + my_group;
           if (q < rpt && rr < n) {
-            const float d = shr[i] ? down_step<BSD, CMAX>(cp + rr * rbs[i], as[i])
-                                   : down_step<BD, CMAX>(cp + rr * rbs[i], as[i]);
+            const float d = shr[i] ? down_dot<BSD>(cp + rr * rbs[i], op[i].s)
+                                   : down_dot<BD>(cp + rr * rbs[i], op[i].r);
+            const float asum = shr[i] ? op[i].s.sum : op[i].r.sum;
             const uint8_t *wr = sp + rr * Gs[i] * 2;
-            acc[q] += fmaf(lds_half(wr), d * twoS[i], lds_half(wr + wins) * asum[i]);
+            acc[q] += fmaf(lds_half(wr), d, lds_half(wr + wins) * asum);
           }
         }
       }
@@ -862,6 +834,20 @@ __device__ void consume_b(const LayerShape &s, const DownGeom &g, const int *ids
     else
       static_cast<uint16_t *>(out)[i0 + t] = float_to_bf16_rn(o);
   }
+}
+
+// Phase B with the activation registers sized for the plan's steps per thread.
+template <int BD, int BSD>
+__device__ void consume_b(const LayerShape &s, const DownGeom &g, const int *ids_s,
+                          const float *act, const float *resid_s, void *out, int out_f32,
+                          Ring &r, SmemB &sm, int tid) {
+  constexpr int CMAX = Fmt<BD>::kCodes > Fmt<BSD>::kCodes ? Fmt<BD>::kCodes : Fmt<BSD>::kCodes;
+  constexpr int SPT_LIMIT = kMaxActRegs / CMAX > 0 ? kMaxActRegs / CMAX : 1;
+  if (SPT_LIMIT >= 2 && g.spt >= 2)
+    consume_b_spt<BD, BSD, (SPT_LIMIT >= 2 ? 2 : 1)>(s, g, ids_s, act, resid_s, out, out_f32, r,
+                                                      sm, tid);
+  else
+    consume_b_spt<BD, BSD, 1>(s, g, ids_s, act, resid_s, out, out_f32, r, sm, tid);
 }
 
 }  // namespace moe
