@@ -168,3 +168,31 @@ int oracle_moe_token(int32_t din, int32_t dff, int32_t top_k, const oracle_proj 
   free(x); free(routed); free(shared); free(y); free(act);
   return 0;
 }
+
+/* Route inversion for m tokens of k routed slots each: the distinct valid expert ids in
+ * ascending order, and for each of them the (token, slot) pairs whose id names it, written as
+ * p = token * k + slot in ascending order.  Ids outside [0, n_experts) belong to no expert.
+ * This is the grouping of the routers' top-k pools ("Red Lite dev39 -- fused expert tail",
+ * Change) by expert, which lets a batch of tokens read each selected expert once.
+ * Writes uniq[U], offs[U + 1] (the pairs of uniq[u] are pairs[offs[u]] .. pairs[offs[u + 1] - 1])
+ * and pairs[offs[U]]; returns U.  Plain definition: one pass over the pairs per expert id. */
+int32_t oracle_route_invert(const int32_t *ids, int32_t m, int32_t k, int32_t n_experts,
+                            int32_t *uniq, int32_t *offs, int32_t *pairs) {
+  int32_t u = 0, n = 0;
+  offs[0] = 0;
+  for (int32_t e = 0; e < n_experts; ++e) {
+    int32_t found = 0;
+    for (int32_t p = 0; p < m * k; ++p) {
+      if (ids[p] == e) {
+        pairs[n++] = p;
+        found = 1;
+      }
+    }
+    if (found) {
+      uniq[u++] = e;
+      offs[u] = n;
+    }
+  }
+  return u;
+}
+

@@ -73,6 +73,10 @@ def lib():
                 + [ctypes.c_int32] * 2 + [ctypes.POINTER(Proj)] * 3
                 + [ctypes.c_void_p] * 3 + [ctypes.c_int32] + [ctypes.c_void_p] * 2
                 + [ctypes.c_int32])
+            L.oracle_route_invert.restype = ctypes.c_int32
+            L.oracle_route_invert.argtypes = [ctypes.c_void_p, ctypes.c_int32, ctypes.c_int32,
+                                              ctypes.c_int32, ctypes.c_void_p, ctypes.c_void_p,
+                                              ctypes.c_void_p]
             _lib = L
     return _lib
 
@@ -215,3 +219,17 @@ def moe_token(x_bf16, resid, scores, gate, up, down, sh_gate=(), sh_up=(), sh_do
     if rc != 0:
         raise ValueError("oracle_moe_token: shape mismatch")
     return out
+
+
+def route_invert(ids: np.ndarray, n_experts: int):
+    """(uniq, offs, pairs) of ids [m, k]: the distinct valid experts ascending, and per expert the
+    pairs p = token * k + slot that name it, ascending (see oracle_route_invert)."""
+    ids = np.ascontiguousarray(ids, dtype=np.int32)
+    m, k = ids.shape
+    n = m * k
+    uniq = np.empty(max(n, 1), np.int32)
+    offs = np.empty(max(n, 1) + 1, np.int32)
+    pairs = np.empty(max(n, 1), np.int32)
+    u = lib().oracle_route_invert(_ptr(ids), m, k, n_experts, _ptr(uniq), _ptr(offs), _ptr(pairs))
+    return uniq[:u].copy(), offs[:u + 1].copy(), pairs[:offs[u]].copy()
+

@@ -37,6 +37,10 @@ MUTANTS = {
                               "out[t] = r + (routed[t] + shared[t]);"),
     "shared term dropped": ("shared[t] += y[t];", "shared[t] += 0.0 * y[t];"),
     "bf16 read as fp16 bits": ("uint32_t u = (uint32_t)b << 16;", "uint32_t u = (uint32_t)b << 13;"),
+    "inversion keeps the last expert id": ("    if (found) {\n      uniq[u++] = e;",
+                                           "    if (found) {\n      uniq[u++] = n_experts - 1 - e;"),
+    "inversion drops the last pair": ("for (int32_t p = 0; p < m * k; ++p) {",
+                                      "for (int32_t p = 0; p < m * k - 1; ++p) {"),
 }
 
 

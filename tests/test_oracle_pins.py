@@ -329,3 +329,51 @@ def test_block_rejects_mismatched_shapes():
     x = synth.activations(13, 0, 0, 128)
     with pytest.raises(ValueError):
         O.moe_token(x, np.zeros(128, np.float32), np.ones(1, np.float32), gate, up, down)
+
+
+# ---------------------------------------------------------------- route inversion (batches of tokens)
+
+def _brute_invert(ids, n_experts):
+    """Independent restatement: a dict from expert to its pairs, built in one scan."""
+    groups = {}
+    for p, e in enumerate(np.asarray(ids).reshape(-1).tolist()):
+        if 0 <= e < n_experts:
+            groups.setdefault(e, []).append(p)
+    return groups
+
+
+@pytest.mark.parametrize("m,k,E,seed", [(1, 8, 128, 1), (8, 6, 128, 2), (32, 6, 128, 3),
+                                        (4, 4, 5, 4), (16, 10, 512, 5)])
+def test_route_invert_matches_brute_force(m, k, E, seed):
+    rng = np.random.default_rng(seed)
+    ids = np.stack([rng.choice(E, size=k, replace=False) for _ in range(m)]).astype(np.int32)
+    uniq, offs, pairs = O.route_invert(ids, E)
+    groups = _brute_invert(ids, E)
+    assert uniq.tolist() == sorted(groups)
+    for u, e in enumerate(uniq):
+        assert pairs[offs[u]:offs[u + 1]].tolist() == groups[e]
+    # every pair appears exactly once, and each names its expert
+    assert sorted(pairs.tolist()) == list(range(m * k))
+    for u, e in enumerate(uniq):
+        assert all(ids.reshape(-1)[p] == e for p in pairs[offs[u]:offs[u + 1]])
+
+
+def test_route_invert_special_cases():
+    # one token: every slot its own expert, experts ascending, pairs follow the ids' order
+    ids = np.array([[7, 3, 9]], np.int32)
+    uniq, offs, pairs = O.route_invert(ids, 10)
+    assert uniq.tolist() == [3, 7, 9] and offs.tolist() == [0, 1, 2, 3]
+    assert pairs.tolist() == [1, 0, 2]
+    # every token picks the same experts: one group per expert with all tokens in order
+    ids = np.array([[2, 0]] * 4, np.int32)
+    uniq, offs, pairs = O.route_invert(ids, 3)
+    assert uniq.tolist() == [0, 2]
+    assert pairs[offs[0]:offs[1]].tolist() == [1, 3, 5, 7]
+    assert pairs[offs[1]:offs[2]].tolist() == [0, 2, 4, 6]
+    # invalid ids belong to no group; a repeated id inside one token gives two pairs
+    ids = np.array([[-1, 4, 4], [5, 9, 0]], np.int32)
+    uniq, offs, pairs = O.route_invert(ids, 5)
+    assert uniq.tolist() == [0, 4] and pairs.tolist() == [5, 1, 2]
+    # nothing valid
+    uniq, offs, pairs = O.route_invert(np.array([[-3, 7]], np.int32), 5)
+    assert len(uniq) == 0 and offs.tolist() == [0] and len(pairs) == 0
