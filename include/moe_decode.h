@@ -215,6 +215,17 @@ int moe_synth_scales(void *dst, uint64_t key, int32_t expert0, int32_t n_experts
 int moe_synth_biases(void *dst, const void *scales, uint64_t key, int32_t expert0,
                      int32_t n_experts, int64_t per_expert, int32_t bits, void *stream);
 
+/* Route inversion of a batch of tokens, as the grouped kernels compute it (a debug export, so the
+ * integer result can be compared bit for bit with an independent implementation).  ids is int32
+ * [m][k] device; out is int32 device with room for 2 + 2*m*k + m*k values and receives U (the
+ * number of distinct ids in [0, n_experts)), then those ids ascending (uniq[U]), then offs[U + 1]
+ * and then the pairs p = token * k + slot grouped by expert, ascending within each (the pairs
+ * of uniq[u] are at offs[u] .. offs[u + 1] - 1).  Asynchronous on stream.  Limits: m * k <= 256,
+ * n_experts <= 1024 (MOE_ERR_UNSUPPORTED beyond).  The pages group the routers' top-k pools by
+ * expert only implicitly ("Red Lite dev39 -- fused expert tail", Change). */
+int moe_route_invert_device(const int32_t *ids, int32_t m, int32_t k, int32_t n_experts,
+                            int32_t *out, void *stream);
+
 #ifdef __cplusplus
 }
 #endif

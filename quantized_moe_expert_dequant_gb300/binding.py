@@ -33,7 +33,7 @@ EXPORTS = ["moe_decode_create", "moe_decode_forward", "moe_decode_get_error", "m
            "moe_stack_create", "moe_stack_step", "moe_stack_step_parts", "moe_stack_step_host",
            "moe_stack_get_error",
            "moe_stack_destroy", "moe_pack_codes", "moe_unpack_codes", "moe_unpack_codes_device",
-           "moe_synth_codes", "moe_synth_scales", "moe_synth_biases"]
+           "moe_synth_codes", "moe_synth_scales", "moe_synth_biases", "moe_route_invert_device"]
 
 
 class MoeError(RuntimeError):
@@ -93,6 +93,7 @@ def lib() -> ctypes.CDLL:
                 "moe_synth_codes": [vp, u64, i32, i32, i64, vp],
                 "moe_synth_scales": [vp, u64, i32, i32, i64, vp],
                 "moe_synth_biases": [vp, vp, u64, i32, i32, i64, i32, vp],
+                "moe_route_invert_device": [vp, i32, i32, i32, vp, vp],
             }
             for name, args in sig.items():
                 f = getattr(L, name)
@@ -346,3 +347,18 @@ def unpack_codes_device(packed: torch.Tensor, cols: int, bits: int, stream=None)
     check("moe_unpack_codes_device", lib().moe_unpack_codes_device(
         packed.data_ptr(), rows, cols, bits, out.data_ptr(), _stream(stream)))
     return out
+
+
+def route_invert_device(ids: torch.Tensor, n_experts: int, stream=None):
+    """The kernels' route inversion of ids int32 [m, k] (device): (uniq, offs, pairs) as numpy."""
+    m, k = ids.shape
+    out = torch.full((2 + 3 * m * k,), -7, dtype=torch.int32, device=ids.device)
+    check("moe_route_invert_device", lib().moe_route_invert_device(
+        _p(ids.contiguous()), m, k, n_experts, _p(out), _stream(stream)))
+    o = out.cpu().numpy()
+    u = int(o[0])
+    uniq = o[1:1 + u]
+    offs = o[1 + u:2 + 2 * u]
+    pairs = o[2 + 2 * u:2 + 2 * u + int(offs[-1])]
+    return uniq.copy(), offs.copy(), pairs.copy()
+

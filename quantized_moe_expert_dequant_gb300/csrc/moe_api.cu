@@ -616,3 +616,17 @@ extern "C" int moe_unpack_codes_device(const void *packed, int64_t rows, int64_t
              ? MOE_OK
              : MOE_ERR_CUDA;
 }
+
+// ====================================================================== debug route inversion
+extern "C" int moe_route_invert_device(const int32_t *ids, int32_t m, int32_t k,
+                                       int32_t n_experts, int32_t *out, void *stream) {
+  if (!ids || !out || m < 1 || k < 1) return MOE_ERR_INVALID_ARG;
+  if ((int64_t)m * k > moe::kMaxPairs || n_experts < 1 || n_experts > moe::kMaxGroupExperts)
+    return MOE_ERR_UNSUPPORTED;
+  if (!aligned(ids, 4) || !aligned(out, 4)) return MOE_ERR_INVALID_ARG;
+  return moe::launch_route_invert(ids, m, k, n_experts, out, static_cast<cudaStream_t>(stream)) ==
+                 cudaSuccess
+             ? MOE_OK
+             : MOE_ERR_CUDA;
+}
+

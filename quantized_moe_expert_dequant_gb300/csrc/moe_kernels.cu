@@ -192,6 +192,21 @@ __global__ void unpack_kernel(const uint8_t *packed, int64_t rows, int64_t cols,
   }
 }
 
+// ================================================================== debug route inversion
+__global__ void route_invert_kernel(const int32_t *ids, int n, int n_experts, int32_t *out) {
+  __shared__ Route rt;
+  __shared__ int ids_s[kMaxPairs];
+  for (int p = threadIdx.x; p < n; p += 32) ids_s[p] = ids[p];
+  __syncwarp();
+  route_invert_warp(ids_s, n, n_experts, rt, threadIdx.x);
+  __syncwarp();
+  const int U = rt.n_uniq;
+  if (threadIdx.x == 0) out[0] = U;
+  for (int u = threadIdx.x; u < U; u += 32) out[1 + u] = rt.uniq[u];
+  for (int u = threadIdx.x; u <= U; u += 32) out[1 + U + u] = rt.offs[u];
+  for (int q = threadIdx.x; q < rt.n_pairs; q += 32) out[2 + 2 * U + q] = rt.pairs[q];
+}
+
 // ================================================================== host side
 static int fmt_codes(int bits) { return bits == 4 ? 32 : bits == 8 ? 16 : 64; }
 static int align_up(int v, int a) { return (v + a - 1) / a * a; }
@@ -378,6 +393,12 @@ cudaError_t launch_unpack(const uint8_t *packed, int64_t rows, int64_t cols, int
   int grid = (int)((steps + 255) / 256);
   grid = grid < 1 ? 1 : (grid > 65535 ? 65535 : grid);
   MOE_BITS_SWITCH(bits, B, unpack_kernel<B><<<grid, 256, 0, stream>>>(packed, rows, cols, codes));
+  return cudaGetLastError();
+}
+
+cudaError_t launch_route_invert(const int32_t *ids, int m, int k, int n_experts, int32_t *out,
+                                cudaStream_t stream) {
+  route_invert_kernel<<<1, 32, 0, stream>>>(ids, m * k, n_experts, out);
   return cudaGetLastError();
 }
 

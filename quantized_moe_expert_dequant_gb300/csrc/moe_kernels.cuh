@@ -23,6 +23,9 @@ struct LayerPtrs {
 };
 
 constexpr int kMaxTopK = 64;
+constexpr int kMaxPairs = 256;          // grouped tokens: m * top_k at most
+constexpr int kMaxGroupTokens = 64;     // grouped tokens: m at most
+constexpr int kMaxGroupExperts = 1024;  // grouped tokens: n_experts at most (one bitmap word a lane)
 constexpr int kConsumerWarps = 16;
 constexpr int kConsumers = kConsumerWarps * 32;
 constexpr int kProducerWarps = 1;           // issues the weight stream (bulk copies)
@@ -121,5 +124,9 @@ cudaError_t prepare_kernels(int smem_optin, int bits_gu, int bits_d, int bits_sh
 int fused_grid_limit(const Plan &plan, int bits_gu, int bits_d, int bits_sh);
 cudaError_t launch_unpack(const uint8_t *packed, int64_t rows, int64_t cols, int bits,
                           uint8_t *codes, cudaStream_t stream);
+// Route inversion of ids [m][k] by the device code the grouped kernels use; writes
+// out[0] = U, then uniq[U], offs[U + 1], pairs[offs[U]].
+cudaError_t launch_route_invert(const int32_t *ids, int m, int k, int n_experts, int32_t *out,
+                                cudaStream_t stream);
 
 }  // namespace moe

@@ -291,6 +291,116 @@ __device__ __forceinline__ void producer_load_token(const LayerShape &s, const i
   producer_sync();
 }
 
+// ================================================================== route inversion
+// A batch of tokens is grouped by expert so that each selected expert is streamed once per
+// layer: the distinct valid ids in ascending order, and for each the (token, slot) pairs that
+// name it, p = token * K + slot, ascending.  The grouping of the routers' top-k pools by expert
+// ("Red Lite dev39 -- fused expert tail", Change) is the step before that stream.
+struct Route {
+  int n_uniq;                                // U
+  int n_pairs;                               // valid pairs (offs[U])
+  int uniq[kMaxPairs];                       // expert ids, ascending
+  int offs[kMaxPairs + 1];                   // pairs of uniq[u]: pairs[offs[u] .. offs[u + 1])
+  short pairs[kMaxPairs];                    // token * K + slot
+  int cnt[kMaxPairs];                        // scratch: pairs per expert, then placement cursor
+  uint32_t bitmap[kMaxGroupExperts / 32];    // scratch: which experts occur
+  int wbase[kMaxGroupExperts / 32];          // scratch: experts below each bitmap word
+};
+
+__device__ __forceinline__ int route_rank(const Route &rt, int e) {
+  const int w = e >> 5;
+  return rt.wbase[w] + __popc(rt.bitmap[w] & ((1u << (e & 31)) - 1u));
+}
+
+// One warp inverts ids[0 .. n) (n = m * K <= kMaxPairs; n_experts <= kMaxGroupExperts) into rt.
+// Deterministic: experts by bitmap rank, pairs placed in index order within each expert.
+__device__ __forceinline__ void route_invert_warp(const int *ids, int n, int n_experts, Route &rt,
+                                                  int lane) {
+  const int words = (n_experts + 31) >> 5;
+  for (int w = lane; w < kMaxGroupExperts / 32; w += 32) rt.bitmap[w] = 0u;
+  __syncwarp();
+  for (int p = lane; p < n; p += 32) {
+    const int e = ids[p];
+    if (e >= 0 && e < n_experts) atomicOr(&rt.bitmap[e >> 5], 1u << (e & 31));
+  }
+  __syncwarp();
+  // experts below each word (exclusive scan of popcounts; one word per lane)
+  const int c = lane < words ? __popc(rt.bitmap[lane]) : 0;
+  int incl = c;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int t = __shfl_up_sync(0xffffffffu, incl, o);
+    if (lane >= o) incl += t;
+  }
+  rt.wbase[lane] = incl - c;
+  const int U = __shfl_sync(0xffffffffu, incl, 31);
+  if (lane < words) {
+    uint32_t bits = rt.bitmap[lane];
+    int r = incl - c;
+    while (bits) {
+      const int b = __ffs(bits) - 1;
+      rt.uniq[r++] = (lane << 5) + b;
+      bits &= bits - 1u;
+    }
+  }
+  for (int u = lane; u < U; u += 32) rt.cnt[u] = 0;
+  __syncwarp();
+  for (int p = lane; p < n; p += 32) {
+    const int e = ids[p];
+    if (e >= 0 && e < n_experts) atomicAdd(&rt.cnt[route_rank(rt, e)], 1);
+  }
+  __syncwarp();
+  // offsets: exclusive scan of the counts, U <= kMaxPairs = 8 per lane
+  constexpr int PER = kMaxPairs / 32;
+  int local[PER];
+  int lsum = 0;
+#pragma unroll
+  for (int j = 0; j < PER; ++j) {
+    const int u = lane * PER + j;
+    local[j] = u < U ? rt.cnt[u] : 0;
+    lsum += local[j];
+  }
+  int lin = lsum;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int t = __shfl_up_sync(0xffffffffu, lin, o);
+    if (lane >= o) lin += t;
+  }
+  int run = lin - lsum;
+#pragma unroll
+  for (int j = 0; j < PER; ++j) {
+    const int u = lane * PER + j;
+    if (u < U) rt.offs[u] = run;
+    run += local[j];
+  }
+  const int total = __shfl_sync(0xffffffffu, lin, 31);
+  if (lane == 0) {
+    rt.offs[U] = total;
+    rt.n_uniq = U;
+    rt.n_pairs = total;
+  }
+  __syncwarp();
+  for (int u = lane; u < U; u += 32) rt.cnt[u] = 0;
+  __syncwarp();
+  // stable placement, 32 pairs at a time: equal experts in one batch are ordered by lane
+  for (int b = 0; b < n; b += 32) {
+    const int p = b + lane;
+    const int e = p < n ? ids[p] : -1;
+    const bool valid = e >= 0 && e < n_experts;
+    const int key = valid ? e : -1 - lane;  // invalid lanes match nobody
+    const uint32_t peers = __match_any_sync(0xffffffffu, key);
+    int r = 0, pos = 0;
+    if (valid) {
+      r = route_rank(rt, e);
+      pos = rt.offs[r] + rt.cnt[r] + __popc(peers & ((1u << lane) - 1u));
+      rt.pairs[pos] = static_cast<short>(p);
+    }
+    __syncwarp();
+    if (valid && (__ffs(peers) - 1) == lane) rt.cnt[r] += __popc(peers);
+    __syncwarp();
+  }
+}
+
 // ================================================================== phase A
 struct ChunkA {
   int k;   // slot (routed) or shared expert index
