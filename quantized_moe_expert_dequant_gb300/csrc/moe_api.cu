@@ -81,6 +81,8 @@ struct Prepared {
   int bits_sh;       // shared-expert code width as the kernels see it
   int grid_sep;      // CTAs of the separate kernels
   int grid_fused;    // CTAs of the fused kernel (all resident)
+  bool grouped_ok;   // m > 1 forwards stream each selected expert once (fused mode)
+  moe::GroupPlan gplan;
 };
 
 int prepare(const moe_decode_config *c, Prepared &P) {
@@ -107,6 +109,11 @@ int prepare(const moe_decode_config *c, Prepared &P) {
     return MOE_ERR_CUDA;
   }
   if (P.plan.smem > (size_t)dyn_limit) return MOE_ERR_UNSUPPORTED;
+  // Batches of tokens run grouped by expert when the shape allows it; otherwise token by token.
+  P.grouped_ok = c->max_tokens > 1 && c->kernel_mode == MOE_KERNELS_FUSED &&
+                 moe::make_group_plan(P.shape, c->bits_gate, c->bits_down, P.bits_sh,
+                                      c->max_tokens, &P.gplan) &&
+                 P.gplan.smem <= (size_t)dyn_limit;
   P.grid_sep = sms;
   const int lim = moe::fused_grid_limit(P.plan, c->bits_gate, c->bits_down, P.bits_sh);
   P.grid_fused = lim < sms ? lim : sms;
@@ -161,9 +168,10 @@ cudaError_t enqueue_separate(const Prepared &P, const moe::LayerPtrs &w, float *
 
 // Fused kernel over L layers (device array `layers`) and m tokens.
 cudaError_t enqueue_fused(const Prepared &P, const moe::LayerPtrs *layers, int L, float *act,
-                          int32_t *err, uint32_t *bar, float *ping0, float *ping1, const void *x,
-                          int m, const int32_t *ids, const float *scores, const void *resid0,
-                          int resid_dtype, void *out, int out_dtype, cudaStream_t stream) {
+                          float *y, int32_t *err, uint32_t *bar, float *ping0, float *ping1,
+                          const void *x, int m, const int32_t *ids, const float *scores,
+                          const void *resid0, int resid_dtype, void *out, int out_dtype,
+                          cudaStream_t stream) {
   cudaError_t e = cudaMemsetAsync(bar, 0, sizeof(uint32_t), stream);
   if (e != cudaSuccess) return e;
   moe::StackParams p;
@@ -184,6 +192,10 @@ cudaError_t enqueue_fused(const Prepared &P, const moe::LayerPtrs *layers, int L
   p.act = act;
   p.err = err;
   p.bar = bar;
+  p.grouped = m > 1 && P.grouped_ok;
+  p.gp = P.gplan;
+  p.y = y;
+  p.act_stride = static_cast<int>(act_floats(P.cfg));
   return moe::launch_fused(p, P.grid_fused, stream);
 }
 
@@ -200,13 +212,17 @@ int read_and_clear_error(int32_t *err, int32_t *out) {
 // Device workspace of a handle or a stack.
 struct Workspace {
   float *act = nullptr;
+  float *y = nullptr;
   int32_t *err = nullptr;
   uint32_t *bar = nullptr;
   moe::LayerPtrs *layers = nullptr;
 
-  bool alloc(const moe_decode_config &c, int n_layers) {
-    const size_t na = act_floats(c);
+  // Grouped forwards keep every token's activations and per-slot partial outputs at once.
+  bool alloc(const moe_decode_config &c, int n_layers, bool grouped) {
+    const size_t na = act_floats(c) * (grouped ? c.max_tokens : 1);
+    const size_t ny = grouped ? (size_t)c.max_tokens * (c.top_k + c.n_shared) * c.din : 1;
     bool ok = cudaMalloc(&act, (na > 0 ? na : 1) * sizeof(float)) == cudaSuccess &&
+              cudaMalloc(&y, ny * sizeof(float)) == cudaSuccess &&
               cudaMalloc(&err, sizeof(int32_t)) == cudaSuccess &&
               cudaMemset(err, 0, sizeof(int32_t)) == cudaSuccess &&
               cudaMalloc(&bar, sizeof(uint32_t)) == cudaSuccess &&
@@ -216,6 +232,7 @@ struct Workspace {
   }
   void release() {
     cudaFree(act);
+    cudaFree(y);
     cudaFree(err);
     cudaFree(bar);
     cudaFree(layers);
@@ -247,7 +264,7 @@ extern "C" int moe_decode_create(const moe_decode_config *cfg, const moe_layer_w
     return rc;
   }
   h->w = layer_ptrs(*cfg, *weights);
-  if (!h->ws.alloc(*cfg, 1)) {
+  if (!h->ws.alloc(*cfg, 1, h->P.grouped_ok)) {
     h->ws.release();
     delete h;
     return MOE_ERR_OOM;
@@ -276,8 +293,8 @@ extern "C" int moe_decode_forward(moe_decode_t *h, const void *x, int32_t m, con
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   cudaError_t e;
   if (c.kernel_mode == MOE_KERNELS_FUSED)
-    e = enqueue_fused(h->P, h->ws.layers, 1, h->ws.act, h->ws.err, h->ws.bar, nullptr, nullptr, x,
-                      m, ids, scores, resid, c.resid_dtype, out, c.out_dtype, st);
+    e = enqueue_fused(h->P, h->ws.layers, 1, h->ws.act, h->ws.y, h->ws.err, h->ws.bar, nullptr,
+                      nullptr, x, m, ids, scores, resid, c.resid_dtype, out, c.out_dtype, st);
   else
     e = enqueue_separate(h->P, h->w, h->ws.act, h->ws.err, x, m, ids, scores, resid,
                          c.resid_dtype, out, c.out_dtype, st,
@@ -457,7 +474,7 @@ extern "C" int moe_stack_create(const moe_decode_config *cfg, int32_t n_layers,
   s->layers.resize(n_layers);
   for (int l = 0; l < n_layers; ++l) s->layers[l] = layer_ptrs(*cfg, layers[l]);
   const size_t M = cfg->max_tokens, din = cfg->din, K = cfg->top_k;
-  bool ok = s->ws.alloc(*cfg, n_layers) &&
+  bool ok = s->ws.alloc(*cfg, n_layers, s->P.grouped_ok) &&
             cudaMalloc(&s->ping[0], M * din * sizeof(float)) == cudaSuccess &&
             cudaMalloc(&s->ping[1], M * din * sizeof(float)) == cudaSuccess &&
             cudaMalloc(&s->x_dev, (size_t)n_layers * M * din * 2) == cudaSuccess &&
@@ -489,9 +506,9 @@ cudaError_t enqueue_stack(moe_stack *s, const void *x, int m, const int32_t *ids
   const int L = (int)s->layers.size();
   const moe_decode_config &c = s->P.cfg;
   if (c.kernel_mode == MOE_KERNELS_FUSED && parts == (MOE_PART_GATE_UP | MOE_PART_DOWN))
-    return enqueue_fused(s->P, s->ws.layers, L, s->ws.act, s->ws.err, s->ws.bar, s->ping[0],
-                         s->ping[1], x, m, ids, scores, resid0, c.resid_dtype, out, MOE_DTYPE_F32,
-                         st);
+    return enqueue_fused(s->P, s->ws.layers, L, s->ws.act, s->ws.y, s->ws.err, s->ws.bar,
+                         s->ping[0], s->ping[1], x, m, ids, scores, resid0, c.resid_dtype, out,
+                         MOE_DTYPE_F32, st);
   const size_t din = c.din, K = c.top_k;
   for (int l = 0; l < L; ++l) {
     const void *xl = static_cast<const uint16_t *>(x) + (size_t)l * m * din;

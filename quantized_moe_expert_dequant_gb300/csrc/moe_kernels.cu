@@ -16,7 +16,7 @@
 // that split (every row is computed once by threads spread over all SMs) and replaces the kernel
 // boundary with a device-wide barrier, which on GB300 also lets the second phase's weight stream
 // run under the first phase's arithmetic.
-#include "moe_phases.cuh"
+#include "moe_grouped.cuh"
 
 namespace moe {
 
@@ -101,10 +101,15 @@ __global__ void __launch_bounds__(kThreads, 1) fused_kernel(const StackParams p)
   __shared__ LayerPtrs wl;   // the consumers' copy of the current layer's pointers
   __shared__ LayerPtrs wpr;  // the producers' copy
   __shared__ int stop_pr;
-  init_ring(rs.full, rs.empty, p.plan.nst, &rs.abort);
+  init_ring(rs.full, rs.empty, p.grouped ? p.gp.nst : p.plan.nst, &rs.abort);
   __syncthreads();
-  Ring r = make_ring(rs.full, rs.empty, ring, rs.desc, p.plan, &rs.abort, p.err);
   const int tid = threadIdx.x, warp = tid >> 5;
+  if (p.grouped) {
+    fused_grouped<BR, BD, BSH>(p, ring, rs.full, rs.empty, rs.desc, &rs.abort, sm.a, wl, wpr,
+                               stop_pr, tid);
+    return;
+  }
+  Ring r = make_ring(rs.full, rs.empty, ring, rs.desc, p.plan, &rs.abort, p.err);
   const LayerShape &s = p.s;
   const uint32_t n = gridDim.x;
   const int64_t xs = static_cast<int64_t>(s.din), ks = s.top_k;
@@ -278,6 +283,49 @@ bool make_plan(const LayerShape &s, int bits_gu, int bits_d, int bits_sh, Plan *
   return true;
 }
 
+bool make_group_plan(const LayerShape &s, int bits_gu, int bits_d, int bits_sh, int m,
+                     GroupPlan *gp) {
+  if (m < 2 || m > kMaxGroupTokens || m * s.top_k > kMaxPairs || s.n_experts > kMaxGroupExperts)
+    return false;
+  const int dsh = s.n_shared > 0 ? s.dff_shared : s.dff;
+  if (!geom_a(s.din, bits_gu, &gp->ga_r) || !geom_a(s.din, bits_sh, &gp->ga_s) ||
+      !geom_a(s.dff, bits_d, &gp->gb_r) || !geom_a(dsh, bits_sh, &gp->gb_s))
+    return false;
+  const GateUpGeom *g[4] = {&gp->ga_r, &gp->ga_s, &gp->gb_r, &gp->gb_s};
+  const int op_bytes[4] = {s.din * 2, s.din * 2, s.dff * 4, dsh * 4};
+  for (int c = 0; c < 4; ++c) {
+    const int nproj = c < 2 ? 2 : 1;
+    gp->op_off[c] = align_up(nproj * g[c]->R * g[c]->rb + 2 * nproj * g[c]->sw, 16);
+  }
+  // as many pairs per stage as keep at least four stages in the ring (at least one pair)
+  const int ring_bytes = kRingBytes - kGroupSmemBytes;  // the route state precedes the ring
+  int t = m < 8 ? m : 8, st = 0;
+  for (; t >= 1; --t) {
+    st = 0;
+    for (int c = 0; c < 4; ++c) {
+      const int b = align_up(gp->op_off[c] + t * op_bytes[c], 128);
+      st = b > st ? b : st;
+    }
+    if (st * 4 <= ring_bytes) break;
+  }
+  if (t < 1) {
+    t = 1;
+    st = 0;
+    for (int c = 0; c < 4; ++c) {
+      const int b = align_up(gp->op_off[c] + op_bytes[c], 128);
+      st = b > st ? b : st;
+    }
+  }
+  int n = ring_bytes / st;
+  if (n > kMaxStages) n = kMaxStages;
+  if (n < 2) return false;
+  gp->t_sub = t;
+  gp->nst = n;
+  gp->stage_bytes = st;
+  gp->smem = static_cast<size_t>(kGroupSmemBytes) + static_cast<size_t>(n) * st;
+  return true;
+}
+
 template <typename Kern, typename P>
 static cudaError_t launch(Kern kern, const P &p, int grid, size_t smem, cudaStream_t stream,
                           bool pdl, bool cooperative) {
@@ -327,9 +375,10 @@ cudaError_t launch_down(const DownParams &p, int grid, cudaStream_t stream, bool
 static int sh_bits(const Plan &plan) { return plan.geo_s.bits; }
 
 cudaError_t launch_fused(const StackParams &p, int grid, cudaStream_t stream) {
+  const size_t smem = p.grouped ? p.gp.smem : p.plan.smem;
   MOE_BITS_SWITCH(p.plan.geo_r.bits, BR, MOE_BITS_SWITCH(p.plan.geo_b.bits_r, BD,
       MOE_BITS_SWITCH(sh_bits(p.plan), BSH,
-          return launch(fused_kernel<BR, BD, BSH>, p, grid, p.plan.smem, stream, false, true))));
+          return launch(fused_kernel<BR, BD, BSH>, p, grid, smem, stream, false, true))));
   return cudaErrorInvalidValue;
 }
 

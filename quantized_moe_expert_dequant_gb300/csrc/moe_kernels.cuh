@@ -68,6 +68,16 @@ struct Plan {
   size_t smem;
 };
 
+// Stage plan of the grouped kernels (m > 1 tokens, each selected expert streamed once).
+struct GroupPlan {
+  GateUpGeom ga_r, ga_s;   // phase A rows (length din) of routed / shared experts
+  GateUpGeom gb_r, gb_s;   // phase B rows (length dff / dff_shared) of routed / shared experts
+  int t_sub;               // (token, slot) pairs whose operand rows one stage carries
+  int op_off[4];           // operand rows' offset in a stage: A routed, A shared, B routed, B shared
+  int nst, stage_bytes;
+  size_t smem;
+};
+
 // Kernel A alone.
 struct GateUpParams {
   LayerShape s;
@@ -111,10 +121,18 @@ struct StackParams {
   float *act;
   int32_t *err;
   uint32_t *bar;            // grid-barrier counter, zero at launch
+  // grouped mode (m > 1): each selected expert streamed once per layer for all m tokens
+  int grouped;
+  GroupPlan gp;
+  float *y;                 // [m][top_k + n_shared][din] partial outputs
+  int act_stride;           // floats per token in act: top_k * dff + n_shared * dff_shared
 };
 
 // Host-side plan; false when the shape is outside what the kernels support.
 bool make_plan(const LayerShape &s, int bits_gu, int bits_d, int bits_sh, Plan *plan);
+// Grouped plan for up to m tokens; false when the shape or m is outside the grouped kernels.
+bool make_group_plan(const LayerShape &s, int bits_gu, int bits_d, int bits_sh, int m,
+                     GroupPlan *gp);
 
 cudaError_t launch_gate_up(const GateUpParams &p, int grid, cudaStream_t stream, bool pdl);
 cudaError_t launch_down(const DownParams &p, int grid, cudaStream_t stream, bool pdl);

@@ -26,13 +26,13 @@ def stack_inputs(shape, m=1, step=0):
     return x, ids, sc, resid0
 
 
-def run_chain(layers, x, ids, sc, resid0, m):
-    """The same layers, one moe_decode_forward each; returns every layer's output."""
+def run_chain(layers, x, ids, sc, resid0, m, mode=Bn.KERNELS_FUSED):
+    """The same layers, one moe_decode_forward each (same kernel mode); every layer's output."""
     outs = []
     prev = C.dev(resid0, torch.bfloat16)
     for l, ld in enumerate(layers):
         blk = Bn.MoeDecode(ld, max_tokens=m,
-                           resid_dtype=Bn.DTYPE_BF16 if l == 0 else Bn.DTYPE_F32)
+                           resid_dtype=Bn.DTYPE_BF16 if l == 0 else Bn.DTYPE_F32, kernel_mode=mode)
         o = blk.forward(C.dev(x[l], torch.bfloat16), C.dev(ids[l], torch.int32),
                         C.dev(sc[l], torch.float32), prev)
         torch.cuda.synchronize()
@@ -96,7 +96,7 @@ def test_small_stack_several_tokens(mode):
     stack.step(C.dev(x, torch.bfloat16), C.dev(ids, torch.int32), C.dev(sc, torch.float32),
                C.dev(resid0, torch.bfloat16), out)
     torch.cuda.synchronize()
-    outs = run_chain(layers, x, ids, sc, resid0, m)
+    outs = run_chain(layers, x, ids, sc, resid0, m, mode)
     assert torch.equal(out.view(torch.int32), outs[-1].view(torch.int32))
     check_layers(shape, x, ids, sc, resid0, outs, range(shape.layers), np.arange(shape.din),
                  tokens=range(m))
