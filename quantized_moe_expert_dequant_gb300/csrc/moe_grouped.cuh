@@ -12,7 +12,7 @@
 // to t_sub of its (token, slot) pairs (x rows in phase A, activation rows in phase B), all copied
 // by the bulk-copy engine, so consumers build each pair's operand from shared memory.  A shared
 // expert, or a routed expert selected by more than t_sub pairs, is staged once per group of
-// t_sub pairs; the repeats of its rows come from L2.
+// t_sub pairs (a segment); the repeats of its rows come from L2.
 #pragma once
 
 #include "moe_phases.cuh"
@@ -26,7 +26,8 @@ struct GroupDesc {
   int e;       // expert of the class: distinct-expert rank (routed) or shared expert index
   int pb, pe;  // the stage's pairs: [pb, pe) of the expert's pair list
   int delta;   // offset in bytes of the first row's first group inside each window
-  int pad0, pad1;
+  int cls;     // class of the phase: 0 routed, 1 shared
+  int j0;      // first row inside the expert
 };
 
 // Shared state of a grouped layer, written by the producer warp after it read the ids (except
@@ -41,6 +42,12 @@ struct GroupSmem {
   float sscal[kMaxGroupTokens]; // per-token shared scalar (consumers)
   int ids[kMaxPairs];           // the layer's ids [m][top_k] and scores
   float scores[kMaxPairs];
+  // Work is split into segments: one distinct expert and one group of at most t_sub of its pairs
+  // (shared experts: of the tokens).  Every segment spans the expert's rows once, so splitting
+  // the flattened segment rows evenly across CTAs balances stages, not just weight rows.
+  short seg_e[kMaxPairs];       // routed segment -> distinct-expert rank
+  short seg_pb[kMaxPairs];      // -> its first pair in that expert's list
+  int n_seg;                    // routed segments
 };
 
 constexpr int kGroupSmemBytes = (static_cast<int>(sizeof(GroupSmem)) + 127) / 128 * 128;
@@ -78,13 +85,56 @@ __device__ __forceinline__ int pair_count(const GroupSmem &gs, const GClass &c, 
   return c.shared ? m : gs.rt.offs[e + 1] - gs.rt.offs[e];
 }
 
-// Stages of a class in [a, b): one per chunk and group of t_sub pairs.
-__device__ __forceinline__ int count_g(const GroupSmem &gs, const GClass &c, const GateUpGeom &g,
-                                       int64_t a, int64_t b, int m, int t_sub) {
+// Segment k of a class: its expert (rank or shared index) and first pair; groups_sh = segments
+// per shared expert.
+__device__ __forceinline__ void segment(const GroupSmem &gs, const GClass &c, int k, int t_sub,
+                                        int groups_sh, int &e, int &pb) {
+  if (c.shared) {
+    e = k / groups_sh;
+    pb = (k - e * groups_sh) * t_sub;
+  } else {
+    e = gs.seg_e[k];
+    pb = gs.seg_pb[k];
+  }
+}
+
+// Routed segments after the route inversion: ceil(pairs / t_sub) per distinct expert, in rank
+// order (one warp; U <= kMaxPairs, so eight experts per lane).
+__device__ __forceinline__ void build_segments(GroupSmem &gs, int t_sub, int lane) {
+  constexpr int PER = kMaxPairs / 32;
+  const int U = gs.rt.n_uniq;
+  int cnt[PER], sum = 0;
+#pragma unroll
+  for (int j = 0; j < PER; ++j) {
+    const int u = lane * PER + j;
+    cnt[j] = u < U ? (gs.rt.offs[u + 1] - gs.rt.offs[u] + t_sub - 1) / t_sub : 0;
+    sum += cnt[j];
+  }
+  int incl = sum;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int t = __shfl_up_sync(0xffffffffu, incl, o);
+    if (lane >= o) incl += t;
+  }
+  int k = incl - sum;
+#pragma unroll
+  for (int j = 0; j < PER; ++j) {
+    const int u = lane * PER + j;
+    for (int g = 0; g < cnt[j]; ++g, ++k) {
+      gs.seg_e[k] = static_cast<short>(u);
+      gs.seg_pb[k] = static_cast<short>(g * t_sub);
+    }
+  }
+  if (lane == 31) gs.n_seg = incl;
+  __syncwarp();
+}
+
+// Stages of a class in [a, b): one per chunk (a chunk never crosses a segment).
+__device__ __forceinline__ int count_g(const GClass &c, const GateUpGeom &g, int64_t a, int64_t b) {
   ChunkIterA it(a, b, c.base, c.rows_pe, g.R);
   ChunkA ch;
   int n = 0;
-  while (it.next(ch)) n += (pair_count(gs, c, ch.k, m) + t_sub - 1) / t_sub;
+  while (it.next(ch)) ++n;
   return n;
 }
 
@@ -143,11 +193,11 @@ __device__ void complete_deferred(const LayerShape &s, const GroupSmem &gs, cons
   for (int i = df.begin; i < r.used; ++i) {
     const int st = i % r.nst;
     const GroupDesc d = gs.desc[st];
-    const GClass &c = cls[d.pad0];
+    const GClass &c = cls[d.cls];
     if (lane == 0)
       mbar_arrive_expect_tx(&r.full[st], static_cast<uint32_t>(d.pe - d.pb) * c.op_bytes);
     __syncwarp();
-    copy_operands(s, gs, c, d, r.base + static_cast<size_t>(st) * r.stage_bytes, op_off[d.pad0],
+    copy_operands(s, gs, c, d, r.base + static_cast<size_t>(st) * r.stage_bytes, op_off[d.cls],
                   x_l, act, act_stride, &r.full[st], lane, pol);
   }
   df.begin = r.used;
@@ -163,21 +213,26 @@ __device__ void produce_g_class(const LayerShape &s, const GroupSmem &gs, const 
                                 Deferred &df, int lane, uint64_t pol) {
   const GClass &c = cls[ci];
   const int G = c.cols / kGroup;
+  const int groups_sh = (m + t_sub - 1) / t_sub;
   ChunkIterA it(a, b, c.base, c.rows_pe, g.R);
   ChunkA ch;
   const int nproj = c.gated ? 2 : 1;
+  const uint64_t pol_first = policy_evict_first(), pol_again = policy_evict_normal();
   while (it.next(ch)) {
-    const int e = ch.k;
+    int e, pb;
+    segment(gs, c, ch.k, t_sub, groups_sh, e, pb);
     const int expert = c.shared ? e : gs.rt.uniq[e];
     const int np = pair_count(gs, c, e, m);
+    const int pe = pb + t_sub < np ? pb + t_sub : np;
+    // rows staged again for the expert's other pair groups stay in L2 for them
+    const uint64_t pol = np > t_sub ? pol_again : pol_first;
     const int64_t row = static_cast<int64_t>(expert) * c.rows_pe + ch.j;
     const uint32_t code_bytes = static_cast<uint32_t>(ch.n) * g.rb;
     const int64_t ng = static_cast<int64_t>(ch.n) * G;
-    for (int pb = 0; pb < np; pb += t_sub) {
-      const int pe = pb + t_sub < np ? pb + t_sub : np;
+    {
       // the slot's previous use must be releasable: complete waiting stages first
       if (df.on && !df.ready && df.begin < r.used && r.used - r.nst >= df.begin)
-        complete_deferred(s, gs, cls, op_off, df, r, lane, x_l, act, act_stride, pol);
+        complete_deferred(s, gs, cls, op_off, df, r, lane, x_l, act, act_stride, pol_first);
       if (!ring_claim(r, lane)) return;
       uint8_t *sb = r.stage();
       const Window w0 = window_of(c.p0.scales + row * G, ng);
@@ -192,7 +247,7 @@ __device__ void produce_g_class(const LayerShape &s, const GroupSmem &gs, const 
       const uint32_t obytes = static_cast<uint32_t>(pe - pb) * c.op_bytes;
       const bool later = df.on && !df.ready;
       const GroupDesc d{ch.u - static_cast<int>(c.base), ch.n, e, pb, pe,
-                        static_cast<int>(w0.delta), ci, 0};
+                        static_cast<int>(w0.delta), ci, ch.j};
       uint8_t *wb = sb + nproj * g.R * g.rb;
       if (lane == 0) {
         desc[r.st] = d;
@@ -212,15 +267,16 @@ __device__ void produce_g_class(const LayerShape &s, const GroupSmem &gs, const 
         if (lane == 5) bulk_g2s(wb + 3 * g.sw, w3.src, w3.bytes, &r.full[r.st], pol);
       }
       if (!later)
-        copy_operands(s, gs, c, d, sb, op_off[ci], x_l, act, act_stride, &r.full[r.st], lane, pol);
+        copy_operands(s, gs, c, d, sb, op_off[ci], x_l, act, act_stride, &r.full[r.st], lane,
+                      pol_first);
       r.advance();
     }
   }
 }
 
-// Producer of one grouped phase (two classes): counts its stages into cnt[0..1], streams them,
-// and hands out one empty stage when the CTA has none.  With deferred operands, the waiting
-// stages are completed at the end.
+// Producer of one grouped phase (two classes of n_r and n_s segments): counts its stages into
+// cnt[0..1], streams them, and hands out one empty stage when the CTA has none.  With deferred
+// operands, the waiting stages are completed at the end.
 __device__ void produce_g_phase(const LayerShape &s, const GroupSmem &gs, GroupDesc *desc,
                                 int *cnt, const GClass *cls, const GateUpGeom &gr,
                                 const GateUpGeom &gsh, int64_t n_r, int64_t n_s, int m,
@@ -228,8 +284,8 @@ __device__ void produce_g_phase(const LayerShape &s, const GroupSmem &gs, GroupD
                                 const float *act, int act_stride, Deferred &df, Ring &r,
                                 int lane, uint64_t pol) {
   const RangeG rg = range_g(n_r, cls[0].rows_pe, n_s, cls[1].rows_pe);
-  const int nr = count_g(gs, cls[0], gr, rg.ra, rg.rb, m, t_sub);
-  const int ns = count_g(gs, cls[1], gsh, rg.sa, rg.sb, m, t_sub);
+  const int nr = count_g(cls[0], gr, rg.ra, rg.rb);
+  const int ns = count_g(cls[1], gsh, rg.sa, rg.sb);
   if (lane == 0) {
     cnt[0] = nr;
     cnt[1] = ns;
@@ -320,7 +376,7 @@ __device__ int consume_g_class(const LayerShape &s, const GroupSmem &gs, const G
                                const float *scores_s, float *outp, Ring &r, SmemA &sm,
                                bool &waited, bool &ok, int tid) {
   constexpr int VEC = Fmt<BITS>::kVecs, C = Operand<BITS>::C;
-  constexpr int RPT = rows_per_thread_a<BITS>();
+  constexpr int RPT = GATED ? rows_per_thread_a<BITS>() : rows_per_thread_gb<BITS>();
   constexpr int V = GATED ? 2 * RPT : RPT;
   int held = 0;
   if (count == 0) return held;
@@ -346,7 +402,7 @@ __device__ int consume_g_class(const LayerShape &s, const GroupSmem &gs, const G
     const GroupDesc d = gs.desc[r.st];
     const uint8_t *sb = r.stage();
     const uint8_t *ws = sb + wbase + d.delta;
-    const int j0 = d.u - d.e * c.rows_pe;  // first row inside the expert
+    const int j0 = d.j0;
     for (int q = d.pb; q < d.pe; ++q) {
       int m, col;
       float coef;
@@ -474,15 +530,16 @@ __device__ __forceinline__ void shared_scalars_g(const LayerShape &s, const uint
   }
 }
 
-// The classes of a grouped layer: phase A (gate/up) and phase B (down), routed then shared.
-__device__ __forceinline__ void group_classes(const LayerShape &s, const LayerPtrs &w, int n_uniq,
+// The classes of a grouped layer: phase A (gate/up) and phase B (down), routed then shared; the
+// shared class's rows follow n_seg routed segments.
+__device__ __forceinline__ void group_classes(const LayerShape &s, const LayerPtrs &w, int n_seg,
                                               GClass *ca, GClass *cb) {
   const int dsh = s.n_shared > 0 ? s.dff_shared : s.dff;
   ca[0] = GClass{true, false, s.dff, 0, w.gate, w.up, s.din, s.din * 2};
-  ca[1] = GClass{true, true, dsh, static_cast<int64_t>(n_uniq) * s.dff, w.sh_gate, w.sh_up, s.din,
+  ca[1] = GClass{true, true, dsh, static_cast<int64_t>(n_seg) * s.dff, w.sh_gate, w.sh_up, s.din,
                  s.din * 2};
   cb[0] = GClass{false, false, s.din, 0, w.down, w.down, s.dff, s.dff * 4};
-  cb[1] = GClass{false, true, s.din, static_cast<int64_t>(n_uniq) * s.din, w.sh_down, w.sh_down,
+  cb[1] = GClass{false, true, s.din, static_cast<int64_t>(n_seg) * s.din, w.sh_down, w.sh_down,
                  dsh, dsh * 4};
 }
 
@@ -529,18 +586,18 @@ __device__ void fused_grouped(const StackParams &p, uint8_t *dyn, uint64_t *full
         gs.pm[q] = static_cast<unsigned char>(pp / K);
         gs.pk[q] = static_cast<unsigned char>(pp % K);
       }
-      __syncwarp();
+      build_segments(gs, p.gp.t_sub, pl);
+      const int n_seg_s = s.n_shared * ((m + p.gp.t_sub - 1) / p.gp.t_sub);
       const uint16_t *x_l = p.x + static_cast<int64_t>(l) * m * s.din;
       GClass ca[2], cb[2];
-      group_classes(s, wpr, gs.rt.n_uniq, ca, cb);
+      group_classes(s, wpr, gs.n_seg, ca, cb);
       Deferred none{false, true, 0, p.bar, 0};
-      produce_g_phase(s, gs, gs.desc, gs.cnt, ca, p.gp.ga_r, p.gp.ga_s, gs.rt.n_uniq, s.n_shared, m,
+      produce_g_phase(s, gs, gs.desc, gs.cnt, ca, p.gp.ga_r, p.gp.ga_s, gs.n_seg, n_seg_s, m,
                       p.gp.t_sub, p.gp.op_off, x_l, p.act, p.act_stride, none, r, pl, pol);
       if (flag_abort(abort)) break;
       Deferred df{true, false, 0, p.bar, (3u * l + 1u) * n};
-      produce_g_phase(s, gs, gs.desc, gs.cnt + 2, cb, p.gp.gb_r, p.gp.gb_s, gs.rt.n_uniq,
-                      s.n_shared, m, p.gp.t_sub, p.gp.op_off + 2, x_l, p.act, p.act_stride, df, r,
-                      pl, pol);
+      produce_g_phase(s, gs, gs.desc, gs.cnt + 2, cb, p.gp.gb_r, p.gp.gb_s, gs.n_seg, n_seg_s, m,
+                      p.gp.t_sub, p.gp.op_off + 2, x_l, p.act, p.act_stride, df, r, pl, pol);
       if (flag_abort(abort)) break;
     }
     ring_drain(r, pl);  // never leave with copies in flight

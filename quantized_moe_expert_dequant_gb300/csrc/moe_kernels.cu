@@ -216,18 +216,23 @@ __global__ void route_invert_kernel(const int32_t *ids, int n, int n_experts, in
 static int fmt_codes(int bits) { return bits == 4 ? 32 : bits == 8 ? 16 : 64; }
 static int align_up(int v, int a) { return (v + a - 1) / a * a; }
 
-static bool geom_a(int din, int bits, GateUpGeom *g) {
+// Rows of `cols` codes, `rpt` rows per thread in a stage; the rows' partial sums are parked per
+// warp, so R * warps-per-row must fit the parking area (kRedA entries, kBatchA rows).
+static bool geom_rows(int cols, int bits, int rpt, GateUpGeom *g) {
   const int C = fmt_codes(bits);
   g->bits = bits;
-  g->T = din / C;
+  g->T = cols / C;
   if (g->T < 1 || g->T > kConsumers) return false;
   g->tpr = align_up(g->T, 32);
   g->groups = kConsumers / g->tpr;
-  const int rpt = bits == 6 ? 1 : 2;
   g->R = rpt * g->groups;
-  g->rb = din * bits / 8;
-  g->sw = align_up(g->R * (din / 64) * 2 + 14, 16);
-  return g->R * (g->tpr / 32) <= 32;
+  g->rb = cols * bits / 8;
+  g->sw = align_up(g->R * (cols / 64) * 2 + 14, 16);
+  return g->R * (g->tpr / 32) <= kRedA && g->R <= kBatchA;
+}
+
+static bool geom_a(int din, int bits, GateUpGeom *g) {
+  return geom_rows(din, bits, rows_per_thread_a_host(bits), g);
 }
 
 static int stage_a(const GateUpGeom &g) { return align_up(2 * g.R * g.rb + 4 * g.sw, 128); }
@@ -289,7 +294,8 @@ bool make_group_plan(const LayerShape &s, int bits_gu, int bits_d, int bits_sh, 
     return false;
   const int dsh = s.n_shared > 0 ? s.dff_shared : s.dff;
   if (!geom_a(s.din, bits_gu, &gp->ga_r) || !geom_a(s.din, bits_sh, &gp->ga_s) ||
-      !geom_a(s.dff, bits_d, &gp->gb_r) || !geom_a(dsh, bits_sh, &gp->gb_s))
+      !geom_rows(s.dff, bits_d, rows_per_thread_gb_host(bits_d), &gp->gb_r) ||
+      !geom_rows(dsh, bits_sh, rows_per_thread_gb_host(bits_sh), &gp->gb_s))
     return false;
   const GateUpGeom *g[4] = {&gp->ga_r, &gp->ga_s, &gp->gb_r, &gp->gb_s};
   const int op_bytes[4] = {s.din * 2, s.din * 2, s.dff * 4, dsh * 4};

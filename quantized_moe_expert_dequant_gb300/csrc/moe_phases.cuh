@@ -30,6 +30,15 @@ __host__ __device__ constexpr int rows_per_thread_a() {
   return BITS == 6 ? 1 : 2;
 }
 
+// Grouped phase B builds an operand per (stage, pair) and uses it for this many rows per thread.
+template <int BITS>
+__host__ __device__ constexpr int rows_per_thread_gb() {
+  return BITS == 6 ? 2 : 4;
+}
+
+inline int rows_per_thread_a_host(int bits) { return bits == 6 ? 1 : 2; }
+inline int rows_per_thread_gb_host(int bits) { return bits == 6 ? 2 : 4; }
+
 template <int V>
 struct Log2 {
   static constexpr int v = V == 1 ? 0 : V == 2 ? 1 : V == 4 ? 2 : V == 8 ? 3 : -1;
@@ -836,7 +845,6 @@ __device__ void consume_b_spt(const LayerShape &s, const DownGeom &g, const int 
                               const float *act, const float *resid_s, void *out, int out_f32,
                               Ring &r, SmemB &sm, int tid) {
   constexpr int CR = Fmt<BD>::kCodes, CS = Fmt<BSD>::kCodes;
-  constexpr int CMAX = CR > CS ? CR : CS;
   constexpr int VS = 4;             // rows per thread per stage, at most
   const int warp = tid >> 5, lane = tid & 31;
   int i0, i1;

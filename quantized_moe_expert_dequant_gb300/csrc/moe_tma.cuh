@@ -109,6 +109,13 @@ __device__ __forceinline__ uint64_t policy_evict_first() {
   return p;
 }
 
+// L2 policy for weights that are read again soon (a grouped expert staged once per pair group).
+__device__ __forceinline__ uint64_t policy_evict_normal() {
+  uint64_t p;
+  asm volatile("createpolicy.fractional.L2::evict_normal.b64 %0, 1.0;" : "=l"(p));
+  return p;
+}
+
 // Named barrier over the producer warps only.
 __device__ __forceinline__ void producer_sync() {
   asm volatile("bar.sync 2, %0;" ::"n"(32) : "memory");
