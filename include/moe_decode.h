@@ -226,6 +226,15 @@ int moe_synth_biases(void *dst, const void *scales, uint64_t key, int32_t expert
 int moe_route_invert_device(const int32_t *ids, int32_t m, int32_t k, int32_t n_experts,
                             int32_t *out, void *stream);
 
+/* Exercises the bounded-wait path of the kernels without any fault: one thread waits, with the
+ * kernels' own wait functions and a limit of about 0.1 s, on a condition nothing satisfies --
+ * kind 0 a grid-barrier count (in scratch, which the call zeroes; int32 device, 4-byte aligned),
+ * kind 1 an mbarrier stage that no producer fills.  The wait gives up, ORs the time-out bit (2)
+ * into device_error (int32 device) and the kernel returns; the context stays usable.  Asynchronous
+ * on stream.  No counterpart on the pages: it checks this implementation's guarantee that no
+ * wait runs forever. */
+int moe_debug_wait_timeout(int32_t kind, int32_t *scratch, int32_t *device_error, void *stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -33,7 +33,8 @@ EXPORTS = ["moe_decode_create", "moe_decode_forward", "moe_decode_get_error", "m
            "moe_stack_create", "moe_stack_step", "moe_stack_step_parts", "moe_stack_step_host",
            "moe_stack_get_error",
            "moe_stack_destroy", "moe_pack_codes", "moe_unpack_codes", "moe_unpack_codes_device",
-           "moe_synth_codes", "moe_synth_scales", "moe_synth_biases", "moe_route_invert_device"]
+           "moe_synth_codes", "moe_synth_scales", "moe_synth_biases", "moe_route_invert_device",
+           "moe_debug_wait_timeout"]
 
 
 class MoeError(RuntimeError):
@@ -94,6 +95,7 @@ def lib() -> ctypes.CDLL:
                 "moe_synth_scales": [vp, u64, i32, i32, i64, vp],
                 "moe_synth_biases": [vp, vp, u64, i32, i32, i64, i32, vp],
                 "moe_route_invert_device": [vp, i32, i32, i32, vp, vp],
+                "moe_debug_wait_timeout": [i32, vp, vp, vp],
             }
             for name, args in sig.items():
                 f = getattr(L, name)
@@ -361,4 +363,12 @@ def route_invert_device(ids: torch.Tensor, n_experts: int, stream=None):
     offs = o[1 + u:2 + 2 * u]
     pairs = o[2 + 2 * u:2 + 2 * u + int(offs[-1])]
     return uniq.copy(), offs.copy(), pairs.copy()
+
+
+def debug_wait_timeout(kind: int, device_error: torch.Tensor, stream=None) -> None:
+    """Runs the kernels' bounded wait on a condition nothing satisfies (kind 0: grid-barrier
+    count, 1: mbarrier stage); the time-out bit lands in device_error (int32 [1], device)."""
+    scratch = torch.zeros(1, dtype=torch.int32, device=device_error.device)
+    check("moe_debug_wait_timeout", lib().moe_debug_wait_timeout(kind, _p(scratch), _p(device_error),
+                                                                 _stream(stream)))
 

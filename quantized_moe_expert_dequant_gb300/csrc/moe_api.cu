@@ -647,3 +647,17 @@ extern "C" int moe_route_invert_device(const int32_t *ids, int32_t m, int32_t k,
              : MOE_ERR_CUDA;
 }
 
+// ====================================================================== bounded-wait check
+extern "C" int moe_debug_wait_timeout(int32_t kind, int32_t *scratch, int32_t *device_error,
+                                      void *stream) {
+  if ((kind != 0 && kind != 1) || !scratch || !device_error) return MOE_ERR_INVALID_ARG;
+  if (!aligned(scratch, 4) || !aligned(device_error, 4)) return MOE_ERR_INVALID_ARG;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  if (cudaMemsetAsync(scratch, 0, sizeof(int32_t), st) != cudaSuccess) return MOE_ERR_CUDA;
+  // about 0.1 s at GB300 clocks
+  return moe::launch_wait_timeout(kind, reinterpret_cast<uint32_t *>(scratch), device_error,
+                                  200000000LL, st) == cudaSuccess
+             ? MOE_OK
+             : MOE_ERR_CUDA;
+}
+

@@ -197,6 +197,27 @@ __global__ void unpack_kernel(const uint8_t *packed, int64_t rows, int64_t cols,
   }
 }
 
+// ================================================================== bounded waits
+// Waits, with the kernels' own wait functions and a short limit, on a condition nothing will
+// satisfy: kind 0 a grid-barrier count (a zeroed counter that nobody increments), kind 1 an
+// mbarrier stage that no producer fills.  The wait gives up, records the time-out in the error
+// word and the kernel returns normally.
+__global__ void wait_timeout_kernel(int kind, uint32_t *cnt, int32_t *err, long long limit) {
+  __shared__ __align__(8) uint64_t bar;
+  __shared__ int abort_s;
+  if (threadIdx.x == 0) {
+    mbar_init(&bar, 1);
+    abort_s = 0;
+    mbar_fence_init();
+  }
+  __syncthreads();
+  if (threadIdx.x != 0) return;
+  if (kind == 0)
+    wait_count(cnt, 1u, &abort_s, err, limit);
+  else
+    ring_wait(&bar, 0u, &abort_s, err, limit);
+}
+
 // ================================================================== debug route inversion
 __global__ void route_invert_kernel(const int32_t *ids, int n, int n_experts, int32_t *out) {
   __shared__ Route rt;
@@ -448,6 +469,12 @@ cudaError_t launch_unpack(const uint8_t *packed, int64_t rows, int64_t cols, int
   int grid = (int)((steps + 255) / 256);
   grid = grid < 1 ? 1 : (grid > 65535 ? 65535 : grid);
   MOE_BITS_SWITCH(bits, B, unpack_kernel<B><<<grid, 256, 0, stream>>>(packed, rows, cols, codes));
+  return cudaGetLastError();
+}
+
+cudaError_t launch_wait_timeout(int kind, uint32_t *cnt, int32_t *err, long long limit,
+                                cudaStream_t stream) {
+  wait_timeout_kernel<<<1, 32, 0, stream>>>(kind, cnt, err, limit);
   return cudaGetLastError();
 }
 

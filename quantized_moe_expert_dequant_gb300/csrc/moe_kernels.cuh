@@ -142,6 +142,10 @@ cudaError_t prepare_kernels(int smem_optin, int bits_gu, int bits_d, int bits_sh
 int fused_grid_limit(const Plan &plan, int bits_gu, int bits_d, int bits_sh);
 cudaError_t launch_unpack(const uint8_t *packed, int64_t rows, int64_t cols, int bits,
                           uint8_t *codes, cudaStream_t stream);
+// The kernels' bounded wait on a condition nothing satisfies (kind 0: grid-barrier count at cnt,
+// which must be zero; kind 1: an mbarrier stage), giving up after `limit` cycles.
+cudaError_t launch_wait_timeout(int kind, uint32_t *cnt, int32_t *err, long long limit,
+                                cudaStream_t stream);
 // Route inversion of ids [m][k] by the device code the grouped kernels use; writes
 // out[0] = U, then uniq[U], offs[U + 1], pairs[offs[U]].
 cudaError_t launch_route_invert(const int32_t *ids, int m, int k, int n_experts, int32_t *out,

@@ -194,13 +194,13 @@ __device__ __forceinline__ void set_timeout(int *abort, int32_t *err) {
 }
 
 __device__ __forceinline__ bool ring_wait(uint64_t *bar, uint32_t parity, int *abort,
-                                          int32_t *err) {
+                                          int32_t *err, long long limit = kWaitCycles) {
   if (flag_abort(abort)) return false;
   if (mbar_try_wait(bar, parity)) return true;
   const long long t0 = clock64();
   while (!mbar_try_wait(bar, parity)) {
     if (flag_abort(abort)) return false;
-    if (clock64() - t0 > kWaitCycles) {
+    if (clock64() - t0 > limit) {
       set_timeout(abort, err);
       return false;
     }
@@ -258,12 +258,12 @@ __device__ __forceinline__ void red_release_add(uint32_t *p, uint32_t v) {
 
 // Waits until *cnt >= target (bounded).  Only meaningful when every CTA of the grid is resident.
 __device__ __forceinline__ bool wait_count(const uint32_t *cnt, uint32_t target, int *abort,
-                                           int32_t *err) {
+                                           int32_t *err, long long limit = kWaitCycles) {
   if (ld_acquire(cnt) >= target) return true;
   const long long t0 = clock64();
   while (ld_acquire(cnt) < target) {
     if (flag_abort(abort)) return false;
-    if (clock64() - t0 > kWaitCycles) {
+    if (clock64() - t0 > limit) {
       set_timeout(abort, err);
       return false;
     }
