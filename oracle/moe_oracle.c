@@ -196,3 +196,27 @@ int32_t oracle_route_invert(const int32_t *ids, int32_t m, int32_t k, int32_t n_
   return u;
 }
 
+/* Router of one token: the k largest of n_experts logits (fp32), larger first and, between equal
+ * logits, the lower expert id first; scores are the softmax of the chosen logits over those k
+ * ("Red Lite dev39 -- fused expert tail": the GPU-routed decode takes a top-k pool with weights
+ * before the expert tail).  The ids are decided on the fp32 values as given (comparisons only);
+ * the scores are computed in double and rounded to fp32.  Plain definition: k passes, each
+ * taking the best remaining logit. */
+void oracle_router(const float *logits, int32_t n_experts, int32_t k, int32_t *ids,
+                   float *scores) {
+  for (int32_t t = 0; t < k; ++t) {
+    int32_t best = -1;
+    for (int32_t e = 0; e < n_experts; ++e) {
+      int32_t taken = 0;
+      for (int32_t q = 0; q < t; ++q) taken |= ids[q] == e;
+      if (taken) continue;
+      if (best < 0 || logits[e] > logits[best]) best = e;  /* ties keep the lower id */
+    }
+    ids[t] = best;
+  }
+  double mx = -INFINITY, sum = 0.0;
+  for (int32_t t = 0; t < k; ++t) mx = fmax(mx, (double)logits[ids[t]]);
+  for (int32_t t = 0; t < k; ++t) sum += exp((double)logits[ids[t]] - mx);
+  for (int32_t t = 0; t < k; ++t) scores[t] = (float)(exp((double)logits[ids[t]] - mx) / sum);
+}
+

@@ -77,6 +77,9 @@ def lib():
             L.oracle_route_invert.argtypes = [ctypes.c_void_p, ctypes.c_int32, ctypes.c_int32,
                                               ctypes.c_int32, ctypes.c_void_p, ctypes.c_void_p,
                                               ctypes.c_void_p]
+            L.oracle_router.restype = None
+            L.oracle_router.argtypes = [ctypes.c_void_p, ctypes.c_int32, ctypes.c_int32,
+                                        ctypes.c_void_p, ctypes.c_void_p]
             _lib = L
     return _lib
 
@@ -232,4 +235,13 @@ def route_invert(ids: np.ndarray, n_experts: int):
     pairs = np.empty(max(n, 1), np.int32)
     u = lib().oracle_route_invert(_ptr(ids), m, k, n_experts, _ptr(uniq), _ptr(offs), _ptr(pairs))
     return uniq[:u].copy(), offs[:u + 1].copy(), pairs[:offs[u]].copy()
+
+
+def router(logits: np.ndarray, k: int):
+    """(ids int32 [k], scores float32 [k]) of one token's fp32 logits [E] (see oracle_router)."""
+    logits = np.ascontiguousarray(logits, dtype=np.float32)
+    ids = np.empty(k, np.int32)
+    scores = np.empty(k, np.float32)
+    lib().oracle_router(_ptr(logits), len(logits), k, _ptr(ids), _ptr(scores))
+    return ids, scores
 

@@ -41,6 +41,10 @@ MUTANTS = {
                                            "    if (found) {\n      uniq[u++] = n_experts - 1 - e;"),
     "inversion drops the last pair": ("for (int32_t p = 0; p < m * k; ++p) {",
                                       "for (int32_t p = 0; p < m * k - 1; ++p) {"),
+    "router ties keep the higher id": ("if (best < 0 || logits[e] > logits[best]) best = e;",
+                                       "if (best < 0 || logits[e] >= logits[best]) best = e;"),
+    "router softmax without the max shift": ("sum += exp((double)logits[ids[t]] - mx);",
+                                             "sum += exp((double)logits[ids[t]]);"),
 }
 
 

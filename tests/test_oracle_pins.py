@@ -377,3 +377,46 @@ def test_route_invert_special_cases():
     # nothing valid
     uniq, offs, pairs = O.route_invert(np.array([[-3, 7]], np.int32), 5)
     assert len(uniq) == 0 and offs.tolist() == [0] and len(pairs) == 0
+
+
+# ---------------------------------------------------------------- router (top-k pool with softmax weights)
+
+def _brute_router(logits, k):
+    """Independent restatement: a stable sort on (-logit, id), softmax with numpy in float64."""
+    order = sorted(range(len(logits)), key=lambda e: (-float(logits[e]), e))[:k]
+    z = np.array([float(logits[e]) for e in order])
+    w = np.exp(z - z.max())
+    return np.array(order, np.int32), (w / w.sum()).astype(np.float32)
+
+
+@pytest.mark.parametrize("E,k,seed", [(128, 8, 1), (60, 4, 2), (512, 10, 3), (128, 6, 4), (5, 5, 5),
+                                      (1024, 64, 6)])
+def test_router_matches_brute_force(E, k, seed):
+    logits = np.random.default_rng(seed).standard_normal(E).astype(np.float32)
+    ids, scores = O.router(logits, k)
+    bi, bs = _brute_router(logits, k)
+    assert np.array_equal(ids, bi)
+    np.testing.assert_allclose(scores, bs, rtol=1e-6, atol=0)
+    assert abs(float(np.sum(scores.astype(np.float64))) - 1.0) < 1e-6
+    assert np.all(np.diff(logits[ids]) <= 0)          # larger logits first
+
+
+def test_router_ties_and_special_cases():
+    logits = np.array([0.5, 2.0, 2.0, -1.0, 2.0, 0.5], np.float32)
+    ids, scores = O.router(logits, 4)
+    assert ids.tolist() == [1, 2, 4, 0]                  # equal logits: lower id first
+    assert np.allclose(scores[:3], scores[0]) and scores[3] < scores[0]
+    ids, scores = O.router(logits, 1)
+    assert ids.tolist() == [1] and scores.tolist() == [1.0]   # one slot: weight exactly 1
+    # k = E: every expert, ordered; the weights are the full softmax
+    z = np.array([3.0, -2.0, 0.0], np.float32)
+    ids, scores = O.router(z, 3)
+    assert ids.tolist() == [0, 2, 1]
+    e = np.exp(np.array([3.0, 0.0, -2.0]) - 3.0)
+    np.testing.assert_allclose(scores, e / e.sum(), rtol=1e-7)
+    # shifting every logit by a constant changes no id and no weight (beyond rounding)
+    logits = np.random.default_rng(9).standard_normal(64).astype(np.float32)
+    i1, s1 = O.router(logits, 8)
+    i2, s2 = O.router(logits + np.float32(4.0), 8)
+    assert np.array_equal(i1, i2)
+    np.testing.assert_allclose(s1, s2, rtol=1e-5)
