@@ -226,6 +226,19 @@ int moe_synth_biases(void *dst, const void *scales, uint64_t key, int32_t expert
 int moe_route_invert_device(const int32_t *ids, int32_t m, int32_t k, int32_t n_experts,
                             int32_t *out, void *stream);
 
+/* The router step before the block: for each of m tokens, the top_k of n_experts fp32 logits
+ * (larger first; between equal logits the lower expert id first) and the softmax of the chosen
+ * logits over those top_k -- the top-k pool with weights that "Red Lite dev39 -- fused expert tail"
+ * (Change) feeds to the expert tail in GPU-routed decode.
+ *   logits  fp32 [m][n_experts] device (no NaN)
+ *   ids     int32 [m][top_k] device: expert ids in pool order
+ *   scores  fp32 [m][top_k] device: weights in the same order, summing to 1 (fp32 rounding)
+ * Asynchronous on stream.  Limits: 1 <= top_k <= min(64, n_experts), n_experts <= 1024
+ * (MOE_ERR_UNSUPPORTED beyond).  The pages give the pool and its weights, not the selection rule;
+ * ties to the lower id is this implementation's. */
+int moe_router_topk(const float *logits, int32_t m, int32_t n_experts, int32_t top_k,
+                    int32_t *ids, float *scores, void *stream);
+
 /* Exercises the bounded-wait path of the kernels without any fault: one thread waits, with the
  * kernels' own wait functions and a limit of about 0.1 s, on a condition nothing satisfies --
  * kind 0 a grid-barrier count (in scratch, which the call zeroes; int32 device, 4-byte aligned),

@@ -34,7 +34,7 @@ EXPORTS = ["moe_decode_create", "moe_decode_forward", "moe_decode_get_error", "m
            "moe_stack_get_error",
            "moe_stack_destroy", "moe_pack_codes", "moe_unpack_codes", "moe_unpack_codes_device",
            "moe_synth_codes", "moe_synth_scales", "moe_synth_biases", "moe_route_invert_device",
-           "moe_debug_wait_timeout"]
+           "moe_debug_wait_timeout", "moe_router_topk"]
 
 
 class MoeError(RuntimeError):
@@ -96,6 +96,7 @@ def lib() -> ctypes.CDLL:
                 "moe_synth_biases": [vp, vp, u64, i32, i32, i64, i32, vp],
                 "moe_route_invert_device": [vp, i32, i32, i32, vp, vp],
                 "moe_debug_wait_timeout": [i32, vp, vp, vp],
+                "moe_router_topk": [vp, i32, i32, i32, vp, vp, vp],
             }
             for name, args in sig.items():
                 f = getattr(L, name)
@@ -371,4 +372,14 @@ def debug_wait_timeout(kind: int, device_error: torch.Tensor, stream=None) -> No
     scratch = torch.zeros(1, dtype=torch.int32, device=device_error.device)
     check("moe_debug_wait_timeout", lib().moe_debug_wait_timeout(kind, _p(scratch), _p(device_error),
                                                                  _stream(stream)))
+
+
+def router_topk(logits: torch.Tensor, top_k: int, stream=None):
+    """moe_router_topk on fp32 logits [m, E] (device): (ids int32 [m, top_k], scores fp32)."""
+    m, E = logits.shape
+    ids = torch.empty((m, top_k), dtype=torch.int32, device=logits.device)
+    scores = torch.empty((m, top_k), dtype=torch.float32, device=logits.device)
+    check("moe_router_topk", lib().moe_router_topk(_p(logits.contiguous()), m, E, top_k, _p(ids),
+                                                   _p(scores), _stream(stream)))
+    return ids, scores
 

@@ -661,3 +661,16 @@ extern "C" int moe_debug_wait_timeout(int32_t kind, int32_t *scratch, int32_t *d
              : MOE_ERR_CUDA;
 }
 
+// ====================================================================== router
+extern "C" int moe_router_topk(const float *logits, int32_t m, int32_t n_experts, int32_t top_k,
+                               int32_t *ids, float *scores, void *stream) {
+  if (!logits || !ids || !scores || m < 1 || n_experts < 1 || top_k < 1 || top_k > n_experts)
+    return MOE_ERR_INVALID_ARG;
+  if (n_experts > 1024 || top_k > moe::kMaxTopK) return MOE_ERR_UNSUPPORTED;
+  if (!aligned(logits, 4) || !aligned(ids, 4) || !aligned(scores, 4)) return MOE_ERR_INVALID_ARG;
+  return moe::launch_router(logits, m, n_experts, top_k, ids, scores,
+                            static_cast<cudaStream_t>(stream)) == cudaSuccess
+             ? MOE_OK
+             : MOE_ERR_CUDA;
+}
+

@@ -197,6 +197,74 @@ __global__ void unpack_kernel(const uint8_t *packed, int64_t rows, int64_t cols,
   }
 }
 
+// ================================================================== router
+// One warp per token: lane l holds logits l, l + 32, ... (n_experts <= 1024).  k rounds of a warp
+// arg-max on (logit, then lower id) pick the pool in order; the weights are the softmax of the
+// picked logits, exponentials by lanes t < k and a fixed-order warp sum.
+__device__ __forceinline__ bool better(float a, int ia, float b, int ib) {
+  return a > b || (a == b && ia < ib);
+}
+
+__global__ void router_kernel(const float *logits, int m, int n_experts, int k, int32_t *ids,
+                              float *scores) {
+  const int warp = (blockIdx.x * blockDim.x + threadIdx.x) >> 5, lane = threadIdx.x & 31;
+  if (warp >= m) return;
+  const float *lg = logits + static_cast<int64_t>(warp) * n_experts;
+  float v[32];
+#pragma unroll
+  for (int j = 0; j < 32; ++j) {
+    const int e = lane + 32 * j;
+    v[j] = e < n_experts ? lg[e] : 0.f;
+  }
+  uint32_t taken = 0u;       // bit j: expert lane + 32 j is in the pool
+  float first = 0.f;         // the largest logit (first pick)
+  float pick0 = 0.f, pick1 = 0.f;  // this lane's picks: pool positions lane and lane + 32
+  int id0 = 0, id1 = 0;
+  for (int t = 0; t < k; ++t) {
+    float bv = 0.f;
+    int bi = -1;
+#pragma unroll
+    for (int j = 0; j < 32; ++j) {
+      const int e = lane + 32 * j;
+      if (e < n_experts && !((taken >> j) & 1u) && (bi < 0 || better(v[j], e, bv, bi))) {
+        bv = v[j];
+        bi = e;
+      }
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+      const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
+      const int oi = __shfl_xor_sync(0xffffffffu, bi, o);
+      if (oi >= 0 && (bi < 0 || better(ov, oi, bv, bi))) {
+        bv = ov;
+        bi = oi;
+      }
+    }
+    if ((bi & 31) == lane) taken |= 1u << (bi >> 5);
+    if (t == 0) first = bv;
+    if (t == lane) {
+      pick0 = bv;
+      id0 = bi;
+    } else if (t == lane + 32) {
+      pick1 = bv;
+      id1 = bi;
+    }
+  }
+  const float w0 = lane < k ? expf(pick0 - first) : 0.f;
+  const float w1 = lane + 32 < k ? expf(pick1 - first) : 0.f;
+  const float sum = warp_sum(w0 + w1);
+  int32_t *ids_t = ids + static_cast<int64_t>(warp) * k;
+  float *sc_t = scores + static_cast<int64_t>(warp) * k;
+  if (lane < k) {
+    ids_t[lane] = id0;
+    sc_t[lane] = w0 / sum;
+  }
+  if (lane + 32 < k) {
+    ids_t[lane + 32] = id1;
+    sc_t[lane + 32] = w1 / sum;
+  }
+}
+
 // ================================================================== bounded waits
 // Waits, with the kernels' own wait functions and a short limit, on a condition nothing will
 // satisfy: kind 0 a grid-barrier count (a zeroed counter that nobody increments), kind 1 an
@@ -469,6 +537,14 @@ cudaError_t launch_unpack(const uint8_t *packed, int64_t rows, int64_t cols, int
   int grid = (int)((steps + 255) / 256);
   grid = grid < 1 ? 1 : (grid > 65535 ? 65535 : grid);
   MOE_BITS_SWITCH(bits, B, unpack_kernel<B><<<grid, 256, 0, stream>>>(packed, rows, cols, codes));
+  return cudaGetLastError();
+}
+
+cudaError_t launch_router(const float *logits, int m, int n_experts, int k, int32_t *ids,
+                          float *scores, cudaStream_t stream) {
+  const int warps_per_block = 8;
+  const int grid = (m + warps_per_block - 1) / warps_per_block;
+  router_kernel<<<grid, warps_per_block * 32, 0, stream>>>(logits, m, n_experts, k, ids, scores);
   return cudaGetLastError();
 }
 

@@ -142,6 +142,10 @@ cudaError_t prepare_kernels(int smem_optin, int bits_gu, int bits_d, int bits_sh
 int fused_grid_limit(const Plan &plan, int bits_gu, int bits_d, int bits_sh);
 cudaError_t launch_unpack(const uint8_t *packed, int64_t rows, int64_t cols, int bits,
                           uint8_t *codes, cudaStream_t stream);
+// Router: per token the top_k of n_experts fp32 logits (ties to the lower id) and their softmax
+// weights; n_experts <= 1024, top_k <= kMaxTopK.
+cudaError_t launch_router(const float *logits, int m, int n_experts, int k, int32_t *ids,
+                          float *scores, cudaStream_t stream);
 // The kernels' bounded wait on a condition nothing satisfies (kind 0: grid-barrier count at cnt,
 // which must be zero; kind 1: an mbarrier stage), giving up after `limit` cycles.
 cudaError_t launch_wait_timeout(int kind, uint32_t *cnt, int32_t *err, long long limit,
