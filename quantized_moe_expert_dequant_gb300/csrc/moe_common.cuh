@@ -151,24 +151,6 @@ __device__ __forceinline__ void step_masks(const uint4 *v, uint32_t (&m)[Fmt<BIT
   }
 }
 
-// sum_j q_j * x_j * 2^-S over one step; xs holds the step's pre-scaled activations (16-B aligned).
-template <int BITS>
-__device__ __forceinline__ float step_dot(const uint4 *v, const float *xs) {
-  constexpr int N = Fmt<BITS>::kCodes;
-  uint32_t m[N];
-  step_masks<BITS>(v, m);
-  float a0 = 0.f, a1 = 0.f, a2 = 0.f, a3 = 0.f;
-#pragma unroll
-  for (int j = 0; j < N; j += 4) {
-    const float4 x4 = *reinterpret_cast<const float4 *>(xs + j);
-    a0 = fmaf(__uint_as_float(m[j + 0]), x4.x, a0);
-    a1 = fmaf(__uint_as_float(m[j + 1]), x4.y, a1);
-    a2 = fmaf(__uint_as_float(m[j + 2]), x4.z, a2);
-    a3 = fmaf(__uint_as_float(m[j + 3]), x4.w, a3);
-  }
-  return (a0 + a1) + (a2 + a3);
-}
-
 // ------------------------------------------------------------------ integer dot products
 // For 4- and 8-bit codes the activations of a step become 23-bit two's-complement fixed point
 // with one binary exponent per step, f_i = rint(v_i * 2^(22 - E)) with max|v| < 2^E, split into

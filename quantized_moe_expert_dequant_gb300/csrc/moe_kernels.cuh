@@ -34,7 +34,8 @@ constexpr int kThreads = kConsumers + kProducers;
 constexpr int kRingBytes = 208 * 1024;      // shared-memory ring of one CTA
 constexpr int kMaxStages = 8;
 constexpr int kMaxRowsB = 128;              // phase B: output rows one CTA owns, at most
-constexpr int kMaxActRegs = 32;             // phase B: activation registers per thread (6-bit: 64)
+constexpr int kMaxActRegs = 32;             // phase B: a thread owns at most this many codes' worth
+                                            // of steps (one step at 4 and 6 bits, two at 8 bits)
 
 // Phase A geometry of one class (routed or shared) of gate/up rows.
 struct GateUpGeom {
