@@ -845,7 +845,7 @@ __device__ void consume_b_spt(const LayerShape &s, const DownGeom &g, const int 
                               const float *act, const float *resid_s, void *out, int out_f32,
                               Ring &r, SmemB &sm, int tid) {
   constexpr int CR = Fmt<BD>::kCodes, CS = Fmt<BSD>::kCodes;
-  constexpr int VS = 4;             // rows per thread per stage, at most
+  constexpr int VS = 8;             // rows per thread per stage, at most
   const int warp = tid >> 5, lane = tid & 31;
   int i0, i1;
   range_b(s, i0, i1);
