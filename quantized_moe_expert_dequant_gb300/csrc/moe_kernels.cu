@@ -347,8 +347,9 @@ static bool geom_b(const LayerShape &s, int bits_d, int bits_sd, DownGeom *g) {
   if (g->spt < 1 || g->spt > sptmax) return false;
   const int row_bytes =
       s.top_k * (g->rb_r + 4 * g->G_r) + s.n_shared * (g->rb_s + 4 * g->G_s);
+  const int rmax = rows_per_thread_b_max(bits_d, bits_sd);
   int rpt = (64 * 1024) / (g->groups * row_bytes);
-  rpt = rpt < 1 ? 1 : (rpt > 8 ? 8 : rpt);
+  rpt = rpt < 1 ? 1 : (rpt > rmax ? rmax : rpt);
   g->R = rpt * g->groups;
   g->sw_r = align_up(g->R * g->G_r * 2 + 14, 16);
   g->sw_s = s.n_shared > 0 ? align_up(g->R * g->G_s * 2 + 14, 16) : 0;

@@ -39,6 +39,12 @@ __host__ __device__ constexpr int rows_per_thread_gb() {
 inline int rows_per_thread_a_host(int bits) { return bits == 6 ? 1 : 2; }
 inline int rows_per_thread_gb_host(int bits) { return bits == 6 ? 2 : 4; }
 
+// Phase B (token path): rows per thread in a stage, at most.  A 6-bit operand holds 64 registers,
+// which leaves room for fewer accumulators.
+__host__ __device__ constexpr int rows_per_thread_b_max(int bits_d, int bits_sd) {
+  return bits_d == 6 || bits_sd == 6 ? 4 : 8;
+}
+
 template <int V>
 struct Log2 {
   static constexpr int v = V == 1 ? 0 : V == 2 ? 1 : V == 4 ? 2 : V == 8 ? 3 : -1;
@@ -646,24 +652,33 @@ __device__ int consume_a_class(const LayerShape &s, const GateUpGeom &g, bool sh
     float v[V];
 #pragma unroll
     for (int q = 0; q < V; ++q) v[q] = 0.f;
-    if (active && ok) {
+    // rows q < nq of this stage are the thread's (row q sits at q * groups + my_group)
+    int nq = (d.n - my_group + g.groups - 1) / g.groups;
+    nq = nq > RPT ? RPT : nq;
+    if (active && ok && nq > 0) {
+      // every row's codes, scales and biases first, then the dot products; a row past nq reads
+      // row 0's bytes (in the stage) and is dropped
+      uint4 cg[RPT][VEC], cu[RPT][VEC];
+      float h[RPT][4];
 #pragma unroll
       for (int q = 0; q < RPT; ++q) {
-        const int rr = q * g.groups + my_group;
-        if (rr < d.n) {
-          uint4 cg[VEC], cu[VEC];
-          const uint8_t *pg = sb + rr * g.rb + code_off;
-          const uint8_t *pu = pg + g.R * g.rb;
+        const int rr = (q < nq ? q : 0) * g.groups + my_group;
+        const uint8_t *pg = sb + rr * g.rb + code_off;
+        const uint8_t *pu = pg + g.R * g.rb;
 #pragma unroll
-          for (int w = 0; w < VEC; ++w) {
-            cg[w] = lds_u4(pg + 16 * w);
-            cu[w] = lds_u4(pu + 16 * w);
-          }
-          const float dg = xo.dot(cg);
-          const float du = xo.dot(cu);
-          const uint8_t *wr = ws + rr * G * 2;
-          v[q] = fmaf(lds_half(wr), dg * xunit, lds_half(wr + g.sw) * xsum);
-          v[RPT + q] = fmaf(lds_half(wr + 2 * g.sw), du * xunit, lds_half(wr + 3 * g.sw) * xsum);
+        for (int w = 0; w < VEC; ++w) {
+          cg[q][w] = lds_u4(pg + 16 * w);
+          cu[q][w] = lds_u4(pu + 16 * w);
+        }
+        const uint8_t *wr = ws + rr * G * 2;
+#pragma unroll
+        for (int k = 0; k < 4; ++k) h[q][k] = lds_half(wr + k * g.sw);
+      }
+#pragma unroll
+      for (int q = 0; q < RPT; ++q) {
+        if (q < nq) {
+          v[q] = fmaf(h[q][0], xo.dot(cg[q]) * xunit, h[q][1] * xsum);
+          v[RPT + q] = fmaf(h[q][2], xo.dot(cu[q]) * xunit, h[q][3] * xsum);
         }
       }
     }
@@ -798,13 +813,36 @@ struct DownOperand {
   };
 };
 
-template <int BITS>
-__device__ __forceinline__ float down_dot(const uint8_t *codes, const Operand<BITS> &op) {
+// One thread's step of a stage's rows q < nq (row q sits at q * groups + my_group): the codes,
+// scales and biases of QB rows are loaded before any of their dot products, so the loads and the
+// rows' integer chains overlap.  A row past nq reads row q0's bytes (in the stage) and adds
+// nothing; each acc[q] sums its terms in the order of the callers' step loop.
+template <int BITS, int VS>
+__device__ __forceinline__ void down_rows(const uint8_t *cp, const uint8_t *sp, int rb, int G,
+                                          int wins, int groups, int my_group, int nq,
+                                          const Operand<BITS> &op, float (&acc)[VS]) {
   constexpr int VEC = Fmt<BITS>::kVecs;
-  uint4 cv[VEC];
+  constexpr int QB = VEC == 1 ? 4 : 1;  // rows in flight (a 6-bit operand already holds 64 registers)
 #pragma unroll
-  for (int w = 0; w < VEC; ++w) cv[w] = lds_u4(codes + 16 * w);
-  return op.dot(cv) * op.unit;
+  for (int q0 = 0; q0 < VS; q0 += QB) {
+    if (q0 >= nq) break;
+    uint4 cv[QB][VEC];
+    float hs[QB], hb[QB];
+#pragma unroll
+    for (int j = 0; j < QB; ++j) {
+      const int rr = (q0 + j < nq ? q0 + j : q0) * groups + my_group;
+#pragma unroll
+      for (int w = 0; w < VEC; ++w) cv[j][w] = lds_u4(cp + rr * rb + 16 * w);
+      const uint8_t *wr = sp + rr * G * 2;
+      hs[j] = lds_half(wr);
+      hb[j] = lds_half(wr + wins);
+    }
+#pragma unroll
+    for (int j = 0; j < QB; ++j) {
+      const float t = fmaf(hs[j], op.dot(cv[j]) * op.unit, hb[j] * op.sum);
+      if (q0 + j < nq) acc[q0 + j] += t;
+    }
+  }
 }
 
 // The Operand of C activations from act + base (16-byte aligned); zeros when not owned.
@@ -845,7 +883,7 @@ __device__ void consume_b_spt(const LayerShape &s, const DownGeom &g, const int 
                               const float *act, const float *resid_s, void *out, int out_f32,
                               Ring &r, SmemB &sm, int tid) {
   constexpr int CR = Fmt<BD>::kCodes, CS = Fmt<BSD>::kCodes;
-  constexpr int VS = 8;             // rows per thread per stage, at most
+  constexpr int VS = rows_per_thread_b_max(BD, BSD);  // rows per thread per stage, at most
   const int warp = tid >> 5, lane = tid & 31;
   int i0, i1;
   range_b(s, i0, i1);
@@ -916,6 +954,9 @@ __device__ void consume_b_spt(const LayerShape &s, const DownGeom &g, const int 
     float acc[VS];
 #pragma unroll
     for (int q = 0; q < VS; ++q) acc[q] = 0.f;
+    // rows q < nq of this stage are the thread's: q < rpt and q * groups + my_group < n
+    int nq = (n - my_group + g.groups - 1) / g.groups;
+    nq = nq < 0 ? 0 : (nq > rpt ? rpt : nq);
     if (ok) {
 #pragma unroll
       for (int i = 0; i < SPTMAX; ++i) {
@@ -925,17 +966,10 @@ __device__ void consume_b_spt(const LayerShape &s, const DownGeom &g, const int 
         const uint32_t delta = (((rowbase[i] + r0) * static_cast<uint32_t>(Gs[i])) & 7u) * 2u;
         const uint8_t *cp = sb + cbase[i];
         const uint8_t *sp = wb + sbase[i] + delta;
-#pragma unroll
-        for (int q = 0; q < VS; ++q) {
-          const int rr = q * g.groups + my_group;
-          if (q < rpt && rr < n) {
-            const float d = shr[i] ? down_dot<BSD>(cp + rr * rbs[i], op[i].s)
-                                   : down_dot<BD>(cp + rr * rbs[i], op[i].r);
-            const float asum = shr[i] ? op[i].s.sum : op[i].r.sum;
-            const uint8_t *wr = sp + rr * Gs[i] * 2;
-            acc[q] += fmaf(lds_half(wr), d, lds_half(wr + wins) * asum);
-          }
-        }
+        if (shr[i])
+          down_rows<BSD, VS>(cp, sp, rbs[i], Gs[i], wins, g.groups, my_group, nq, op[i].s, acc);
+        else
+          down_rows<BD, VS>(cp, sp, rbs[i], Gs[i], wins, g.groups, my_group, nq, op[i].r, acc);
       }
     }
     warp_release(r, lane);
