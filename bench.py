@@ -41,7 +41,11 @@ from quantized_moe_expert_dequant_gb300.workloads import ALL, Shape  # noqa: E40
 
 METRIC = "MoE decode tok/s (full layer stack) and achieved HBM GB/s vs peak, 1 GB300"
 DEFAULT_WORKLOAD = "qwen3_stack_8bit"
+NORM_EPS = 1e-6   # RMSNorm epsilon of the chained stack (--chain-norm)
 KERNEL_SOURCES = ["quantized_moe_expert_dequant_gb300/csrc/moe_kernels.cu",
+                  "quantized_moe_expert_dequant_gb300/csrc/moe_fused.cuh",
+                  "quantized_moe_expert_dequant_gb300/csrc/moe_kernels_g8.cu",
+                  "quantized_moe_expert_dequant_gb300/csrc/moe_grouped.cuh",
                   "quantized_moe_expert_dequant_gb300/csrc/moe_kernels.cuh",
                   "quantized_moe_expert_dequant_gb300/csrc/moe_phases.cuh",
                   "quantized_moe_expert_dequant_gb300/csrc/moe_tma.cuh",
@@ -54,14 +58,19 @@ def proj_bytes(rows, cols, bits):
     return rows * cols * bits // 8 + (rows * cols // 64) * 4
 
 
-def layer_bytes(shape: Shape, m: int, unique_experts: int, first_layer: bool):
+def layer_bytes(shape: Shape, m: int, unique_experts: int, first_layer: bool,
+                chained: bool = False):
     """(kernel A bytes, kernel B bytes) of one layer for m tokens whose slots name
-    `unique_experts` distinct experts: each selected weight byte is counted once."""
+    `unique_experts` distinct experts: each selected weight byte is counted once.  A chained
+    layer after the first reads the previous output (fp32) and the norm weight instead of x."""
     act = shape.top_k * shape.dff + shape.n_shared * shape.dff_shared
     a = unique_experts * (proj_bytes(shape.dff, shape.din, shape.bits_gate)
                           + proj_bytes(shape.dff, shape.din, shape.bits_up))
     a += shape.n_shared * 2 * proj_bytes(shape.dff_shared, shape.din, shape.bits_shared)
-    a += m * (shape.din * 2 + act * 4 + shape.top_k * 8)
+    normed = chained and not first_layer
+    a += m * ((shape.din * 4 if normed else shape.din * 2) + act * 4 + shape.top_k * 8)
+    if normed:
+        a += shape.din * 2
     if shape.n_shared and shape.shared_gate:
         a += shape.din * 2
     b = unique_experts * proj_bytes(shape.din, shape.dff, shape.bits_down)
@@ -76,10 +85,10 @@ def per_token_layer_weight_bytes(shape: Shape):
 
 # ---------------------------------------------------------------- inputs
 
-def input_set(shape: Shape, m: int, step: int):
+def input_set(shape: Shape, m: int, step: int, chained: bool = False):
     L = shape.layers
     x = np.stack([np.stack([synth.activations(shape.seed, l, t + 1000 * step, shape.din)
-                            for t in range(m)]) for l in range(L)])
+                            for t in range(m)]) for l in range(1 if chained else L)])
     ids = np.stack([np.stack([synth.topk_ids(shape.seed, l, t, shape.n_experts, shape.top_k, step)
                               for t in range(m)]) for l in range(L)]).astype(np.int32)
     sc = np.stack([np.stack([synth.scores(shape.seed, l, t, shape.top_k, step)
@@ -299,8 +308,16 @@ def run_ours(args, shape: Shape):
         raise SystemExit(f"workload needs {need / 1e9:.1f} GB, {free / 1e9:.1f} GB free")
     layers = [Bn.synth_layer_device(shape, l) for l in range(L)]
     mode = Bn.KERNELS_FUSED if args.kernels == "fused" else Bn.KERNELS_SEPARATE
-    stack = Bn.MoeStack(layers, max_tokens=m, kernel_mode=mode)
-    parts_stack = Bn.MoeStack(layers, max_tokens=m, kernel_mode=Bn.KERNELS_SEPARATE)
+    chained = args.chain_norm
+    norm = None
+    if chained and L > 1:
+        rows = np.stack([synth.norm_weight(shape.seed, l, shape.din) for l in range(1, L)])
+        norm = torch.from_numpy(rows.view(np.int16)).view(torch.bfloat16).to(device)
+    elif chained:
+        norm = torch.ones((1, shape.din), dtype=torch.bfloat16, device=device)
+    stack = Bn.MoeStack(layers, max_tokens=m, kernel_mode=mode, norm_weight=norm, eps=NORM_EPS)
+    parts_stack = Bn.MoeStack(layers, max_tokens=m, kernel_mode=Bn.KERNELS_SEPARATE,
+                              norm_weight=norm, eps=NORM_EPS)
 
     def dev(a, dt):
         a = np.ascontiguousarray(a)
@@ -310,13 +327,15 @@ def run_ours(args, shape: Shape):
 
     sets, uniq = [], []
     for s in range(S):
-        x, ids, sc, r0 = input_set(shape, m, s)
+        x, ids, sc, r0 = input_set(shape, m, s, chained)
         uniq.append(unique_per_layer(ids))
         sets.append((dev(x, torch.bfloat16), dev(ids, torch.int32), dev(sc, torch.float32),
                      dev(r0, torch.bfloat16), torch.empty((m, shape.din), dtype=torch.float32,
                                                           device=device), (x, ids, sc, r0)))
-    bytes_a = [sum(layer_bytes(shape, m, u[l], l == 0)[0] for l in range(L)) for u in uniq]
-    bytes_b = [sum(layer_bytes(shape, m, u[l], l == 0)[1] for l in range(L)) for u in uniq]
+    bytes_a = [sum(layer_bytes(shape, m, u[l], l == 0, chained)[0] for l in range(L))
+               for u in uniq]
+    bytes_b = [sum(layer_bytes(shape, m, u[l], l == 0, chained)[1] for l in range(L))
+               for u in uniq]
 
     stream = torch.cuda.current_stream(device)
 
@@ -417,7 +436,7 @@ def run_ours(args, shape: Shape):
                                                 step_bytes, ms_per_step * 1e3)
     else:
         ach, per_launch_bytes, per_launch_us = ach_a, mean_a, ms_a * 1e3
-    traffic = profiled_traffic(dominant, args.workload)
+    traffic = profiled_traffic(dominant, args.workload + ("_chained" if chained else ""))
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
@@ -439,6 +458,7 @@ def run_ours(args, shape: Shape):
                    "bits": [shape.bits_gate, shape.bits_up, shape.bits_down],
                    "shared": [shape.n_shared, shape.dff_shared, shape.bits_shared],
                    "layers": L, "tokens_per_step": m, "input_sets": S,
+                   "chain_norm": bool(chained),
                    "parallelism": f"replicas x{world}",
                    "l2": f"inputs larger than L2: {step_bytes / 1e9:.3f} GB of selected weights "
                          f"per step, ids re-drawn per step"},
@@ -478,6 +498,9 @@ def main(argv=None):
     ap.add_argument("--kernels", choices=["fused", "separate"], default="fused",
                     help="one persistent kernel per step, or kernel A and kernel B per layer")
     ap.add_argument("--input-sets", type=int, default=4)
+    ap.add_argument("--chain-norm", action="store_true",
+                    help="fold the next layer's RMSNorm in: layer l >= 1 reads RMSNorm(out of "
+                         "layer l - 1) instead of its own x")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--layers", type=int, default=0,

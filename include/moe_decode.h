@@ -165,6 +165,25 @@ int moe_decode_forward_noalloc(const moe_decode_config *cfg, const moe_layer_wei
 int moe_stack_create(const moe_decode_config *cfg, int32_t n_layers,
                      const moe_layer_weights *layers, moe_stack_t **out);
 
+/* The same stack with the next layer's RMSNorm folded in: layer l >= 1 does not read x_l but
+ * normalises the previous layer's fp32 output,
+ *   x_l[c] = bf16( gamma_l[c] * (out_{l-1}[c] * r) ),  r = 1 / sqrt(mean_c out_{l-1}[c]^2 + eps)
+ * "Red Lite dev39 -- fused expert tail" (Measurements) records a tail that also folded in the
+ * next layer's RMSNorm and names the step without a formula; this is the usual RMSNorm.  Every
+ * CTA of layer l's first phase computes r itself: the squares summed in fp64 in a fixed order, r
+ * rounded once to fp32, the two products in fp32, the result rounded to the nearest bf16 (ties
+ * to even), so the fused and the separate kernel modes give identical bytes.
+ *   norm_weight  bf16 [n_layers - 1][din] device, 16-byte aligned, borrowed for the stack's life:
+ *                row l - 1 is gamma_l
+ *   eps          in [0, 1]
+ * moe_stack_step then reads x as [m][din] (layer 0 only; moe_stack_step_host copies m*din
+ * values).  Batches (m > 1) run token by token.  Other arguments and returns as for
+ * moe_stack_create (MOE_ERR_INVALID_ARG also for a null or misaligned norm_weight or an eps
+ * outside [0, 1]). */
+int moe_stack_create_chained(const moe_decode_config *cfg, int32_t n_layers,
+                             const moe_layer_weights *layers, const void *norm_weight, float eps,
+                             moe_stack_t **out);
+
 /* Enqueues one decode step of the whole stack on `stream` (device pointers as above).  The first
  * call with a given (x, ids, scores, resid0, out, m) captures and instantiates a CUDA graph
  * (not asynchronous, allocates); later calls with the same pointers only launch it. */

@@ -24,9 +24,17 @@
  *               weights[e] tmp[e][i] in the pool's order, then x = resid +
  *               (routed + shared * scalar))
  *
- * No intermediate value is rounded: codes are exact integers, fp16 and bf16 inputs convert to
- * double exactly, and every sum runs left to right in double.  Pins: tests/test_oracle_pins.py.
+ *   norm     (a stack with the next layer's RMSNorm folded in) the next layer's input
+ *            x_c = gamma_c * v_c / sqrt((1/n) sum_j v_j^2 + eps), rounded to bf16
+ *            -- "Red Lite dev39 -- fused expert tail", Measurements (the tail variant that
+ *               also folded in the next layer's RMSNorm); see oracle_rmsnorm_bf16
+ *
+ * No intermediate value of the block is rounded: codes are exact integers, fp16 and bf16 inputs
+ * convert to double exactly, and every sum runs left to right in double.  The norm's output is a
+ * bf16 code, so its last steps follow the precision the norm is defined in (oracle_rmsnorm_bf16).
+ * Pins: tests/test_oracle_pins.py.
  */
+#include <float.h>
 #include <math.h>
 #include <stdint.h>
 #include <stdlib.h>
@@ -220,3 +228,43 @@ void oracle_router(const float *logits, int32_t n_experts, int32_t k, int32_t *i
   for (int32_t t = 0; t < k; ++t) scores[t] = (float)(exp((double)logits[ids[t]] - mx) / sum);
 }
 
+
+/* The bf16 nearest to y, ties to even (bit pattern).  bf16 keeps 8 significant bits, so y is
+ * rounded at the spacing 2^(e-8) of its binade [2^(e-1), 2^e), never finer than the subnormal
+ * spacing 2^-133; a value that rounds beyond the largest finite bf16 becomes an infinity. */
+uint16_t oracle_round_bf16(double y) {
+  if (isnan(y)) return 0x7fc0;
+  const uint16_t sign = signbit(y) ? 0x8000 : 0;
+  if (isinf(y)) return sign | 0x7f80;
+  if (y == 0.0) return sign;
+  int e;
+  frexp(y, &e);
+  int s = e - 8;
+  if (s < -133) s = -133;
+  const double q = ldexp(nearbyint(ldexp(y, -s)), s);  /* nearbyint: to nearest, ties to even */
+  if (fabs(q) > FLT_MAX) return sign | 0x7f80;
+  const float f = (float)q;                           /* exact: at most 8 significant bits */
+  uint32_t u;
+  memcpy(&u, &f, sizeof u);
+  return (uint16_t)(u >> 16);
+}
+
+/* The next layer's input from a layer's fp32 output v when the RMSNorm is folded into the tail
+ * ("Red Lite dev39 -- fused expert tail", Measurements: the reverted tail that also folded in the
+ * next layer's RMSNorm).  The page names the step without a formula; this is the usual RMSNorm,
+ *   x_c = gamma_c * v_c * r,   r = 1 / sqrt((1/n) sum_j v_j^2 + eps),
+ * rounded to the nearest bf16.  Where the rounding is decided matters, so the steps are those of
+ * the stack's definition: the sum of squares and r in double, r rounded to fp32, then v_c * r and
+ * gamma_c * (v_c * r) as fp32 products, then the fp32 value rounded to bf16 (ties to even).
+ * v fp32 [n]; gamma bf16 [n]; x receives bf16 bit patterns [n]. */
+void oracle_rmsnorm_bf16(const float *v, int32_t n, const uint16_t *gamma, float eps,
+                         uint16_t *x) {
+  double ss = 0.0;
+  for (int32_t c = 0; c < n; ++c) ss += (double)v[c] * (double)v[c];
+  const float r = (float)(1.0 / sqrt(ss / n + (double)eps));
+  for (int32_t c = 0; c < n; ++c) {
+    const float t = v[c] * r;
+    const float u = (float)oracle_bf16(gamma[c]) * t;
+    x[c] = oracle_round_bf16((double)u);
+  }
+}

@@ -80,6 +80,11 @@ def lib():
             L.oracle_router.restype = None
             L.oracle_router.argtypes = [ctypes.c_void_p, ctypes.c_int32, ctypes.c_int32,
                                         ctypes.c_void_p, ctypes.c_void_p]
+            L.oracle_round_bf16.restype = ctypes.c_uint16
+            L.oracle_round_bf16.argtypes = [ctypes.c_double]
+            L.oracle_rmsnorm_bf16.restype = None
+            L.oracle_rmsnorm_bf16.argtypes = [ctypes.c_void_p, ctypes.c_int32, ctypes.c_void_p,
+                                              ctypes.c_float, ctypes.c_void_p]
             _lib = L
     return _lib
 
@@ -245,3 +250,19 @@ def router(logits: np.ndarray, k: int):
     lib().oracle_router(_ptr(logits), len(logits), k, _ptr(ids), _ptr(scores))
     return ids, scores
 
+
+
+def round_bf16(y: float) -> int:
+    """bf16 bit pattern nearest to y, ties to even (see oracle_round_bf16)."""
+    return int(lib().oracle_round_bf16(float(y)))
+
+
+def rmsnorm_bf16(v: np.ndarray, gamma_bf16: np.ndarray, eps: float) -> np.ndarray:
+    """bf16 bits [n] of the next layer's input from a layer's fp32 output v (see
+    oracle_rmsnorm_bf16)."""
+    v = np.ascontiguousarray(v, dtype=np.float32)
+    g = np.ascontiguousarray(gamma_bf16, dtype=np.uint16)
+    assert g.shape == v.shape
+    x = np.empty(len(v), np.uint16)
+    lib().oracle_rmsnorm_bf16(_ptr(v), len(v), _ptr(g), float(eps), _ptr(x))
+    return x

@@ -30,7 +30,8 @@ _STATUS = {0: "MOE_OK", -1: "MOE_ERR_INVALID_ARG", -2: "MOE_ERR_UNSUPPORTED", -3
 
 EXPORTS = ["moe_decode_create", "moe_decode_forward", "moe_decode_get_error", "moe_decode_destroy",
            "moe_decode_forward_noalloc",
-           "moe_stack_create", "moe_stack_step", "moe_stack_step_parts", "moe_stack_step_host",
+           "moe_stack_create", "moe_stack_create_chained", "moe_stack_step",
+           "moe_stack_step_parts", "moe_stack_step_host",
            "moe_stack_get_error",
            "moe_stack_destroy", "moe_pack_codes", "moe_unpack_codes", "moe_unpack_codes_device",
            "moe_synth_codes", "moe_synth_scales", "moe_synth_biases", "moe_route_invert_device",
@@ -83,6 +84,9 @@ def lib() -> ctypes.CDLL:
                                                vp, i32, vp, vp, vp, vp, vp, vp],
                 "moe_stack_create": [ctypes.POINTER(Config), i32, ctypes.POINTER(LayerWeights),
                                      ctypes.POINTER(vp)],
+                "moe_stack_create_chained": [ctypes.POINTER(Config), i32,
+                                             ctypes.POINTER(LayerWeights), vp, ctypes.c_float,
+                                             ctypes.POINTER(vp)],
                 "moe_stack_step": [vp, vp, i32, vp, vp, vp, vp, vp],
                 "moe_stack_step_parts": [vp, i32, vp, i32, vp, vp, vp, vp, vp],
                 "moe_stack_step_host": [vp, vp, i32, vp, vp, vp, vp, vp],
@@ -269,19 +273,28 @@ def forward_noalloc(layer: "DeviceLayer", x: torch.Tensor, ids: torch.Tensor | N
 
 
 class MoeStack:
-    """A stack of layers replayed as one CUDA graph per decode step."""
+    """A stack of layers replayed as one CUDA graph per decode step.
+
+    norm_weight (bf16 [L - 1, din] on the device) folds the next layer's RMSNorm in
+    (moe_stack_create_chained): layer l >= 1 then reads RMSNorm(out of layer l - 1) instead of x,
+    and step() reads x as [m, din]."""
 
     def __init__(self, layers: list[DeviceLayer], max_tokens: int = 1, resid_dtype=DTYPE_BF16,
-                 kernel_mode: int = KERNELS_FUSED):
+                 kernel_mode: int = KERNELS_FUSED, norm_weight=None, eps: float = 1e-6):
         self.layers = layers
         self.cfg = config(layers[0].shape, max_tokens, resid_dtype, DTYPE_F32, kernel_mode)
         arr = (LayerWeights * len(layers))()
         for i, l in enumerate(layers):
             arr[i] = l.struct()
         self._w = arr
+        self._norm = norm_weight
         h = ctypes.c_void_p()
-        check("moe_stack_create", lib().moe_stack_create(ctypes.byref(self.cfg), len(layers), arr,
-                                                         ctypes.byref(h)))
+        if norm_weight is None:
+            check("moe_stack_create", lib().moe_stack_create(ctypes.byref(self.cfg), len(layers),
+                                                             arr, ctypes.byref(h)))
+        else:
+            check("moe_stack_create_chained", lib().moe_stack_create_chained(
+                ctypes.byref(self.cfg), len(layers), arr, _p(norm_weight), eps, ctypes.byref(h)))
         self.handle = h
 
     def step(self, x, ids, scores, resid0, out, stream=None):

@@ -129,11 +129,20 @@ size_t act_floats(const moe_decode_config &c) {
 
 size_t dtype_bytes(int dt) { return dt == MOE_DTYPE_F32 ? 4 : 2; }
 
+// Kernel A's input when the previous layer's RMSNorm is folded in: x = RMSNorm(v) with weight
+// gamma, v fp32 [m][din] (v null: kernel A reads x).
+struct NormIn {
+  const float *v = nullptr;
+  const uint16_t *gamma = nullptr;
+  float eps = 0.f;
+};
+
 // Separate kernels: kernel A then kernel B for each token of one layer.
 cudaError_t enqueue_separate(const Prepared &P, const moe::LayerPtrs &w, float *act,
                              int32_t *err, const void *x, int m, const int32_t *ids,
                              const float *scores, const void *resid, int resid_dtype, void *out,
-                             int out_dtype, cudaStream_t stream, int parts) {
+                             int out_dtype, cudaStream_t stream, int parts,
+                             const NormIn &norm = NormIn{}) {
   const moe_decode_config &c = P.cfg;
   for (int t = 0; t < m; ++t) {
     const int32_t *it = ids ? ids + (size_t)t * c.top_k : nullptr;
@@ -141,7 +150,10 @@ cudaError_t enqueue_separate(const Prepared &P, const moe::LayerPtrs &w, float *
     a.s = P.shape;
     a.w = w;
     a.plan = P.plan;
-    a.x = static_cast<const uint16_t *>(x) + (size_t)t * c.din;
+    a.x = norm.v ? nullptr : static_cast<const uint16_t *>(x) + (size_t)t * c.din;
+    a.v = norm.v ? norm.v + (size_t)t * c.din : nullptr;
+    a.gamma = norm.gamma;
+    a.eps = norm.eps;
     a.ids = it;
     a.scores = scores ? scores + (size_t)t * c.top_k : nullptr;
     a.act = act;
@@ -171,7 +183,8 @@ cudaError_t enqueue_fused(const Prepared &P, const moe::LayerPtrs *layers, int L
                           float *y, int32_t *err, uint32_t *bar, float *ping0, float *ping1,
                           const void *x, int m, const int32_t *ids, const float *scores,
                           const void *resid0, int resid_dtype, void *out, int out_dtype,
-                          cudaStream_t stream) {
+                          cudaStream_t stream, const uint16_t *norm_w = nullptr,
+                          float norm_eps = 0.f) {
   cudaError_t e = cudaMemsetAsync(bar, 0, sizeof(uint32_t), stream);
   if (e != cudaSuccess) return e;
   moe::StackParams p;
@@ -181,6 +194,8 @@ cudaError_t enqueue_fused(const Prepared &P, const moe::LayerPtrs *layers, int L
   p.L = L;
   p.m = m;
   p.x = static_cast<const uint16_t *>(x);
+  p.norm_w = norm_w;
+  p.norm_eps = norm_eps;
   p.ids = ids;
   p.scores = scores;
   p.resid0 = resid0;
@@ -192,7 +207,7 @@ cudaError_t enqueue_fused(const Prepared &P, const moe::LayerPtrs *layers, int L
   p.act = act;
   p.err = err;
   p.bar = bar;
-  p.grouped = m > 1 && P.grouped_ok;
+  p.grouped = m > 1 && P.grouped_ok && norm_w == nullptr;  // the grouped path reads x only
   p.gp = P.gplan;
   p.y = y;
   p.act_stride = static_cast<int>(act_floats(P.cfg));
@@ -431,6 +446,9 @@ struct moe_stack {
   cudaStream_t cap = nullptr;
   std::vector<GraphEntry> graphs;
   uint64_t clock = 0;
+  // the next layer's RMSNorm folded in (moe_stack_create_chained): bf16 [L - 1][din] weights
+  const uint16_t *norm_w = nullptr;
+  float norm_eps = 0.f;
   // device staging for moe_stack_step_host
   void *x_dev = nullptr, *resid_dev = nullptr;
   int32_t *ids_dev = nullptr;
@@ -452,8 +470,9 @@ extern "C" void moe_stack_destroy(moe_stack_t *s) {
   delete s;
 }
 
-extern "C" int moe_stack_create(const moe_decode_config *cfg, int32_t n_layers,
-                                const moe_layer_weights *layers, moe_stack_t **out) {
+namespace {
+int stack_create(const moe_decode_config *cfg, int32_t n_layers, const moe_layer_weights *layers,
+                 const void *norm_weight, float eps, moe_stack_t **out) {
   if (!out) return MOE_ERR_INVALID_ARG;
   *out = nullptr;
   if (!cfg || !layers || n_layers < 1) return MOE_ERR_INVALID_ARG;
@@ -470,6 +489,11 @@ extern "C" int moe_stack_create(const moe_decode_config *cfg, int32_t n_layers,
   if (rc != MOE_OK) {
     delete s;
     return rc;
+  }
+  if (norm_weight) {
+    s->norm_w = static_cast<const uint16_t *>(norm_weight);
+    s->norm_eps = eps;
+    s->P.grouped_ok = false;  // batches run token by token: the grouped path reads x only
   }
   s->layers.resize(n_layers);
   for (int l = 0; l < n_layers; ++l) s->layers[l] = layer_ptrs(*cfg, layers[l]);
@@ -497,6 +521,21 @@ extern "C" int moe_stack_create(const moe_decode_config *cfg, int32_t n_layers,
   *out = s;
   return MOE_OK;
 }
+}  // namespace
+
+extern "C" int moe_stack_create(const moe_decode_config *cfg, int32_t n_layers,
+                                const moe_layer_weights *layers, moe_stack_t **out) {
+  return stack_create(cfg, n_layers, layers, nullptr, 0.f, out);
+}
+
+extern "C" int moe_stack_create_chained(const moe_decode_config *cfg, int32_t n_layers,
+                                        const moe_layer_weights *layers,
+                                        const void *norm_weight, float eps, moe_stack_t **out) {
+  if (out) *out = nullptr;
+  if (!norm_weight || !aligned(norm_weight, 16) || !(eps >= 0.f) || eps > 1.f)
+    return MOE_ERR_INVALID_ARG;
+  return stack_create(cfg, n_layers, layers, norm_weight, eps, out);
+}
 
 namespace {
 
@@ -508,17 +547,23 @@ cudaError_t enqueue_stack(moe_stack *s, const void *x, int m, const int32_t *ids
   if (c.kernel_mode == MOE_KERNELS_FUSED && parts == (MOE_PART_GATE_UP | MOE_PART_DOWN))
     return enqueue_fused(s->P, s->ws.layers, L, s->ws.act, s->ws.y, s->ws.err, s->ws.bar,
                          s->ping[0], s->ping[1], x, m, ids, scores, resid0, c.resid_dtype, out,
-                         MOE_DTYPE_F32, st);
+                         MOE_DTYPE_F32, st, s->norm_w, s->norm_eps);
   const size_t din = c.din, K = c.top_k;
   for (int l = 0; l < L; ++l) {
-    const void *xl = static_cast<const uint16_t *>(x) + (size_t)l * m * din;
+    NormIn norm;
+    if (s->norm_w && l > 0) {
+      norm.v = s->ping[(l - 1) & 1];
+      norm.gamma = s->norm_w + (size_t)(l - 1) * din;
+      norm.eps = s->norm_eps;
+    }
+    const void *xl = static_cast<const uint16_t *>(x) + (s->norm_w ? 0 : (size_t)l * m * din);
     const int32_t *il = ids ? ids + (size_t)l * m * K : nullptr;
     const float *sl = scores ? scores + (size_t)l * m * K : nullptr;
     const void *rl = l == 0 ? resid0 : s->ping[(l - 1) & 1];
     const int rdt = l == 0 ? c.resid_dtype : MOE_DTYPE_F32;
     void *ol = l == L - 1 ? out : s->ping[l & 1];
     cudaError_t e = enqueue_separate(s->P, s->layers[l], s->ws.act, s->ws.err, xl, m, il, sl, rl,
-                                     rdt, ol, MOE_DTYPE_F32, st, parts);
+                                     rdt, ol, MOE_DTYPE_F32, st, parts, norm);
     if (e != cudaSuccess) return e;
   }
   return cudaSuccess;
@@ -595,8 +640,9 @@ extern "C" int moe_stack_step_host(moe_stack_t *s, const void *x_host, int32_t m
   const size_t L = s->layers.size(), din = s->P.cfg.din, K = s->P.cfg.top_k;
   if (K > 0 && (!ids_host || !scores_host)) return MOE_ERR_INVALID_ARG;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
+  const size_t x_layers = s->norm_w ? 1 : L;  // a chained stack reads layer 0's x only
   bool ok =
-      cudaMemcpyAsync(s->x_dev, x_host, L * m * din * 2, cudaMemcpyHostToDevice, st) ==
+      cudaMemcpyAsync(s->x_dev, x_host, x_layers * m * din * 2, cudaMemcpyHostToDevice, st) ==
           cudaSuccess &&
       cudaMemcpyAsync(s->resid_dev, resid0_host, m * din * dtype_bytes(s->P.cfg.resid_dtype),
                       cudaMemcpyHostToDevice, st) == cudaSuccess;

@@ -178,7 +178,7 @@ __device__ __forceinline__ void copy_operands(const LayerShape &s, const GroupSm
 
 // Completes the waiting stages [df.begin, r.used): waits for the barrier, then per stage adds the
 // operand bytes with the producer's arrival and copies the rows.
-__device__ void complete_deferred(const LayerShape &s, const GroupSmem &gs, const GClass *cls,
+__device__ inline void complete_deferred(const LayerShape &s, const GroupSmem &gs, const GClass *cls,
                                   const int *op_off, Deferred &df, Ring &r, int lane,
                                   const uint16_t *x_l, const float *act, int act_stride,
                                   uint64_t pol) {
@@ -206,7 +206,7 @@ __device__ void complete_deferred(const LayerShape &s, const GroupSmem &gs, cons
 // Producer of one class (index ci of cls): stages of R rows of one expert plus the operand rows
 // of up to t_sub of its pairs.  Stage layout: codes (gated: gate then up, R rows each), 2 or 4
 // scale/bias windows of g.sw bytes, then the operand rows at op_off[ci].
-__device__ void produce_g_class(const LayerShape &s, const GroupSmem &gs, const GClass *cls,
+__device__ inline void produce_g_class(const LayerShape &s, const GroupSmem &gs, const GClass *cls,
                                 int ci, const GateUpGeom &g, int64_t a, int64_t b, int m,
                                 int t_sub, const int *op_off, const uint16_t *x_l,
                                 const float *act, int act_stride, Ring &r, GroupDesc *desc,
@@ -277,7 +277,7 @@ __device__ void produce_g_class(const LayerShape &s, const GroupSmem &gs, const 
 // Producer of one grouped phase (two classes of n_r and n_s segments): counts its stages into
 // cnt[0..1], streams them, and hands out one empty stage when the CTA has none.  With deferred
 // operands, the waiting stages are completed at the end.
-__device__ void produce_g_phase(const LayerShape &s, const GroupSmem &gs, GroupDesc *desc,
+__device__ inline void produce_g_phase(const LayerShape &s, const GroupSmem &gs, GroupDesc *desc,
                                 int *cnt, const GClass *cls, const GateUpGeom &gr,
                                 const GateUpGeom &gsh, int64_t n_r, int64_t n_s, int m,
                                 int t_sub, const int *op_off, const uint16_t *x_l,
@@ -484,7 +484,7 @@ __device__ void consume_g_phase(const LayerShape &s, const GroupSmem &gs, const 
 
 // Tail of a grouped layer for the CTA's output rows: out = resid + (routed + shared), routed
 // summed over the valid slots in slot order.  y and the residual are complete (grid barrier).
-__device__ void tail_g(const LayerShape &s, const int *ids_s, int m, const float *y, int y_stride,
+__device__ inline void tail_g(const LayerShape &s, const int *ids_s, int m, const float *y, int y_stride,
                        const void *resid, int resid_f32, void *out, int out_f32, int tid) {
   int i0, i1;
   range_b(s, i0, i1);

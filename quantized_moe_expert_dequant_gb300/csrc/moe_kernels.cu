@@ -1,180 +1,10 @@
-// moe_kernels.cu -- the decode MoE kernels built from the phases of moe_phases.cuh:
-//
-//   gate_up_kernel   kernel A alone (phase A), launched with programmatic dependent launch
-//   down_kernel      kernel B alone (phase B); its producer streams down weights before the
-//                    activations are ready, its consumers wait for kernel A
-//   fused_kernel     both phases for every layer and token of a stack in one cooperative launch:
-//                    phase A, grid barrier (activations complete), phase B, grid barrier (layer
-//                    output complete).  The producer warp streams phase B's down weights right
-//                    after phase A's gate/up weights, so the down weights are in shared memory
-//                    when the barrier opens; it starts the next layer's gate/up weights only
-//                    after the barrier that completes the previous layer's output, because in a
-//                    decoder a layer's expert ids depend on that output.
-//
-// The split into two GEMV phases with the activation in global memory between them follows
-// "two-kernel decode-MoE that beats gather_qmm" (What changed, step 2); the fused launch keeps
-// that split (every row is computed once by threads spread over all SMs) and replaces the kernel
-// boundary with a device-wide barrier, which on GB300 also lets the second phase's weight stream
-// run under the first phase's arithmetic.
+// moe_kernels.cu -- host side of the decode MoE kernels: geometry and plans, and the dispatch
+// to the kernels of moe_fused.cuh (instantiated per gate/up code width in moe_kernels_g4.cu,
+// moe_kernels_g6.cu and moe_kernels_g8.cu); plus the small kernels (debug unpack, router, bounded
+// waits, debug route inversion).
 #include "moe_grouped.cuh"
 
 namespace moe {
-
-__device__ __forceinline__ void init_ring(uint64_t *full, uint64_t *empty, int nst, int *abort) {
-  if (threadIdx.x == 0) {
-    for (int s = 0; s < nst; ++s) {
-      mbar_init(&full[s], 1);  // the producer's arrive.expect_tx; the bulk copies complete it
-      mbar_init(&empty[s], kConsumerWarps);
-    }
-    *abort = 0;
-    mbar_fence_init();
-  }
-}
-
-// Shared state of the stage ring besides the stages themselves.
-struct RingSmem {
-  uint64_t full[kMaxStages];
-  uint64_t empty[kMaxStages];
-  StageDesc desc[kMaxStages];
-  int cnt[2];              // phase A chunks of the current token: routed, shared
-  int ids[kMaxTopK];       // the producer's copy of the current token's expert ids
-  float scores[kMaxTopK];  // and scores
-  int abort;
-};
-
-template <int BR, int BS>
-__global__ void __launch_bounds__(kThreads, 1) gate_up_kernel(const GateUpParams p) {
-  extern __shared__ __align__(128) uint8_t ring[];
-  __shared__ __align__(16) RingSmem rs;
-  __shared__ SmemA sm;
-  init_ring(rs.full, rs.empty, p.plan.nst, &rs.abort);
-  // Token data (x, ids, scores) may come from the previous kernel on the stream.
-  pdl_wait();
-  pdl_launch_dependents();
-  __syncthreads();
-  Ring r = make_ring(rs.full, rs.empty, ring, rs.desc, p.plan, &rs.abort, p.err);
-  const int tid = threadIdx.x, warp = tid >> 5;
-  if (warp >= kConsumerWarps) {
-    const int pl = tid - kConsumers;
-    producer_load_token(p.s, p.ids, p.scores, rs.ids, rs.scores, p.err, pl);
-    produce_a<BR, BS>(p.s, p.w, p.plan.geo_r, p.plan.geo_s, rs.ids, rs.scores, rs.cnt, r, pl,
-                      policy_evict_first());
-    ring_drain(r, pl);
-    return;
-  }
-  consume_a<BR, BS>(p.s, p.w, p.plan.geo_r, p.plan.geo_s, p.x, rs.cnt, p.act, r, sm, tid);
-}
-
-template <int BD, int BSD>
-__global__ void __launch_bounds__(kThreads, 1) down_kernel(const DownParams p) {
-  extern __shared__ __align__(128) uint8_t ring[];
-  __shared__ __align__(16) RingSmem rs;
-  __shared__ SmemB sm;
-  __shared__ float resid_s[kMaxRowsB];
-  init_ring(rs.full, rs.empty, p.plan.nst, &rs.abort);
-  pdl_launch_dependents();
-  __syncthreads();
-  Ring r = make_ring(rs.full, rs.empty, ring, rs.desc, p.plan, &rs.abort, p.err);
-  const int tid = threadIdx.x, warp = tid >> 5;
-  if (warp >= kConsumerWarps) {
-    // The ids were complete before kernel A started (A waits on its predecessor before it lets
-    // this kernel launch), so the weight stream may start before the activations are ready.
-    const int pl = tid - kConsumers;
-    producer_load_token(p.s, p.ids, nullptr, rs.ids, rs.scores, p.err, pl);
-    produce_b(p.s, p.w, p.plan.geo_b, rs.ids, r, pl, policy_evict_first());
-    ring_drain(r, pl);
-    return;
-  }
-  pdl_wait();  // the activations come from kernel A (and, in a stack, resid from the kernel
-               // before it)
-  load_resid_rows(p.s, p.resid, p.resid_f32, resid_s, tid);
-  consumer_sync(kConsumers);  // publishes resid_s
-  consume_b<BD, BSD>(p.s, p.plan.geo_b, rs.ids, p.act, resid_s, p.out, p.out_f32, r, sm, tid);
-}
-
-template <int BR, int BD, int BSH>
-__global__ void __launch_bounds__(kThreads, 1) fused_kernel(const StackParams p) {
-  extern __shared__ __align__(128) uint8_t ring[];
-  __shared__ __align__(16) RingSmem rs;
-  __shared__ SmemAB sm;
-  __shared__ float resid_s[kMaxRowsB];
-  __shared__ LayerPtrs wl;   // the consumers' copy of the current layer's pointers
-  __shared__ LayerPtrs wpr;  // the producers' copy
-  __shared__ int stop_pr;
-  init_ring(rs.full, rs.empty, p.grouped ? p.gp.nst : p.plan.nst, &rs.abort);
-  __syncthreads();
-  const int tid = threadIdx.x, warp = tid >> 5;
-  if (p.grouped) {
-    fused_grouped<BR, BD, BSH>(p, ring, rs.full, rs.empty, rs.desc, &rs.abort, sm.a, wl, wpr,
-                               stop_pr, tid);
-    return;
-  }
-  Ring r = make_ring(rs.full, rs.empty, ring, rs.desc, p.plan, &rs.abort, p.err);
-  const LayerShape &s = p.s;
-  const uint32_t n = gridDim.x;
-  const int64_t xs = static_cast<int64_t>(s.din), ks = s.top_k;
-
-  if (warp >= kConsumerWarps) {
-    // Producers work from their own shared copies of the layer's pointers and expert ids.
-    const uint64_t pol = policy_evict_first();
-    const int pl = tid - kConsumers;
-    int pass = 0;
-    for (int l = 0; l < p.L; ++l) {
-      for (int t = 0; t < p.m; ++t, ++pass) {
-        producer_sync();  // every producer is done with the previous pass's copies
-        if (pl == 0) {
-          wpr = p.layers[l];  // weight addresses do not depend on the ids: fetch them early
-          // the previous (layer, token) output is complete before these ids are read
-          if (pass > 0) wait_count(p.bar, 2u * pass * n, &rs.abort, p.err);
-          stop_pr = flag_abort(&rs.abort);
-        }
-        producer_sync();      // orders every lane's id loads after lane 0's acquire
-        if (stop_pr) break;
-        const int64_t tok = static_cast<int64_t>(l) * p.m + t;
-        producer_load_token(s, p.ids + tok * ks, p.scores + tok * ks, rs.ids, rs.scores, p.err,
-                            pl);
-        produce_a<BR, BSH>(s, wpr, p.plan.geo_r, p.plan.geo_s, rs.ids, rs.scores, rs.cnt, r, pl,
-                           pol);
-        produce_b(s, wpr, p.plan.geo_b, rs.ids, r, pl, pol);
-      }
-      if (stop_pr) break;
-    }
-    ring_drain(r, pl);  // never leave with copies in flight
-    return;
-  }
-
-  int pass = 0;
-  for (int l = 0; l < p.L; ++l) {
-    if (tid == 0) wl = p.layers[l];
-    consumer_sync(kConsumers);
-    const LayerPtrs &w = wl;
-    for (int t = 0; t < p.m; ++t, ++pass) {
-      const int64_t tok = static_cast<int64_t>(l) * p.m + t;
-      // The residual is an input (layer 0) or the previous layer's output, complete since the
-      // last grid barrier: fetch it now, off the path between the two phases.
-      if (l == 0)
-        load_resid_rows(s, static_cast<const char *>(p.resid0) + t * xs * (p.resid0_f32 ? 4 : 2),
-                        p.resid0_f32, resid_s, tid);
-      else
-        load_resid_rows(s, ((l - 1) & 1 ? p.ping1 : p.ping0) + t * xs, 1, resid_s, tid);
-      consume_a<BR, BSH>(s, w, p.plan.geo_r, p.plan.geo_s, p.x + tok * xs, rs.cnt, p.act, r, sm.a,
-                         tid);
-      consumers_grid_barrier(p.bar, (2u * pass + 1u) * n, tid, &rs.abort, p.err);
-      void *out;
-      int out_f32;
-      if (l == p.L - 1) {
-        out = static_cast<char *>(p.out) + t * xs * (p.out_f32 ? 4 : 2);
-        out_f32 = p.out_f32;
-      } else {
-        out = (l & 1 ? p.ping1 : p.ping0) + t * xs;
-        out_f32 = 1;
-      }
-      consume_b<BD, BSH>(s, p.plan.geo_b, rs.ids, p.act, resid_s, out, out_f32, r, sm.b, tid);
-      if (!(l == p.L - 1 && t == p.m - 1))
-        consumers_grid_barrier(p.bar, (2u * pass + 2u) * n, tid, &rs.abort, p.err);
-    }
-  }
-}
 
 // ================================================================== debug unpack
 template <int BITS>
@@ -422,31 +252,6 @@ bool make_group_plan(const LayerShape &s, int bits_gu, int bits_d, int bits_sh, 
   return true;
 }
 
-template <typename Kern, typename P>
-static cudaError_t launch(Kern kern, const P &p, int grid, size_t smem, cudaStream_t stream,
-                          bool pdl, bool cooperative) {
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(grid);
-  cfg.blockDim = dim3(kThreads);
-  cfg.dynamicSmemBytes = smem;
-  cfg.stream = stream;
-  cudaLaunchAttribute attr[2];
-  int na = 0;
-  if (pdl) {
-    attr[na].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    attr[na].val.programmaticStreamSerializationAllowed = 1;
-    ++na;
-  }
-  if (cooperative) {
-    attr[na].id = cudaLaunchAttributeCooperative;
-    attr[na].val.cooperative = 1;
-    ++na;
-  }
-  cfg.attrs = attr;
-  cfg.numAttrs = na;
-  return cudaLaunchKernelEx(&cfg, kern, p);
-}
-
 #define MOE_BITS_SWITCH(B, NAME, ...)                       \
   switch (B) {                                              \
     case 4: { constexpr int NAME = 4; __VA_ARGS__; break; } \
@@ -455,52 +260,60 @@ static cudaError_t launch(Kern kern, const P &p, int grid, size_t smem, cudaStre
     default: return cudaErrorInvalidValue;                  \
   }
 
+// Two translation units per gate/up code width hold the launchable kernels (moe_fused.cuh):
+// moe_kernels_g<B>.cu (kernel A, kernel B, fused token kernels), moe_grouped_g<B>.cu (fused
+// grouped kernels).
+#define MOE_FAMILY_DECL(B)                                                                    \
+  cudaError_t launch_fused_g##B(const StackParams &, int, size_t, cudaStream_t);              \
+  cudaError_t launch_gate_up_g##B(const GateUpParams &, int, cudaStream_t, bool);             \
+  cudaError_t launch_down_g##B(const DownParams &, int, cudaStream_t, bool);                  \
+  cudaError_t prepare_g##B(int, int, int, bool, int *);                                       \
+  cudaError_t fused_occupancy_g##B(int, int, size_t, int *);                                 \
+  cudaError_t launch_grouped_g##B(const StackParams &, int, size_t, cudaStream_t);            \
+  cudaError_t prepare_grouped_g##B(int, int, int, int *);                                     \
+  cudaError_t grouped_occupancy_g##B(int, int, size_t, int *);
+MOE_FAMILY_DECL(4)
+MOE_FAMILY_DECL(6)
+MOE_FAMILY_DECL(8)
+#undef MOE_FAMILY_DECL
+
+#define MOE_FAMILY_CALL(B, FN, ...)                   \
+  switch (B) {                                        \
+    case 4: return FN##_g4(__VA_ARGS__);              \
+    case 6: return FN##_g6(__VA_ARGS__);              \
+    case 8: return FN##_g8(__VA_ARGS__);              \
+    default: return cudaErrorInvalidValue;            \
+  }
+
 cudaError_t launch_gate_up(const GateUpParams &p, int grid, cudaStream_t stream, bool pdl) {
-  MOE_BITS_SWITCH(p.plan.geo_r.bits, BR, MOE_BITS_SWITCH(p.plan.geo_s.bits, BS,
-      return launch(gate_up_kernel<BR, BS>, p, grid, p.plan.smem, stream, pdl, false)));
-  return cudaErrorInvalidValue;
+  MOE_FAMILY_CALL(p.plan.geo_r.bits, launch_gate_up, p, grid, stream, pdl);
 }
 
 cudaError_t launch_down(const DownParams &p, int grid, cudaStream_t stream, bool pdl) {
-  MOE_BITS_SWITCH(p.plan.geo_b.bits_r, BD, MOE_BITS_SWITCH(p.plan.geo_b.bits_s, BSD,
-      return launch(down_kernel<BD, BSD>, p, grid, p.plan.smem, stream, pdl, false)));
-  return cudaErrorInvalidValue;
+  MOE_FAMILY_CALL(p.plan.geo_b.bits_r, launch_down, p, grid, stream, pdl);
 }
-
-// shared-expert bits as the kernels see them: the routed ones when there is no shared expert
-static int sh_bits(const Plan &plan) { return plan.geo_s.bits; }
 
 cudaError_t launch_fused(const StackParams &p, int grid, cudaStream_t stream) {
-  const size_t smem = p.grouped ? p.gp.smem : p.plan.smem;
-  MOE_BITS_SWITCH(p.plan.geo_r.bits, BR, MOE_BITS_SWITCH(p.plan.geo_b.bits_r, BD,
-      MOE_BITS_SWITCH(sh_bits(p.plan), BSH,
-          return launch(fused_kernel<BR, BD, BSH>, p, grid, smem, stream, false, true))));
-  return cudaErrorInvalidValue;
+  if (p.grouped) {
+    MOE_FAMILY_CALL(p.plan.geo_r.bits, launch_grouped, p, grid, p.gp.smem, stream);
+  }
+  MOE_FAMILY_CALL(p.plan.geo_r.bits, launch_fused, p, grid, p.plan.smem, stream);
 }
 
+// Sets every kernel's shared-memory limit; *dyn_limit is the smallest of them.
 cudaError_t prepare_kernels(int smem_optin, int bits_gu, int bits_d, int bits_sh,
                             int *dyn_limit) {
-  // The attribute is global to a kernel instance: set it to the most the device allows next to
-  // the kernel's static shared memory, so one handle can never lower it below what another
-  // handle launches with.  *dyn_limit is the smallest of the three kernels' limits.
-  cudaError_t e = cudaSuccess;
   int lim = smem_optin;
-  auto set = [&](const void *fn) {
-    cudaFuncAttributes fa;
-    e = cudaFuncGetAttributes(&fa, fn);
-    if (e != cudaSuccess) return;
-    const int dyn = smem_optin - static_cast<int>(fa.sharedSizeBytes);
-    if (dyn < lim) lim = dyn;
-    e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, dyn);
+  cudaError_t e;
+  auto fam = [&](int b, int bd, int bs, bool down) -> cudaError_t {
+    MOE_FAMILY_CALL(b, prepare, smem_optin, bd, bs, down, &lim);
   };
-  MOE_BITS_SWITCH(bits_gu, BR, MOE_BITS_SWITCH(bits_sh, BS,
-      set(reinterpret_cast<const void *>(gate_up_kernel<BR, BS>))));
-  if (e != cudaSuccess) return e;
-  MOE_BITS_SWITCH(bits_d, BD, MOE_BITS_SWITCH(bits_sh, BSD,
-      set(reinterpret_cast<const void *>(down_kernel<BD, BSD>))));
-  if (e != cudaSuccess) return e;
-  MOE_BITS_SWITCH(bits_gu, BR, MOE_BITS_SWITCH(bits_d, BD, MOE_BITS_SWITCH(bits_sh, BSH,
-      set(reinterpret_cast<const void *>(fused_kernel<BR, BD, BSH>)))));
+  auto grp = [&]() -> cudaError_t {
+    MOE_FAMILY_CALL(bits_gu, prepare_grouped, smem_optin, bits_d, bits_sh, &lim);
+  };
+  e = fam(bits_gu, bits_d, bits_sh, false);
+  if (e == cudaSuccess) e = fam(bits_d, bits_d, bits_sh, true);
+  if (e == cudaSuccess) e = grp();
   *dyn_limit = lim;
   return e;
 }
@@ -511,26 +324,17 @@ int fused_grid_limit(const Plan &plan, int bits_gu, int bits_d, int bits_sh) {
   if (cudaGetDevice(&dev) != cudaSuccess ||
       cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
     return 0;
-  cudaError_t e = cudaErrorInvalidValue;
-  switch (bits_gu * 100 + bits_d * 10 + bits_sh) {
-#define MOE_OCC(a, b, c)                                                                        \
-  case a * 100 + b * 10 + c:                                                                   \
-    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, fused_kernel<a, b, c>, kThreads, \
-                                                      plan.smem);                              \
-    break;
-    MOE_OCC(4, 4, 4) MOE_OCC(4, 4, 6) MOE_OCC(4, 4, 8) MOE_OCC(4, 6, 4) MOE_OCC(4, 6, 6)
-    MOE_OCC(4, 6, 8) MOE_OCC(4, 8, 4) MOE_OCC(4, 8, 6) MOE_OCC(4, 8, 8)
-    MOE_OCC(6, 4, 4) MOE_OCC(6, 4, 6) MOE_OCC(6, 4, 8) MOE_OCC(6, 6, 4) MOE_OCC(6, 6, 6)
-    MOE_OCC(6, 6, 8) MOE_OCC(6, 8, 4) MOE_OCC(6, 8, 6) MOE_OCC(6, 8, 8)
-    MOE_OCC(8, 4, 4) MOE_OCC(8, 4, 6) MOE_OCC(8, 4, 8) MOE_OCC(8, 6, 4) MOE_OCC(8, 6, 6)
-    MOE_OCC(8, 6, 8) MOE_OCC(8, 8, 4) MOE_OCC(8, 8, 6) MOE_OCC(8, 8, 8)
-#undef MOE_OCC
-    default:
-      break;
-  }
-  if (e != cudaSuccess) return 0;
+  per_sm = 1 << 30;
+  auto occ = [&]() -> cudaError_t {
+    MOE_FAMILY_CALL(bits_gu, fused_occupancy, bits_d, bits_sh, plan.smem, &per_sm);
+  };
+  auto occ_g = [&]() -> cudaError_t {
+    MOE_FAMILY_CALL(bits_gu, grouped_occupancy, bits_d, bits_sh, plan.smem, &per_sm);
+  };
+  if (occ() != cudaSuccess || occ_g() != cudaSuccess) return 0;
   return per_sm * sms;
 }
+#undef MOE_FAMILY_CALL
 
 cudaError_t launch_unpack(const uint8_t *packed, int64_t rows, int64_t cols, int bits,
                           uint8_t *codes, cudaStream_t stream) {

@@ -84,7 +84,10 @@ struct GateUpParams {
   LayerShape s;
   LayerPtrs w;
   Plan plan;
-  const uint16_t *x;        // bf16 [din]
+  const uint16_t *x;        // bf16 [din], read when v is null
+  const float *v;           // fp32 [din] or null: x = RMSNorm(v) with weight gamma (bf16 [din])
+  const uint16_t *gamma;
+  float eps;
   const int32_t *ids;       // [top_k]
   const float *scores;      // [top_k]
   float *act;               // [top_k*dff + n_shared*dff_shared]
@@ -111,7 +114,9 @@ struct StackParams {
   Plan plan;
   const LayerPtrs *layers;  // device array [L]
   int L, m;
-  const uint16_t *x;        // bf16 [L][m][din]
+  const uint16_t *x;        // bf16 [L][m][din]; [m][din] (layer 0 only) when norm_w is set
+  const uint16_t *norm_w;   // bf16 [L - 1][din] or null: layer l >= 1 reads x = RMSNorm(out of
+  float norm_eps;           // layer l - 1) with weight row l - 1
   const int32_t *ids;       // [L][m][top_k]
   const float *scores;      // [L][m][top_k]
   const void *resid0;       // [m][din], bf16 or fp32: residual of layer 0

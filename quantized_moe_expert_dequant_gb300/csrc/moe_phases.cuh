@@ -137,6 +137,102 @@ __device__ __forceinline__ void load_x_operand(Operand<BITS> &op, const uint16_t
   op.set(v);
 }
 
+// Phase A's input vector x: bf16 values in memory, or, in a stack with the next layer's RMSNorm
+// folded in ("Red Lite dev39 -- fused expert tail", Measurements: the tail variant that also
+// folded in the next layer's RMSNorm), the previous layer's fp32 output v normalised on the fly:
+//   x_c = bf16( gamma_c * (v_c * r) ),  r = 1 / sqrt(mean(v^2) + eps)
+// with both products in fp32 and the result rounded to the nearest bf16 (ties to even).
+struct XSource {
+  const uint16_t *x;      // bf16 [din] (v == nullptr)
+  const float *v;         // fp32 [din]: the previous layer's output
+  const uint16_t *gamma;  // bf16 [din]: the norm's weight
+  float eps;
+  float r;                // set by load_x_class_norm before any value is read
+};
+
+__device__ __forceinline__ XSource xsource_plain(const uint16_t *x) {
+  return XSource{x, nullptr, nullptr, 0.f, 1.f};
+}
+
+__device__ __forceinline__ float norm_value(float v, float gamma, float r) {
+  return bf16_to_float(float_to_bf16_rn(gamma * (v * r)));
+}
+
+__device__ __forceinline__ float x_value(const XSource &xs, int c) {
+  return xs.v == nullptr ? bf16_to_float(xs.x[c])
+                         : norm_value(xs.v[c], bf16_to_float(xs.gamma[c]), xs.r);
+}
+
+// The Operand of C values of x from column c0 (16-byte aligned) once x.r is known; zeros when the
+// thread has no step.
+template <int BITS>
+__device__ __forceinline__ void load_x_operand(Operand<BITS> &op, const XSource &xs, int c0,
+                                               bool active) {
+  if (xs.v == nullptr) {
+    load_x_operand<BITS>(op, xs.x, c0, active);
+    return;
+  }
+  constexpr int C = Operand<BITS>::C;
+  float v[C];
+#pragma unroll
+  for (int q = 0; q < C / 8; ++q) {
+    const float4 zero = make_float4(0.f, 0.f, 0.f, 0.f);
+    const float4 a = active ? *reinterpret_cast<const float4 *>(xs.v + c0 + 8 * q) : zero;
+    const float4 b = active ? *reinterpret_cast<const float4 *>(xs.v + c0 + 8 * q + 4) : zero;
+    const uint4 g =
+        active ? *reinterpret_cast<const uint4 *>(xs.gamma + c0 + 8 * q) : make_uint4(0, 0, 0, 0);
+    const float vv[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
+    const uint32_t gw[4] = {g.x, g.y, g.z, g.w};
+#pragma unroll
+    for (int h = 0; h < 4; ++h) {
+      v[8 * q + 2 * h] = norm_value(vv[2 * h], __uint_as_float(gw[h] << 16), xs.r);
+      v[8 * q + 2 * h + 1] = norm_value(vv[2 * h + 1], __uint_as_float(gw[h] & 0xffff0000u), xs.r);
+    }
+  }
+  op.set(v);
+}
+
+// The thread's operand of a class of rows when x is normalised on the fly (XSource with v set):
+// computes r, sets x.r and builds the operand.  The threads of the first row group hold every
+// column once, so r comes from their steps: squares summed in fp32 per thread, then in fp64
+// across those warps in a fixed order (the same in every CTA and in both kernel modes), and
+// 1 / sqrt(mean + eps) in fp64 by one thread, rounded to fp32.  The operand then re-reads the
+// thread's values (from L1 for the first group).
+template <int BITS>
+__device__ __forceinline__ void load_x_class_norm(Operand<BITS> &op, const GateUpGeom &g,
+                                                  XSource &x, int din, double *red, float *rsh,
+                                                  int warp, int lane, int tid) {
+  constexpr int C = Operand<BITS>::C;
+  const int my_group = tid / g.tpr, my_step = tid % g.tpr;
+  const bool active = my_group < g.groups && my_step < g.T;
+  if (tid < g.tpr) {  // the first group's warps (tpr is a multiple of 32)
+    float ss = 0.f;
+    if (my_step < g.T) {
+#pragma unroll
+      for (int q = 0; q < C / 4; ++q) {
+        const float4 a = *reinterpret_cast<const float4 *>(x.v + my_step * C + 4 * q);
+        ss = fmaf(a.x, a.x, ss);
+        ss = fmaf(a.y, a.y, ss);
+        ss = fmaf(a.z, a.z, ss);
+        ss = fmaf(a.w, a.w, ss);
+      }
+    }
+    double d = ss;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) d += __shfl_xor_sync(0xffffffffu, d, o);
+    if (lane == 0) red[warp] = d;
+  }
+  consumer_sync(kConsumers);
+  if (tid == 0) {
+    double t = 0.0;
+    for (int w = 0; w < g.tpr / 32; ++w) t += red[w];
+    *rsh = static_cast<float>(1.0 / sqrt(t / din + static_cast<double>(x.eps)));
+  }
+  consumer_sync(kConsumers);
+  x.r = *rsh;
+  load_x_operand<BITS>(op, x, my_step * C, active);
+}
+
 __device__ __forceinline__ float silu_f(float z) { return z / (1.0f + expf(-z)); }
 
 // ------------------------------------------------------------------ ring and grid barrier
@@ -568,6 +664,8 @@ struct SmemA {
   int row_u[kBatchA];         // act index of each held row
   float coef[kBatchA];        // its coefficient: the slot's score or the shared scalar
   float stat[kConsumerWarps];
+  double dstat[kConsumerWarps];
+  float rnorm;                // r of the folded RMSNorm, broadcast
 };
 
 struct SmemB {
@@ -602,9 +700,9 @@ __device__ __forceinline__ void flush_a(SmemA &sm, int held, int wpg, float *act
 // waited before the counts are read).  Returns the rows still parked, which the caller flushes
 // (the two classes may have different warps per row, so a batch never mixes them).
 // The thread's x operand for one class's geometry.
-template <int BITS>
+template <int BITS, typename XS>
 __device__ __forceinline__ void load_x_class(Operand<BITS> &op, const GateUpGeom &g,
-                                             const uint16_t *x, int tid) {
+                                             const XS &x, int tid) {
   const int my_group = tid / g.tpr, my_step = tid % g.tpr;
   load_x_operand<BITS>(op, x, my_step * Operand<BITS>::C, my_group < g.groups && my_step < g.T);
 }
@@ -693,21 +791,31 @@ __device__ int consume_a_class(const LayerShape &s, const GateUpGeom &g, bool sh
 // Consumers of phase A for one token of one layer: x is read here; the stages' descriptors carry
 // the rest.  Ends with the activations written and a consumer_sync-free tail: callers
 // synchronise as needed.
-template <int BR, int BS>
+// CHAIN: x may be normalised on the fly (XSource with v set); otherwise x.x is read.
+template <int BR, int BS, bool CHAIN>
 __device__ void consume_a(const LayerShape &s, const LayerPtrs &w, const GateUpGeom &gr,
-                          const GateUpGeom &gs, const uint16_t *x, const int *cnt, float *act,
+                          const GateUpGeom &gs, XSource x, const int *cnt, float *act,
                           Ring &r, SmemA &sm, int tid) {
   const int warp = tid >> 5, lane = tid & 31;
+  Operand<BR> xr;   // x for the routed rows, loaded while the first stage is in flight
+  if constexpr (CHAIN) {
+    if (x.v != nullptr)
+      load_x_class_norm<BR>(xr, gr, x, s.din, sm.dstat, &sm.rnorm, warp, lane, tid);
+    else
+      load_x_class<BR>(xr, gr, x.x, tid);
+  } else {
+    load_x_class<BR>(xr, gr, x.x, tid);
+  }
   float shared_scalar = 1.0f;
   if (w.gate_vec != nullptr && s.n_shared > 0) {
     float dot = 0.f;
-    for (int c = tid; c < s.din; c += kConsumers)
-      dot = fmaf(bf16_to_float(x[c]), bf16_to_float(w.gate_vec[c]), dot);
+    for (int c = tid; c < s.din; c += kConsumers) {
+      const float xc = CHAIN ? x_value(x, c) : bf16_to_float(x.x[c]);
+      dot = fmaf(xc, bf16_to_float(w.gate_vec[c]), dot);
+    }
     dot = consumers_sum(dot, sm.stat, warp, lane);
     shared_scalar = 1.0f / (1.0f + expf(-dot));
   }
-  Operand<BR> xr;   // x for the routed rows, loaded while the first stage is in flight
-  load_x_class<BR>(xr, gr, x, tid);
   // the phase's first stage publishes the counts
   bool ok = warp_wait_full(r, lane), waited = true;
   const int nr = cnt[0], ns = cnt[1];
@@ -719,7 +827,10 @@ __device__ void consume_a(const LayerShape &s, const LayerPtrs &w, const GateUpG
   if (held > 0) flush_a(sm, held, gr.tpr / 32, act, tid, ns > 0);
   if (ns > 0) {
     Operand<BS> xsh;
-    load_x_class<BS>(xsh, gs, x, tid);
+    if constexpr (CHAIN)
+      load_x_class<BS>(xsh, gs, x, tid);
+    else
+      load_x_class<BS>(xsh, gs, x.x, tid);
     held = consume_a_class<BS>(s, gs, true, ns, xsh, act, shared_scalar, r, sm, waited, ok, tid);
     if (held > 0) flush_a(sm, held, gs.tpr / 32, act, tid, false);
   }
@@ -765,7 +876,7 @@ __device__ __forceinline__ void range_b(const LayerShape &s, int &i0, int &i1) {
 // Producer of phase B: per stage, lane q handles segment q (and q + 32, ...): the codes of R
 // output rows of that slot's (or shared expert's) down projection plus their scale and bias
 // windows.  `ids` is the producer's shared copy.
-__device__ void produce_b(const LayerShape &s, const LayerPtrs &w, const DownGeom &g,
+__device__ inline void produce_b(const LayerShape &s, const LayerPtrs &w, const DownGeom &g,
                           const int *ids, Ring &r, int lane, uint64_t pol) {
   int i0, i1;
   range_b(s, i0, i1);
@@ -822,7 +933,8 @@ __device__ __forceinline__ void down_rows(const uint8_t *cp, const uint8_t *sp, 
                                           int wins, int groups, int my_group, int nq,
                                           const Operand<BITS> &op, float (&acc)[VS]) {
   constexpr int VEC = Fmt<BITS>::kVecs;
-  constexpr int QB = VEC == 1 ? 4 : 1;  // rows in flight (a 6-bit operand already holds 64 registers)
+  // rows in flight (a 6-bit operand already holds 64 registers)
+  constexpr int QB = VEC == 1 ? 4 : 1;
 #pragma unroll
   for (int q0 = 0; q0 < VS; q0 += QB) {
     if (q0 >= nq) break;

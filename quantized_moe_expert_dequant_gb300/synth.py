@@ -27,6 +27,8 @@ Activations and router outputs:
   bf16 (round to nearest even) for x, resid and the shared gate vector g.
 * ids: K distinct experts of E by a partial Fisher-Yates shuffle driven by ``mix64``.
 * scores: softmax, in fp64, of K standard-normal logits, rounded to fp32.
+* RMSNorm weight of a chained stack (one row per layer after the first): ``1 + 0.2 * normal``
+  in fp64, rounded to fp32 and to bf16.
 """
 from __future__ import annotations
 
@@ -38,7 +40,7 @@ M64 = (1 << 64) - 1
 # tensor roles in the key chain
 GATE, UP, DOWN, SH_GATE, SH_UP, SH_DOWN = 0, 1, 2, 3, 4, 5
 CODES, SCALES, BIASES = 0, 1, 2
-ROLE_X, ROLE_RESID, ROLE_GVEC, ROLE_IDS, ROLE_LOGITS = 10, 11, 12, 13, 14
+ROLE_X, ROLE_RESID, ROLE_GVEC, ROLE_IDS, ROLE_LOGITS, ROLE_NORM = 10, 11, 12, 13, 14, 15
 
 _C1 = np.uint64(0xBF58476D1CE4E5B9)
 _C2 = np.uint64(0x94D049BB133111EB)
@@ -159,6 +161,13 @@ def residual(seed, layer, token, din):
 
 def gate_vector(seed, layer, din, std=0.02):
     return normal_bf16(key(seed, layer, ROLE_GVEC), din, std)
+
+
+def norm_weight(seed, layer, din):
+    """bf16 [din]: the RMSNorm weight that turns layer ``layer - 1``'s output into layer
+    ``layer``'s input in a chained stack."""
+    return f32_to_bf16_bits((1.0 + 0.2 * normals_f64(key(seed, layer, ROLE_NORM), din))
+                            .astype(np.float32))
 
 
 def topk_ids(seed, layer, token, n_experts, top_k, step=0) -> np.ndarray:

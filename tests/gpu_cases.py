@@ -105,3 +105,33 @@ def assert_parity_bf16(gpu_bf16: torch.Tensor, ref: np.ndarray, what=""):
     _, e = np.frexp(r)
     ulp = np.ldexp(1.0, e - 8)  # |r| in [2^(e-1), 2^e): bf16 spacing 2^(e-8)
     assert np.all(np.abs(g - r) <= ulp), f"{what}: bf16 output beyond one ulp"
+
+
+def oracle_stack(shape: Shape, x, ids, sc, resid0, m: int = 1, rows=None, norm=None,
+                 eps: float = 0.0, layers: int | None = None):
+    """The oracle's own chain through the first `layers` layers of a stack: [layers][m][rows].
+
+    Every layer's residual is the oracle's previous output rounded to fp32 (the stack keeps layer
+    outputs in fp32).  x is [L][m][din] (bf16 bits); with norm (bf16 [L - 1][din]) only x[0] is
+    read and layer l >= 1 takes RMSNorm(previous output) with row l - 1, which needs every row of
+    that output (rows must then be None).  No value comes from the GPU."""
+    L = shape.layers if layers is None else layers
+    assert norm is None or rows is None
+    oras = [OracleLayer(shape, l) for l in range(L)]
+    out = []
+    for l in range(L):
+        per = []
+        for t in range(m):
+            if l == 0:
+                xt, resid = x[0][t], resid0[t]
+            else:
+                prev = out[l - 1][t].astype(np.float32)
+                xt = x[l][t] if norm is None else O.rmsnorm_bf16(prev, norm[l - 1], eps)
+                resid = prev
+                if rows is not None:   # only the sampled rows of the previous output exist
+                    full = np.zeros(shape.din, np.float32)
+                    full[rows] = prev
+                    resid = full
+            per.append(oras[l].token(xt, resid, ids[l][t], sc[l][t], rows=rows))
+        out.append(np.stack(per))
+    return out

@@ -1,9 +1,10 @@
 """GPU parity of the layer-stack driver (one CUDA graph per decode step) through the C ABI.
 
-The graph replay must equal the same layers run one forward at a time, byte for byte, and every
-sampled layer must match the oracle given the GPU's own previous output as its residual (so each
-layer is checked on identical inputs).  The full-size stacks run in the configuration the
-benchmark times.
+The graph replay must equal the same layers run one forward at a time, byte for byte.  Small
+stacks match the oracle's own chain (its outputs feed its next layer) at every layer and row; the
+full-size stacks, run in the configuration the benchmark times, are checked on sampled rows of
+sampled layers through each layer's block term (out_l - out_{l-1}), which the oracle computes from
+the seeded inputs alone.
 """
 import numpy as np
 import pytest
@@ -43,14 +44,28 @@ def run_chain(layers, x, ids, sc, resid0, m, mode=Bn.KERNELS_FUSED):
     return outs
 
 
-def check_layers(shape, x, ids, sc, resid0, outs, layers_to_check, rows, tokens=(0,)):
+def check_layers(shape, x, ids, sc, resid0, outs, rows, tokens=(0,)):
+    """Every layer's output against the oracle's own chain (rows: the rows the oracle computes)."""
+    ref = C.oracle_stack(shape, x, ids, sc, resid0, m=max(tokens) + 1, rows=rows)
+    for l in range(shape.layers):
+        for t in tokens:
+            got = outs[l][t].cpu().numpy()[rows]
+            C.assert_parity(got, ref[l][t], f"{shape.name}: layer {l} token {t}")
+
+
+def check_contributions(shape, x, ids, sc, resid0, outs, layers_to_check, rows):
+    """Layers of a full-size stack, on sampled rows, through a property that holds at any size:
+    a layer adds its block term to its residual, so out_l - out_{l-1} is the oracle's block output
+    with a zero residual on the same seeded inputs (layer 0: out_0 - resid0).  The fp32 sum in the
+    tail rounds once, far below the parity bar."""
+    zero = np.zeros(shape.din, np.float32)
     for l in layers_to_check:
         ora = C.OracleLayer(shape, l)
-        for t in tokens:
-            resid = resid0[t] if l == 0 else outs[l - 1][t].cpu().numpy()
-            ref = ora.token(x[l][t], resid, ids[l][t], sc[l][t], rows=rows)
-            got = outs[l][t].cpu().numpy()[rows]
-            C.assert_parity(got, ref, f"{shape.name}: layer {l} token {t}")
+        got = outs[l][0].cpu().numpy().astype(np.float64)
+        prev = (synth.bf16_bits_to_f32(resid0[0]) if l == 0
+                else outs[l - 1][0].cpu().numpy()).astype(np.float64)
+        ref = ora.token(x[l][0], zero, ids[l][0], sc[l][0], rows=rows)
+        C.assert_parity((got - prev)[rows], ref, f"{shape.name}: layer {l} block term")
 
 
 def test_small_stack_graph_equals_chain_and_oracle():
@@ -66,7 +81,7 @@ def test_small_stack_graph_equals_chain_and_oracle():
     assert stack.get_error() == 0
     outs = run_chain(layers, x, ids, sc, resid0, 1)
     assert torch.equal(out.view(torch.int32), outs[-1].view(torch.int32))
-    check_layers(shape, x, ids, sc, resid0, outs, range(shape.layers), np.arange(shape.din))
+    check_layers(shape, x, ids, sc, resid0, outs, np.arange(shape.din))
     # the graph is cached per pointer set: a second step with the same buffers replays it
     out2 = torch.empty_like(out)
     xd, idd, scd, rd = (C.dev(x, torch.bfloat16), C.dev(ids, torch.int32),
@@ -98,8 +113,7 @@ def test_small_stack_several_tokens(mode):
     torch.cuda.synchronize()
     outs = run_chain(layers, x, ids, sc, resid0, m, mode)
     assert torch.equal(out.view(torch.int32), outs[-1].view(torch.int32))
-    check_layers(shape, x, ids, sc, resid0, outs, range(shape.layers), np.arange(shape.din),
-                 tokens=range(m))
+    check_layers(shape, x, ids, sc, resid0, outs, np.arange(shape.din), tokens=range(m))
     stack.close()
 
 
@@ -125,7 +139,7 @@ def test_full_size_stack(name):
         rows = np.unique(np.concatenate([[0, shape.din - 1],
                                          rng.choice(shape.din, 62, replace=False)]))
         L = shape.layers
-        check_layers(shape, x, ids, sc, resid0, outs, [0, 1, L // 2, L - 1], rows)
+        check_contributions(shape, x, ids, sc, resid0, outs, [0, 1, L // 2, L - 1], rows)
     finally:
         layers = None
         torch.cuda.empty_cache()

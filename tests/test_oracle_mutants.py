@@ -45,6 +45,12 @@ MUTANTS = {
                                        "if (best < 0 || logits[e] >= logits[best]) best = e;"),
     "router softmax without the max shift": ("sum += exp((double)logits[ids[t]] - mx);",
                                              "sum += exp((double)logits[ids[t]]);"),
+    "rmsnorm without eps": ("sqrt(ss / n + (double)eps)", "sqrt(ss / n)"),
+    "rmsnorm sums instead of averaging": ("sqrt(ss / n + (double)eps)", "sqrt(ss + (double)eps)"),
+    "rmsnorm weight dropped": ("const float u = (float)oracle_bf16(gamma[c]) * t;",
+                               "const float u = t;"),
+    "bf16 rounding truncates": ("ldexp(nearbyint(ldexp(y, -s)), s)", "ldexp(trunc(ldexp(y, -s)), s)"),
+    "bf16 ties away from zero": ("ldexp(nearbyint(ldexp(y, -s)), s)", "ldexp(round(ldexp(y, -s)), s)"),
 }
 
 

@@ -420,3 +420,67 @@ def test_router_ties_and_special_cases():
     i2, s2 = O.router(logits + np.float32(4.0), 8)
     assert np.array_equal(i1, i2)
     np.testing.assert_allclose(s1, s2, rtol=1e-5)
+
+
+# ------------------------------------------------------------------ the folded RMSNorm (chained stack)
+# "Red Lite dev39 -- fused expert tail", Measurements: a tail that also folded in the next layer's
+# RMSNorm.  The page gives no formula; the oracle takes the usual RMSNorm, rounded to bf16.
+
+def test_round_bf16_ties_to_even_and_edges():
+    one = 0x3F80
+    assert O.round_bf16(1.0) == one
+    assert O.round_bf16(1 + 2.0 ** -8) == one              # halfway to 1 + 2^-7: the even one
+    assert O.round_bf16(1 + 3 * 2.0 ** -8) == 0x3F82       # halfway to 1 + 2^-6: the even one
+    assert O.round_bf16(1 + 2.0 ** -8 + 2.0 ** -30) == 0x3F81
+    assert O.round_bf16(-(1 + 2.0 ** -8 + 2.0 ** -30)) == 0xBF81
+    assert O.round_bf16(2.0 ** -133) == 0x0001             # smallest subnormal
+    assert O.round_bf16(2.0 ** -134) == 0x0000             # halfway to zero: even
+    assert O.round_bf16(3 * 2.0 ** -134) == 0x0002
+    assert O.round_bf16(3.39e38) == 0x7F7F                 # largest finite bf16 is 3.3895e38
+    assert O.round_bf16(3.4e38) == 0x7F80 and O.round_bf16(-3.4e38) == 0xFF80
+    assert O.round_bf16(float("inf")) == 0x7F80 and O.round_bf16(float("-inf")) == 0xFF80
+    assert O.round_bf16(0.0) == 0 and O.round_bf16(-0.0) == 0x8000
+    nan = O.round_bf16(float("nan"))
+    assert nan & 0x7F80 == 0x7F80 and nan & 0x7F
+
+
+def test_round_bf16_matches_an_independent_fp32_rounding():
+    v = np.random.default_rng(3).standard_normal(4000).astype(np.float32)
+    v *= np.float32(2.0) ** np.random.default_rng(4).integers(-60, 60, 4000).astype(np.float32)
+    got = np.array([O.round_bf16(float(a)) for a in v], dtype=np.uint16)
+    assert np.array_equal(got, synth.f32_to_bf16_bits(v))
+
+
+def test_rmsnorm_matches_torch_rms_norm():
+    torch = pytest.importorskip("torch")
+    rng = np.random.default_rng(5)
+    for n, eps, scale in ((2048, 1e-6, 1.0), (4096, 1e-5, 30.0), (64, 1e-6, 1e-3), (192, 0.0, 1.0)):
+        v = (rng.standard_normal(n) * scale).astype(np.float32)
+        g = synth.f32_to_bf16_bits((1 + 0.2 * rng.standard_normal(n)).astype(np.float32))
+        x = synth.bf16_bits_to_f32(O.rmsnorm_bf16(v, g, eps)).astype(np.float64)
+        w = torch.from_numpy(synth.bf16_bits_to_f32(g).astype(np.float64))
+        ref = torch.nn.functional.rms_norm(torch.from_numpy(v.astype(np.float64))[None], (n,),
+                                           weight=w, eps=eps)[0].numpy()
+        # x is ref rounded to bf16 (half a spacing) after r and two products in fp32 (2^-22)
+        _, e = np.frexp(ref)
+        assert np.all(np.abs(x - ref) <= np.ldexp(1.0, e - 9) + 2.0 ** -22 * np.abs(ref)), (n, eps)
+
+
+def test_rmsnorm_closed_forms_and_scale_invariance():
+    n = 256
+    unit = np.full(n, 0x3F80, np.uint16)
+    for c in (3.0, -0.125, 7e30, 1e-20):
+        x = O.rmsnorm_bf16(np.full(n, c, np.float32), unit, 0.0)
+        assert np.all(x == (0x3F80 if c > 0 else 0xBF80)), c   # v / rms(v) = sign(v)
+    x = O.rmsnorm_bf16(np.zeros(n, np.float32), unit, 1e-6)
+    assert np.all(x & 0x7FFF == 0)
+    rng = np.random.default_rng(6)
+    v = rng.standard_normal(n).astype(np.float32)
+    g = synth.f32_to_bf16_bits((1 + 0.2 * rng.standard_normal(n)).astype(np.float32))
+    base = O.rmsnorm_bf16(v, g, 0.0)
+    for k in (-20, -1, 7):                                    # powers of two scale exactly
+        assert np.array_equal(O.rmsnorm_bf16(v * np.float32(2.0 ** k), g, 0.0), base)
+    assert np.all(O.rmsnorm_bf16(v, np.zeros(n, np.uint16), 1e-6) & 0x7FFF == 0)
+    # mean of x^2 / gamma^2 is 1 up to bf16 rounding (eps 0)
+    xf = synth.bf16_bits_to_f32(base).astype(np.float64) / synth.bf16_bits_to_f32(g)
+    assert abs(np.mean(xf ** 2) - 1.0) < 2 ** -7
