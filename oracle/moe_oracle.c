@@ -268,3 +268,19 @@ void oracle_rmsnorm_bf16(const float *v, int32_t n, const uint16_t *gamma, float
     x[c] = oracle_round_bf16((double)u);
   }
 }
+
+/* Dense bf16 decode GEMV, the attention projections that "Measure attention projections instead
+ * of serving them, and record the amortisation trap" measures at 1, 8 and 32 rows:
+ *   y[t][o] = sum_i W[o][i] * x[t][i]
+ * W bf16 [n_out][n_in] row-major, x bf16 [m][n_in], y double [m][n_out]; plain loops in double,
+ * every sum left to right. */
+void oracle_gemv_bf16(const uint16_t *W, const uint16_t *x, int32_t m, int32_t n_out,
+                      int32_t n_in, double *y) {
+  for (int32_t t = 0; t < m; ++t)
+    for (int32_t o = 0; o < n_out; ++o) {
+      double acc = 0.0;
+      for (int32_t i = 0; i < n_in; ++i)
+        acc += oracle_bf16(W[(int64_t)o * n_in + i]) * oracle_bf16(x[(int64_t)t * n_in + i]);
+      y[(int64_t)t * n_out + o] = acc;
+    }
+}

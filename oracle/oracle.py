@@ -80,6 +80,9 @@ def lib():
             L.oracle_router.restype = None
             L.oracle_router.argtypes = [ctypes.c_void_p, ctypes.c_int32, ctypes.c_int32,
                                         ctypes.c_void_p, ctypes.c_void_p]
+            L.oracle_gemv_bf16.restype = None
+            L.oracle_gemv_bf16.argtypes = [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int32,
+                                           ctypes.c_int32, ctypes.c_int32, ctypes.c_void_p]
             L.oracle_round_bf16.restype = ctypes.c_uint16
             L.oracle_round_bf16.argtypes = [ctypes.c_double]
             L.oracle_rmsnorm_bf16.restype = None
@@ -266,3 +269,16 @@ def rmsnorm_bf16(v: np.ndarray, gamma_bf16: np.ndarray, eps: float) -> np.ndarra
     x = np.empty(len(v), np.uint16)
     lib().oracle_rmsnorm_bf16(_ptr(v), len(v), _ptr(g), float(eps), _ptr(x))
     return x
+
+
+def gemv_bf16(W_bf16: np.ndarray, x_bf16: np.ndarray) -> np.ndarray:
+    """y [m, n_out] (fp64) = x [m, n_in] times W [n_out, n_in] transposed, both bf16 bit patterns
+    (see oracle_gemv_bf16)."""
+    W = np.ascontiguousarray(W_bf16, dtype=np.uint16)
+    x = np.ascontiguousarray(x_bf16, dtype=np.uint16)
+    n_out, n_in = W.shape
+    m = x.shape[0]
+    assert x.shape == (m, n_in)
+    y = np.empty((m, n_out), np.float64)
+    lib().oracle_gemv_bf16(_ptr(W), _ptr(x), m, n_out, n_in, _ptr(y))
+    return y

@@ -51,6 +51,12 @@ MUTANTS = {
                                "const float u = t;"),
     "bf16 rounding truncates": ("ldexp(nearbyint(ldexp(y, -s)), s)", "ldexp(trunc(ldexp(y, -s)), s)"),
     "bf16 ties away from zero": ("ldexp(nearbyint(ldexp(y, -s)), s)", "ldexp(round(ldexp(y, -s)), s)"),
+    "gemv drops the last column": ("for (int32_t i = 0; i < n_in; ++i)\n        acc +=",
+                                   "for (int32_t i = 0; i < n_in - 1; ++i)\n        acc +="),
+    "gemv reads W transposed": ("oracle_bf16(W[(int64_t)o * n_in + i])",
+                                "oracle_bf16(W[((int64_t)i * n_out + o) % ((int64_t)n_out * n_in)])"),
+    "gemv reads the first token for all": ("oracle_bf16(x[(int64_t)t * n_in + i])",
+                                           "oracle_bf16(x[i])"),
 }
 
 

@@ -484,3 +484,36 @@ def test_rmsnorm_closed_forms_and_scale_invariance():
     # mean of x^2 / gamma^2 is 1 up to bf16 rounding (eps 0)
     xf = synth.bf16_bits_to_f32(base).astype(np.float64) / synth.bf16_bits_to_f32(g)
     assert abs(np.mean(xf ** 2) - 1.0) < 2 ** -7
+
+
+# ------------------------------------------------------------------ dense bf16 decode GEMV
+# "Measure attention projections instead of serving them, and record the amortisation trap": the
+# q/k/v/o projections of a decode token, y = x W^T with bf16 W and x, measured at 1, 8, 32 rows.
+
+def test_gemv_matches_numpy_matmul():
+    rng = np.random.default_rng(8)
+    for m, n_out, n_in in ((1, 48, 64), (8, 33, 72), (32, 17, 40), (3, 1, 8)):
+        W = synth.f32_to_bf16_bits(rng.standard_normal((n_out, n_in)).astype(np.float32))
+        x = synth.f32_to_bf16_bits(rng.standard_normal((m, n_in)).astype(np.float32))
+        ref = (synth.bf16_bits_to_f32(x).astype(np.float64)
+               @ synth.bf16_bits_to_f32(W).astype(np.float64).T)
+        np.testing.assert_allclose(O.gemv_bf16(W, x), ref, rtol=1e-12, atol=1e-12)
+
+
+def test_gemv_one_hot_inputs_pick_columns_and_rows_stay_apart():
+    rng = np.random.default_rng(9)
+    n_out, n_in = 12, 24
+    W = synth.f32_to_bf16_bits(rng.standard_normal((n_out, n_in)).astype(np.float32))
+    Wf = synth.bf16_bits_to_f32(W).astype(np.float64)
+    one = synth.f32_to_bf16_bits(np.float32(1.0))
+    for i in (0, 7, n_in - 1):
+        x = np.zeros((2, n_in), np.uint16)
+        x[1, i] = one                                    # token 1 picks column i, token 0 is zero
+        y = O.gemv_bf16(W, x)
+        assert np.all(y[0] == 0.0)
+        assert np.array_equal(y[1], Wf[:, i])
+    # a unit row of W returns the matching input element for every token
+    Wi = np.zeros((n_in, n_in), np.uint16)
+    Wi[np.arange(n_in), np.arange(n_in)] = one
+    x = synth.f32_to_bf16_bits(rng.standard_normal((3, n_in)).astype(np.float32))
+    assert np.array_equal(O.gemv_bf16(Wi, x), synth.bf16_bits_to_f32(x).astype(np.float64))
