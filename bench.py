@@ -42,6 +42,7 @@ from quantized_moe_expert_dequant_gb300.workloads import ALL, Shape  # noqa: E40
 METRIC = "MoE decode tok/s (full layer stack) and achieved HBM GB/s vs peak, 1 GB300"
 DEFAULT_WORKLOAD = "qwen3_stack_8bit"
 NORM_EPS = 1e-6   # RMSNorm epsilon of the chained stack (--chain-norm)
+GEMV_NAMES = ("qwen25_1p5b_qo", "qwen25_1p5b_kv", "qwen3_8b_qo", "qwen3_8b_kv")
 KERNEL_SOURCES = ["quantized_moe_expert_dequant_gb300/csrc/moe_kernels.cu",
                   "quantized_moe_expert_dequant_gb300/csrc/moe_fused.cuh",
                   "quantized_moe_expert_dequant_gb300/csrc/moe_kernels_g8.cu",
@@ -487,6 +488,112 @@ def run_ours(args, shape: Shape):
     return 0
 
 
+# ---------------------------------------------------------------- the dense bf16 GEMV workload
+
+GEMV_METRIC = "dense bf16 decode GEMV GB/s (weights streamed), 1 GB300"
+
+
+def run_gemv(args):
+    """A projection of "Measure attention projections instead of serving them, and record the
+    amortisation trap" at --rows rows: one launch streams R distinct copies of the weight matrix,
+    R chosen so that a launch moves at least 1 GiB (the page's rule: never time cache-resident
+    weights), all rows multiplied by one seeded input."""
+    import torch
+
+    from quantized_moe_expert_dequant_gb300 import binding as Bn
+    from quantized_moe_expert_dequant_gb300.workloads import GEMV
+
+    rank, world, local = dist_setup("nccl")
+    torch.cuda.set_device(local)
+    device = torch.device("cuda", local)
+    g, m = GEMV[args.gemv], args.rows
+    if not 1 <= m <= 32:
+        raise SystemExit("--rows must be in 1..32")
+    R = -(-(1 << 30) // g.weight_bytes())
+    W1 = synth.dense_weight(g.seed, g.n_out, g.n_in)
+    x_host = synth.dense_input(g.seed, m, g.n_in)
+    w1 = torch.from_numpy(W1.view(np.int16)).view(torch.bfloat16).to(device)
+    W = w1.unsqueeze(0).repeat(R, 1, 1).contiguous()          # R distinct copies in HBM
+    x = torch.from_numpy(x_host.view(np.int16)).view(torch.bfloat16).to(device)
+    y = torch.empty((R, m, g.n_out), dtype=torch.float32, device=device)
+    stream = torch.cuda.current_stream(device)
+    bus = None
+    try:
+        bus = torch.cuda.get_device_properties(device).pci_bus_id
+    except AttributeError:
+        bus = None
+    sampler = ClockSampler(bus if bus else str(local))
+    for _ in range(args.warmup):
+        Bn.gemv_bf16(W, x, y, stream=stream)
+    torch.cuda.synchronize(device)
+    barrier(device)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(args.steps):
+        Bn.gemv_bf16(W, x, y, stream=stream)
+    e1.record(stream)
+    torch.cuda.synchronize(device)
+    barrier(device)
+    ms = max_over_ranks(e0.elapsed_time(e1), device) / args.steps
+    wbytes = R * g.weight_bytes()
+    io = R * m * g.n_out * 4 + m * g.n_in * 2
+    value = world * wbytes / (ms * 1e-3) / 1e9
+    # end to end: pinned host input in, launch, host result out, every step
+    xh = torch.from_numpy(x_host.view(np.int16)).view(torch.bfloat16).pin_memory()
+    yh = torch.empty((R, m, g.n_out), dtype=torch.float32).pin_memory()
+    e2e_steps = max(args.steps // 4, 5)
+    torch.cuda.synchronize(device)
+    t0 = time.perf_counter()
+    for _ in range(e2e_steps):
+        x.copy_(xh, non_blocking=True)
+        Bn.gemv_bf16(W, x, y, stream=stream)
+        yh.copy_(y, non_blocking=True)
+        torch.cuda.synchronize(device)
+    e2e_s = max_over_ranks(time.perf_counter() - t0, device)
+    clocks = sampler.stop()
+    err = float((y[0].cpu().double() - y[R - 1].cpu().double()).abs().max())
+    assert err == 0.0, "copies of one matrix gave different results"
+    peaks = measured_peaks()
+    peak = peaks["hbm_gbs"] if peaks else 6800.0
+    note = "of measured" if peaks else "of fallback"
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        from oracle import oracle as O
+        n = 0
+        t0 = time.perf_counter()
+        while time.perf_counter() - t0 < min(args.cpu_seconds, 10.0):
+            O.gemv_bf16(W1, x_host)
+            n += 1
+        spent = time.perf_counter() - t0
+        cpu = {"value": n * g.weight_bytes() / spent / 1e9, "unit": "GB/s", "cores": 1,
+               "kind": "oracle",
+               "sample": f"{n} products of one {g.n_out}x{g.n_in} matrix with {m} rows through "
+                         f"the single-threaded fp64 oracle in {spent:.1f} s"}
+    kernel = "gemv_cc_kernel" if m <= 4 else "gemv_mma_kernel"
+    line = {
+        "metric": GEMV_METRIC, "value": value, "unit": "GB/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic (seeded bf16 weights and inputs)",
+        "config": {"workload": g.name, "n_out": g.n_out, "n_in": g.n_in, "rows": m,
+                   "matrices_per_launch": R, "parallelism": f"replicas x{world}",
+                   "l2": f"inputs larger than L2: {wbytes / 1e9:.2f} GB of distinct weight "
+                         f"copies per launch"},
+        "roofline": {"kernel": kernel, "bound": "hbm", "achieved": (wbytes + io) / (ms * 1e-3) / 1e9,
+                     "peak": peak, "unit": "GB/s", "frac": (wbytes + io) / (ms * 1e-3) / 1e9 / peak,
+                     "traffic": None, "bytes_per_launch": wbytes + io, "us_per_launch": ms * 1e3,
+                     "note": note + " (copy peak)"},
+        "cpu_baseline": cpu,
+        "e2e": {"value": world * wbytes * e2e_steps / e2e_s / 1e9, "unit": "GB/s",
+                "h2d_bytes_per_step": m * g.n_in * 2, "d2h_bytes_per_step": R * m * g.n_out * 4},
+        "gpu_launches": args.steps,
+        "clocks": clocks,
+    }
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    return 0
+
+
 def main(argv=None):
     ap = argparse.ArgumentParser(description=__doc__.splitlines()[0])
     ap.add_argument("--gpus", type=int, default=1)
@@ -505,9 +612,18 @@ def main(argv=None):
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--layers", type=int, default=0,
                     help="run only the first N layers of the workload (profiling runs)")
+    ap.add_argument("--gemv", choices=sorted(GEMV_NAMES), default=None,
+                    help="measure the dense bf16 decode GEMV of this projection instead")
+    ap.add_argument("--rows", type=int, default=1, help="rows (tokens) of the --gemv product")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")
+    if args.gemv:
+        if args.impl == "reference":
+            print(json.dumps({"impl": "reference", "unavailable": "the GEMV workload has no "
+                              "reference arm; its oracle baseline is in the line's cpu_baseline"}))
+            return 0
+        return run_gemv(args)
     shape = ALL[args.workload]
     if args.layers:
         shape = shape.with_(layers=args.layers, name=f"{shape.name} (first {args.layers} layers)")

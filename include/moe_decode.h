@@ -209,6 +209,24 @@ int moe_stack_step_host(moe_stack_t *s, const void *x_host, int32_t m, const int
 int moe_stack_get_error(moe_stack_t *s, int32_t *device_error);
 void moe_stack_destroy(moe_stack_t *s);
 
+/* ---- dense bf16 decode GEMV ------------------------------------------------------------------
+ * The q/k/v/o attention projections that "Measure attention projections instead of serving
+ * them, and record the amortisation trap" measures beside the block at 1, 8 and 32 rows.  For
+ * each of n_mats weight matrices r:
+ *   y[r][t][o] = sum_i W[r][o][i] * x_r[t][i]          (bf16 products, fp32 accumulation)
+ *   W        bf16 [n_mats][n_out][n_in] device, 16-byte aligned; n_in a multiple of 8
+ *   x        bf16 device, 16-byte aligned: x_r = x + r * x_stride elements is [m][n_in]
+ *            (x_stride 0: one input for every matrix; otherwise a multiple of 8)
+ *   y        fp32 [n_mats][m][n_out] device
+ *   m        rows (tokens), 1..32.  Up to 4 rows CUDA cores stream W (the product is HBM-bound);
+ *            from 5 rows bf16 tensor-core tiles (16 weight rows x 8 tokens) take the products.
+ * One launch covers every matrix, so a caller can stream far more than L2 per launch (the page's
+ * rule against timing cache-resident weights).  The sum order is fixed: repeat calls give
+ * identical bytes.  Asynchronous on `stream`.  Returns MOE_OK, MOE_ERR_INVALID_ARG on a size or
+ * alignment outside the above (nothing enqueued), or MOE_ERR_CUDA if the launch fails. */
+int moe_gemv_bf16(const void *W, const void *x, int64_t x_stride, float *y, int32_t n_mats,
+                  int32_t m, int32_t n_out, int32_t n_in, void *stream);
+
 /* ---- canonical packing (host) ---------------------------------------------------------------
  * codes: uint8 [rows][cols], one code per byte, each < 2^bits; packed: [rows][cols*bits/8].
  * cols must be a multiple of 64.  Returns MOE_ERR_INVALID_ARG on a code out of range. */

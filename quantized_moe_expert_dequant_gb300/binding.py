@@ -30,6 +30,7 @@ _STATUS = {0: "MOE_OK", -1: "MOE_ERR_INVALID_ARG", -2: "MOE_ERR_UNSUPPORTED", -3
 
 EXPORTS = ["moe_decode_create", "moe_decode_forward", "moe_decode_get_error", "moe_decode_destroy",
            "moe_decode_forward_noalloc",
+           "moe_gemv_bf16",
            "moe_stack_create", "moe_stack_create_chained", "moe_stack_step",
            "moe_stack_step_parts", "moe_stack_step_host",
            "moe_stack_get_error",
@@ -84,6 +85,7 @@ def lib() -> ctypes.CDLL:
                                                vp, i32, vp, vp, vp, vp, vp, vp],
                 "moe_stack_create": [ctypes.POINTER(Config), i32, ctypes.POINTER(LayerWeights),
                                      ctypes.POINTER(vp)],
+                "moe_gemv_bf16": [vp, vp, ctypes.c_int64, vp, i32, i32, i32, i32, vp],
                 "moe_stack_create_chained": [ctypes.POINTER(Config), i32,
                                              ctypes.POINTER(LayerWeights), vp, ctypes.c_float,
                                              ctypes.POINTER(vp)],
@@ -396,3 +398,19 @@ def router_topk(logits: torch.Tensor, top_k: int, stream=None):
                                                    _p(scores), _stream(stream)))
     return ids, scores
 
+
+
+# ---------------------------------------------------------------- dense bf16 decode GEMV
+
+def gemv_bf16(W, x, y=None, shared_x: bool = True, stream=None):
+    """y [n_mats, m, n_out] fp32 = x W^T for every matrix of W (bf16 [n_mats, n_out, n_in] on
+    the device).  x is bf16 [m, n_in] (shared_x) or [n_mats, m, n_in]."""
+    import torch
+    n_mats, n_out, n_in = W.shape
+    m = x.shape[-2]
+    if y is None:
+        y = torch.empty((n_mats, m, n_out), dtype=torch.float32, device=W.device)
+    x_stride = 0 if shared_x else m * n_in
+    check("moe_gemv_bf16", lib().moe_gemv_bf16(_p(W), _p(x), x_stride, _p(y), n_mats, m, n_out,
+                                               n_in, _stream(stream)))
+    return y

@@ -29,6 +29,8 @@ Activations and router outputs:
 * scores: softmax, in fp64, of K standard-normal logits, rounded to fp32.
 * RMSNorm weight of a chained stack (one row per layer after the first): ``1 + 0.2 * normal``
   in fp64, rounded to fp32 and to bf16.
+* Dense projection (bf16 GEMV workload): weights ``0.02 * normal`` and inputs ``normal``, rounded
+  to fp32 and to bf16.
 """
 from __future__ import annotations
 
@@ -41,6 +43,7 @@ M64 = (1 << 64) - 1
 GATE, UP, DOWN, SH_GATE, SH_UP, SH_DOWN = 0, 1, 2, 3, 4, 5
 CODES, SCALES, BIASES = 0, 1, 2
 ROLE_X, ROLE_RESID, ROLE_GVEC, ROLE_IDS, ROLE_LOGITS, ROLE_NORM = 10, 11, 12, 13, 14, 15
+ROLE_DENSE_W, ROLE_DENSE_X = 16, 17
 
 _C1 = np.uint64(0xBF58476D1CE4E5B9)
 _C2 = np.uint64(0x94D049BB133111EB)
@@ -188,3 +191,15 @@ def scores(seed, layer, token, top_k, step=0) -> np.ndarray:
     logits = normals_f64(key(seed, layer, ROLE_LOGITS, token, step), top_k)
     e = np.exp(logits - logits.max())
     return (e / e.sum()).astype(np.float32)
+
+
+def dense_weight(seed, n_out, n_in, matrix=0):
+    """bf16 [n_out, n_in] weights of one dense projection."""
+    k = key(seed, matrix, ROLE_DENSE_W)
+    return normal_bf16(k, n_out * n_in, 0.02).reshape(n_out, n_in)
+
+
+def dense_input(seed, m, n_in, matrix=0):
+    """bf16 [m, n_in] rows (tokens) multiplied by a dense projection."""
+    k = key(seed, matrix, ROLE_DENSE_X)
+    return normal_bf16(k, m * n_in).reshape(m, n_in)

@@ -88,3 +88,24 @@ ALL = {
     "e512_stack": E512_TOP10_STACK,
     "dots_stack_mixed": DOTS_MIXED_STACK,
 }
+
+
+@dataclasses.dataclass(frozen=True)
+class GemvShape:
+    """A dense bf16 projection [n_out, n_in] of a decode token ("Measure attention projections
+    instead of serving them, and record the amortisation trap": q/o and k/v of two models)."""
+    name: str
+    n_out: int
+    n_in: int
+    seed: int
+
+    def weight_bytes(self) -> int:
+        return self.n_out * self.n_in * 2
+
+
+GEMV = {
+    "qwen25_1p5b_qo": GemvShape("Qwen2.5-1.5B q/o projection, bf16", 1536, 1536, 0x5EED0101),
+    "qwen25_1p5b_kv": GemvShape("Qwen2.5-1.5B k/v projection, bf16", 256, 1536, 0x5EED0102),
+    "qwen3_8b_qo": GemvShape("Qwen3-8B q/o projection, bf16", 4096, 4096, 0x5EED0103),
+    "qwen3_8b_kv": GemvShape("Qwen3-8B k/v projection, bf16", 1024, 4096, 0x5EED0104),
+}
