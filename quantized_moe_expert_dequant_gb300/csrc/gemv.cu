@@ -197,10 +197,12 @@ static cudaError_t launch(K kern, Params p, int rows_per_task, cudaStream_t stre
     e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, kThreads, 0);
   if (e != cudaSuccess) return e;
   if (per_sm < 1) per_sm = 1;
-  // every SM busy with whole waves of resident blocks; fewer blocks when there are few tasks
-  int64_t grid = static_cast<int64_t>(sms) * per_sm;
-  const int64_t need = (p.tasks + kWarps - 1) / kWarps;
-  if (need < grid) grid = need;
+  // Tasks are equal, so the launch takes as many rounds as the resident warps need, and the grid
+  // shrinks until every warp has the same number of tasks (no partly filled last round).
+  const int64_t resident = static_cast<int64_t>(sms) * per_sm * kWarps;
+  const int64_t rounds = (p.tasks + resident - 1) / resident;
+  const int64_t warps = (p.tasks + rounds - 1) / rounds;
+  const int64_t grid = (warps + kWarps - 1) / kWarps;
   kern<<<static_cast<int>(grid), kThreads, 0, stream>>>(p);
   return cudaGetLastError();
 }
