@@ -308,7 +308,8 @@ def run_ours(args, shape: Shape):
     if free < need * 1.05:
         raise SystemExit(f"workload needs {need / 1e9:.1f} GB, {free / 1e9:.1f} GB free")
     layers = [Bn.synth_layer_device(shape, l) for l in range(L)]
-    mode = Bn.KERNELS_FUSED if args.kernels == "fused" else Bn.KERNELS_SEPARATE
+    mode = {"fused": Bn.KERNELS_FUSED, "separate": Bn.KERNELS_SEPARATE,
+            "columns": Bn.KERNELS_COLUMNS}[args.kernels]
     chained = args.chain_norm
     norm = None
     if chained and L > 1:
@@ -430,8 +431,9 @@ def run_ours(args, shape: Shape):
     peak_note = "of measured" if peaks else "of fallback"
     ach_a = mean_a / (ms_a * 1e-3) / 1e9
     ach_b = mean_b / (ms_b * 1e-3) / 1e9
-    dominant = "fused_kernel" if mode == Bn.KERNELS_FUSED else "gate_up_kernel"
-    if mode == Bn.KERNELS_FUSED:
+    dominant = {Bn.KERNELS_FUSED: "fused_kernel", Bn.KERNELS_COLUMNS: "cols_kernel"}.get(
+        mode, "gate_up_kernel")
+    if mode in (Bn.KERNELS_FUSED, Bn.KERNELS_COLUMNS):
         # one launch per step: the step's bytes over the step's device time
         ach, per_launch_bytes, per_launch_us = (step_bytes / (ms_per_step * 1e-3) / 1e9,
                                                 step_bytes, ms_per_step * 1e3)
@@ -478,7 +480,8 @@ def run_ours(args, shape: Shape):
         "cpu_baseline": cpu,
         "e2e": {"value": world * m * e2e_steps / e2e_s, "unit": "tok/s",
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
-        "gpu_launches": args.steps if mode == Bn.KERNELS_FUSED else args.steps * L * m * 2,
+        "gpu_launches": (args.steps if mode in (Bn.KERNELS_FUSED, Bn.KERNELS_COLUMNS)
+                         else args.steps * L * m * 2),
         "clocks": clocks,
     }
     if rank == 0:
@@ -602,8 +605,10 @@ def main(argv=None):
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", choices=sorted(ALL), default=DEFAULT_WORKLOAD)
     ap.add_argument("--tokens", type=int, default=1)
-    ap.add_argument("--kernels", choices=["fused", "separate"], default="fused",
-                    help="one persistent kernel per step, or kernel A and kernel B per layer")
+    ap.add_argument("--kernels", choices=["fused", "separate", "columns"], default="fused",
+                    help="one persistent kernel per step (row split, two device-wide barriers "
+                         "per layer), kernel A and kernel B per layer, or one persistent kernel "
+                         "per step with the column split (one barrier per layer)")
     ap.add_argument("--input-sets", type=int, default=4)
     ap.add_argument("--chain-norm", action="store_true",
                     help="fold the next layer's RMSNorm in: layer l >= 1 reads RMSNorm(out of "

@@ -65,14 +65,25 @@ typedef struct moe_decode_config {
   int32_t shared_gate;     /* 0: scalar 1;  1: scalar = sigmoid(x . gate_vec) */
   int32_t resid_dtype;     /* MOE_DTYPE_BF16 or MOE_DTYPE_F32 */
   int32_t out_dtype;       /* MOE_DTYPE_F32 (default) or MOE_DTYPE_BF16 (rounded to nearest) */
-  int32_t kernel_mode;     /* MOE_KERNELS_FUSED (default) or MOE_KERNELS_SEPARATE */
+  int32_t kernel_mode;     /* MOE_KERNELS_FUSED (default), _SEPARATE or _COLUMNS */
 } moe_decode_config;
 
 /* How a layer is launched.  FUSED: one cooperative persistent kernel per forward (or per stack
  * step) runs the gate/up phase, a device-wide barrier, then the down phase, streaming the down
  * weights into shared memory while the gate/up phase computes.  SEPARATE: kernel A then kernel B
- * per layer with programmatic dependent launch (the unfused form, kept for comparison). */
-enum { MOE_KERNELS_FUSED = 0, MOE_KERNELS_SEPARATE = 1 };
+ * per layer with programmatic dependent launch (the unfused form, kept for comparison).
+ * COLUMNS: one cooperative persistent kernel per forward or stack step in which each CTA carries
+ * a contiguous range of activation columns through gate/up, SwiGLU and the matching columns of
+ * the down projection (the same sums as kernel A and kernel B of "two-kernel decode-MoE that
+ * beats gather_qmm", What changed, step 2, and the tail of "Red Lite dev39 -- fused expert tail",
+ * Change), writing per-CTA partial outputs that the row owners sum in a fixed order: one
+ * device-wide barrier per layer.  Requires max_tokens == 1, bits_down (and bits_shared when
+ * n_shared > 0) of 4 or 8, din <= 4096; create returns MOE_ERR_UNSUPPORTED otherwise.  Create
+ * makes a column-block-major copy of every down projection (owned by the handle: about the size
+ * of the down weights) and a partial-sum buffer; the chained stack and moe_stack_step_parts
+ * (one phase) do not take this mode.  Results are deterministic (fixed summation order) and equal
+ * the other modes within the parity bound, not bit for bit (the sums associate differently). */
+enum { MOE_KERNELS_FUSED = 0, MOE_KERNELS_SEPARATE = 1, MOE_KERNELS_COLUMNS = 2 };
 
 /*
  * One projection of every expert of a class, canonical packed layout, all device pointers:

@@ -21,7 +21,8 @@ INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(ROOT, "_build")
 LIB = os.path.join(PKG, "libmoe_decode.so")
 SOURCES = ["moe_kernels_g4.cu", "moe_kernels_g6.cu", "moe_kernels_g8.cu", "moe_grouped_g4.cu",
-           "moe_grouped_g6.cu", "moe_grouped_g8.cu", "moe_kernels.cu",
+           "moe_grouped_g6.cu", "moe_grouped_g8.cu", "moe_cols_g4.cu", "moe_cols_g6.cu",
+           "moe_cols_g8.cu", "moe_kernels.cu",
            "moe_api.cu", "moe_pack.cpp", "synth.cu", "gemv.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 

@@ -36,7 +36,8 @@ int validate_config(const moe_decode_config *c) {
   if (c->resid_dtype != MOE_DTYPE_BF16 && c->resid_dtype != MOE_DTYPE_F32)
     return MOE_ERR_INVALID_ARG;
   if (c->out_dtype != MOE_DTYPE_BF16 && c->out_dtype != MOE_DTYPE_F32) return MOE_ERR_INVALID_ARG;
-  if (c->kernel_mode != MOE_KERNELS_FUSED && c->kernel_mode != MOE_KERNELS_SEPARATE)
+  if (c->kernel_mode != MOE_KERNELS_FUSED && c->kernel_mode != MOE_KERNELS_SEPARATE &&
+      c->kernel_mode != MOE_KERNELS_COLUMNS)
     return MOE_ERR_INVALID_ARG;
   // int32 indexing of the activation vector and of one expert's rows
   const int64_t act = (int64_t)c->top_k * c->dff + (int64_t)c->n_shared * c->dff_shared;
@@ -83,6 +84,10 @@ struct Prepared {
   int grid_fused;    // CTAs of the fused kernel (all resident)
   bool grouped_ok;   // m > 1 forwards stream each selected expert once (fused mode)
   moe::GroupPlan gplan;
+  // column-split mode
+  moe::Plan col_plan;
+  moe::ColPlan cplan;
+  int grid_cols = 0;
 };
 
 int prepare(const moe_decode_config *c, Prepared &P) {
@@ -120,6 +125,22 @@ int prepare(const moe_decode_config *c, Prepared &P) {
   if (c->kernel_mode == MOE_KERNELS_FUSED && P.grid_fused < 1) return MOE_ERR_UNSUPPORTED;
   const int grid = c->kernel_mode == MOE_KERNELS_FUSED ? P.grid_fused : P.grid_sep;
   if ((c->din + grid - 1) / grid > moe::kMaxRowsB) return MOE_ERR_UNSUPPORTED;
+  if (c->kernel_mode == MOE_KERNELS_COLUMNS) {
+    if (c->max_tokens != 1) return MOE_ERR_UNSUPPORTED;
+    int lim = 0;
+    if (moe::prepare_cols(smem_optin, c->bits_gate, c->bits_down, P.bits_sh, &lim) !=
+        cudaSuccess) {
+      cudaGetLastError();
+      return MOE_ERR_UNSUPPORTED;  // no column-split kernel for these code widths
+    }
+    const int ring = lim < moe::kRingBytes ? lim : moe::kRingBytes;
+    if (!moe::make_col_plan(P.shape, c->bits_gate, c->bits_down, P.bits_sh, sms, ring, &P.cplan,
+                            &P.col_plan))
+      return MOE_ERR_UNSUPPORTED;
+    const int per = moe::cols_grid_limit(P.col_plan.smem, c->bits_gate, c->bits_down, P.bits_sh);
+    if (per < sms) return MOE_ERR_UNSUPPORTED;  // one CTA per SM, all resident
+    P.grid_cols = sms;
+  }
   return MOE_OK;
 }
 
@@ -224,6 +245,101 @@ int read_and_clear_error(int32_t *err, int32_t *out) {
   return MOE_OK;
 }
 
+// Column-split launch over L layers (m = 1): see moe_cols.cuh.
+cudaError_t enqueue_cols(const Prepared &P, const moe::LayerPtrs *layers,
+                         const moe::ColPtrs *cols, int L, float *slab, int32_t *err,
+                         uint32_t *bar, const void *x, const int32_t *ids, const float *scores,
+                         const void *resid0, int resid_dtype, void *out, int out_dtype,
+                         cudaStream_t stream) {
+  cudaError_t e = cudaMemsetAsync(bar, 0, sizeof(uint32_t), stream);
+  if (e != cudaSuccess) return e;
+  moe::StackParams p;
+  std::memset(&p, 0, sizeof p);
+  p.s = P.shape;
+  p.plan = P.col_plan;
+  p.layers = layers;
+  p.L = L;
+  p.m = 1;
+  p.x = static_cast<const uint16_t *>(x);
+  p.ids = ids;
+  p.scores = scores;
+  p.resid0 = resid0;
+  p.resid0_f32 = resid_dtype == MOE_DTYPE_F32;
+  p.out = out;
+  p.out_f32 = out_dtype == MOE_DTYPE_F32;
+  p.err = err;
+  p.bar = bar;
+  p.cols = cols;
+  p.cp = P.cplan;
+  p.slab = slab;
+  return moe::launch_cols(p, P.grid_cols, stream);
+}
+
+// The column-block-major copies of every layer's down projections (column-split mode), owned by
+// a handle or a stack.
+struct ColWeights {
+  std::vector<void *> bufs;
+  moe::ColPtrs *dev = nullptr;  // device array [L]
+
+  bool repack(int experts, int din, int dff, int bits, const moe_proj &p, moe::ColDownDev *out) {
+    const size_t words = (size_t)experts * (dff * bits / 32) * din;
+    const size_t pairs = (size_t)experts * (dff / 64) * din;
+    void *c = nullptr, *b = nullptr;
+    if (cudaMalloc(&c, words * 4) != cudaSuccess) return false;
+    bufs.push_back(c);
+    if (cudaMalloc(&b, pairs * 4) != cudaSuccess) return false;
+    bufs.push_back(b);
+    out->codes = static_cast<const uint32_t *>(c);
+    out->sb = static_cast<const __half2 *>(b);
+    return moe::launch_repack_down(static_cast<const uint8_t *>(p.codes),
+                                   static_cast<const __half *>(p.scales),
+                                   static_cast<const __half *>(p.biases), experts, din, dff, bits,
+                                   static_cast<uint32_t *>(c), static_cast<__half2 *>(b),
+                                   nullptr) == cudaSuccess;
+  }
+  // MOE_OK, MOE_ERR_OOM or MOE_ERR_CUDA.
+  int build(const moe_decode_config &c, const moe_layer_weights *w, int L) {
+    // the caller's weights may still be written by work on other streams
+    if (cudaDeviceSynchronize() != cudaSuccess) return MOE_ERR_CUDA;
+    std::vector<moe::ColPtrs> host(L);
+    for (int l = 0; l < L; ++l) {
+      moe::ColPtrs cp;
+      std::memset(&cp, 0, sizeof cp);
+      if (c.top_k > 0 && !repack(c.n_experts, c.din, c.dff, c.bits_down, w[l].down, &cp.r)) {
+        cudaGetLastError();
+        return MOE_ERR_OOM;
+      }
+      if (c.n_shared > 0 &&
+          !repack(c.n_shared, c.din, c.dff_shared, c.bits_shared, w[l].sh_down, &cp.s)) {
+        cudaGetLastError();
+        return MOE_ERR_OOM;
+      }
+      host[l] = cp;
+    }
+    if (cudaMalloc(&dev, sizeof(moe::ColPtrs) * L) != cudaSuccess) {
+      cudaGetLastError();
+      return MOE_ERR_OOM;
+    }
+    if (cudaMemcpy(dev, host.data(), sizeof(moe::ColPtrs) * L, cudaMemcpyHostToDevice) !=
+            cudaSuccess ||
+        cudaDeviceSynchronize() != cudaSuccess)
+      return MOE_ERR_CUDA;
+    return MOE_OK;
+  }
+  void release() {
+    for (void *b : bufs) cudaFree(b);
+    bufs.clear();
+    cudaFree(dev);
+    dev = nullptr;
+  }
+};
+
+size_t slab_floats(const Prepared &P) {
+  return P.cfg.kernel_mode == MOE_KERNELS_COLUMNS
+             ? (size_t)2 * P.grid_cols * P.grid_cols * P.cplan.ro
+             : 0;
+}
+
 // Device workspace of a handle or a stack.
 struct Workspace {
   float *act = nullptr;
@@ -231,9 +347,10 @@ struct Workspace {
   int32_t *err = nullptr;
   uint32_t *bar = nullptr;
   moe::LayerPtrs *layers = nullptr;
+  float *slab = nullptr;  // column-split mode: [2][grid][grid][rows per owner] partial outputs
 
   // Grouped forwards keep every token's activations and per-slot partial outputs at once.
-  bool alloc(const moe_decode_config &c, int n_layers, bool grouped) {
+  bool alloc(const moe_decode_config &c, int n_layers, bool grouped, size_t nslab = 0) {
     const size_t na = act_floats(c) * (grouped ? c.max_tokens : 1);
     const size_t ny = grouped ? (size_t)c.max_tokens * (c.top_k + c.n_shared) * c.din : 1;
     bool ok = cudaMalloc(&act, (na > 0 ? na : 1) * sizeof(float)) == cudaSuccess &&
@@ -241,7 +358,8 @@ struct Workspace {
               cudaMalloc(&err, sizeof(int32_t)) == cudaSuccess &&
               cudaMemset(err, 0, sizeof(int32_t)) == cudaSuccess &&
               cudaMalloc(&bar, sizeof(uint32_t)) == cudaSuccess &&
-              cudaMalloc(&layers, sizeof(moe::LayerPtrs) * n_layers) == cudaSuccess;
+              cudaMalloc(&layers, sizeof(moe::LayerPtrs) * n_layers) == cudaSuccess &&
+              (nslab == 0 || cudaMalloc(&slab, nslab * sizeof(float)) == cudaSuccess);
     if (!ok) cudaGetLastError();
     return ok;
   }
@@ -251,6 +369,7 @@ struct Workspace {
     cudaFree(err);
     cudaFree(bar);
     cudaFree(layers);
+    cudaFree(slab);
   }
 };
 
@@ -261,6 +380,7 @@ struct moe_decode {
   Prepared P;
   moe::LayerPtrs w;
   Workspace ws;
+  ColWeights cw;
 };
 
 extern "C" int moe_decode_create(const moe_decode_config *cfg, const moe_layer_weights *weights,
@@ -279,10 +399,19 @@ extern "C" int moe_decode_create(const moe_decode_config *cfg, const moe_layer_w
     return rc;
   }
   h->w = layer_ptrs(*cfg, *weights);
-  if (!h->ws.alloc(*cfg, 1, h->P.grouped_ok)) {
+  if (!h->ws.alloc(*cfg, 1, h->P.grouped_ok, slab_floats(h->P))) {
     h->ws.release();
     delete h;
     return MOE_ERR_OOM;
+  }
+  if (cfg->kernel_mode == MOE_KERNELS_COLUMNS) {
+    rc = h->cw.build(*cfg, weights, 1);
+    if (rc != MOE_OK) {
+      h->cw.release();
+      h->ws.release();
+      delete h;
+      return rc;
+    }
   }
   if (cudaMemcpy(h->ws.layers, &h->w, sizeof h->w, cudaMemcpyHostToDevice) != cudaSuccess) {
     h->ws.release();
@@ -307,7 +436,10 @@ extern "C" int moe_decode_forward(moe_decode_t *h, const void *x, int32_t m, con
   if (x == out) return MOE_ERR_INVALID_ARG;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   cudaError_t e;
-  if (c.kernel_mode == MOE_KERNELS_FUSED)
+  if (c.kernel_mode == MOE_KERNELS_COLUMNS)
+    e = enqueue_cols(h->P, h->ws.layers, h->cw.dev, 1, h->ws.slab, h->ws.err, h->ws.bar, x, ids,
+                     scores, resid, c.resid_dtype, out, c.out_dtype, st);
+  else if (c.kernel_mode == MOE_KERNELS_FUSED)
     e = enqueue_fused(h->P, h->ws.layers, 1, h->ws.act, h->ws.y, h->ws.err, h->ws.bar, nullptr,
                       nullptr, x, m, ids, scores, resid, c.resid_dtype, out, c.out_dtype, st);
   else
@@ -324,6 +456,7 @@ extern "C" int moe_decode_get_error(moe_decode_t *h, int32_t *device_error) {
 
 extern "C" void moe_decode_destroy(moe_decode_t *h) {
   if (!h) return;
+  h->cw.release();
   h->ws.release();
   delete h;
 }
@@ -442,6 +575,7 @@ struct moe_stack {
   Prepared P;
   std::vector<moe::LayerPtrs> layers;
   Workspace ws;
+  ColWeights cw;
   float *ping[2] = {nullptr, nullptr};
   cudaStream_t cap = nullptr;
   std::vector<GraphEntry> graphs;
@@ -459,6 +593,7 @@ extern "C" void moe_stack_destroy(moe_stack_t *s) {
   if (!s) return;
   for (auto &g : s->graphs) cudaGraphExecDestroy(g.exec);
   if (s->cap) cudaStreamDestroy(s->cap);
+  s->cw.release();
   s->ws.release();
   cudaFree(s->ping[0]);
   cudaFree(s->ping[1]);
@@ -479,6 +614,7 @@ int stack_create(const moe_decode_config *cfg, int32_t n_layers, const moe_layer
   int rc = validate_config(cfg);
   if (rc != MOE_OK) return rc;
   if (cfg->out_dtype != MOE_DTYPE_F32) return MOE_ERR_INVALID_ARG;
+  if (norm_weight && cfg->kernel_mode == MOE_KERNELS_COLUMNS) return MOE_ERR_UNSUPPORTED;
   for (int l = 0; l < n_layers; ++l) {
     rc = validate_weights(cfg, &layers[l]);
     if (rc != MOE_OK) return rc;
@@ -498,7 +634,7 @@ int stack_create(const moe_decode_config *cfg, int32_t n_layers, const moe_layer
   s->layers.resize(n_layers);
   for (int l = 0; l < n_layers; ++l) s->layers[l] = layer_ptrs(*cfg, layers[l]);
   const size_t M = cfg->max_tokens, din = cfg->din, K = cfg->top_k;
-  bool ok = s->ws.alloc(*cfg, n_layers, s->P.grouped_ok) &&
+  bool ok = s->ws.alloc(*cfg, n_layers, s->P.grouped_ok, slab_floats(s->P)) &&
             cudaMalloc(&s->ping[0], M * din * sizeof(float)) == cudaSuccess &&
             cudaMalloc(&s->ping[1], M * din * sizeof(float)) == cudaSuccess &&
             cudaMalloc(&s->x_dev, (size_t)n_layers * M * din * 2) == cudaSuccess &&
@@ -517,6 +653,13 @@ int stack_create(const moe_decode_config *cfg, int32_t n_layers, const moe_layer
       cudaStreamCreateWithFlags(&s->cap, cudaStreamNonBlocking) != cudaSuccess) {
     moe_stack_destroy(s);
     return MOE_ERR_CUDA;
+  }
+  if (cfg->kernel_mode == MOE_KERNELS_COLUMNS) {
+    rc = s->cw.build(*cfg, layers, n_layers);
+    if (rc != MOE_OK) {
+      moe_stack_destroy(s);
+      return rc;
+    }
   }
   *out = s;
   return MOE_OK;
@@ -544,6 +687,9 @@ cudaError_t enqueue_stack(moe_stack *s, const void *x, int m, const int32_t *ids
                           int parts) {
   const int L = (int)s->layers.size();
   const moe_decode_config &c = s->P.cfg;
+  if (c.kernel_mode == MOE_KERNELS_COLUMNS)
+    return enqueue_cols(s->P, s->ws.layers, s->cw.dev, L, s->ws.slab, s->ws.err, s->ws.bar, x, ids,
+                        scores, resid0, c.resid_dtype, out, MOE_DTYPE_F32, st);
   if (c.kernel_mode == MOE_KERNELS_FUSED && parts == (MOE_PART_GATE_UP | MOE_PART_DOWN))
     return enqueue_fused(s->P, s->ws.layers, L, s->ws.act, s->ws.y, s->ws.err, s->ws.bar,
                          s->ping[0], s->ping[1], x, m, ids, scores, resid0, c.resid_dtype, out,
@@ -597,6 +743,8 @@ extern "C" int moe_stack_step_parts(moe_stack_t *s, int32_t parts, const void *x
                                     void *out, void *stream) {
   if (!s || !x || !resid0 || !out) return MOE_ERR_INVALID_ARG;
   if (parts < 1 || parts > (MOE_PART_GATE_UP | MOE_PART_DOWN)) return MOE_ERR_INVALID_ARG;
+  if (s->P.cfg.kernel_mode == MOE_KERNELS_COLUMNS && parts != (MOE_PART_GATE_UP | MOE_PART_DOWN))
+    return MOE_ERR_UNSUPPORTED;
   if (m < 1 || m > s->P.cfg.max_tokens) return MOE_ERR_INVALID_ARG;
   if (s->P.cfg.top_k > 0 && (!ids || !scores)) return MOE_ERR_INVALID_ARG;
   if (!aligned(out, 4) || !aligned(x, 16) || !aligned(resid0, dtype_bytes(s->P.cfg.resid_dtype)))

@@ -2,6 +2,8 @@
 // to the kernels of moe_fused.cuh (instantiated per gate/up code width in moe_kernels_g4.cu,
 // moe_kernels_g6.cu and moe_kernels_g8.cu); plus the small kernels (debug unpack, router, bounded
 // waits, debug route inversion).
+#include <cstring>
+
 #include "moe_grouped.cuh"
 
 namespace moe {
@@ -131,6 +133,30 @@ __global__ void route_invert_kernel(const int32_t *ids, int n, int n_experts, in
   for (int q = threadIdx.x; q < rt.n_pairs; q += 32) out[2 + 2 * U + q] = rt.pairs[q];
 }
 
+// ================================================================== column-block-major down copy
+// out_codes[e][jb][i] = word jb of canonical row (e, i); out_sb[e][g][i] = (scale, bias)[e][i][g].
+// Consecutive threads write consecutive rows i.
+__global__ void repack_down_kernel(const uint32_t *codes, const __half *scales,
+                                   const __half *biases, int experts, int din, int words,
+                                   int groups, uint32_t *out_codes, __half2 *out_sb) {
+  const int64_t nc = static_cast<int64_t>(experts) * words * din;
+  const int64_t ns = static_cast<int64_t>(experts) * groups * din;
+  const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
+  for (int64_t x = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; x < nc;
+       x += stride) {
+    const int64_t i = x % din, t = x / din;
+    const int64_t jb = t % words, e = t / words;
+    out_codes[x] = codes[(e * din + i) * words + jb];
+  }
+  for (int64_t x = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; x < ns;
+       x += stride) {
+    const int64_t i = x % din, t = x / din;
+    const int64_t g = t % groups, e = t / groups;
+    const int64_t src = (e * din + i) * groups + g;
+    out_sb[x] = __halves2half2(scales[src], biases[src]);
+  }
+}
+
 // ================================================================== host side
 static int fmt_codes(int bits) { return bits == 4 ? 32 : bits == 8 ? 16 : 64; }
 static int align_up(int v, int a) { return (v + a - 1) / a * a; }
@@ -252,6 +278,48 @@ bool make_group_plan(const LayerShape &s, int bits_gu, int bits_d, int bits_sh, 
   return true;
 }
 
+bool make_col_plan(const LayerShape &s, int bits_gu, int bits_d, int bits_sh, int grid,
+                   int ring_bytes, ColPlan *cp, Plan *plan) {
+  const bool sh = s.n_shared > 0;
+  if (grid < 1 || (bits_d != 4 && bits_d != 8) || (sh && bits_sh != 4 && bits_sh != 8))
+    return false;
+  if (s.din > 4 * 2 * kConsumers || s.din % 4) return false;  // two row quads per thread
+  if (!geom_a(s.din, bits_gu, &plan->geo_r) || !geom_a(s.din, bits_sh, &plan->geo_s))
+    return false;
+  cp->cb_r = 32 / bits_d;
+  cp->cb_s = sh ? 32 / bits_sh : cp->cb_r;
+  const int blk = s.din * 4;  // one column block of all din rows
+  int sa = 0;
+  if (s.top_k > 0) sa = stage_a(plan->geo_r);
+  if (sh && stage_a(plan->geo_s) > sa) sa = stage_a(plan->geo_s);
+  int nbs = sa / blk - 1;
+  nbs = nbs < 1 ? 1 : (nbs > 16 ? 16 : nbs);
+  int st = align_up((nbs + 1) * blk, 128);
+  st = st > sa ? st : sa;
+  int n = ring_bytes / st;
+  if (n > kMaxStages) n = kMaxStages;
+  if (n < 2) return false;
+  cp->nbs = nbs;
+  cp->ro = align_up((s.din + grid - 1) / grid, 4);
+  if (cp->ro > kMaxOwnRows) return false;
+  // every CTA's pieces within the kernel's limits
+  const int64_t U = (int64_t)s.top_k * s.dff + (int64_t)s.n_shared * s.dff_shared;
+  if ((U + grid - 1) / grid > kMaxColsCta) return false;
+  for (int c = 0; c < grid; ++c) {
+    ColPiece pc[kMaxColPieces];
+    int nbk = 0;
+    int64_t u0 = 0;
+    if (col_pieces(s.top_k, s.dff, s.n_shared, s.dff_shared, cp->cb_r, cp->cb_s, c, grid, pc,
+                   &nbk, &u0) < 0)
+      return false;
+  }
+  std::memset(&plan->geo_b, 0, sizeof plan->geo_b);
+  plan->nst = n;
+  plan->stage_bytes = st;
+  plan->smem = static_cast<size_t>(n) * st;
+  return true;
+}
+
 #define MOE_BITS_SWITCH(B, NAME, ...)                       \
   switch (B) {                                              \
     case 4: { constexpr int NAME = 4; __VA_ARGS__; break; } \
@@ -271,7 +339,10 @@ bool make_group_plan(const LayerShape &s, int bits_gu, int bits_d, int bits_sh, 
   cudaError_t fused_occupancy_g##B(int, int, size_t, int *);                                 \
   cudaError_t launch_grouped_g##B(const StackParams &, int, size_t, cudaStream_t);            \
   cudaError_t prepare_grouped_g##B(int, int, int, int *);                                     \
-  cudaError_t grouped_occupancy_g##B(int, int, size_t, int *);
+  cudaError_t grouped_occupancy_g##B(int, int, size_t, int *);                               \
+  cudaError_t launch_cols_g##B(const StackParams &, int, cudaStream_t);                       \
+  cudaError_t prepare_cols_g##B(int, int, int, int *);                                        \
+  cudaError_t cols_occupancy_g##B(int, int, size_t, int *);
 MOE_FAMILY_DECL(4)
 MOE_FAMILY_DECL(6)
 MOE_FAMILY_DECL(8)
@@ -334,7 +405,46 @@ int fused_grid_limit(const Plan &plan, int bits_gu, int bits_d, int bits_sh) {
   if (occ() != cudaSuccess || occ_g() != cudaSuccess) return 0;
   return per_sm * sms;
 }
+cudaError_t launch_cols(const StackParams &p, int grid, cudaStream_t stream) {
+  MOE_FAMILY_CALL(p.plan.geo_r.bits, launch_cols, p, grid, stream);
+}
+
+cudaError_t prepare_cols(int smem_optin, int bits_gu, int bits_d, int bits_sh, int *dyn_limit) {
+  int lim = smem_optin;
+  auto fam = [&]() -> cudaError_t {
+    MOE_FAMILY_CALL(bits_gu, prepare_cols, smem_optin, bits_d, bits_sh, &lim);
+  };
+  const cudaError_t e = fam();
+  *dyn_limit = lim;
+  return e;
+}
+
+int cols_grid_limit(size_t smem, int bits_gu, int bits_d, int bits_sh) {
+  int per_sm = 0, dev = 0, sms = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+    return 0;
+  auto occ = [&]() -> cudaError_t {
+    MOE_FAMILY_CALL(bits_gu, cols_occupancy, bits_d, bits_sh, smem, &per_sm);
+  };
+  if (occ() != cudaSuccess) return 0;
+  return per_sm * sms;
+}
 #undef MOE_FAMILY_CALL
+
+cudaError_t launch_repack_down(const uint8_t *codes, const __half *scales, const __half *biases,
+                               int experts, int din, int dff, int bits, uint32_t *out_codes,
+                               __half2 *out_sb, cudaStream_t stream) {
+  if (experts < 1) return cudaSuccess;
+  const int words = dff * bits / 32, groups = dff / 64;
+  const int64_t n = static_cast<int64_t>(experts) * din * (words > groups ? words : groups);
+  int64_t grid = (n + 255) / 256;
+  grid = grid < 1 ? 1 : (grid > 4096 ? 4096 : grid);
+  repack_down_kernel<<<static_cast<int>(grid), 256, 0, stream>>>(
+      reinterpret_cast<const uint32_t *>(codes), scales, biases, experts, din, words, groups,
+      out_codes, out_sb);
+  return cudaGetLastError();
+}
 
 cudaError_t launch_unpack(const uint8_t *packed, int64_t rows, int64_t cols, int bits,
                           uint8_t *codes, cudaStream_t stream) {

@@ -79,6 +79,98 @@ struct GroupPlan {
   size_t smem;
 };
 
+// ------------------------------------------------------------------ column-split mode
+// The column-split kernel (moe_cols.cuh) gives each CTA a contiguous range of activation columns
+// (the flattened routed-then-shared row space of the gate/up projections); it computes those
+// activations locally and multiplies them into the matching columns of the down projections, so
+// the down weights are read in a column-block-major copy made at create time:
+//   codes  [experts][dff / cb][din] 32-bit words; word (jb, i) holds the cb = 32 / bits codes of
+//          row i, columns jb * cb .. jb * cb + cb - 1, exactly as in the canonical row (LSB first)
+//   sb     [experts][dff / 64][din] (scale, bias) pairs of row i, group g
+constexpr int kMaxColsCta = 256;     // activation columns one CTA owns, at most
+constexpr int kMaxColPieces = 16;    // (segment, group) pieces of one CTA's columns, at most
+constexpr int kMaxColBlocks = 64;    // down column blocks one CTA reads, at most
+constexpr int kMaxOwnRows = 32;      // output rows one CTA sums from the partials, at most
+
+struct ColDownDev {
+  const uint32_t *codes;   // [experts][dff / cb][din]
+  const __half2 *sb;       // [experts][dff / 64][din]
+};
+
+struct ColPtrs {
+  ColDownDev r, s;         // routed experts, shared experts
+};
+
+struct ColPlan {
+  int cb_r, cb_s;          // codes per 32-bit word of the routed / shared down projection
+  int nbs;                 // column blocks per down stage, at most
+  int ro;                  // rows per owner in the partial-sum slab (padded)
+};
+
+// One piece of a CTA's columns: the columns [j0, j1) of one segment (routed slot or shared expert)
+// that lie in one group of 64.
+struct ColPiece {
+  int seg;      // routed slot k (< top_k) or top_k + shared expert index
+  int j0, j1;   // columns, expert coordinates
+  int a0;       // index of column j0 in the CTA's activation range
+  int blk0;     // first column block: j0 / cb
+  int nb;       // column blocks
+  int pb;       // index of the piece's first block in the CTA's block list
+  int grp;      // group: j0 / 64
+};
+
+// The activation columns [u0, u1) of CTA c out of n (balanced split of U columns).
+__host__ __device__ inline void col_range(int64_t U, int c, int n, int64_t *u0, int64_t *u1) {
+  *u0 = U * c / n;
+  *u1 = U * (c + 1) / n;
+}
+
+// Cuts CTA c's columns into pieces; returns the piece count (-1 when more than kMaxColPieces or
+// the blocks exceed kMaxColBlocks) and the block count in *nblocks.
+__host__ __device__ inline int col_pieces(int top_k, int dff, int n_shared, int dff_shared,
+                                          int cb_r, int cb_s, int c, int n, ColPiece *pc,
+                                          int *nblocks, int64_t *u0_out) {
+  const int64_t Ur = static_cast<int64_t>(top_k) * dff;
+  const int64_t U = Ur + static_cast<int64_t>(n_shared) * dff_shared;
+  int64_t u0, u1;
+  col_range(U, c, n, &u0, &u1);
+  *u0_out = u0;
+  int np = 0, nbk = 0;
+  for (int64_t u = u0; u < u1;) {
+    int seg, j, width, cb;
+    if (u < Ur) {
+      seg = static_cast<int>(u / dff);
+      j = static_cast<int>(u - static_cast<int64_t>(seg) * dff);
+      width = dff;
+      cb = cb_r;
+    } else {
+      const int t = static_cast<int>((u - Ur) / dff_shared);
+      seg = top_k + t;
+      j = static_cast<int>(u - Ur - static_cast<int64_t>(t) * dff_shared);
+      width = dff_shared;
+      cb = cb_s;
+    }
+    int jend = (j / 64 + 1) * 64;
+    if (jend > width) jend = width;
+    if (static_cast<int64_t>(jend - j) > u1 - u) jend = j + static_cast<int>(u1 - u);
+    if (np == kMaxColPieces) return -1;
+    ColPiece &q = pc[np++];
+    q.seg = seg;
+    q.j0 = j;
+    q.j1 = jend;
+    q.a0 = static_cast<int>(u - u0);
+    q.blk0 = j / cb;
+    q.nb = (jend - 1) / cb - j / cb + 1;
+    q.pb = nbk;
+    q.grp = j / 64;
+    nbk += q.nb;
+    if (nbk > kMaxColBlocks) return -1;
+    u += jend - j;
+  }
+  *nblocks = nbk;
+  return np;
+}
+
 // Kernel A alone.
 struct GateUpParams {
   LayerShape s;
@@ -132,6 +224,10 @@ struct StackParams {
   GroupPlan gp;
   float *y;                 // [m][top_k + n_shared][din] partial outputs
   int act_stride;           // floats per token in act: top_k * dff + n_shared * dff_shared
+  // column-split mode (m = 1): repacked down projections per layer, plan, partial-sum slab
+  const ColPtrs *cols;      // device array [L]
+  ColPlan cp;
+  float *slab;              // [2][grid][grid][cp.ro]
 };
 
 // Host-side plan; false when the shape is outside what the kernels support.
@@ -139,6 +235,19 @@ bool make_plan(const LayerShape &s, int bits_gu, int bits_d, int bits_sh, Plan *
 // Grouped plan for up to m tokens; false when the shape or m is outside the grouped kernels.
 bool make_group_plan(const LayerShape &s, int bits_gu, int bits_d, int bits_sh, int m,
                      GroupPlan *gp);
+
+// Column-split plan for a grid of `grid` CTAs (phase-A geometry and ring in *plan); false when
+// the shape is outside the column-split kernels (down codes of 4 or 8 bits, din <= 4096, and the
+// per-CTA limits above).
+bool make_col_plan(const LayerShape &s, int bits_gu, int bits_d, int bits_sh, int grid,
+                   int ring_bytes, ColPlan *cp, Plan *plan);
+cudaError_t launch_cols(const StackParams &p, int grid, cudaStream_t stream);
+cudaError_t prepare_cols(int smem_optin, int bits_gu, int bits_d, int bits_sh, int *dyn_limit);
+int cols_grid_limit(size_t smem, int bits_gu, int bits_d, int bits_sh);
+// Writes the column-block-major copy of `experts` down projections (rows din, cols dff, bits).
+cudaError_t launch_repack_down(const uint8_t *codes, const __half *scales, const __half *biases,
+                               int experts, int din, int dff, int bits, uint32_t *out_codes,
+                               __half2 *out_sb, cudaStream_t stream);
 
 cudaError_t launch_gate_up(const GateUpParams &p, int grid, cudaStream_t stream, bool pdl);
 cudaError_t launch_down(const DownParams &p, int grid, cudaStream_t stream, bool pdl);

@@ -682,7 +682,7 @@ union SmemAB {
 // Sums the parked partials of the held rows across warps (fixed order) and writes the
 // activations.  `trailing` adds the barrier that frees the buffer for reuse.
 __device__ __forceinline__ void flush_a(SmemA &sm, int held, int wpg, float *act, int tid,
-                                        bool trailing) {
+                                        bool trailing, int u_base = 0) {
   consumer_sync(kConsumers);
   for (int t = tid; t < held; t += kConsumers) {
     float gs = 0.f, us = 0.f;
@@ -690,7 +690,7 @@ __device__ __forceinline__ void flush_a(SmemA &sm, int held, int wpg, float *act
       gs += sm.red[0][t * wpg + w];
       us += sm.red[1][t * wpg + w];
     }
-    act[sm.row_u[t]] = sm.coef[t] * (silu_f(gs) * us);
+    act[sm.row_u[t] - u_base] = sm.coef[t] * (silu_f(gs) * us);
   }
   if (trailing) consumer_sync(kConsumers);
 }
@@ -710,7 +710,8 @@ __device__ __forceinline__ void load_x_class(Operand<BITS> &op, const GateUpGeom
 template <int BITS>
 __device__ int consume_a_class(const LayerShape &s, const GateUpGeom &g, bool shared_class,
                                int count, const Operand<BITS> &xo, float *act, float shared_scalar,
-                               Ring &r, SmemA &sm, bool &waited, bool &ok, int tid) {
+                               Ring &r, SmemA &sm, bool &waited, bool &ok, int tid,
+                               int u_base = 0) {
   constexpr int C = Fmt<BITS>::kCodes, VEC = Fmt<BITS>::kVecs;
   constexpr int RPT = rows_per_thread_a<BITS>();
   constexpr int V = 2 * RPT;        // values per stage: gate and up of RPT rows
@@ -738,7 +739,7 @@ __device__ int consume_a_class(const LayerShape &s, const GateUpGeom &g, bool sh
     waited = false;
     const StageDesc d = r.desc[r.st];
     if (held + d.n > cap) {
-      flush_a(sm, held, wpg, act, tid, true);
+      flush_a(sm, held, wpg, act, tid, true, u_base);
       held = 0;
     }
     if (tid < d.n) {
@@ -795,7 +796,7 @@ __device__ int consume_a_class(const LayerShape &s, const GateUpGeom &g, bool sh
 template <int BR, int BS, bool CHAIN>
 __device__ void consume_a(const LayerShape &s, const LayerPtrs &w, const GateUpGeom &gr,
                           const GateUpGeom &gs, XSource x, const int *cnt, float *act,
-                          Ring &r, SmemA &sm, int tid) {
+                          Ring &r, SmemA &sm, int tid, int u_base = 0) {
   const int warp = tid >> 5, lane = tid & 31;
   Operand<BR> xr;   // x for the routed rows, loaded while the first stage is in flight
   if constexpr (CHAIN) {
@@ -823,16 +824,18 @@ __device__ void consume_a(const LayerShape &s, const LayerPtrs &w, const GateUpG
     warp_release(r, lane);
     return;
   }
-  int held = consume_a_class<BR>(s, gr, false, nr, xr, act, 1.f, r, sm, waited, ok, tid);
-  if (held > 0) flush_a(sm, held, gr.tpr / 32, act, tid, ns > 0);
+  int held =
+      consume_a_class<BR>(s, gr, false, nr, xr, act, 1.f, r, sm, waited, ok, tid, u_base);
+  if (held > 0) flush_a(sm, held, gr.tpr / 32, act, tid, ns > 0, u_base);
   if (ns > 0) {
     Operand<BS> xsh;
     if constexpr (CHAIN)
       load_x_class<BS>(xsh, gs, x, tid);
     else
       load_x_class<BS>(xsh, gs, x.x, tid);
-    held = consume_a_class<BS>(s, gs, true, ns, xsh, act, shared_scalar, r, sm, waited, ok, tid);
-    if (held > 0) flush_a(sm, held, gs.tpr / 32, act, tid, false);
+    held = consume_a_class<BS>(s, gs, true, ns, xsh, act, shared_scalar, r, sm, waited, ok, tid,
+                               u_base);
+    if (held > 0) flush_a(sm, held, gs.tpr / 32, act, tid, false, u_base);
   }
 }
 
