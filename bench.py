@@ -43,7 +43,9 @@ METRIC = "MoE decode tok/s (full layer stack) and achieved HBM GB/s vs peak, 1 G
 DEFAULT_WORKLOAD = "qwen3_stack_8bit"
 NORM_EPS = 1e-6   # RMSNorm epsilon of the chained stack (--chain-norm)
 GEMV_NAMES = ("qwen25_1p5b_qo", "qwen25_1p5b_kv", "qwen3_8b_qo", "qwen3_8b_kv")
-KERNEL_SOURCES = ["quantized_moe_expert_dequant_gb300/csrc/moe_kernels.cu",
+KERNEL_SOURCES = ["quantized_moe_expert_dequant_gb300/csrc/moe_cols.cuh",
+                  "quantized_moe_expert_dequant_gb300/csrc/moe_cols_g8.cu",
+                  "quantized_moe_expert_dequant_gb300/csrc/moe_kernels.cu",
                   "quantized_moe_expert_dequant_gb300/csrc/moe_fused.cuh",
                   "quantized_moe_expert_dequant_gb300/csrc/moe_kernels_g8.cu",
                   "quantized_moe_expert_dequant_gb300/csrc/moe_grouped.cuh",
@@ -605,7 +607,7 @@ def main(argv=None):
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", choices=sorted(ALL), default=DEFAULT_WORKLOAD)
     ap.add_argument("--tokens", type=int, default=1)
-    ap.add_argument("--kernels", choices=["fused", "separate", "columns"], default="fused",
+    ap.add_argument("--kernels", choices=["fused", "separate", "columns"], default="columns",
                     help="one persistent kernel per step (row split, two device-wide barriers "
                          "per layer), kernel A and kernel B per layer, or one persistent kernel "
                          "per step with the column split (one barrier per layer)")
