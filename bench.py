@@ -310,9 +310,14 @@ def run_ours(args, shape: Shape):
     if free < need * 1.05:
         raise SystemExit(f"workload needs {need / 1e9:.1f} GB, {free / 1e9:.1f} GB free")
     layers = [Bn.synth_layer_device(shape, l) for l in range(L)]
-    mode = {"fused": Bn.KERNELS_FUSED, "separate": Bn.KERNELS_SEPARATE,
-            "columns": Bn.KERNELS_COLUMNS}[args.kernels]
     chained = args.chain_norm
+    kernels = args.kernels
+    if kernels == "auto":   # the column split where it runs, else the row split
+        cols_ok = (m == 1 and not chained and shape.bits_down in (4, 8)
+                   and (shape.n_shared == 0 or shape.bits_shared in (4, 8)) and shape.din <= 4096)
+        kernels = "columns" if cols_ok else "fused"
+    mode = {"fused": Bn.KERNELS_FUSED, "separate": Bn.KERNELS_SEPARATE,
+            "columns": Bn.KERNELS_COLUMNS}[kernels]
     norm = None
     if chained and L > 1:
         rows = np.stack([synth.norm_weight(shape.seed, l, shape.din) for l in range(1, L)])
@@ -463,7 +468,7 @@ def run_ours(args, shape: Shape):
                    "bits": [shape.bits_gate, shape.bits_up, shape.bits_down],
                    "shared": [shape.n_shared, shape.dff_shared, shape.bits_shared],
                    "layers": L, "tokens_per_step": m, "input_sets": S,
-                   "chain_norm": bool(chained),
+                   "chain_norm": bool(chained), "kernels": kernels,
                    "parallelism": f"replicas x{world}",
                    "l2": f"inputs larger than L2: {step_bytes / 1e9:.3f} GB of selected weights "
                          f"per step, ids re-drawn per step"},
@@ -607,10 +612,13 @@ def main(argv=None):
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", choices=sorted(ALL), default=DEFAULT_WORKLOAD)
     ap.add_argument("--tokens", type=int, default=1)
-    ap.add_argument("--kernels", choices=["fused", "separate", "columns"], default="columns",
+    ap.add_argument("--kernels", choices=["auto", "fused", "separate", "columns"],
+                    default="auto",
                     help="one persistent kernel per step (row split, two device-wide barriers "
-                         "per layer), kernel A and kernel B per layer, or one persistent kernel "
-                         "per step with the column split (one barrier per layer)")
+                         "per layer), kernel A and kernel B per layer, one persistent kernel "
+                         "per step with the column split (one barrier per layer), or auto: the "
+                         "column split where it runs (1 token, 4/8-bit down codes, no folded "
+                         "norm), else the row split")
     ap.add_argument("--input-sets", type=int, default=4)
     ap.add_argument("--chain-norm", action="store_true",
                     help="fold the next layer's RMSNorm in: layer l >= 1 reads RMSNorm(out of "
