@@ -296,6 +296,25 @@ int moe_router_topk(const float *logits, int32_t m, int32_t n_experts, int32_t t
  * wait runs forever. */
 int moe_debug_wait_timeout(int32_t kind, int32_t *scratch, int32_t *device_error, void *stream);
 
+/* The column split's cut of one CTA's activation columns into pieces, exactly as the
+ * MOE_KERNELS_COLUMNS kernel computes it on the device (host only, no CUDA call: a debug export so
+ * that the decomposition can be checked on a machine without a GPU).  The activation columns are
+ * the flattened routed-then-shared rows of the gate/up projections (top_k * dff routed, then
+ * n_shared * dff_shared); CTA `cta` of `grid` owns [U * cta / grid, U * (cta + 1) / grid), cut at
+ * every segment (routed slot or shared expert) and every group of 64 columns.
+ *   bits_down, bits_shared  4 or 8: the down projection's code width (32 / bits codes per word)
+ *   out   int32 host, room for 2 + 8 * max_pieces values: u0 (the CTA's first column), the piece
+ *         count, then per piece seg (slot, or top_k + shared index), j0, j1 (columns inside the
+ *         expert), a0 (index of j0 in the CTA's range), blk0 (first 32-bit column block), nb
+ *         (blocks), pb (index of the first block in the CTA's block list), grp (j0 / 64)
+ * Returns the piece count (>= 0), MOE_ERR_UNSUPPORTED when the CTA owns more columns, pieces or
+ * blocks than the kernel holds (or more pieces than max_pieces), MOE_ERR_INVALID_ARG for bad
+ * arguments.  No
+ * counterpart on the pages: the split by columns is this implementation's. */
+int moe_debug_col_pieces(int32_t top_k, int32_t dff, int32_t n_shared, int32_t dff_shared,
+                         int32_t bits_down, int32_t bits_shared, int32_t cta, int32_t grid,
+                         int32_t *out, int32_t max_pieces);
+
 #ifdef __cplusplus
 }
 #endif

@@ -36,7 +36,7 @@ EXPORTS = ["moe_decode_create", "moe_decode_forward", "moe_decode_get_error", "m
            "moe_stack_get_error",
            "moe_stack_destroy", "moe_pack_codes", "moe_unpack_codes", "moe_unpack_codes_device",
            "moe_synth_codes", "moe_synth_scales", "moe_synth_biases", "moe_route_invert_device",
-           "moe_debug_wait_timeout", "moe_router_topk"]
+           "moe_debug_wait_timeout", "moe_router_topk", "moe_debug_col_pieces"]
 
 
 class MoeError(RuntimeError):
@@ -103,6 +103,7 @@ def lib() -> ctypes.CDLL:
                 "moe_route_invert_device": [vp, i32, i32, i32, vp, vp],
                 "moe_debug_wait_timeout": [i32, vp, vp, vp],
                 "moe_router_topk": [vp, i32, i32, i32, vp, vp, vp],
+                "moe_debug_col_pieces": [i32, i32, i32, i32, i32, i32, i32, i32, vp, i32],
             }
             for name, args in sig.items():
                 f = getattr(L, name)
@@ -398,6 +399,18 @@ def router_topk(logits: torch.Tensor, top_k: int, stream=None):
                                                    _p(scores), _stream(stream)))
     return ids, scores
 
+
+def col_pieces(top_k: int, dff: int, n_shared: int, dff_shared: int, bits_down: int,
+               bits_shared: int, cta: int, grid: int, max_pieces: int = 64):
+    """The column split's pieces of one CTA (host only): (u0, [(seg, j0, j1, a0, blk0, nb, pb,
+    grp), ...])."""
+    import numpy as np
+    out = np.zeros(2 + 8 * max_pieces, dtype=np.int32)
+    rc = lib().moe_debug_col_pieces(top_k, dff, n_shared, dff_shared, bits_down, bits_shared, cta,
+                                    grid, out.ctypes.data, max_pieces)
+    check("moe_debug_col_pieces", min(rc, 0))
+    n = int(out[1])
+    return int(out[0]), [tuple(int(v) for v in out[2 + 8 * q:10 + 8 * q]) for q in range(n)]
 
 
 # ---------------------------------------------------------------- dense bf16 decode GEMV

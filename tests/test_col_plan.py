@@ -1,0 +1,78 @@
+"""The column split's decomposition of the activation columns, on the host (no GPU).
+
+moe_debug_col_pieces returns, for one CTA, the pieces the MOE_KERNELS_COLUMNS kernel computes on
+the device (the same function).  Over all CTAs of a grid the pieces must tile the activation
+index space exactly once, in order, each piece inside one segment and one group of 64 columns,
+with column blocks that cover its columns and stay inside the expert, and a block list that the
+kernel's per-CTA buffers hold.
+"""
+import pytest
+
+from quantized_moe_expert_dequant_gb300 import binding as Bn
+from quantized_moe_expert_dequant_gb300.workloads import ALL, Shape
+
+MAX_PIECES, MAX_BLOCKS, MAX_COLS = 16, 64, 256   # the kernel's per-CTA limits
+
+
+@pytest.fixture(scope="module")
+def built():
+    import __graft_entry__
+    __graft_entry__.build()
+
+
+CASES = [ALL["qwen3_stack_8bit"], ALL["e512_stack"], ALL["qwen3_layer_4bit"],
+         ALL["qwen15_layer_shared"],
+         Shape("small", 256, 128, 8, 2, 8, 8, 8, n_shared=1, dff_shared=128, bits_shared=4),
+         Shape("ragged", 384, 192, 10, 3, 6, 6, 4),
+         Shape("fewer columns than CTAs", 64, 64, 4, 2, 8, 8, 4),
+         Shape("shared only", 256, 64, 1, 0, 8, 8, 8, n_shared=2, dff_shared=128, bits_shared=8)]
+
+
+@pytest.mark.parametrize("grid", [152, 148, 7, 1])
+@pytest.mark.parametrize("shape", CASES, ids=lambda s: s.name)
+def test_pieces_tile_the_columns_once(built, shape, grid):
+    K, dff, nsh, dsh = shape.top_k, shape.dff, shape.n_shared, shape.dff_shared
+    bsh = shape.bits_shared if nsh else shape.bits_down
+    U = K * dff + nsh * dsh
+    if -(-U // grid) > MAX_COLS:
+        c = max(range(grid), key=lambda c: U * (c + 1) // grid - U * c // grid)
+        with pytest.raises(Bn.MoeError) as e:   # beyond the kernel's per-CTA buffers
+            Bn.col_pieces(K, dff, nsh, dsh, shape.bits_down, bsh, c, grid)
+        assert e.value.rc == Bn.MOE_ERR_UNSUPPORTED
+        return
+    nxt = 0
+    for c in range(grid):
+        u0, pieces = Bn.col_pieces(K, dff, nsh, dsh, shape.bits_down, bsh, c, grid)
+        assert u0 == U * c // grid == nxt
+        u1 = U * (c + 1) // grid
+        assert u1 - u0 <= MAX_COLS and len(pieces) <= MAX_PIECES
+        nblocks = 0
+        for seg, j0, j1, a0, blk0, nb, pb, grp in pieces:
+            routed = seg < K
+            width, bits = (dff, shape.bits_down) if routed else (dsh, bsh)
+            cb = 32 // bits
+            base = seg * dff if routed else K * dff + (seg - K) * dsh
+            assert 0 <= seg < K + nsh
+            assert base + j0 == u0 + a0 == nxt          # contiguous, in column order
+            assert 0 <= j0 < j1 <= width and j0 // 64 == (j1 - 1) // 64 == grp
+            assert blk0 == j0 // cb and blk0 * cb <= j0
+            assert (blk0 + nb) * cb >= j1 and (blk0 + nb - 1) * cb < j1   # blocks cover, no more
+            assert (blk0 + nb) * cb <= width
+            assert pb == nblocks
+            nblocks += nb
+            nxt = base + j1
+        assert nxt == u1
+        assert nblocks <= MAX_BLOCKS
+    assert nxt == U
+
+
+def test_bad_arguments_are_rejected(built):
+    with pytest.raises(Bn.MoeError) as e:
+        Bn.col_pieces(8, 768, 0, 0, 8, 8, 152, 152)     # cta outside the grid
+    assert e.value.rc == Bn.MOE_ERR_INVALID_ARG
+    with pytest.raises(Bn.MoeError) as e:
+        Bn.col_pieces(8, 768, 0, 0, 6, 6, 0, 152)       # 6-bit down codes: not this kernel
+    assert e.value.rc == Bn.MOE_ERR_UNSUPPORTED
+    with pytest.raises(Bn.MoeError) as e:
+        Bn.col_pieces(8, 100, 0, 0, 8, 8, 0, 152)       # width not a multiple of 64
+    assert e.value.rc == Bn.MOE_ERR_INVALID_ARG
