@@ -317,7 +317,7 @@ def run_ours(args, shape: Shape):
                    and (shape.n_shared == 0 or shape.bits_shared in (4, 8)) and shape.din <= 4096)
         kernels = "columns" if cols_ok else "fused"
     mode = {"fused": Bn.KERNELS_FUSED, "separate": Bn.KERNELS_SEPARATE,
-            "columns": Bn.KERNELS_COLUMNS}[kernels]
+            "columns": Bn.KERNELS_COLUMNS, "columns-ahead": Bn.KERNELS_COLUMNS_AHEAD}[kernels]
     norm = None
     if chained and L > 1:
         rows = np.stack([synth.norm_weight(shape.seed, l, shape.din) for l in range(1, L)])
@@ -438,15 +438,17 @@ def run_ours(args, shape: Shape):
     peak_note = "of measured" if peaks else "of fallback"
     ach_a = mean_a / (ms_a * 1e-3) / 1e9
     ach_b = mean_b / (ms_b * 1e-3) / 1e9
-    dominant = {Bn.KERNELS_FUSED: "fused_kernel", Bn.KERNELS_COLUMNS: "cols_kernel"}.get(
-        mode, "gate_up_kernel")
-    if mode in (Bn.KERNELS_FUSED, Bn.KERNELS_COLUMNS):
+    one_launch = (Bn.KERNELS_FUSED, Bn.KERNELS_COLUMNS, Bn.KERNELS_COLUMNS_AHEAD)
+    dominant = {Bn.KERNELS_FUSED: "fused_kernel", Bn.KERNELS_COLUMNS: "cols_kernel",
+                Bn.KERNELS_COLUMNS_AHEAD: "cols_kernel"}.get(mode, "gate_up_kernel")
+    if mode in one_launch:
         # one launch per step: the step's bytes over the step's device time
         ach, per_launch_bytes, per_launch_us = (step_bytes / (ms_per_step * 1e-3) / 1e9,
                                                 step_bytes, ms_per_step * 1e3)
     else:
         ach, per_launch_bytes, per_launch_us = ach_a, mean_a, ms_a * 1e3
-    traffic = profiled_traffic(dominant, args.workload + ("_chained" if chained else ""))
+    traffic = (None if mode == Bn.KERNELS_COLUMNS_AHEAD else
+               profiled_traffic(dominant, args.workload + ("_chained" if chained else "")))
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
@@ -469,6 +471,7 @@ def run_ours(args, shape: Shape):
                    "shared": [shape.n_shared, shape.dff_shared, shape.bits_shared],
                    "layers": L, "tokens_per_step": m, "input_sets": S,
                    "chain_norm": bool(chained), "kernels": kernels,
+                   "ids_known_ahead": mode == Bn.KERNELS_COLUMNS_AHEAD,
                    "parallelism": f"replicas x{world}",
                    "l2": f"inputs larger than L2: {step_bytes / 1e9:.3f} GB of selected weights "
                          f"per step, ids re-drawn per step"},
@@ -487,8 +490,7 @@ def run_ours(args, shape: Shape):
         "cpu_baseline": cpu,
         "e2e": {"value": world * m * e2e_steps / e2e_s, "unit": "tok/s",
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
-        "gpu_launches": (args.steps if mode in (Bn.KERNELS_FUSED, Bn.KERNELS_COLUMNS)
-                         else args.steps * L * m * 2),
+        "gpu_launches": args.steps if mode in one_launch else args.steps * L * m * 2,
         "clocks": clocks,
     }
     if rank == 0:
@@ -612,13 +614,15 @@ def main(argv=None):
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", choices=sorted(ALL), default=DEFAULT_WORKLOAD)
     ap.add_argument("--tokens", type=int, default=1)
-    ap.add_argument("--kernels", choices=["auto", "fused", "separate", "columns"],
+    ap.add_argument("--kernels", choices=["auto", "fused", "separate", "columns", "columns-ahead"],
                     default="auto",
                     help="one persistent kernel per step (row split, two device-wide barriers "
                          "per layer), kernel A and kernel B per layer, one persistent kernel "
                          "per step with the column split (one barrier per layer), or auto: the "
                          "column split where it runs (1 token, 4/8-bit down codes, no folded "
-                         "norm), else the row split")
+                         "norm), else the row split.  columns-ahead: the column split with every "
+                         "layer's ids treated as inputs known before the step (the weight stream "
+                         "runs on into the next layer; not the decode dependency)")
     ap.add_argument("--input-sets", type=int, default=4)
     ap.add_argument("--chain-norm", action="store_true",
                     help="fold the next layer's RMSNorm in: layer l >= 1 reads RMSNorm(out of "

@@ -65,7 +65,7 @@ typedef struct moe_decode_config {
   int32_t shared_gate;     /* 0: scalar 1;  1: scalar = sigmoid(x . gate_vec) */
   int32_t resid_dtype;     /* MOE_DTYPE_BF16 or MOE_DTYPE_F32 */
   int32_t out_dtype;       /* MOE_DTYPE_F32 (default) or MOE_DTYPE_BF16 (rounded to nearest) */
-  int32_t kernel_mode;     /* MOE_KERNELS_FUSED (default), _SEPARATE or _COLUMNS */
+  int32_t kernel_mode;     /* MOE_KERNELS_FUSED (default), _SEPARATE, _COLUMNS, _COLUMNS_AHEAD */
 } moe_decode_config;
 
 /* How a layer is launched.  FUSED: one cooperative persistent kernel per forward (or per stack
@@ -82,8 +82,19 @@ typedef struct moe_decode_config {
  * makes a column-block-major copy of every down projection (owned by the handle: about the size
  * of the down weights) and a partial-sum buffer; the chained stack and moe_stack_step_parts
  * (one phase) do not take this mode.  Results are deterministic (fixed summation order) and equal
- * the other modes within the parity bound, not bit for bit (the sums associate differently). */
-enum { MOE_KERNELS_FUSED = 0, MOE_KERNELS_SEPARATE = 1, MOE_KERNELS_COLUMNS = 2 };
+ * the other modes within the parity bound, not bit for bit (the sums associate differently).
+ * COLUMNS_AHEAD: the same kernel and arithmetic (results byte-identical to COLUMNS) for steps
+ * whose expert ids are all inputs known before the step, as when ids are drawn per layer from a
+ * seed: the weight stream of layer l + 1 starts as soon as the CTA's consumers are done with
+ * layer l's gate/up phase instead of after layer l's device-wide barrier.  It is not the decode
+ * dependency (there a router needs layer l's output to pick layer l + 1's experts); it measures
+ * how far the stream itself goes when that dependency is lifted. */
+enum {
+  MOE_KERNELS_FUSED = 0,
+  MOE_KERNELS_SEPARATE = 1,
+  MOE_KERNELS_COLUMNS = 2,
+  MOE_KERNELS_COLUMNS_AHEAD = 3
+};
 
 /*
  * One projection of every expert of a class, canonical packed layout, all device pointers:

@@ -12,6 +12,10 @@
 namespace {
 
 bool bits_ok(int b) { return b == 4 || b == 6 || b == 8; }
+// The column-split kernel serves both column modes (strict layer order, or ids known ahead).
+bool cols_mode(int kernel_mode) {
+  return kernel_mode == MOE_KERNELS_COLUMNS || kernel_mode == MOE_KERNELS_COLUMNS_AHEAD;
+}
 bool aligned(const void *p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 
 bool proj_ok(const moe_proj &p) {
@@ -37,7 +41,7 @@ int validate_config(const moe_decode_config *c) {
     return MOE_ERR_INVALID_ARG;
   if (c->out_dtype != MOE_DTYPE_BF16 && c->out_dtype != MOE_DTYPE_F32) return MOE_ERR_INVALID_ARG;
   if (c->kernel_mode != MOE_KERNELS_FUSED && c->kernel_mode != MOE_KERNELS_SEPARATE &&
-      c->kernel_mode != MOE_KERNELS_COLUMNS)
+      !cols_mode(c->kernel_mode))
     return MOE_ERR_INVALID_ARG;
   // int32 indexing of the activation vector and of one expert's rows
   const int64_t act = (int64_t)c->top_k * c->dff + (int64_t)c->n_shared * c->dff_shared;
@@ -125,7 +129,7 @@ int prepare(const moe_decode_config *c, Prepared &P) {
   if (c->kernel_mode == MOE_KERNELS_FUSED && P.grid_fused < 1) return MOE_ERR_UNSUPPORTED;
   const int grid = c->kernel_mode == MOE_KERNELS_FUSED ? P.grid_fused : P.grid_sep;
   if ((c->din + grid - 1) / grid > moe::kMaxRowsB) return MOE_ERR_UNSUPPORTED;
-  if (c->kernel_mode == MOE_KERNELS_COLUMNS) {
+  if (cols_mode(c->kernel_mode)) {
     if (c->max_tokens != 1) return MOE_ERR_UNSUPPORTED;
     int lim = 0;
     if (moe::prepare_cols(smem_optin, c->bits_gate, c->bits_down, P.bits_sh, &lim) !=
@@ -272,6 +276,7 @@ cudaError_t enqueue_cols(const Prepared &P, const moe::LayerPtrs *layers,
   p.cols = cols;
   p.cp = P.cplan;
   p.slab = slab;
+  p.ahead = P.cfg.kernel_mode == MOE_KERNELS_COLUMNS_AHEAD;
   return moe::launch_cols(p, P.grid_cols, stream);
 }
 
@@ -335,7 +340,7 @@ struct ColWeights {
 };
 
 size_t slab_floats(const Prepared &P) {
-  return P.cfg.kernel_mode == MOE_KERNELS_COLUMNS
+  return cols_mode(P.cfg.kernel_mode)
              ? (size_t)2 * P.grid_cols * P.grid_cols * P.cplan.ro
              : 0;
 }
@@ -404,7 +409,7 @@ extern "C" int moe_decode_create(const moe_decode_config *cfg, const moe_layer_w
     delete h;
     return MOE_ERR_OOM;
   }
-  if (cfg->kernel_mode == MOE_KERNELS_COLUMNS) {
+  if (cols_mode(cfg->kernel_mode)) {
     rc = h->cw.build(*cfg, weights, 1);
     if (rc != MOE_OK) {
       h->cw.release();
@@ -436,7 +441,7 @@ extern "C" int moe_decode_forward(moe_decode_t *h, const void *x, int32_t m, con
   if (x == out) return MOE_ERR_INVALID_ARG;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   cudaError_t e;
-  if (c.kernel_mode == MOE_KERNELS_COLUMNS)
+  if (cols_mode(c.kernel_mode))
     e = enqueue_cols(h->P, h->ws.layers, h->cw.dev, 1, h->ws.slab, h->ws.err, h->ws.bar, x, ids,
                      scores, resid, c.resid_dtype, out, c.out_dtype, st);
   else if (c.kernel_mode == MOE_KERNELS_FUSED)
@@ -614,7 +619,7 @@ int stack_create(const moe_decode_config *cfg, int32_t n_layers, const moe_layer
   int rc = validate_config(cfg);
   if (rc != MOE_OK) return rc;
   if (cfg->out_dtype != MOE_DTYPE_F32) return MOE_ERR_INVALID_ARG;
-  if (norm_weight && cfg->kernel_mode == MOE_KERNELS_COLUMNS) return MOE_ERR_UNSUPPORTED;
+  if (norm_weight && cols_mode(cfg->kernel_mode)) return MOE_ERR_UNSUPPORTED;
   for (int l = 0; l < n_layers; ++l) {
     rc = validate_weights(cfg, &layers[l]);
     if (rc != MOE_OK) return rc;
@@ -654,7 +659,7 @@ int stack_create(const moe_decode_config *cfg, int32_t n_layers, const moe_layer
     moe_stack_destroy(s);
     return MOE_ERR_CUDA;
   }
-  if (cfg->kernel_mode == MOE_KERNELS_COLUMNS) {
+  if (cols_mode(cfg->kernel_mode)) {
     rc = s->cw.build(*cfg, layers, n_layers);
     if (rc != MOE_OK) {
       moe_stack_destroy(s);
@@ -687,7 +692,7 @@ cudaError_t enqueue_stack(moe_stack *s, const void *x, int m, const int32_t *ids
                           int parts) {
   const int L = (int)s->layers.size();
   const moe_decode_config &c = s->P.cfg;
-  if (c.kernel_mode == MOE_KERNELS_COLUMNS)
+  if (cols_mode(c.kernel_mode))
     return enqueue_cols(s->P, s->ws.layers, s->cw.dev, L, s->ws.slab, s->ws.err, s->ws.bar, x, ids,
                         scores, resid0, c.resid_dtype, out, MOE_DTYPE_F32, st);
   if (c.kernel_mode == MOE_KERNELS_FUSED && parts == (MOE_PART_GATE_UP | MOE_PART_DOWN))
@@ -743,7 +748,7 @@ extern "C" int moe_stack_step_parts(moe_stack_t *s, int32_t parts, const void *x
                                     void *out, void *stream) {
   if (!s || !x || !resid0 || !out) return MOE_ERR_INVALID_ARG;
   if (parts < 1 || parts > (MOE_PART_GATE_UP | MOE_PART_DOWN)) return MOE_ERR_INVALID_ARG;
-  if (s->P.cfg.kernel_mode == MOE_KERNELS_COLUMNS && parts != (MOE_PART_GATE_UP | MOE_PART_DOWN))
+  if (cols_mode(s->P.cfg.kernel_mode) && parts != (MOE_PART_GATE_UP | MOE_PART_DOWN))
     return MOE_ERR_UNSUPPORTED;
   if (m < 1 || m > s->P.cfg.max_tokens) return MOE_ERR_INVALID_ARG;
   if (s->P.cfg.top_k > 0 && (!ids || !scores)) return MOE_ERR_INVALID_ARG;

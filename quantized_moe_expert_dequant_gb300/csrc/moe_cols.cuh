@@ -19,7 +19,10 @@
 //      memory from layer to layer.
 // The next layer's expert ids are read only after that barrier, when every CTA has finished the
 // layer (its output exists as the partials), so no weight of a layer is requested before the
-// previous layer is done.
+// previous layer is done.  With p.ahead (every layer's ids are inputs known before the step) the
+// producer instead starts layer l + 1 as soon as its own CTA's consumers have finished layer l's
+// gate/up phase (a CTA-local mbarrier), so the weight stream runs on across the layer boundary;
+// the arithmetic and its order are the same.
 //
 // The down contraction over a CTA's columns uses integer dot products like the row kernels
 // (moe_common.cuh): within one (segment, group of 64) piece the activations become 23-bit fixed
@@ -260,11 +263,17 @@ __global__ void __launch_bounds__(kThreads, 1) cols_kernel(const StackParams p) 
   __shared__ LayerPtrs wpr;  // the producers' copy
   __shared__ ColPtrs cpr;
   __shared__ int stop_pr;
+  // the expert ids and scores of layers l and l + 1 (the producer may be a layer ahead)
+  __shared__ int ids2[2][kMaxTopK];
+  __shared__ float sc2[2][kMaxTopK];
+  __shared__ __align__(8) uint64_t a_done;  // phase l completes when layer l's gate/up phase has
+                                            // been consumed (consumer thread 0 arrives)
   const LayerShape &s = p.s;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int n = gridDim.x;
   init_ring(rs.full, rs.empty, p.plan.nst, &rs.abort);
   if (tid == 0) {
+    mbar_init(&a_done, 1);
     int nbk = 0;
     int64_t u0 = 0;
     cs.np = col_pieces(s.top_k, s.dff, s.n_shared, s.dff_shared, p.cp.cb_r, p.cp.cb_s,
@@ -288,17 +297,22 @@ __global__ void __launch_bounds__(kThreads, 1) cols_kernel(const StackParams p) 
       if (pl == 0) {
         wpr = p.layers[l];
         cpr = p.cols[l];
-        // every CTA has finished the previous layer before its ids are read
-        if (l > 0) wait_count(p.bar, static_cast<uint32_t>(l) * n, &rs.abort, p.err);
+        if (l > 0) {
+          if (p.ahead)  // this CTA's consumers are done with the ids and counts of layer l - 2
+            ring_wait(&a_done, static_cast<uint32_t>(l - 1) & 1u, &rs.abort, p.err);
+          else          // every CTA has finished the previous layer before its ids are read
+            wait_count(p.bar, static_cast<uint32_t>(l) * n, &rs.abort, p.err);
+        }
         stop_pr = flag_abort(&rs.abort);
       }
       producer_sync();
       if (stop_pr) break;
       const int64_t ks = s.top_k;
-      producer_load_token(s, p.ids + l * ks, p.scores + l * ks, rs.ids, rs.scores, p.err, pl);
-      produce_a<BR, BSH>(s, wpr, p.plan.geo_r, p.plan.geo_s, rs.ids, rs.scores, rs.cnt, r, pl,
-                         pol);
-      produce_down_cols(s, p.cp, cpr, cs, rs.ids, r, pl, pol);
+      int *ids_l = ids2[l & 1];
+      float *sc_l = sc2[l & 1];
+      producer_load_token(s, p.ids + l * ks, p.scores + l * ks, ids_l, sc_l, p.err, pl);
+      produce_a<BR, BSH>(s, wpr, p.plan.geo_r, p.plan.geo_s, ids_l, sc_l, rs.cnt, r, pl, pol);
+      produce_down_cols(s, p.cp, cpr, cs, ids_l, r, pl, pol);
     }
     ring_drain(r, pl);
     return;
@@ -324,7 +338,9 @@ __global__ void __launch_bounds__(kThreads, 1) cols_kernel(const StackParams p) 
                               xsource_plain(p.x + static_cast<int64_t>(l) * s.din), rs.cnt,
                               cs.act, r, sma, tid, cs.u0);
     consumer_sync(kConsumers);  // activations complete; the ids were published by phase A
-    col_planes<BD, BSH>(s, p.cp, cs, rs.ids, warp, lane);
+    if (tid == 0) mbar_arrive(&a_done);
+    const int *ids_l = ids2[l & 1];
+    col_planes<BD, BSH>(s, p.cp, cs, ids_l, warp, lane);
     consumer_sync(kConsumers);
     float part[2][4];
 #pragma unroll
@@ -334,7 +350,7 @@ __global__ void __launch_bounds__(kThreads, 1) cols_kernel(const StackParams p) 
     for (int qi = 0; qi < cs.np; ++qi) {
       const ColPiece q = cs.pc[qi];
       int e;
-      if (!col_valid(s, q, rs.ids, &e)) continue;
+      if (!col_valid(s, q, ids_l, &e)) continue;
       const bool two = s.din > 4 * kConsumers;  // a second row quad per thread
       if (q.seg < s.top_k) {
         if (two)

@@ -228,6 +228,8 @@ struct StackParams {
   const ColPtrs *cols;      // device array [L]
   ColPlan cp;
   float *slab;              // [2][grid][grid][cp.ro]
+  int ahead;                // 1: every layer's ids are inputs known before the step: the weight
+                            // stream runs on into the next layer (not the decode dependency)
 };
 
 // Host-side plan; false when the shape is outside what the kernels support.

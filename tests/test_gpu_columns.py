@@ -4,8 +4,8 @@ In this mode every CTA carries a range of activation columns through gate/up, Sw
 matching columns of a column-block-major copy of the down projections, and the row owners sum the
 per-CTA partial outputs in a fixed order: one device-wide barrier per layer.  Its sums associate
 differently from the row-split modes, so it is held to the oracle's parity bar (not to the other
-modes bit for bit), to itself (stack graph == chain of single-layer forwards, byte for byte) and to
-repeatability.
+modes bit for bit), to itself (stack graph == chain of single-layer forwards, byte for byte; the
+ids-ahead variant == the strict one, byte for byte) and to repeatability.
 """
 import numpy as np
 import pytest
@@ -133,6 +133,14 @@ def test_columns_small_stack_equals_chain_and_oracle(shape):
     assert torch.equal(out.view(torch.int32), outs[-1].view(torch.int32))
     check_layers(shape, x, ids, sc, resid0, outs, np.arange(shape.din))
     stack.close()
+    # ids known ahead: the same arithmetic, the weight stream running on across layers
+    ahead = Bn.MoeStack(layers, max_tokens=1, kernel_mode=Bn.KERNELS_COLUMNS_AHEAD)
+    out3 = torch.empty_like(out)
+    ahead.step(*args, out3)
+    torch.cuda.synchronize()
+    assert ahead.get_error() == 0
+    assert torch.equal(out.view(torch.int32), out3.view(torch.int32))
+    ahead.close()
 
 
 @pytest.mark.parametrize("name", ["qwen3_stack_8bit", "e512_stack"])
@@ -151,6 +159,14 @@ def test_columns_full_size_stack(name):
         torch.cuda.synchronize()
         assert stack.get_error() == 0
         stack.close()
+        ahead = Bn.MoeStack(layers, max_tokens=1, kernel_mode=Bn.KERNELS_COLUMNS_AHEAD)
+        out_ahead = torch.empty_like(out)
+        ahead.step(C.dev(x, torch.bfloat16), C.dev(ids, torch.int32), C.dev(sc, torch.float32),
+                   C.dev(resid0, torch.bfloat16), out_ahead)
+        torch.cuda.synchronize()
+        assert ahead.get_error() == 0
+        ahead.close()
+        assert torch.equal(out.view(torch.int32), out_ahead.view(torch.int32))
         outs = run_chain(layers, x, ids, sc, resid0)
         assert torch.equal(out.view(torch.int32), outs[-1].view(torch.int32))
         rng = np.random.default_rng(8)
