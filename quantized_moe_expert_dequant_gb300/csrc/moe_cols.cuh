@@ -298,7 +298,8 @@ __global__ void __launch_bounds__(kThreads, 1) cols_kernel(const StackParams p) 
         wpr = p.layers[l];
         cpr = p.cols[l];
         if (l > 0) {
-          if (p.ahead)  // this CTA's consumers are done with the ids and counts of layer l - 2
+          if (p.ahead)  // this CTA's consumers are past layer l - 1's gate/up phase: they no
+                        // longer read its stage counts, nor the ids of layer l - 2 (same slot)
             ring_wait(&a_done, static_cast<uint32_t>(l - 1) & 1u, &rs.abort, p.err);
           else          // every CTA has finished the previous layer before its ids are read
             wait_count(p.bar, static_cast<uint32_t>(l) * n, &rs.abort, p.err);
