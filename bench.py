@@ -480,6 +480,9 @@ def run_ours(args, shape: Shape):
                 "note": peak_note},
         "roofline": {"kernel": dominant, "bound": "hbm", "achieved": ach, "peak": peak,
                      "unit": "GB/s", "frac": ach / peak, "traffic": traffic,
+                     # far above the copy peak means the timed kernel skipped bytes
+                     "sanity": ("ok" if ach <= 1.1 * peak else
+                                "achieved bandwidth above 1.1x the copy peak: harness error"),
                      "bytes_per_launch": per_launch_bytes, "us_per_launch": per_launch_us,
                      "note": peak_note + " (copy peak)"},
         "separate_kernels": {

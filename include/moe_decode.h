@@ -326,6 +326,17 @@ int moe_debug_col_pieces(int32_t top_k, int32_t dff, int32_t n_shared, int32_t d
                          int32_t bits_down, int32_t bits_shared, int32_t cta, int32_t grid,
                          int32_t *out, int32_t max_pieces);
 
+/* The column split's launch plan for a config on a grid of `grid` CTAs with `ring_bytes` of
+ * dynamic shared memory, exactly as moe_decode_create makes it (host only, no CUDA call: a debug
+ * export for checks without a GPU).  cfg's kernel_mode is ignored.  out (int32 host, 8 values)
+ * receives: stages in the ring, bytes per stage, column blocks per down stage (nbs), rows per
+ * owner in the partial-sum slab (ro), the routed and the shared down projection's codes per
+ * 32-bit word, the gate/up rows per routed and per shared phase-A stage.  Returns MOE_OK, or
+ * MOE_ERR_UNSUPPORTED when the column split does not take the config (or the grid),
+ * MOE_ERR_INVALID_ARG for an invalid config.  No counterpart on the pages. */
+int moe_debug_col_plan(const moe_decode_config *cfg, int32_t grid, int32_t ring_bytes,
+                       int32_t *out);
+
 #ifdef __cplusplus
 }
 #endif

@@ -36,7 +36,8 @@ EXPORTS = ["moe_decode_create", "moe_decode_forward", "moe_decode_get_error", "m
            "moe_stack_get_error",
            "moe_stack_destroy", "moe_pack_codes", "moe_unpack_codes", "moe_unpack_codes_device",
            "moe_synth_codes", "moe_synth_scales", "moe_synth_biases", "moe_route_invert_device",
-           "moe_debug_wait_timeout", "moe_router_topk", "moe_debug_col_pieces"]
+           "moe_debug_wait_timeout", "moe_router_topk", "moe_debug_col_pieces",
+           "moe_debug_col_plan"]
 
 
 class MoeError(RuntimeError):
@@ -104,6 +105,7 @@ def lib() -> ctypes.CDLL:
                 "moe_debug_wait_timeout": [i32, vp, vp, vp],
                 "moe_router_topk": [vp, i32, i32, i32, vp, vp, vp],
                 "moe_debug_col_pieces": [i32, i32, i32, i32, i32, i32, i32, i32, vp, i32],
+                "moe_debug_col_plan": [ctypes.POINTER(Config), i32, i32, vp],
             }
             for name, args in sig.items():
                 f = getattr(L, name)
@@ -411,6 +413,17 @@ def col_pieces(top_k: int, dff: int, n_shared: int, dff_shared: int, bits_down: 
     check("moe_debug_col_pieces", min(rc, 0))
     n = int(out[1])
     return int(out[0]), [tuple(int(v) for v in out[2 + 8 * q:10 + 8 * q]) for q in range(n)]
+
+
+def col_plan(shape, grid: int, ring_bytes: int) -> dict:
+    """The column split's launch plan for a workload shape (host only)."""
+    import numpy as np
+    cfg = config(shape, 1, DTYPE_BF16, DTYPE_F32, KERNELS_COLUMNS)
+    out = np.zeros(8, dtype=np.int32)
+    check("moe_debug_col_plan", lib().moe_debug_col_plan(ctypes.byref(cfg), grid, ring_bytes,
+                                                         out.ctypes.data))
+    keys = ("stages", "stage_bytes", "nbs", "ro", "cb_r", "cb_s", "rows_a_r", "rows_a_s")
+    return dict(zip(keys, (int(v) for v in out)))
 
 
 # ---------------------------------------------------------------- dense bf16 decode GEMV

@@ -905,3 +905,24 @@ extern "C" int moe_debug_col_pieces(int32_t top_k, int32_t dff, int32_t n_shared
   }
   return np;
 }
+
+extern "C" int moe_debug_col_plan(const moe_decode_config *cfg, int32_t grid, int32_t ring_bytes,
+                                  int32_t *out) {
+  if (!out || grid < 1 || ring_bytes < 1) return MOE_ERR_INVALID_ARG;
+  const int rc = validate_config(cfg);
+  if (rc != MOE_OK) return rc;
+  const moe::LayerShape shape{cfg->din, cfg->dff, cfg->top_k, cfg->n_experts, cfg->n_shared,
+                              cfg->dff_shared};
+  const int bits_sh = cfg->n_shared > 0 ? cfg->bits_shared : cfg->bits_down;
+  moe::ColPlan cp;
+  moe::Plan plan;
+  std::memset(&cp, 0, sizeof cp);
+  std::memset(&plan, 0, sizeof plan);
+  if (!moe::make_col_plan(shape, cfg->bits_gate, cfg->bits_down, bits_sh, grid, ring_bytes, &cp,
+                          &plan))
+    return MOE_ERR_UNSUPPORTED;
+  const int32_t v[8] = {plan.nst, plan.stage_bytes, cp.nbs, cp.ro,
+                        cp.cb_r, cp.cb_s, plan.geo_r.R, plan.geo_s.R};
+  std::memcpy(out, v, sizeof v);
+  return MOE_OK;
+}

@@ -1,4 +1,5 @@
-"""The column split's decomposition of the activation columns, on the host (no GPU).
+"""The column split's decomposition of the activation columns and its launch plan, on the host
+(no GPU).
 
 moe_debug_col_pieces returns, for one CTA, the pieces the MOE_KERNELS_COLUMNS kernel computes on
 the device (the same function).  Over all CTAs of a grid the pieces must tile the activation
@@ -76,3 +77,41 @@ def test_bad_arguments_are_rejected(built):
     with pytest.raises(Bn.MoeError) as e:
         Bn.col_pieces(8, 100, 0, 0, 8, 8, 0, 152)       # width not a multiple of 64
     assert e.value.rc == Bn.MOE_ERR_INVALID_ARG
+
+
+RING = 208 * 1024   # the ring the library asks for (the device's limit is above it on GB300)
+
+
+@pytest.mark.parametrize("shape", CASES, ids=lambda s: s.name)
+def test_plan_stages_fit_the_ring_and_the_slab_rows(built, shape):
+    grid = 152
+    p = Bn.col_plan(shape, grid, RING)
+    bsh = shape.bits_shared if shape.n_shared else shape.bits_down
+    assert p["cb_r"] == 32 // shape.bits_down and p["cb_s"] == 32 // bsh
+    assert 2 <= p["stages"] <= 8 and p["stages"] * p["stage_bytes"] <= RING
+    assert p["stage_bytes"] % 128 == 0
+    assert 1 <= p["nbs"] <= 16 and (p["nbs"] + 1) * shape.din * 4 <= p["stage_bytes"]
+    # a phase-A stage of each class present: its gate and up rows
+    classes = [(p["rows_a_r"], shape.bits_gate)] if shape.top_k else []
+    classes += [(p["rows_a_s"], bsh)] if shape.n_shared else []
+    for rows, bits in classes:
+        assert 2 * rows * shape.din * bits // 8 <= p["stage_bytes"]
+    # every output row has an owner CTA and a slot below ro in the owner's block of the slab
+    ro = p["ro"]
+    assert ro % 4 == 0 and ro <= 32 and ro >= -(-shape.din // grid)
+    for i in range(shape.din):
+        o = ((i + 1) * grid - 1) // shape.din
+        rr = i - shape.din * o // grid
+        assert shape.din * o // grid <= i < shape.din * (o + 1) // grid and 0 <= rr < ro
+
+
+def test_plan_refuses_what_the_kernel_does_not_take(built):
+    six = Shape("6-bit down", 256, 128, 8, 2, 8, 8, 6)
+    wide = Shape("din 8192", 8192, 128, 4, 2, 8, 8, 8)
+    for shape in (six, wide):
+        with pytest.raises(Bn.MoeError) as e:
+            Bn.col_plan(shape, 152, RING)
+        assert e.value.rc == Bn.MOE_ERR_UNSUPPORTED
+    with pytest.raises(Bn.MoeError) as e:     # a ring too small for two stages
+        Bn.col_plan(ALL["qwen3_stack_8bit"], 152, 40 * 1024)
+    assert e.value.rc == Bn.MOE_ERR_UNSUPPORTED
