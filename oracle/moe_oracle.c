@@ -31,7 +31,7 @@
  *
  * No intermediate value of the block is rounded: codes are exact integers, fp16 and bf16 inputs
  * convert to double exactly, and every sum runs left to right in double.  The norm's output is a
- * bf16 code, so its last steps follow the precision the norm is defined in (oracle_rmsnorm_bf16).
+ * bf16 code: computed in double and rounded once (oracle_rmsnorm_bf16).
  * Pins: tests/test_oracle_pins.py.
  */
 #include <float.h>
@@ -253,20 +253,14 @@ uint16_t oracle_round_bf16(double y) {
  * ("Red Lite dev39 -- fused expert tail", Measurements: the reverted tail that also folded in the
  * next layer's RMSNorm).  The page names the step without a formula; this is the usual RMSNorm,
  *   x_c = gamma_c * v_c * r,   r = 1 / sqrt((1/n) sum_j v_j^2 + eps),
- * rounded to the nearest bf16.  Where the rounding is decided matters, so the steps are those of
- * the stack's definition: the sum of squares and r in double, r rounded to fp32, then v_c * r and
- * gamma_c * (v_c * r) as fp32 products, then the fp32 value rounded to bf16 (ties to even).
+ * computed in double and rounded once, at the end, to the nearest bf16 (ties to even).
  * v fp32 [n]; gamma bf16 [n]; x receives bf16 bit patterns [n]. */
 void oracle_rmsnorm_bf16(const float *v, int32_t n, const uint16_t *gamma, float eps,
                          uint16_t *x) {
   double ss = 0.0;
   for (int32_t c = 0; c < n; ++c) ss += (double)v[c] * (double)v[c];
-  const float r = (float)(1.0 / sqrt(ss / n + (double)eps));
-  for (int32_t c = 0; c < n; ++c) {
-    const float t = v[c] * r;
-    const float u = (float)oracle_bf16(gamma[c]) * t;
-    x[c] = oracle_round_bf16((double)u);
-  }
+  const double r = 1.0 / sqrt(ss / n + (double)eps);
+  for (int32_t c = 0; c < n; ++c) x[c] = oracle_round_bf16(oracle_bf16(gamma[c]) * ((double)v[c] * r));
 }
 
 /* Dense bf16 decode GEMV, the attention projections that "Measure attention projections instead

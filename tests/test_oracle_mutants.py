@@ -47,8 +47,8 @@ MUTANTS = {
                                              "sum += exp((double)logits[ids[t]]);"),
     "rmsnorm without eps": ("sqrt(ss / n + (double)eps)", "sqrt(ss / n)"),
     "rmsnorm sums instead of averaging": ("sqrt(ss / n + (double)eps)", "sqrt(ss + (double)eps)"),
-    "rmsnorm weight dropped": ("const float u = (float)oracle_bf16(gamma[c]) * t;",
-                               "const float u = t;"),
+    "rmsnorm weight dropped": ("oracle_round_bf16(oracle_bf16(gamma[c]) * ((double)v[c] * r))",
+                               "oracle_round_bf16((double)v[c] * r)"),
     "bf16 rounding truncates": ("ldexp(nearbyint(ldexp(y, -s)), s)", "ldexp(trunc(ldexp(y, -s)), s)"),
     "bf16 ties away from zero": ("ldexp(nearbyint(ldexp(y, -s)), s)", "ldexp(round(ldexp(y, -s)), s)"),
     "gemv drops the last column": ("for (int32_t i = 0; i < n_in; ++i)\n        acc +=",
