@@ -82,10 +82,6 @@ def layer_bytes(shape: Shape, m: int, unique_experts: int, first_layer: bool,
     return a, b
 
 
-def per_token_layer_weight_bytes(shape: Shape):
-    return shape.top_k * shape.expert_bytes() + shape.shared_bytes()
-
-
 # ---------------------------------------------------------------- inputs
 
 def input_set(shape: Shape, m: int, step: int, chained: bool = False):
@@ -106,60 +102,86 @@ def unique_per_layer(ids: np.ndarray):
 
 # ---------------------------------------------------------------- the oracle on the host
 
-def oracle_units(shape: Shape):
-    """Endless sequence of (oracle call, weight bytes): whole expert MLPs of input set 0, each one
-    routed slot or one shared expert of one layer for one token with all output rows, cycling
-    over the layers.  Drawing the packed experts on the host happens here, outside any timing."""
+def host_cores() -> int:
+    try:
+        return len(os.sched_getaffinity(0))
+    except AttributeError:
+        return os.cpu_count() or 1
+
+
+def oracle_layer_calls(shape: Shape, layers):
+    """One call per layer: that layer's block term (every output row, every slot and shared
+    expert, residual zero) for token 0 of input set 0 through the unchanged oracle_moe_token.  A
+    layer's block term depends only on its own seeded inputs, so layers are independent units of
+    work.  The packed experts are drawn on the host here, outside any timing."""
     from oracle import oracle as O
-    x, ids, sc, resid0 = input_set(shape, 1, 0)
-    layer = 0
-    while True:
-        l = layer % shape.layers
-        pk = lambda proj, e, r, c, b: O.Packed(*synth.expert_proj(shape.seed, l, proj, e, r, c, b), b)
-        xl = x[l][0]
-        resid = resid0[0]
-        for k in range(shape.top_k):
-            e = int(ids[l][0][k])
-            kw = dict(scores=sc[l][0][k:k + 1],
-                      gate=[pk(synth.GATE, e, shape.dff, shape.din, shape.bits_gate)],
-                      up=[pk(synth.UP, e, shape.dff, shape.din, shape.bits_up)],
-                      down=[pk(synth.DOWN, e, shape.din, shape.dff, shape.bits_down)])
-            yield (lambda kw=kw: O.moe_token(xl, resid, **kw)), shape.expert_bytes()
-        for s in range(shape.n_shared):
+    x, ids, sc, _ = input_set(shape, 1, 0)
+    zero = np.zeros(shape.din, np.float32)
+    calls = []
+    for l in layers:
+        pk = lambda proj, e, r, c, b, l=l: O.Packed(*synth.expert_proj(shape.seed, l, proj, e, r, c, b), b)
+        slots = [int(e) for e in ids[l][0]]
+        kw = dict(scores=sc[l][0],
+                  gate=[pk(synth.GATE, e, shape.dff, shape.din, shape.bits_gate) for e in slots],
+                  up=[pk(synth.UP, e, shape.dff, shape.din, shape.bits_up) for e in slots],
+                  down=[pk(synth.DOWN, e, shape.din, shape.dff, shape.bits_down) for e in slots])
+        if shape.n_shared:
             w, b = shape.dff_shared, shape.bits_shared
-            kw = dict(scores=np.zeros(0, np.float32), gate=[], up=[], down=[],
-                      sh_gate=[pk(synth.SH_GATE, s, w, shape.din, b)],
-                      sh_up=[pk(synth.SH_UP, s, w, shape.din, b)],
-                      sh_down=[pk(synth.SH_DOWN, s, shape.din, w, b)],
+            kw.update(sh_gate=[pk(synth.SH_GATE, t, w, shape.din, b) for t in range(shape.n_shared)],
+                      sh_up=[pk(synth.SH_UP, t, w, shape.din, b) for t in range(shape.n_shared)],
+                      sh_down=[pk(synth.SH_DOWN, t, shape.din, w, b) for t in range(shape.n_shared)],
                       gate_vec_bf16=synth.gate_vector(shape.seed, l, shape.din)
                       if shape.shared_gate else None)
-            yield (lambda kw=kw: O.moe_token(xl, resid, **kw)), shape.shared_bytes() // shape.n_shared
-        layer += 1
+        calls.append(lambda kw=kw, xl=x[l][0]: O.moe_token(xl, zero, **kw))
+    return calls
 
 
-def time_units(units, n: int | None = None, target_s: float | None = None):
-    """Times the oracle, as it stands, on the next units until n calls or target_s seconds of
-    oracle time.  Returns (weight bytes, seconds, calls); only the oracle calls are timed."""
-    nbytes, spent, calls = 0, 0.0, 0
-    while (n is None or calls < n) and (target_s is None or spent < target_s or calls == 0):
-        call, nb = next(units)
+class OracleStack:
+    """The oracle on every host core: one step is every layer of the stack, one layer per thread
+    at a time (ctypes releases the GIL inside the oracle), so a step's wall time is measured,
+    not extrapolated."""
+
+    def __init__(self, shape: Shape, cores: int):
+        import concurrent.futures as cf
+        self.shape, self.cores = shape, cores
+        self.calls = oracle_layer_calls(shape, range(shape.layers))
+        self.pool = cf.ThreadPoolExecutor(max_workers=cores)
+
+    def step(self) -> float:
         t0 = time.perf_counter()
-        call()
-        spent += time.perf_counter() - t0
-        nbytes += nb
-        calls += 1
-    return nbytes, spent, calls
+        list(self.pool.map(lambda c: c(), self.calls))
+        return time.perf_counter() - t0
+
+    def close(self):
+        self.pool.shutdown()
 
 
-def oracle_tok_per_s(shape: Shape, m: int, bps: float) -> float:
-    step_bytes = m * shape.layers * per_token_layer_weight_bytes(shape)
-    return m / (step_bytes / bps)
+def oracle_baseline(shape: Shape, steps: int = 3) -> dict:
+    """Median of `steps` timed steps of the whole stack (one token) on all host cores."""
+    cores = host_cores()
+    os_ = OracleStack(shape, cores)
+    os_.step()                                            # warm-up (page-in, thread start)
+    times = [os_.step() for _ in range(steps)]
+    os_.close()
+    t = statistics.median(times)
+    layers_s = shape.layers / t
+    return {"value": 1.0 / t, "unit": "tok/s", "cores": cores, "kind": "oracle",
+            "layers_per_s": layers_s, "gbs": layers_s * per_token_layer_weight_bytes(shape) / 1e9,
+            "sample": f"median of {steps} steps of the whole {shape.layers}-layer stack (every "
+                      f"output row, every slot, one token) through the unchanged fp64 oracle, "
+                      f"one layer per thread on {cores} host cores ({t:.2f} s per step)"}
+
+
+def per_token_layer_weight_bytes(shape: Shape):
+    return shape.top_k * shape.expert_bytes() + shape.shared_bytes()
 
 
 # ---------------------------------------------------------------- clocks
 
 class ClockSampler:
-    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+    """nvidia-smi every 100 ms from construction to stop(); stop(t0, t1) keeps the samples taken
+    between two wall-clock datetimes (the timed region) when there are any."""
+    FIELDS = ("timestamp,index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
 
@@ -175,15 +197,30 @@ class ClockSampler:
         except OSError:
             self.proc = None
 
-    def stop(self):
+    def stop(self, t0=None, t1=None):
+        import datetime as dt
         if self.proc is None:
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
         self.proc.terminate()
         out, _ = self.proc.communicate(timeout=10)
-        rows = [r.split(", ") for r in out.strip().splitlines() if r.count(",") >= 8]
+        rows = []
+        for line in out.strip().splitlines():
+            r = line.split(", ")
+            if len(r) < 10:
+                continue
+            try:
+                when = dt.datetime.strptime(r[0].strip(), "%Y/%m/%d %H:%M:%S.%f")
+            except ValueError:
+                when = None
+            rows.append((when, r[1:]))
+        window = False
+        if t0 is not None and t1 is not None:
+            inside = [x for x in rows if x[0] is not None and t0 <= x[0] <= t1]
+            if inside:
+                rows, window = inside, True
         sm, smax, reasons = [], [], set()
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        for r in rows:
+        for _, r in rows:
             try:
                 sm.append(float(r[1]))
                 smax.append(float(r[2]))
@@ -194,7 +231,8 @@ class ClockSampler:
                     reasons.add(n)
         return {"sm_mhz": statistics.median(sm) if sm else None,
                 "sm_max_mhz": max(smax) if smax else None,
-                "reasons": sorted(reasons), "samples": len(sm)}
+                "reasons": sorted(reasons), "samples": len(sm),
+                "timed_region_only": window}
 
 
 # ---------------------------------------------------------------- helpers
@@ -270,23 +308,28 @@ def run_reference(args, shape: Shape):
     rank, world, _ = dist_setup("gloo")
     if rank != 0:
         return 0
-    # each step: one expert MLP of the stack through the oracle; the rate scales to the stack
-    units = oracle_units(shape)
-    time_units(units, n=args.warmup)
-    nbytes, spent, calls = time_units(units, n=args.steps)
-    bps = nbytes / spent
-    tok = oracle_tok_per_s(shape, args.tokens, bps)
-    step_s = args.tokens / tok
+    # each step: every layer of the stack through the oracle, on every host core
+    cores = host_cores()
+    os_ = OracleStack(shape, cores)
+    for _ in range(args.warmup):
+        os_.step()
+    times = [os_.step() for _ in range(args.steps)]
+    os_.close()
+    spent = sum(times)
+    tok = args.steps / spent
+    layers_s = shape.layers * tok
     line = {
         "impl": "reference", "metric": METRIC, "value": tok, "unit": "tok/s", "n_gpus": 0,
-        "steps": args.steps, "warmup": args.warmup, "ms_per_step": step_s * 1e3,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": spent / args.steps * 1e3,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
         "data": "synthetic",
-        "config": {"workload": shape.name, "layers": shape.layers, "tokens_per_step": args.tokens},
-        "cpu_baseline": {"value": tok, "unit": "tok/s", "cores": 1, "kind": "oracle",
-                         "sample": f"each step one expert MLP (one slot of one token of one "
-                                   f"layer, all rows) through the fp64 oracle; {calls} timed in "
-                                   f"{spent:.1f} s, scaled by weight bytes to the full stack"},
+        "config": {"workload": shape.name, "layers": shape.layers, "tokens_per_step": 1},
+        "cpu_baseline": {"value": tok, "unit": "tok/s", "cores": cores, "kind": "oracle",
+                         "layers_per_s": layers_s,
+                         "sample": f"each step the whole {shape.layers}-layer stack (every "
+                                   f"output row, every slot, one token) through the unchanged "
+                                   f"fp64 oracle, one layer per thread on {cores} host cores; "
+                                   f"{args.steps} steps in {spent:.1f} s"},
         "e2e": {"value": tok, "unit": "tok/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line), flush=True)
@@ -294,6 +337,12 @@ def run_reference(args, shape: Shape):
 
 
 # ---------------------------------------------------------------- our arm
+
+def mode_of(kernels: str) -> int:
+    from quantized_moe_expert_dequant_gb300 import binding as Bn
+    return {"fused": Bn.KERNELS_FUSED, "separate": Bn.KERNELS_SEPARATE,
+            "columns": Bn.KERNELS_COLUMNS, "columns-ahead": Bn.KERNELS_COLUMNS_AHEAD}[kernels]
+
 
 def run_ours(args, shape: Shape):
     import torch
@@ -304,6 +353,13 @@ def run_ours(args, shape: Shape):
     torch.cuda.set_device(local)
     device = torch.device("cuda", local)
     m, L, S = args.tokens, shape.layers, args.input_sets
+
+    bus = None
+    try:
+        bus = torch.cuda.get_device_properties(device).pci_bus_id
+    except AttributeError:
+        bus = None
+    sampler = ClockSampler(bus if bus else str(local))   # running long before the timed region
 
     free, _ = torch.cuda.mem_get_info()
     need = shape.layer_weight_bytes() * L
@@ -316,8 +372,7 @@ def run_ours(args, shape: Shape):
         cols_ok = (m == 1 and not chained and shape.bits_down in (4, 8)
                    and (shape.n_shared == 0 or shape.bits_shared in (4, 8)) and shape.din <= 4096)
         kernels = "columns" if cols_ok else "fused"
-    mode = {"fused": Bn.KERNELS_FUSED, "separate": Bn.KERNELS_SEPARATE,
-            "columns": Bn.KERNELS_COLUMNS, "columns-ahead": Bn.KERNELS_COLUMNS_AHEAD}[kernels]
+    mode = mode_of(kernels)
     norm = None
     if chained and L > 1:
         rows = np.stack([synth.norm_weight(shape.seed, l, shape.din) for l in range(1, L)])
@@ -347,26 +402,37 @@ def run_ours(args, shape: Shape):
                for u in uniq]
 
     stream = torch.cuda.current_stream(device)
+    ab_stack, ab_kernels = None, None
+    if args.ab:
+        ab_kernels = args.ab
+        ab_stack = Bn.MoeStack(layers, max_tokens=m, kernel_mode=mode_of(ab_kernels),
+                               norm_weight=norm, eps=NORM_EPS)
 
-    def step(i, parts=3):
+    def step(i, parts=3, st=None):
         x, ids, sc, r0, out, _ = sets[i % S]
         if parts == 3:
-            stack.step(x, ids, sc, r0, out, stream)
+            (st or stack).step(x, ids, sc, r0, out, stream)
         else:
             parts_stack.step_parts(parts, x, ids, sc, r0, out, stream)
 
-    bus = None
-    try:
-        bus = torch.cuda.get_device_properties(device).pci_bus_id
-    except AttributeError:
-        bus = None
-    sampler = ClockSampler(bus if bus else str(local))
+    def time_steps(n_steps, st=None):
+        """ms per step of n_steps replays, CUDA events on the launching stream."""
+        torch.cuda.synchronize(device)
+        a0, a1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a0.record(stream)
+        for i in range(n_steps):
+            step(i, st=st)
+        a1.record(stream)
+        torch.cuda.synchronize(device)
+        return a0.elapsed_time(a1) / n_steps
 
     # warm-up: captures every graph, then W untimed steps
     for i in range(S):
         step(i)
         step(i, Bn.PART_GATE_UP)
         step(i, Bn.PART_DOWN)
+        if ab_stack is not None:
+            step(i, st=ab_stack)
     torch.cuda.synchronize(device)
     for i in range(args.warmup):
         step(i)
@@ -374,6 +440,8 @@ def run_ours(args, shape: Shape):
     assert stack.get_error() == 0
 
     # timed region: exactly K steps
+    import datetime as dt
+    tw0 = dt.datetime.now()
     barrier(device)
     torch.cuda.synchronize(device)
     e0 = torch.cuda.Event(enable_timing=True)
@@ -387,6 +455,25 @@ def run_ours(args, shape: Shape):
     ms_local = e0.elapsed_time(e1)
     value, ms = job_rate(m * args.steps, ms_local, device)
     ms_per_step = ms / args.steps
+
+    # the sampling protocol, after the K steps: >= 10 samples of >= 5 replays (about 100 ms each,
+    # so the clock sampler sees them); with --ab the other kernel mode's samples alternate with
+    # this one's
+    reps = max(5, int(np.ceil(100.0 / max(ms_per_step, 1e-3))))
+    samp_a, samp_b = [], []
+    for _ in range(max(10, args.samples)):
+        samp_a.append(time_steps(reps))
+        if ab_stack is not None:
+            samp_b.append(time_steps(reps, ab_stack))
+    tw1 = dt.datetime.now()
+
+    def sample_stats(v):
+        v = np.asarray(v)
+        med = float(np.median(v))
+        return {"n": len(v), "replays": reps, "ms_per_step_median": med,
+                "ms_per_step_min": float(v.min()), "ms_per_step_max": float(v.max()),
+                "spread": float((v.max() - v.min()) / med),
+                "value_median": world * m / (med * 1e-3) * (L if args.single_layer else 1)}
     step_bytes = sum(bytes_a[i % S] + bytes_b[i % S] for i in range(args.steps)) / args.steps
 
     # the two-kernel mode, each phase of every layer replayed alone (for comparison)
@@ -430,8 +517,9 @@ def run_ours(args, shape: Shape):
     e2e_s = max_over_ranks(t1 - t0, device)
     h2d = sum(t.numel() * t.element_size() for t in pinned[0][:4])
     d2h = pinned[0][4].numel() * 4
-    clocks = sampler.stop()
+    clocks = sampler.stop(tw0, tw1)
     assert stack.get_error() == 0 and parts_stack.get_error() == 0
+    assert ab_stack is None or ab_stack.get_error() == 0
 
     peaks = measured_peaks()
     peak = peaks["hbm_gbs"] if peaks else 6800.0
@@ -452,16 +540,16 @@ def run_ours(args, shape: Shape):
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        nbytes, spent, calls = time_units(oracle_units(shape), target_s=args.cpu_seconds)
-        cpu = {"value": oracle_tok_per_s(shape, m, nbytes / spent), "unit": "tok/s", "cores": 1,
-               "kind": "oracle",
-               "sample": f"{calls} expert MLPs (one routed slot or shared expert of one token of "
-                         f"one layer, all rows) through the single-threaded fp64 oracle, "
-                         f"{spent:.1f} s of oracle time, scaled by weight bytes to one step of "
-                         f"the full stack"}
+        cpu = oracle_baseline(shape)
+        if args.single_layer:
+            cpu["value"], cpu["unit"] = cpu["layers_per_s"], "layers/s"
 
+    unit = "tok/s"
+    if args.single_layer:   # one layer per replica: layers per second (SURVEY units)
+        value *= L
+        unit = "layers/s"
     line = {
-        "metric": METRIC, "value": value, "unit": "tok/s", "n_gpus": world,
+        "metric": METRIC, "value": value, "unit": unit, "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_per_step,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
         "data": "synthetic (seeded weights drawn in HBM, seeded token inputs)",
@@ -491,15 +579,129 @@ def run_ours(args, shape: Shape):
             "down_kernel": {"achieved": ach_b, "frac": ach_b / peak,
                             "bytes_per_launch": mean_b, "us_per_launch": ms_b * 1e3}},
         "cpu_baseline": cpu,
-        "e2e": {"value": world * m * e2e_steps / e2e_s, "unit": "tok/s",
-                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+        "e2e": {"value": world * m * e2e_steps / e2e_s * (L if args.single_layer else 1),
+                "unit": unit, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
         "gpu_launches": args.steps if mode in one_launch else args.steps * L * m * 2,
         "clocks": clocks,
+        "samples": sample_stats(samp_a),
     }
+    if args.single_layer:
+        line["config"]["replicas"] = L
+        if shape.din == 2048 and shape.dff == 768 and shape.top_k == 8:
+            line["tok_equivalent_48_layers"] = value / 48
+    if ab_stack is not None:
+        sa, sb = sample_stats(samp_a), sample_stats(samp_b)
+        line["ab"] = {"kernels": [kernels, ab_kernels], "alternated_samples": len(samp_a),
+                      "ms_per_step_median": [sa["ms_per_step_median"], sb["ms_per_step_median"]],
+                      "spread": [sa["spread"], sb["spread"]],
+                      "b_over_a_time": sb["ms_per_step_median"] / sa["ms_per_step_median"]}
+        ab_stack.close()
     if rank == 0:
         print(json.dumps(line), flush=True)
     stack.close()
     parts_stack.close()
+    return 0
+
+
+# ---------------------------------------------------------------- the column kernel's timeline
+
+TL_POINTS = {0: "producer: layer top", 1: "producer: barrier seen", 2: "producer: ids loaded",
+             3: "consumers: activations formed", 4: "producer: down copies issued",
+             5: "consumers: layer top", 6: "consumers: met the helper",
+             7: "consumers: x operand built", 8: "consumers: first stage landed",
+             9: "consumers: thread 0 done with gate/up", 10: "consumers: every warp done with gate/up",
+             11: "consumers: planes built", 12: "consumers: down stages consumed",
+             13: "consumers: partials written", 14: "consumers: arrived",
+             15: "helper: owner's sums and shared scalar done",
+             52: "helper: previous layer's arrivals complete"}
+
+
+def timeline_summary(tl: np.ndarray) -> dict:
+    """Medians over CTAs and the inner layers of the column kernel's per-layer stamps, in us after
+    the consumers' layer top (clock64 within a CTA, converted with that CTA's own cycles per ns):
+    the named points, when each of the layer's first ring stages was issued and found full, and
+    the device-wide arrival count in globaltimer ns after the layer's last arrival."""
+    t = tl.astype(np.int64)
+    C, L, _ = t.shape
+    lo, hi = (2, L - 2) if L > 6 else (1, L - 1)
+    rate = (t[:, hi, 5] - t[:, lo, 5]) / np.maximum(t[:, hi, 56] - t[:, lo, 56], 1)  # cycles/ns
+    base = t[:, lo:hi, 5]
+
+    def rel(k):
+        return (t[:, lo:hi, k] - base) / rate[:, None] / 1e3
+
+    def stat(d):
+        return {"median_us": round(float(np.median(d)), 3),
+                "p10_us": round(float(np.percentile(d, 10)), 3),
+                "p90_us": round(float(np.percentile(d, 90)), 3)}
+
+    pts = {name: stat(rel(k)) for k, name in TL_POINTS.items()}
+    stages = []
+    for i in range(12):
+        got = t[:, lo:hi, 16 + i]
+        if not (got > 0).all():
+            break
+        waited = t[:, lo:hi, 40 + i] > 0
+        wait_us = float(np.median(rel(40 + i)[waited])) if waited.any() else None
+        stages.append({"stage": i, "issued_us": round(float(np.median(rel(28 + i))), 3),
+                       "wait_from_us": None if wait_us is None else round(wait_us, 3),
+                       "full_us": round(float(np.median(rel(16 + i))), 3)})
+    layer_us = (t[:, lo + 1:hi + 1, 5] - t[:, lo:hi, 5]) / rate[:, None] / 1e3
+    arrive = t[:, :, 57]
+    last = arrive.max(axis=0)
+    seen_after = (t[:, lo + 1:hi + 1, 59] - last[None, lo:hi]) / 1e3
+    helper_after = (t[:, lo + 1:hi + 1, 58] - last[None, lo:hi]) / 1e3
+    spread = (last[lo:hi] - np.median(arrive[:, lo:hi], axis=0)) / 1e3
+    slow = np.bincount(np.argmax(arrive[:, lo:hi], axis=0), minlength=C)
+    return {"ctas": C, "layers": L, "inner_layers": [lo, hi],
+            "sm_ghz_median": round(float(np.median(rate)), 3),
+            "layer_us": {"median": round(float(np.median(layer_us)), 3),
+                         "p10": round(float(np.percentile(layer_us, 10)), 3),
+                         "p90": round(float(np.percentile(layer_us, 90)), 3)},
+            "points_after_consumer_layer_top": pts, "stages": stages,
+            "barrier": {"producers_see_after_last_arrival_us": round(float(np.median(seen_after)), 3),
+                        "helpers_see_after_last_arrival_us": round(float(np.median(helper_after)), 3),
+                        "last_arrival_after_median_arrival_us": round(float(np.median(spread)), 3),
+                        "ctas_most_often_last": [int(c) for c in np.argsort(-slow)[:8]],
+                        "times_last": [int(slow[c]) for c in np.argsort(-slow)[:8]]}}
+
+
+def run_timeline(args, shape: Shape):
+    """The column kernel from the timeline build (libmoe_decode_timeline.so), stamped per CTA
+    and layer; prints a summary of the last of --steps steps (not a throughput figure)."""
+    import torch
+
+    from quantized_moe_expert_dequant_gb300 import binding as Bn
+    from quantized_moe_expert_dequant_gb300 import build as B
+
+    B.build(timeline=True)
+    Bn.use_timeline_build()
+    device = torch.device("cuda", 0)
+    torch.cuda.set_device(device)
+    L, S = shape.layers, args.input_sets
+    layers = [Bn.synth_layer_device(shape, l) for l in range(L)]
+    mode = Bn.KERNELS_COLUMNS_AHEAD if args.kernels == "columns-ahead" else Bn.KERNELS_COLUMNS
+    stack = Bn.MoeStack(layers, max_tokens=1, kernel_mode=mode)
+    sets = []
+    for i in range(S):
+        x, ids, sc, r0 = input_set(shape, 1, i)
+        conv = lambda a, dt: (torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).view(dt)
+                              if dt == torch.bfloat16 else torch.from_numpy(np.ascontiguousarray(a)))
+        sets.append((conv(x, torch.bfloat16).to(device), conv(ids, torch.int32).to(device),
+                     conv(sc, torch.float32).to(device), conv(r0, torch.bfloat16).to(device),
+                     torch.empty((1, shape.din), dtype=torch.float32, device=device)))
+    stream = torch.cuda.current_stream(device)
+    for i in range(args.warmup + args.steps):
+        stack.step(*sets[i % S], stream=stream)
+    torch.cuda.synchronize(device)
+    assert stack.get_error() == 0
+    tl = stack.timeline()
+    if args.timeline_out:
+        np.save(args.timeline_out, tl)
+    line = {"timeline": shape.name, "kernel": "cols_kernel (timeline build)",
+            "ids_known_ahead": mode == Bn.KERNELS_COLUMNS_AHEAD, **timeline_summary(tl)}
+    print(json.dumps(line), flush=True)
+    stack.close()
     return 0
 
 
@@ -627,6 +829,13 @@ def main(argv=None):
                          "layer's ids treated as inputs known before the step (the weight stream "
                          "runs on into the next layer; not the decode dependency)")
     ap.add_argument("--input-sets", type=int, default=4)
+    ap.add_argument("--samples", type=int, default=10,
+                    help="timed samples after the K steps (at least 10), each of at least 5 "
+                         "replays and about 100 ms")
+    ap.add_argument("--ab", choices=["fused", "separate", "columns", "columns-ahead"],
+                    default=None,
+                    help="also time this kernel mode, its samples alternating with the main "
+                         "mode's (A/B on the same box and weights)")
     ap.add_argument("--chain-norm", action="store_true",
                     help="fold the next layer's RMSNorm in: layer l >= 1 reads RMSNorm(out of "
                          "layer l - 1) instead of its own x")
@@ -637,6 +846,10 @@ def main(argv=None):
     ap.add_argument("--gemv", choices=sorted(GEMV_NAMES), default=None,
                     help="measure the dense bf16 decode GEMV of this projection instead")
     ap.add_argument("--rows", type=int, default=1, help="rows (tokens) of the --gemv product")
+    ap.add_argument("--timeline", action="store_true",
+                    help="instead of timing, run the column kernel from the timeline build and "
+                         "print where a layer's time goes (per-CTA, per-layer stamps)")
+    ap.add_argument("--timeline-out", default=None, help="also save the raw stamps (.npy)")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")
@@ -647,12 +860,20 @@ def main(argv=None):
             return 0
         return run_gemv(args)
     shape = ALL[args.workload]
+    single = shape.layers == 1
     if args.layers:
         shape = shape.with_(layers=args.layers, name=f"{shape.name} (first {args.layers} layers)")
-    if shape.layers == 1 and not args.layers:
-        ap.error("bench workloads are the layer stacks")
+    elif single:
+        # one layer: a graph over R distinct weight replicas, R >= 48 and >= 1 GB of selected
+        # weights per timed step, so that neither launch overhead nor L2 residency inflates the rate
+        per = per_token_layer_weight_bytes(shape)
+        R = max(48, -(-(1 << 30) // per))
+        shape = shape.with_(layers=R, name=f"{shape.name}, {R} distinct replicas per step")
+    args.single_layer = single and not args.layers
     if args.impl == "reference":
         return run_reference(args, shape)
+    if args.timeline:
+        return run_timeline(args, shape)
     return run_ours(args, shape)
 
 

@@ -43,8 +43,11 @@ typedef enum moe_status {
   MOE_ERR_CUDA = -3,         /* a CUDA runtime call failed (launch, copy, graph) */
   MOE_ERR_OOM = -4,          /* device or pinned allocation failed */
   MOE_ERR_BAD_ID = -5,       /* device error word: an expert id was outside [0, n_experts) */
-  MOE_ERR_TIMEOUT = -6       /* device error word: a pipeline wait gave up after about two seconds
+  MOE_ERR_TIMEOUT = -6,      /* device error word: a pipeline wait gave up after about two seconds
                                 (a bug, never expected); the kernel returned without its result */
+  MOE_ERR_PLAN = -7          /* device error word: a kernel found its launch plan inconsistent with
+                                the shape (a bug, never expected: create checks every CTA's part);
+                                the kernel skipped its work */
 } moe_status;
 
 enum { MOE_DTYPE_BF16 = 0, MOE_DTYPE_F32 = 1 };
@@ -65,7 +68,8 @@ typedef struct moe_decode_config {
   int32_t shared_gate;     /* 0: scalar 1;  1: scalar = sigmoid(x . gate_vec) */
   int32_t resid_dtype;     /* MOE_DTYPE_BF16 or MOE_DTYPE_F32 */
   int32_t out_dtype;       /* MOE_DTYPE_F32 (default) or MOE_DTYPE_BF16 (rounded to nearest) */
-  int32_t kernel_mode;     /* MOE_KERNELS_FUSED (default), _SEPARATE, _COLUMNS, _COLUMNS_AHEAD */
+  int32_t kernel_mode;     /* MOE_KERNELS_FUSED (default), _SEPARATE, _COLUMNS, _COLUMNS_AHEAD,
+                              _POOL */
 } moe_decode_config;
 
 /* How a layer is launched.  FUSED: one cooperative persistent kernel per forward (or per stack
@@ -77,11 +81,13 @@ typedef struct moe_decode_config {
  * the down projection (the same sums as kernel A and kernel B of "two-kernel decode-MoE that
  * beats gather_qmm", What changed, step 2, and the tail of "Red Lite dev39 -- fused expert tail",
  * Change), writing per-CTA partial outputs that the row owners sum in a fixed order: one
- * device-wide barrier per layer.  Requires max_tokens == 1, bits_down (and bits_shared when
- * n_shared > 0) of 4 or 8, din <= 4096; create returns MOE_ERR_UNSUPPORTED otherwise.  Create
- * makes a column-block-major copy of every down projection (owned by the handle: about the size
- * of the down weights) and a partial-sum buffer; the chained stack and moe_stack_step_parts
- * (one phase) do not take this mode.  Results are deterministic (fixed summation order) and equal
+ * device-wide barrier per layer.  Requires max_tokens == 1, gate/up codes of 4 or 8 bits,
+ * bits_down (and bits_shared when n_shared > 0) of 4 or 8, din <= 4096; create returns
+ * MOE_ERR_UNSUPPORTED otherwise.  Create copies every projection into the kernel's own layout
+ * (owned by the handle, about the size of the layer's weights: gate and up rows interleaved with
+ * their scales and biases, the down projection column-block-major) and allocates a partial-sum
+ * buffer; after create the kernel reads only those copies and gate_vec.  The chained stack and
+ * moe_stack_step_parts (one phase) do not take this mode.  Results are deterministic (fixed summation order) and equal
  * the other modes within the parity bound, not bit for bit (the sums associate differently).
  * COLUMNS_AHEAD: the same kernel and arithmetic (results byte-identical to COLUMNS) for steps
  * whose expert ids are all inputs known before the step, as when ids are drawn per layer from a
@@ -89,11 +95,20 @@ typedef struct moe_decode_config {
  * layer l's gate/up phase instead of after layer l's device-wide barrier.  It is not the decode
  * dependency (there a router needs layer l's output to pick layer l + 1's experts); it measures
  * how far the stream itself goes when that dependency is lifted. */
+/* POOL: the pool-and-tail form of "Red Lite dev39 -- fused expert tail" (Change) kept apart, for
+ * any m: one cooperative persistent kernel groups the m tokens' slots by expert, computes every
+ * routed slot's and shared expert's down output WITHOUT its coefficient into a workspace buffer
+ * (device-wide barrier), then a tail forms
+ *   out = resid + (sum_k score_k * y_k  +  scalar * sum_s y_s),  k in slot order,
+ * exactly the page's association.  moe_decode_routes copies the per-slot outputs out.  It is the
+ * unfused counterpart of the other modes, which fold the score or the scalar into the activation
+ * and sum routed and shared terms in one accumulation; results agree within the parity bound. */
 enum {
   MOE_KERNELS_FUSED = 0,
   MOE_KERNELS_SEPARATE = 1,
   MOE_KERNELS_COLUMNS = 2,
-  MOE_KERNELS_COLUMNS_AHEAD = 3
+  MOE_KERNELS_COLUMNS_AHEAD = 3,
+  MOE_KERNELS_POOL = 4
 };
 
 /*
@@ -141,6 +156,18 @@ int moe_decode_forward(moe_decode_t *h, const void *x, int32_t m, const int32_t 
 /* Synchronises the device, returns the sticky device error word in *device_error (MOE_OK,
  * MOE_ERR_BAD_ID or MOE_ERR_TIMEOUT) and clears it. */
 int moe_decode_get_error(moe_decode_t *h, int32_t *device_error);
+
+/* The route the last moe_decode_forward of this handle took, for checking it (no counterpart
+ * beyond the page's tmp-buffer accessor of "Red Lite dev39 -- fused expert tail", Change).
+ *   ids_used  int32 [m][top_k] device or NULL: the expert ids the kernels read, in the order
+ *             they read them (slot order), as written by the kernels themselves
+ *   slot_out  fp32 [m][top_k + n_shared][din] device or NULL (MOE_KERNELS_POOL only): each routed
+ *             slot's down output W_down[id] . act (before its score) and each shared expert's
+ *             (before the scalar); rows of a slot with an invalid id are unspecified
+ * m is the last forward's token count.  Asynchronous on `stream`, ordered after that forward when
+ * both use the same stream.  Returns MOE_ERR_INVALID_ARG for a null handle, both pointers null, a
+ * misaligned pointer or no forward yet, MOE_ERR_UNSUPPORTED for slot_out outside the pool mode. */
+int moe_decode_routes(moe_decode_t *h, int32_t *ids_used, void *slot_out, void *stream);
 
 void moe_decode_destroy(moe_decode_t *h);
 

@@ -23,12 +23,14 @@ MOE_OK, MOE_ERR_INVALID_ARG, MOE_ERR_UNSUPPORTED, MOE_ERR_CUDA, MOE_ERR_OOM, MOE
     0, -1, -2, -3, -4, -5)
 DTYPE_BF16, DTYPE_F32 = 0, 1
 PART_GATE_UP, PART_DOWN = 1, 2
-KERNELS_FUSED, KERNELS_SEPARATE, KERNELS_COLUMNS, KERNELS_COLUMNS_AHEAD = 0, 1, 2, 3
+KERNELS_FUSED, KERNELS_SEPARATE, KERNELS_COLUMNS, KERNELS_COLUMNS_AHEAD, KERNELS_POOL = 0, 1, 2, 3, 4
 NOALLOC_MAX_ACT_FLOATS = 65536
 _STATUS = {0: "MOE_OK", -1: "MOE_ERR_INVALID_ARG", -2: "MOE_ERR_UNSUPPORTED", -3: "MOE_ERR_CUDA",
-           -4: "MOE_ERR_OOM", -5: "MOE_ERR_BAD_ID", -6: "MOE_ERR_TIMEOUT"}
+           -4: "MOE_ERR_OOM", -5: "MOE_ERR_BAD_ID", -6: "MOE_ERR_TIMEOUT",
+           -7: "MOE_ERR_PLAN"}
 
 EXPORTS = ["moe_decode_create", "moe_decode_forward", "moe_decode_get_error", "moe_decode_destroy",
+           "moe_decode_routes",
            "moe_decode_forward_noalloc",
            "moe_gemv_bf16",
            "moe_stack_create", "moe_stack_create_chained", "moe_stack_step",
@@ -64,6 +66,18 @@ class LayerWeights(ctypes.Structure):
 
 _lock = threading.Lock()
 _lib = None
+_timeline = False
+
+
+def use_timeline_build() -> None:
+    """Load libmoe_decode_timeline.so (the column-split kernel records per-CTA, per-layer time
+    stamps, read by MoeStack.timeline) instead of the product library.  Call before lib()."""
+    global LIB_PATH, _timeline
+    with _lock:
+        if _lib is not None:
+            raise RuntimeError("the library is already loaded")
+        LIB_PATH = os.path.join(_HERE, "libmoe_decode_timeline.so")
+        _timeline = True
 
 
 def lib() -> ctypes.CDLL:
@@ -81,6 +95,7 @@ def lib() -> ctypes.CDLL:
                                       ctypes.POINTER(vp)],
                 "moe_decode_forward": [vp, vp, i32, vp, vp, vp, vp, vp],
                 "moe_decode_get_error": [vp, ctypes.POINTER(i32)],
+                "moe_decode_routes": [vp, vp, vp, vp],
                 "moe_decode_destroy": [vp],
                 "moe_decode_forward_noalloc": [ctypes.POINTER(Config), ctypes.POINTER(LayerWeights),
                                                vp, i32, vp, vp, vp, vp, vp, vp],
@@ -107,6 +122,8 @@ def lib() -> ctypes.CDLL:
                 "moe_debug_col_pieces": [i32, i32, i32, i32, i32, i32, i32, i32, vp, i32],
                 "moe_debug_col_plan": [ctypes.POINTER(Config), i32, i32, vp],
             }
+            if _timeline:
+                sig["moe_stack_timeline"] = [vp, vp, i64, ctypes.POINTER(i32)]
             for name, args in sig.items():
                 f = getattr(L, name)
                 f.argtypes = args
@@ -244,6 +261,18 @@ class MoeDecode:
             self.handle, _p(x), m, _p(ids), _p(scores), _p(resid), _p(out), _stream(stream)))
         return out
 
+    def routes(self, m: int, slots: bool = False, stream=None):
+        """The ids the last forward's kernels read, int32 [m, top_k], and (pool mode, slots=True)
+        each slot's and shared expert's down output before its coefficient, fp32
+        [m, top_k + n_shared, din]; device tensors (moe_decode_routes)."""
+        sh = self.layer.shape
+        ids = torch.empty((m, max(sh.top_k, 1)), dtype=torch.int32, device="cuda")
+        y = (torch.empty((m, sh.top_k + sh.n_shared, sh.din), dtype=torch.float32, device="cuda")
+             if slots else None)
+        check("moe_decode_routes", lib().moe_decode_routes(self.handle, _p(ids), _p(y),
+                                                           _stream(stream)))
+        return (ids[:, :sh.top_k], y) if slots else ids[:, :sh.top_k]
+
     def get_error(self) -> int:
         v = ctypes.c_int32()
         check("moe_decode_get_error", lib().moe_decode_get_error(self.handle, ctypes.byref(v)))
@@ -329,6 +358,16 @@ class MoeStack:
         v = ctypes.c_int32()
         check("moe_stack_get_error", lib().moe_stack_get_error(self.handle, ctypes.byref(v)))
         return v.value
+
+    def timeline(self) -> np.ndarray:
+        """Timeline build only: the column-split kernel's stamps of the last step,
+        uint64 [grid, L, points] (see moe_timeline.cuh)."""
+        P = 64  # kTlPoints
+        buf = np.zeros(512 * len(self.layers) * P, np.uint64)
+        g = ctypes.c_int32()
+        check("moe_stack_timeline", lib().moe_stack_timeline(
+            self.handle, buf.ctypes.data, buf.nbytes, ctypes.byref(g)))
+        return buf[:g.value * len(self.layers) * P].reshape(g.value, len(self.layers), P)
 
     def close(self):
         if self.handle:

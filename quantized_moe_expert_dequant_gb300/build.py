@@ -20,6 +20,9 @@ CSRC = os.path.join(PKG, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(ROOT, "_build")
 LIB = os.path.join(PKG, "libmoe_decode.so")
+# The timeline build: the same sources with MOE_TIMELINE defined, so that the column-split kernel
+# records per-CTA, per-layer time stamps (moe_timeline.cuh) readable through moe_stack_timeline.
+LIB_TIMELINE = os.path.join(PKG, "libmoe_decode_timeline.so")
 SOURCES = ["moe_kernels_g4.cu", "moe_kernels_g6.cu", "moe_kernels_g8.cu", "moe_grouped_g4.cu",
            "moe_grouped_g6.cu", "moe_grouped_g8.cu", "moe_cols_g4.cu", "moe_cols_g6.cu",
            "moe_cols_g8.cu", "moe_kernels.cu",
@@ -38,10 +41,13 @@ def cuda_lib_dir() -> str:
     return os.path.join(os.path.dirname(os.path.dirname(os.path.realpath(nvcc()))), "lib64")
 
 
-def _compile(src: str, verbose: bool) -> str:
-    obj = os.path.join(BUILD, os.path.splitext(src)[0] + ".o")
+def _compile(src: str, verbose: bool, timeline: bool = False) -> str:
+    out_dir = os.path.join(BUILD, "timeline") if timeline else BUILD
+    obj = os.path.join(out_dir, os.path.splitext(src)[0] + ".o")
     cmd = [nvcc(), "-c", os.path.join(CSRC, src), "-o", obj, "-O3", "-lineinfo", "-std=c++17",
            "-Xcompiler", "-fPIC", "-I", INCLUDE, "-I", CSRC] + ARCH
+    if timeline:
+        cmd.append("-DMOE_TIMELINE")
     if verbose:
         cmd.append("-Xptxas=-v")
     r = subprocess.run(cmd, capture_output=True, text=True)
@@ -52,30 +58,32 @@ def _compile(src: str, verbose: bool) -> str:
     return obj
 
 
-def _stale() -> bool:
-    if not os.path.exists(LIB):
+def _stale(lib: str = LIB) -> bool:
+    if not os.path.exists(lib):
         return True
-    t = os.path.getmtime(LIB)
+    t = os.path.getmtime(lib)
     deps = [os.path.join(CSRC, f) for f in os.listdir(CSRC)] + [
         os.path.join(INCLUDE, f) for f in os.listdir(INCLUDE)] + [os.path.abspath(__file__)]
     return any(os.path.getmtime(d) > t for d in deps)
 
 
-def build(force: bool = False, verbose: bool = False) -> str:
-    if not force and not _stale():
-        return LIB
-    os.makedirs(BUILD, exist_ok=True)
+def build(force: bool = False, verbose: bool = False, timeline: bool = False) -> str:
+    lib = LIB_TIMELINE if timeline else LIB
+    if not force and not _stale(lib):
+        return lib
+    os.makedirs(os.path.join(BUILD, "timeline") if timeline else BUILD, exist_ok=True)
     with cf.ThreadPoolExecutor(max_workers=len(SOURCES)) as ex:
-        objs = list(ex.map(lambda s: _compile(s, verbose), SOURCES))
-    tmp = LIB + f".{os.getpid()}.tmp"
+        objs = list(ex.map(lambda s: _compile(s, verbose, timeline), SOURCES))
+    tmp = lib + f".{os.getpid()}.tmp"
     cmd = [nvcc(), "-shared", "-o", tmp] + objs + ARCH + [
         "-cudart", "shared", "-Xlinker", "-rpath=" + cuda_lib_dir()]
     r = subprocess.run(cmd, capture_output=True, text=True)
     if r.returncode != 0:
         raise RuntimeError(f"nvcc link failed:\n{r.stdout}\n{r.stderr}")
-    os.replace(tmp, LIB)
-    return LIB
+    os.replace(tmp, lib)
+    return lib
 
 
 if __name__ == "__main__":
-    print(build(force="--force" in sys.argv, verbose="-v" in sys.argv))
+    print(build(force="--force" in sys.argv, verbose="-v" in sys.argv,
+                timeline="--timeline" in sys.argv))

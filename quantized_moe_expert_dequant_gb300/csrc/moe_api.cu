@@ -8,6 +8,7 @@
 
 #include "moe_decode.h"
 #include "moe_kernels.cuh"
+#include "moe_timeline.cuh"
 
 namespace {
 
@@ -41,7 +42,7 @@ int validate_config(const moe_decode_config *c) {
     return MOE_ERR_INVALID_ARG;
   if (c->out_dtype != MOE_DTYPE_BF16 && c->out_dtype != MOE_DTYPE_F32) return MOE_ERR_INVALID_ARG;
   if (c->kernel_mode != MOE_KERNELS_FUSED && c->kernel_mode != MOE_KERNELS_SEPARATE &&
-      !cols_mode(c->kernel_mode))
+      c->kernel_mode != MOE_KERNELS_POOL && !cols_mode(c->kernel_mode))
     return MOE_ERR_INVALID_ARG;
   // int32 indexing of the activation vector and of one expert's rows
   const int64_t act = (int64_t)c->top_k * c->dff + (int64_t)c->n_shared * c->dff_shared;
@@ -119,15 +120,19 @@ int prepare(const moe_decode_config *c, Prepared &P) {
   }
   if (P.plan.smem > (size_t)dyn_limit) return MOE_ERR_UNSUPPORTED;
   // Batches of tokens run grouped by expert when the shape allows it; otherwise token by token.
-  P.grouped_ok = c->max_tokens > 1 && c->kernel_mode == MOE_KERNELS_FUSED &&
+  // The pool mode always runs the grouped kernel (a plan for at least two tokens also serves one).
+  const bool pool = c->kernel_mode == MOE_KERNELS_POOL;
+  P.grouped_ok = ((c->max_tokens > 1 && c->kernel_mode == MOE_KERNELS_FUSED) || pool) &&
                  moe::make_group_plan(P.shape, c->bits_gate, c->bits_down, P.bits_sh,
-                                      c->max_tokens, &P.gplan) &&
+                                      c->max_tokens > 1 ? c->max_tokens : 2, &P.gplan) &&
                  P.gplan.smem <= (size_t)dyn_limit;
+  if (pool && !P.grouped_ok) return MOE_ERR_UNSUPPORTED;
   P.grid_sep = sms;
   const int lim = moe::fused_grid_limit(P.plan, c->bits_gate, c->bits_down, P.bits_sh);
   P.grid_fused = lim < sms ? lim : sms;
-  if (c->kernel_mode == MOE_KERNELS_FUSED && P.grid_fused < 1) return MOE_ERR_UNSUPPORTED;
-  const int grid = c->kernel_mode == MOE_KERNELS_FUSED ? P.grid_fused : P.grid_sep;
+  const bool fused_grid = c->kernel_mode == MOE_KERNELS_FUSED || pool;
+  if (fused_grid && P.grid_fused < 1) return MOE_ERR_UNSUPPORTED;
+  const int grid = fused_grid ? P.grid_fused : P.grid_sep;
   if ((c->din + grid - 1) / grid > moe::kMaxRowsB) return MOE_ERR_UNSUPPORTED;
   if (cols_mode(c->kernel_mode)) {
     if (c->max_tokens != 1) return MOE_ERR_UNSUPPORTED;
@@ -167,7 +172,7 @@ cudaError_t enqueue_separate(const Prepared &P, const moe::LayerPtrs &w, float *
                              int32_t *err, const void *x, int m, const int32_t *ids,
                              const float *scores, const void *resid, int resid_dtype, void *out,
                              int out_dtype, cudaStream_t stream, int parts,
-                             const NormIn &norm = NormIn{}) {
+                             const NormIn &norm = NormIn{}, int32_t *ids_used = nullptr) {
   const moe_decode_config &c = P.cfg;
   for (int t = 0; t < m; ++t) {
     const int32_t *it = ids ? ids + (size_t)t * c.top_k : nullptr;
@@ -183,6 +188,7 @@ cudaError_t enqueue_separate(const Prepared &P, const moe::LayerPtrs &w, float *
     a.scores = scores ? scores + (size_t)t * c.top_k : nullptr;
     a.act = act;
     a.err = err;
+    a.ids_used = ids_used ? ids_used + (size_t)t * c.top_k : nullptr;
     cudaError_t e = cudaSuccess;
     if (parts & MOE_PART_GATE_UP) e = moe::launch_gate_up(a, P.grid_sep, stream, true);
     if (e != cudaSuccess) return e;
@@ -209,7 +215,7 @@ cudaError_t enqueue_fused(const Prepared &P, const moe::LayerPtrs *layers, int L
                           const void *x, int m, const int32_t *ids, const float *scores,
                           const void *resid0, int resid_dtype, void *out, int out_dtype,
                           cudaStream_t stream, const uint16_t *norm_w = nullptr,
-                          float norm_eps = 0.f) {
+                          float norm_eps = 0.f, int32_t *ids_used = nullptr) {
   cudaError_t e = cudaMemsetAsync(bar, 0, sizeof(uint32_t), stream);
   if (e != cudaSuccess) return e;
   moe::StackParams p;
@@ -232,7 +238,10 @@ cudaError_t enqueue_fused(const Prepared &P, const moe::LayerPtrs *layers, int L
   p.act = act;
   p.err = err;
   p.bar = bar;
-  p.grouped = m > 1 && P.grouped_ok && norm_w == nullptr;  // the grouped path reads x only
+  p.pool = P.cfg.kernel_mode == MOE_KERNELS_POOL;
+  // the grouped path reads x only; the pool mode is always grouped
+  p.grouped = (m > 1 && P.grouped_ok && norm_w == nullptr) || p.pool;
+  p.ids_used = ids_used;
   p.gp = P.gplan;
   p.y = y;
   p.act_stride = static_cast<int>(act_floats(P.cfg));
@@ -245,7 +254,7 @@ int read_and_clear_error(int32_t *err, int32_t *out) {
   int32_t v = 0;
   if (cudaMemcpy(&v, err, sizeof v, cudaMemcpyDeviceToHost) != cudaSuccess) return MOE_ERR_CUDA;
   if (cudaMemset(err, 0, sizeof v) != cudaSuccess) return MOE_ERR_CUDA;
-  *out = (v & 2) ? MOE_ERR_TIMEOUT : (v & 1) ? MOE_ERR_BAD_ID : MOE_OK;
+  *out = (v & 4) ? MOE_ERR_PLAN : (v & 2) ? MOE_ERR_TIMEOUT : (v & 1) ? MOE_ERR_BAD_ID : MOE_OK;
   return MOE_OK;
 }
 
@@ -254,7 +263,8 @@ cudaError_t enqueue_cols(const Prepared &P, const moe::LayerPtrs *layers,
                          const moe::ColPtrs *cols, int L, float *slab, int32_t *err,
                          uint32_t *bar, const void *x, const int32_t *ids, const float *scores,
                          const void *resid0, int resid_dtype, void *out, int out_dtype,
-                         cudaStream_t stream) {
+                         cudaStream_t stream, unsigned long long *tl = nullptr,
+                         int32_t *ids_used = nullptr) {
   cudaError_t e = cudaMemsetAsync(bar, 0, sizeof(uint32_t), stream);
   if (e != cudaSuccess) return e;
   moe::StackParams p;
@@ -277,6 +287,8 @@ cudaError_t enqueue_cols(const Prepared &P, const moe::LayerPtrs *layers,
   p.cp = P.cplan;
   p.slab = slab;
   p.ahead = P.cfg.kernel_mode == MOE_KERNELS_COLUMNS_AHEAD;
+  p.tl = tl;
+  p.ids_used = ids_used;
   return moe::launch_cols(p, P.grid_cols, stream);
 }
 
@@ -302,6 +314,19 @@ struct ColWeights {
                                    static_cast<uint32_t *>(c), static_cast<__half2 *>(b),
                                    nullptr) == cudaSuccess;
   }
+  bool records(int experts, int rows, int din, int bits, const moe_proj &g, const moe_proj &u,
+               const uint8_t **out) {
+    void *b = nullptr;
+    const size_t bytes = (size_t)experts * rows * moe::col_record_bytes(din, bits);
+    if (cudaMalloc(&b, bytes) != cudaSuccess) return false;
+    bufs.push_back(b);
+    *out = static_cast<const uint8_t *>(b);
+    return moe::launch_repack_gate_up(
+               static_cast<const uint8_t *>(g.codes), static_cast<const __half *>(g.scales),
+               static_cast<const __half *>(g.biases), static_cast<const uint8_t *>(u.codes),
+               static_cast<const __half *>(u.scales), static_cast<const __half *>(u.biases),
+               experts, rows, din, bits, static_cast<uint8_t *>(b), nullptr) == cudaSuccess;
+  }
   // MOE_OK, MOE_ERR_OOM or MOE_ERR_CUDA.
   int build(const moe_decode_config &c, const moe_layer_weights *w, int L) {
     // the caller's weights may still be written by work on other streams
@@ -316,6 +341,16 @@ struct ColWeights {
       }
       if (c.n_shared > 0 &&
           !repack(c.n_shared, c.din, c.dff_shared, c.bits_shared, w[l].sh_down, &cp.s)) {
+        cudaGetLastError();
+        return MOE_ERR_OOM;
+      }
+      if (c.top_k > 0 &&
+          !records(c.n_experts, c.dff, c.din, c.bits_gate, w[l].gate, w[l].up, &cp.gu_r)) {
+        cudaGetLastError();
+        return MOE_ERR_OOM;
+      }
+      if (c.n_shared > 0 && !records(c.n_shared, c.dff_shared, c.din, c.bits_shared, w[l].sh_gate,
+                                     w[l].sh_up, &cp.gu_s)) {
         cudaGetLastError();
         return MOE_ERR_OOM;
       }
@@ -341,7 +376,7 @@ struct ColWeights {
 
 size_t slab_floats(const Prepared &P) {
   return cols_mode(P.cfg.kernel_mode)
-             ? (size_t)2 * P.grid_cols * P.grid_cols * P.cplan.ro
+             ? (size_t)2 * P.grid_cols * P.cfg.din
              : 0;
 }
 
@@ -352,7 +387,8 @@ struct Workspace {
   int32_t *err = nullptr;
   uint32_t *bar = nullptr;
   moe::LayerPtrs *layers = nullptr;
-  float *slab = nullptr;  // column-split mode: [2][grid][grid][rows per owner] partial outputs
+  float *slab = nullptr;  // column-split mode: [2][grid][din] partial outputs
+  int32_t *ids_used = nullptr;  // handles: [max_tokens][top_k] ids the last forward's kernels read
 
   // Grouped forwards keep every token's activations and per-slot partial outputs at once.
   bool alloc(const moe_decode_config &c, int n_layers, bool grouped, size_t nslab = 0) {
@@ -364,7 +400,9 @@ struct Workspace {
               cudaMemset(err, 0, sizeof(int32_t)) == cudaSuccess &&
               cudaMalloc(&bar, sizeof(uint32_t)) == cudaSuccess &&
               cudaMalloc(&layers, sizeof(moe::LayerPtrs) * n_layers) == cudaSuccess &&
-              (nslab == 0 || cudaMalloc(&slab, nslab * sizeof(float)) == cudaSuccess);
+              (nslab == 0 || cudaMalloc(&slab, nslab * sizeof(float)) == cudaSuccess) &&
+              cudaMalloc(&ids_used, (size_t)c.max_tokens * (c.top_k > 0 ? c.top_k : 1) *
+                                        sizeof(int32_t)) == cudaSuccess;
     if (!ok) cudaGetLastError();
     return ok;
   }
@@ -375,6 +413,7 @@ struct Workspace {
     cudaFree(bar);
     cudaFree(layers);
     cudaFree(slab);
+    cudaFree(ids_used);
   }
 };
 
@@ -386,6 +425,7 @@ struct moe_decode {
   moe::LayerPtrs w;
   Workspace ws;
   ColWeights cw;
+  int last_m = 0;  // tokens of the last forward (moe_decode_routes)
 };
 
 extern "C" int moe_decode_create(const moe_decode_config *cfg, const moe_layer_weights *weights,
@@ -441,17 +481,41 @@ extern "C" int moe_decode_forward(moe_decode_t *h, const void *x, int32_t m, con
   if (x == out) return MOE_ERR_INVALID_ARG;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   cudaError_t e;
+  int32_t *used = c.top_k > 0 ? h->ws.ids_used : nullptr;
   if (cols_mode(c.kernel_mode))
     e = enqueue_cols(h->P, h->ws.layers, h->cw.dev, 1, h->ws.slab, h->ws.err, h->ws.bar, x, ids,
-                     scores, resid, c.resid_dtype, out, c.out_dtype, st);
-  else if (c.kernel_mode == MOE_KERNELS_FUSED)
+                     scores, resid, c.resid_dtype, out, c.out_dtype, st, nullptr, used);
+  else if (c.kernel_mode == MOE_KERNELS_FUSED || c.kernel_mode == MOE_KERNELS_POOL)
     e = enqueue_fused(h->P, h->ws.layers, 1, h->ws.act, h->ws.y, h->ws.err, h->ws.bar, nullptr,
-                      nullptr, x, m, ids, scores, resid, c.resid_dtype, out, c.out_dtype, st);
+                      nullptr, x, m, ids, scores, resid, c.resid_dtype, out, c.out_dtype, st,
+                      nullptr, 0.f, used);
   else
     e = enqueue_separate(h->P, h->w, h->ws.act, h->ws.err, x, m, ids, scores, resid,
                          c.resid_dtype, out, c.out_dtype, st,
-                         MOE_PART_GATE_UP | MOE_PART_DOWN);
+                         MOE_PART_GATE_UP | MOE_PART_DOWN, NormIn{}, used);
+  if (e == cudaSuccess) h->last_m = m;
   return e == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
+}
+
+extern "C" int moe_decode_routes(moe_decode_t *h, int32_t *ids_used, void *slot_out,
+                                 void *stream) {
+  if (!h || (!ids_used && !slot_out)) return MOE_ERR_INVALID_ARG;
+  const moe_decode_config &c = h->P.cfg;
+  if (h->last_m < 1) return MOE_ERR_INVALID_ARG;  // no forward yet
+  if (slot_out && c.kernel_mode != MOE_KERNELS_POOL) return MOE_ERR_UNSUPPORTED;
+  if ((ids_used && !aligned(ids_used, 4)) || (slot_out && !aligned(slot_out, 4)))
+    return MOE_ERR_INVALID_ARG;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  const size_t m = h->last_m;
+  if (ids_used && c.top_k > 0 &&
+      cudaMemcpyAsync(ids_used, h->ws.ids_used, m * c.top_k * sizeof(int32_t),
+                      cudaMemcpyDeviceToDevice, st) != cudaSuccess)
+    return MOE_ERR_CUDA;
+  if (slot_out &&
+      cudaMemcpyAsync(slot_out, h->ws.y, m * (c.top_k + c.n_shared) * c.din * sizeof(float),
+                      cudaMemcpyDeviceToDevice, st) != cudaSuccess)
+    return MOE_ERR_CUDA;
+  return MOE_OK;
 }
 
 extern "C" int moe_decode_get_error(moe_decode_t *h, int32_t *device_error) {
@@ -592,6 +656,7 @@ struct moe_stack {
   void *x_dev = nullptr, *resid_dev = nullptr;
   int32_t *ids_dev = nullptr;
   float *scores_dev = nullptr, *out_dev = nullptr;
+  unsigned long long *tl = nullptr;  // timeline builds: the column-split kernel's time stamps
 };
 
 extern "C" void moe_stack_destroy(moe_stack_t *s) {
@@ -607,6 +672,7 @@ extern "C" void moe_stack_destroy(moe_stack_t *s) {
   cudaFree(s->ids_dev);
   cudaFree(s->scores_dev);
   cudaFree(s->out_dev);
+  cudaFree(s->tl);
   delete s;
 }
 
@@ -665,6 +731,13 @@ int stack_create(const moe_decode_config *cfg, int32_t n_layers, const moe_layer
       moe_stack_destroy(s);
       return rc;
     }
+#ifdef MOE_TIMELINE
+    const size_t n_tl = (size_t)s->P.grid_cols * n_layers * moe::kTlPoints;
+    if (cudaMalloc(&s->tl, n_tl * 8) != cudaSuccess || cudaMemset(s->tl, 0, n_tl * 8) != cudaSuccess) {
+      moe_stack_destroy(s);
+      return MOE_ERR_OOM;
+    }
+#endif
   }
   *out = s;
   return MOE_OK;
@@ -694,7 +767,7 @@ cudaError_t enqueue_stack(moe_stack *s, const void *x, int m, const int32_t *ids
   const moe_decode_config &c = s->P.cfg;
   if (cols_mode(c.kernel_mode))
     return enqueue_cols(s->P, s->ws.layers, s->cw.dev, L, s->ws.slab, s->ws.err, s->ws.bar, x, ids,
-                        scores, resid0, c.resid_dtype, out, MOE_DTYPE_F32, st);
+                        scores, resid0, c.resid_dtype, out, MOE_DTYPE_F32, st, s->tl);
   if (c.kernel_mode == MOE_KERNELS_FUSED && parts == (MOE_PART_GATE_UP | MOE_PART_DOWN))
     return enqueue_fused(s->P, s->ws.layers, L, s->ws.act, s->ws.y, s->ws.err, s->ws.bar,
                          s->ping[0], s->ping[1], x, m, ids, scores, resid0, c.resid_dtype, out,
@@ -814,6 +887,19 @@ extern "C" int moe_stack_step_host(moe_stack_t *s, const void *x_host, int32_t m
     return MOE_ERR_CUDA;
   return MOE_OK;
 }
+
+#ifdef MOE_TIMELINE
+extern "C" int moe_stack_timeline(moe_stack_t *s, void *host, int64_t bytes, int32_t *grid) {
+  if (!s || !host || !grid) return MOE_ERR_INVALID_ARG;
+  if (!s->tl) return MOE_ERR_UNSUPPORTED;
+  const size_t need = (size_t)s->P.grid_cols * s->layers.size() * moe::kTlPoints * 8;
+  if (bytes < (int64_t)need) return MOE_ERR_INVALID_ARG;
+  *grid = s->P.grid_cols;
+  if (cudaDeviceSynchronize() != cudaSuccess) return MOE_ERR_CUDA;
+  return cudaMemcpy(host, s->tl, need, cudaMemcpyDeviceToHost) == cudaSuccess ? MOE_OK
+                                                                               : MOE_ERR_CUDA;
+}
+#endif
 
 extern "C" int moe_stack_get_error(moe_stack_t *s, int32_t *device_error) {
   if (!s) return MOE_ERR_INVALID_ARG;

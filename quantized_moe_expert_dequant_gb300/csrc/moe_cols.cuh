@@ -6,23 +6,28 @@
 //   out    = resid + sum_u W_down[:, u] * act[u]
 // Kernel A and kernel B split that work by ROWS of each projection, so every CTA of kernel B needs
 // every activation and the two phases meet at a device-wide exchange.  Here every CTA owns a
-// contiguous, balanced range of the activation index u instead (the same balanced split phase A
-// uses) and carries its columns through both projections:
-//   1. phase A on the CTA's gate/up rows (the rows u of its range), activations kept in shared
-//      memory;
+// contiguous, balanced range of the activation index u instead and carries its columns through
+// both projections:
+//   1. gate/up: the CTA's rows u, one warp per (gate row, up row) pair of a stage, each lane owning
+//      one group of 64 codes of the row (so its integer sums run over a whole group and one scale
+//      and bias apply to them); the activations stay in shared memory;
 //   2. the matching COLUMNS u of the down projections, read from a column-block-major copy
 //      (moe_kernels.cuh), multiplied by the local activations into a partial output for all din
-//      rows, written to a slab in global memory;
-//   3. one grid barrier;
-//   4. at the start of the next layer (or after the last one) each CTA sums, in a fixed order, the
-//      partials of the din / grid rows it owns and adds the residual, which it keeps in shared
-//      memory from layer to layer.
-// The next layer's expert ids are read only after that barrier, when every CTA has finished the
-// layer (its output exists as the partials), so no weight of a layer is requested before the
-// previous layer is done.  With p.ahead (every layer's ids are inputs known before the step) the
-// producer instead starts layer l + 1 as soon as its own CTA's consumers have finished layer l's
-// gate/up phase (a CTA-local mbarrier), so the weight stream runs on across the layer boundary;
-// the arithmetic and its order are the same.
+//      rows, written to this CTA's vector of a slab in global memory;
+//   3. an arrival on a device-wide counter (the consumers do not wait for it: they go on to the
+//      next layer's x);
+//   4. a helper warp waits for the counter, sums in a fixed order the grid's partials of the rows
+//      this CTA owns and adds them to the running output it keeps in shared memory (and, after the
+//      last layer, writes the output).
+// The next layer's expert ids are read (by the producer warp) only after the counter shows that
+// every CTA has finished the layer (its output exists as the partials), so no weight of a layer is
+// requested before the previous layer is done.  With p.ahead (every layer's ids are inputs known
+// before the step) the producer instead starts layer l + 1 as soon as its own CTA's consumers have
+// finished layer l's gate/up phase (a CTA-local mbarrier); the arithmetic and its order are the
+// same.
+//
+// Warps: 16 consumer warps, one producer warp (the bulk-copy stream of moe_phases.cuh), one helper
+// warp (the owner's sums, the shared-expert scalar, the output).
 //
 // The down contraction over a CTA's columns uses integer dot products like the row kernels
 // (moe_common.cuh): within one (segment, group of 64) piece the activations become 23-bit fixed
@@ -34,17 +39,155 @@
 #pragma once
 
 #include "moe_fused.cuh"
+#include "moe_timeline.cuh"
 
 namespace moe {
 
+constexpr int kColHelperWarp = kConsumerWarps + kProducerWarps;
+constexpr int kColThreads = kThreads + 32;    // consumers, producer, helper
+constexpr int kColMaxWpr = 4;                 // warps per gate/up row pair (32 columns a lane)
+
+// ------------------------------------------------------------------ one lane's operand
+// The lane's 32 values of x (half a group of 64 of a gate/up row) with ONE exponent, in the form
+// its code width's dot product wants: dot() returns sum_c q_c * v_c / unit, the exact integer sum
+// rounded once.  The two 16-byte chunks of an 8-bit lane are read in a rotated order (rot) so that
+// the 8 lanes of a shared-memory wavefront hit distinct banks; the operand holds its chunks in the
+// same order.
+template <int BITS>
+struct LaneOp;
+
+template <>
+struct LaneOp<8> {
+  static constexpr int VEC = 2;  // uint4 chunks per lane and row
+  uint32_t pl[8], pm[8], ph[8];
+  float unit, sum;
+  __device__ __forceinline__ static int rot(int lane) { return (lane >> 2) & 1; }
+  __device__ __forceinline__ void set(const float (&v)[32]) {
+    float mx = 0.f, sm = 0.f;
+#pragma unroll
+    for (int c = 0; c < 32; ++c) {
+      mx = fmaxf(mx, fabsf(v[c]));
+      sm += v[c];
+    }
+    const int E = fixed_exponent(mx);
+    const float sc = pow2f(22 - E);
+    unit = pow2f(E - 22);
+    sum = sm;
+#pragma unroll
+    for (int j = 0; j < 8; ++j)
+      byte_planes(__float2int_rn(v[4 * j] * sc), __float2int_rn(v[4 * j + 1] * sc),
+                  __float2int_rn(v[4 * j + 2] * sc), __float2int_rn(v[4 * j + 3] * sc), pl[j],
+                  pm[j], ph[j]);
+  }
+  __device__ __forceinline__ float dot(const uint4 (&c)[VEC]) const {
+    uint32_t l = 0, m = 0;
+    int h = 0;
+#pragma unroll
+    for (int k = 0; k < VEC; ++k) {
+      const uint32_t w[4] = {c[k].x, c[k].y, c[k].z, c[k].w};
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        l = dp4a_uu(w[i], pl[4 * k + i], l);
+        m = dp4a_uu(w[i], pm[4 * k + i], m);
+        h = dp4a_us(w[i], ph[4 * k + i], h);
+      }
+    }
+    // l, m <= 32 * 255 * 255 < 2^21, so m * 256 + l < 2^30; |h| <= 32 * 255 * 64
+    return fmaf(static_cast<float>(h), 65536.f, static_cast<float>(m * 256u + l));
+  }
+};
+
+template <>
+struct LaneOp<4> {
+  static constexpr int VEC = 1;
+  uint32_t el[4], em[4], eh[4];  // even columns of word j (low nibbles)
+  uint32_t ol[4], om[4], oh[4];  // odd columns of word j (high nibbles, read as 16 q)
+  float unit, sum;
+  __device__ __forceinline__ static int rot(int) { return 0; }  // 16-B lanes: no conflict
+  __device__ __forceinline__ void set(const float (&v)[32]) {
+    float mx = 0.f, sm = 0.f;
+#pragma unroll
+    for (int c = 0; c < 32; ++c) {
+      mx = fmaxf(mx, fabsf(v[c]));
+      sm += v[c];
+    }
+    const int E = fixed_exponent(mx);
+    const float sc = pow2f(22 - E);
+    unit = pow2f(E - 26);  // the dot below is 16 * sum q f
+    sum = sm;
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      byte_planes(__float2int_rn(v[8 * j] * sc), __float2int_rn(v[8 * j + 2] * sc),
+                  __float2int_rn(v[8 * j + 4] * sc), __float2int_rn(v[8 * j + 6] * sc), el[j],
+                  em[j], eh[j]);
+      byte_planes(__float2int_rn(v[8 * j + 1] * sc), __float2int_rn(v[8 * j + 3] * sc),
+                  __float2int_rn(v[8 * j + 5] * sc), __float2int_rn(v[8 * j + 7] * sc), ol[j],
+                  om[j], oh[j]);
+    }
+  }
+  __device__ __forceinline__ float dot(const uint4 (&c)[VEC]) const {
+    const uint32_t w[4] = {c[0].x, c[0].y, c[0].z, c[0].w};
+    uint32_t l0 = 0, m0 = 0, l1 = 0, m1 = 0;
+    int h0 = 0, h1 = 0;
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const uint32_t lo = w[j] & 0x0f0f0f0fu, hi = w[j] & 0xf0f0f0f0u;
+      l0 = dp4a_uu(lo, el[j], l0);
+      m0 = dp4a_uu(lo, em[j], m0);
+      h0 = dp4a_us(lo, eh[j], h0);
+      l1 = dp4a_uu(hi, ol[j], l1);
+      m1 = dp4a_uu(hi, om[j], m1);
+      h1 = dp4a_us(hi, oh[j], h1);
+    }
+    // 16 * sum q f: the even sums scaled by 16 join the odd ones (read as 16 q already);
+    // l, m <= 16 * 15 * 255 * 16 + 16 * 240 * 255 < 2^21, so m * 256 + l < 2^30
+    const uint32_t l = l0 * 16u + l1, m = m0 * 16u + m1;
+    const int h = h0 * 16 + h1;
+    return fmaf(static_cast<float>(h), 65536.f, static_cast<float>(m * 256u + l));
+  }
+};
+
+// The lane's x operand: columns [32 k, 32 k + 32) of x (k = the lane's slot of the row), chunks
+// in the lane's rotated order; zeros for a lane past the row.
+template <int BITS>
+__device__ __forceinline__ void load_lane_x(LaneOp<BITS> &op, const uint16_t *x, int k,
+                                            bool active, int lane) {
+  constexpr int VEC = LaneOp<BITS>::VEC;
+  constexpr int CPC = 32 / VEC;  // columns per chunk
+  const int rt = LaneOp<BITS>::rot(lane);
+  float v[32];
+#pragma unroll
+  for (int j = 0; j < VEC; ++j) {
+    const int src = 32 * k + CPC * ((j + rt) % VEC);  // chunk j holds chunk j + rot
+#pragma unroll
+    for (int q = 0; q < CPC / 8; ++q) {
+      const uint4 w = active ? *reinterpret_cast<const uint4 *>(x + src + 8 * q)
+                             : make_uint4(0, 0, 0, 0);
+      const uint32_t ww[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+      for (int h = 0; h < 4; ++h) {
+        v[CPC * j + 8 * q + 2 * h] = __uint_as_float(ww[h] << 16);
+        v[CPC * j + 8 * q + 2 * h + 1] = __uint_as_float(ww[h] & 0xffff0000u);
+      }
+    }
+  }
+  op.set(v);
+}
+
+// ------------------------------------------------------------------ shared state
 struct ColSmem {
-  float act[kMaxColsCta];                 // the CTA's activations, index u - u0
+  float act[kMaxColsCta];                 // silu(gate) * up of the CTA's columns, index u - u0
+  float2 red[kMaxColsCta][kColMaxWpr];    // (gate, up) sums of each column from each of the
+                                          // warps that share its row pair
   uint32_t planes[kMaxColBlocks * 8];     // per block: byte planes (3 words at 8 bits, 6 at 4)
   float2 us[kMaxColPieces];               // per piece: (unit, sum of its activations)
   ColPiece pc[kMaxColPieces];
   float resid[kMaxOwnRows];               // the owned rows' running output (the next residual)
+  float s_gate[2];                        // the shared-expert scalar of layers of each parity
+  short ck_seg[kMaxColChunks], ck_j[kMaxColChunks], ck_n[kMaxColChunks], ck_u[kMaxColChunks];
+  int nck, nck_r;                         // the CTA's gate/up chunks (col_chunks), routed first
   int np, nbk;
-  int u0;
+  int u0, ncols;
 };
 
 __device__ __forceinline__ bool col_valid(const LayerShape &s, const ColPiece &q, const int *ids,
@@ -58,11 +201,148 @@ __device__ __forceinline__ bool col_valid(const LayerShape &s, const ColPiece &q
   return e >= 0 && e < s.n_experts;
 }
 
-// Producer: the down column blocks of every valid piece, at most cp.nbs blocks per stage; the
-// last stage of a piece also carries the piece's group of (scale, bias) pairs for all din rows.
-__device__ inline void produce_down_cols(const LayerShape &s, const ColPlan &cp, const ColPtrs &cw,
-                                  const ColSmem &cs, const int *ids, Ring &r, int lane,
-                                  uint64_t pol) {
+// Named barrier 3: the consumer warps and the helper warp, once per layer (the helper's shared
+// scalar is ready and its reads of the older slab pass are done).
+__device__ __forceinline__ void consumers_helper_sync() {
+  asm volatile("bar.sync 3, %0;" ::"n"(kConsumers + 32) : "memory");
+}
+
+// ------------------------------------------------------------------ gate/up
+// The stages of one class (routed slots or shared experts) of the CTA's gate/up rows.  A stage
+// holds up to R (gate row, up row) records (see ColPtrs); each pair is taken by wpr warps, each
+// lane of them owning 32 columns of both rows (columns 32 (32 h + lane) ...), so R * wpr warps
+// work on a stage, by turns when they are fewer than 16: with A = 16 / (R * wpr) warp sets, stage
+// i of the phase goes to set i mod A.  Every warp waits for and releases every stage.
+// The warp's (gate, up) sums go to red[u - u0][h]; the caller forms the activations.
+template <int BITS>
+__device__ int cols_a_class(const LayerShape &s, const GateUpGeom &g, int count, int i0,
+                            const LaneOp<BITS> &xo, ColSmem &cs, Ring &r, bool &waited,
+                            bool &ok, int warp, int lane) {
+  constexpr int VEC = LaneOp<BITS>::VEC;
+  const int nk = s.din >> 5;                     // 32-column slots of a row
+  const int wpr = (nk + 31) >> 5;
+  const int per = g.R * wpr;                     // warps working on one stage
+  const int A = kConsumerWarps / per;
+  const int slot = warp % per, turn = warp / per;
+  const int p = slot / wpr, h = slot - p * wpr;
+  const int k = 32 * h + lane;                   // the lane's 32-column slot of the row
+  const bool lane_on = k < nk;
+  const int rt = LaneOp<BITS>::rot(lane);
+  const int lane_off = k * (4 * BITS);           // the lane's bytes inside a row
+  const int rbc = s.din * BITS / 8;              // code bytes of a row
+  const int G = s.din / kGroup;
+  int i = i0;
+  for (int c = 0; c < count; ++c, ++i) {
+    if (!waited) {
+      if (warp == 0 && lane == 0) MOE_TL_STAGE_WAIT(r.used);
+      ok = warp_wait_full(r, lane);
+    }
+    waited = false;
+    if (warp == 0 && lane == 0) MOE_TL_STAGE_C(r.used);
+    const StageDesc d = r.desc[r.st];
+    const bool mine = ok && turn < A && (A == 1 || (i % A) == turn) && p < d.n;
+    if (mine) {  // warp-uniform
+      float gv = 0.f, uv = 0.f;
+      if (lane_on) {
+        const uint8_t *rec = r.stage() + p * g.rb;   // the pair's record
+        const uint8_t *rg = rec + lane_off;
+        const uint8_t *ws = rec + 2 * rbc + (k >> 1) * 2;
+        uint4 cv[VEC];
+#pragma unroll
+        for (int j = 0; j < VEC; ++j) cv[j] = lds_u4(rg + 16 * ((j + rt) % VEC));
+        gv = fmaf(lds_half(ws), xo.dot(cv) * xo.unit, lds_half(ws + 2 * G) * xo.sum);
+#pragma unroll
+        for (int j = 0; j < VEC; ++j) cv[j] = lds_u4(rg + rbc + 16 * ((j + rt) % VEC));
+        uv = fmaf(lds_half(ws + 4 * G), xo.dot(cv) * xo.unit, lds_half(ws + 6 * G) * xo.sum);
+      }
+      warp_release(r, lane);
+      gv = warp_sum(gv);
+      uv = warp_sum(uv);
+      if (lane == 0) cs.red[d.u + p - cs.u0][h] = make_float2(gv, uv);
+    } else {
+      warp_release(r, lane);
+    }
+  }
+  return i;
+}
+
+// Gate/up of one layer for the CTA's columns: x operands (built while the first stage is in
+// flight), then the stages of both classes.  The first stage publishes the per-class stage
+// counts (an empty stage when the CTA has no valid rows).
+template <int BR, int BSH>
+__device__ void cols_phase_a(const LayerShape &s, const GateUpGeom &gr, const GateUpGeom &gs,
+                             const uint16_t *x, const int *cnt, ColSmem &cs, Ring &r, int warp,
+                             int lane) {
+  const int nk = s.din >> 5, wpr = (nk + 31) >> 5;
+  const int kr = 32 * ((warp % (gr.R * wpr)) % wpr) + lane;
+  LaneOp<BR> xr;
+  load_lane_x<BR>(xr, x, kr, kr < nk, lane);
+  if (warp == 0 && lane == 0) {
+    MOE_TL_HOOK(7);
+    MOE_TL_STAGE_WAIT(r.used);
+  }
+  bool ok = warp_wait_full(r, lane), waited = true;
+  if (warp == 0 && lane == 0) MOE_TL_HOOK(8);
+  const int nr = cnt[0], ns = cnt[1];
+  if (nr + ns == 0) {  // an empty stage
+    warp_release(r, lane);
+    return;
+  }
+  int i = cols_a_class<BR>(s, gr, nr, 0, xr, cs, r, waited, ok, warp, lane);
+  if (ns > 0) {
+    const int ks = 32 * ((warp % (gs.R * wpr)) % wpr) + lane;
+    LaneOp<BSH> xs;
+    load_lane_x<BSH>(xs, x, ks, ks < nk, lane);
+    cols_a_class<BSH>(s, gs, ns, i, xs, cs, r, waited, ok, warp, lane);
+  }
+}
+
+// ------------------------------------------------------------------ down
+// ------------------------------------------------------------------ the producer's layer
+// Lane 0 of the producer warp streams one layer, in the order the consumers take the stages: the
+// CTA's gate/up chunks (routed, then shared; one empty stage when it has none), each ONE bulk copy
+// of consecutive records (see ColPtrs), then the down column blocks of every valid piece (at most
+// cp.nbs blocks a stage; the last stage of a piece also carries the piece's (scale, bias) group
+// for all din rows).  false when a ring wait gave up.
+__device__ __forceinline__ bool ring_claim_lane(Ring &r) {
+  return r.used < r.nst || ring_wait(&r.empty[r.st], r.ph ^ 1u, r.abort, r.err);
+}
+
+template <int BR, int BSH>
+__device__ bool cols_produce_layer(const LayerShape &s, const Plan &plan, const ColPlan &cp,
+                                   const ColPtrs &cw, const ColSmem &cs, const int *ids,
+                                   const float *scores, int *cnt, Ring &r, uint64_t pol) {
+  int nr = 0;
+  for (int i = 0; i < cs.nck_r; ++i) {
+    const int e = ids[cs.ck_seg[i]];
+    nr += e >= 0 && e < s.n_experts;
+  }
+  const int ns = cs.nck - cs.nck_r;
+  cnt[0] = nr;
+  cnt[1] = ns;
+  for (int i = 0; i < cs.nck; ++i) {
+    const bool routed = i < cs.nck_r;
+    const int sg = cs.ck_seg[i];
+    const int e = routed ? ids[sg] : sg - s.top_k;
+    if (routed && (e < 0 || e >= s.n_experts)) continue;
+    if (!ring_claim_lane(r)) return false;
+    const GateUpGeom &g = routed ? plan.geo_r : plan.geo_s;
+    const uint8_t *recs = routed ? cw.gu_r : cw.gu_s;
+    const int rows_pe = routed ? s.dff : s.dff_shared;
+    const uint32_t bytes = static_cast<uint32_t>(cs.ck_n[i]) * g.rb;
+    r.desc[r.st] = StageDesc{cs.u0 + cs.ck_u[i], cs.ck_n[i], routed ? scores[sg] : 0.f, 0};
+    mbar_arrive_expect_tx(&r.full[r.st], bytes);
+    bulk_g2s(r.stage(), recs + (static_cast<int64_t>(e) * rows_pe + cs.ck_j[i]) * g.rb, bytes,
+             &r.full[r.st], pol);
+    MOE_TL_STAGE_P(r.used);
+    r.advance();
+  }
+  if (nr + ns == 0) {  // one empty stage, so the consumers always have a first stage to wait on
+    if (!ring_claim_lane(r)) return false;
+    r.desc[r.st] = StageDesc{0, 0, 0.f, 0};
+    mbar_arrive_expect_tx(&r.full[r.st], 0);
+    r.advance();
+  }
   const uint32_t blk_bytes = static_cast<uint32_t>(s.din) * 4u;
   for (int qi = 0; qi < cs.np; ++qi) {
     const ColPiece q = cs.pc[qi];
@@ -76,28 +356,29 @@ __device__ inline void produce_down_cols(const LayerShape &s, const ColPlan &cp,
     for (int bo = 0; bo < q.nb; bo += cp.nbs) {
       const int nk = (q.nb - bo) < cp.nbs ? (q.nb - bo) : cp.nbs;
       const bool ends = bo + nk == q.nb;
-      if (!ring_claim(r, lane)) return;
-      uint8_t *sb = r.stage();
+      if (!ring_claim_lane(r)) return false;
       const uint32_t code_bytes = static_cast<uint32_t>(nk) * blk_bytes;
-      if (lane == 0) mbar_arrive_expect_tx(&r.full[r.st], code_bytes + (ends ? blk_bytes : 0u));
-      __syncwarp();
-      if (lane == 0)
-        bulk_g2s(sb,
-                 d.codes + (static_cast<int64_t>(e) * nblk + q.blk0 + bo) * s.din,
-                 code_bytes, &r.full[r.st], pol);
-      if (lane == 1 && ends)
-        bulk_g2s(sb + code_bytes, d.sb + (static_cast<int64_t>(e) * G + q.grp) * s.din, blk_bytes,
-                 &r.full[r.st], pol);
+      uint8_t *sb = r.stage();
+      mbar_arrive_expect_tx(&r.full[r.st], code_bytes + (ends ? blk_bytes : 0u));
+      bulk_g2s(sb, d.codes + (static_cast<int64_t>(e) * nblk + q.blk0 + bo) * s.din, code_bytes,
+               &r.full[r.st], pol);
+      if (ends)
+        bulk_g2s(sb + code_bytes, d.sb + (static_cast<int64_t>(e) * G + q.grp) * s.din,
+                 blk_bytes, &r.full[r.st], pol);
+      MOE_TL_STAGE_P(r.used);
       r.advance();
     }
   }
+  return true;
 }
 
-// Consumers: byte planes of every block of every valid piece, from the local activations.
+// Consumers: byte planes of every block of every valid piece, from the local activations times
+// the piece's coefficient (the routed slot's score, or the shared scalar).
 // Warp w handles pieces w, w + 16, ...; lane b the piece's block b.
 template <int BD, int BSD>
-__device__ inline void col_planes(const LayerShape &s, const ColPlan &cp, ColSmem &cs, const int *ids,
-                           int warp, int lane) {
+__device__ inline void col_planes(const LayerShape &s, const ColPlan &cp, ColSmem &cs,
+                                  const int *ids, const float *scores, float shared_coef,
+                                  int warp, int lane) {
   for (int qi = warp; qi < cs.np; qi += kConsumerWarps) {
     const ColPiece q = cs.pc[qi];
     int e;
@@ -105,9 +386,10 @@ __device__ inline void col_planes(const LayerShape &s, const ColPlan &cp, ColSme
     const bool routed = q.seg < s.top_k;
     const int bits = routed ? BD : BSD;
     const int cb = routed ? cp.cb_r : cp.cb_s;
+    const float coef = routed ? scores[q.seg] : shared_coef;
     const int n = q.j1 - q.j0;  // at most 64
-    const float v0 = lane < n ? cs.act[q.a0 + lane] : 0.f;
-    const float v1 = lane + 32 < n ? cs.act[q.a0 + lane + 32] : 0.f;
+    const float v0 = lane < n ? coef * cs.act[q.a0 + lane] : 0.f;
+    const float v1 = lane + 32 < n ? coef * cs.act[q.a0 + lane + 32] : 0.f;
     const float mx = warp_max(fmaxf(fabsf(v0), fabsf(v1)));
     const float sm = warp_sum(v0 + v1);
     const int E = fixed_exponent(mx);
@@ -119,8 +401,9 @@ __device__ inline void col_planes(const LayerShape &s, const ColPlan &cp, ColSme
 #pragma unroll
       for (int k = 0; k < 8; ++k) {
         const int c = c0 + k;
-        f[k] = (k < cb && c >= q.j0 && c < q.j1) ? __float2int_rn(cs.act[q.a0 + c - q.j0] * sc)
-                                                 : 0;
+        f[k] = (k < cb && c >= q.j0 && c < q.j1)
+                   ? __float2int_rn(coef * cs.act[q.a0 + c - q.j0] * sc)
+                   : 0;
       }
       uint32_t *pl = cs.planes + (q.pb + b) * 8;
       if (bits == 8) {
@@ -137,8 +420,9 @@ __device__ inline void col_planes(const LayerShape &s, const ColPlan &cp, ColSme
 }
 
 // Consumers: the stages of one piece.  Thread t owns the row quads t and (QPT = 2) t + 512 (rows
-// 4 quad .. 4 quad + 3); its exact integer sums run over all of the piece's blocks, and the
-// piece's last stage applies the group's scale and bias to them into part[][].
+// 4 quad .. 4 quad + 3).  Within a stage its sums over the stage's blocks are exact integers (one
+// quad at a time); they join a per-row fp32 sum at the stage's end, and the piece's last stage
+// applies the group's scale and bias to those sums into part[][].
 template <int BITS, int QPT>
 __device__ __forceinline__ void consume_piece(const ColPiece &q, float2 us, const ColPlan &cp,
                                               int din, const uint32_t *planes, Ring &r,
@@ -146,48 +430,66 @@ __device__ __forceinline__ void consume_piece(const ColPiece &q, float2 us, cons
   constexpr int NPL = BITS == 8 ? 3 : 6;
   const int nquads = din >> 2;
   const uint32_t blk_bytes = static_cast<uint32_t>(din) * 4u;
-  uint32_t al[QPT][4][NPL];  // l and m planes (unsigned) and h planes (two's complement) per row
+  float dsum[QPT][4];
 #pragma unroll
   for (int a = 0; a < QPT; ++a)
 #pragma unroll
-    for (int k = 0; k < 4; ++k)
-#pragma unroll
-      for (int z = 0; z < NPL; ++z) al[a][k][z] = 0u;
+    for (int k = 0; k < 4; ++k) dsum[a][k] = 0.f;
   for (int bo = 0; bo < q.nb; bo += cp.nbs) {
     const int nk = (q.nb - bo) < cp.nbs ? (q.nb - bo) : cp.nbs;
     const bool ends = bo + nk == q.nb;
+    if (tid == 0) MOE_TL_STAGE_WAIT(r.used);
     const bool ok = warp_wait_full(r, lane);
+    if (tid == 0) MOE_TL_STAGE_C(r.used);
     const uint8_t *sb = r.stage();
     if (ok) {
-      for (int b = 0; b < nk; ++b) {
-        const uint4 pa = *reinterpret_cast<const uint4 *>(planes + (q.pb + bo + b) * 8);
-        const uint4 pb = *reinterpret_cast<const uint4 *>(planes + (q.pb + bo + b) * 8 + 4);
-        const uint8_t *cp_b = sb + static_cast<uint32_t>(b) * blk_bytes;
 #pragma unroll
-        for (int a = 0; a < QPT; ++a) {
-          const int quad = tid + a * kConsumers;
-          if (quad < nquads) {
-            const uint4 w4 = lds_u4(cp_b + quad * 16);
+      for (int a = 0; a < QPT; ++a) {
+        const int quad = tid + a * kConsumers;
+        if (quad < nquads) {
+          uint32_t al[4][NPL];  // l and m planes (unsigned) and h planes (two's complement)
+#pragma unroll
+          for (int k = 0; k < 4; ++k)
+#pragma unroll
+            for (int z = 0; z < NPL; ++z) al[k][z] = 0u;
+          for (int b = 0; b < nk; ++b) {
+            const uint4 pa = *reinterpret_cast<const uint4 *>(planes + (q.pb + bo + b) * 8);
+            const uint4 pb = *reinterpret_cast<const uint4 *>(planes + (q.pb + bo + b) * 8 + 4);
+            const uint4 w4 = lds_u4(sb + static_cast<uint32_t>(b) * blk_bytes + quad * 16);
             const uint32_t w[4] = {w4.x, w4.y, w4.z, w4.w};
 #pragma unroll
             for (int k = 0; k < 4; ++k) {
               if constexpr (BITS == 8) {
-                al[a][k][0] = dp4a_uu(w[k], pa.x, al[a][k][0]);
-                al[a][k][1] = dp4a_uu(w[k], pa.y, al[a][k][1]);
-                al[a][k][2] = static_cast<uint32_t>(
-                    dp4a_us(w[k], pa.z, static_cast<int>(al[a][k][2])));
+                al[k][0] = dp4a_uu(w[k], pa.x, al[k][0]);
+                al[k][1] = dp4a_uu(w[k], pa.y, al[k][1]);
+                al[k][2] = static_cast<uint32_t>(dp4a_us(w[k], pa.z, static_cast<int>(al[k][2])));
               } else {
                 const uint32_t lo = w[k] & 0x0f0f0f0fu, hi = w[k] & 0xf0f0f0f0u;
-                al[a][k][0] = dp4a_uu(lo, pa.x, al[a][k][0]);
-                al[a][k][1] = dp4a_uu(lo, pa.y, al[a][k][1]);
-                al[a][k][2] = static_cast<uint32_t>(
-                    dp4a_us(lo, pa.z, static_cast<int>(al[a][k][2])));
-                al[a][k][3] = dp4a_uu(hi, pa.w, al[a][k][3]);
-                al[a][k][4] = dp4a_uu(hi, pb.x, al[a][k][4]);
-                al[a][k][5] = static_cast<uint32_t>(
-                    dp4a_us(hi, pb.y, static_cast<int>(al[a][k][5])));
+                al[k][0] = dp4a_uu(lo, pa.x, al[k][0]);
+                al[k][1] = dp4a_uu(lo, pa.y, al[k][1]);
+                al[k][2] = static_cast<uint32_t>(dp4a_us(lo, pa.z, static_cast<int>(al[k][2])));
+                al[k][3] = dp4a_uu(hi, pa.w, al[k][3]);
+                al[k][4] = dp4a_uu(hi, pb.x, al[k][4]);
+                al[k][5] = static_cast<uint32_t>(dp4a_us(hi, pb.y, static_cast<int>(al[k][5])));
               }
             }
+          }
+#pragma unroll
+          for (int k = 0; k < 4; ++k) {
+            uint32_t l, m;
+            int h;
+            if constexpr (BITS == 8) {
+              l = al[k][0];
+              m = al[k][1];
+              h = static_cast<int>(al[k][2]);
+            } else {
+              // the even sums scaled by 16 join the odd ones (read as 16 q)
+              l = al[k][0] * 16u + al[k][3];
+              m = al[k][1] * 16u + al[k][4];
+              h = static_cast<int>(al[k][2]) * 16 + static_cast<int>(al[k][5]);
+            }
+            // l, m < 2^22 over at most a group of 64 columns, so m * 256 + l < 2^31
+            dsum[a][k] += fmaf(static_cast<float>(h), 65536.f, static_cast<float>(m * 256u + l));
           }
         }
       }
@@ -201,23 +503,9 @@ __device__ __forceinline__ void consume_piece(const ColPiece &q, float2 us, cons
             const uint32_t hw[4] = {h4.x, h4.y, h4.z, h4.w};
 #pragma unroll
             for (int k = 0; k < 4; ++k) {
-              uint32_t l, m;
-              int h;
-              if constexpr (BITS == 8) {
-                l = al[a][k][0];
-                m = al[a][k][1];
-                h = static_cast<int>(al[a][k][2]);
-              } else {
-                // the even sums scaled by 16 join the odd ones (read as 16 q)
-                l = al[a][k][0] * 16u + al[a][k][3];
-                m = al[a][k][1] * 16u + al[a][k][4];
-                h = static_cast<int>(al[a][k][2]) * 16 + static_cast<int>(al[a][k][5]);
-              }
-              // l, m < 2^22 over a group of 64 columns, so m * 256 + l < 2^31
-              const float dot = fmaf(static_cast<float>(h), 65536.f, static_cast<float>(m * 256u + l));
               const __half2 sbh = *reinterpret_cast<const __half2 *>(&hw[k]);
               const float sc = __low2float(sbh), bi = __high2float(sbh);
-              part[a][k] += fmaf(sc, dot * us.x, bi * us.y);
+              part[a][k] += fmaf(sc, dsum[a][k] * us.x, bi * us.y);
             }
           }
         }
@@ -227,40 +515,124 @@ __device__ __forceinline__ void consume_piece(const ColPiece &q, float2 us, cons
   }
 }
 
-// The owner's rows [i0, i1) of the partials of one pass: fixed-order sums over the grid's CTAs,
-// added to the running output in shared memory; `out` (when set) receives the result.
-__device__ __forceinline__ void col_reduce(const float *slab, int din, int ro, ColSmem &cs,
-                                           void *out, int out_f32, int warp, int lane) {
-  const int n = gridDim.x, c = blockIdx.x;
-  const int i0 = static_cast<int>(static_cast<int64_t>(din) * c / n);
-  const int i1 = static_cast<int>(static_cast<int64_t>(din) * (c + 1) / n);
-  const float *blk = slab + static_cast<int64_t>(c) * n * ro;
-  for (int rr = warp; rr < i1 - i0; rr += kConsumerWarps) {
-    float t = 0.f;
-    for (int cc = lane; cc < n; cc += 32) t += __ldcg(blk + static_cast<int64_t>(cc) * ro + rr);
-    t = warp_sum(t);
-    if (lane == 0) {
-      const float o = cs.resid[rr] + t;
-      cs.resid[rr] = o;
-      if (out != nullptr) {
-        if (out_f32)
-          static_cast<float *>(out)[i0 + rr] = o;
-        else
-          static_cast<uint16_t *>(out)[i0 + rr] = float_to_bf16_rn(o);
+// ------------------------------------------------------------------ the owner's sums
+// CTA c owns the output rows of the row quads [nq c / n, nq (c + 1) / n), nq = din / 4.
+__device__ __forceinline__ void col_owned_quads(int din, int c, int n, int *q0, int *q1) {
+  const int nq = din >> 2;
+  *q0 = static_cast<int>(static_cast<int64_t>(nq) * c / n);
+  *q1 = static_cast<int>(static_cast<int64_t>(nq) * (c + 1) / n);
+}
+
+// Helper warp: the owned rows of one pass of the slab ([grid][din] partial vectors), summed over
+// the grid's CTAs in a fixed order (lane l takes CTAs l, l + 32, ... in order, then a butterfly
+// over the lanes), added to the running output; `out` (when set) receives the result.  Loads are
+// issued for two quads at a time so that their L2 round trips overlap.
+__device__ __forceinline__ void col_reduce(const float *slab, int din, ColSmem &cs, void *out,
+                                           int out_f32, int lane) {
+  const int n = gridDim.x;
+  int q0, q1;
+  col_owned_quads(din, blockIdx.x, n, &q0, &q1);
+  for (int qa = q0; qa < q1; qa += 2) {
+    float4 acc[2];
+#pragma unroll
+    for (int j = 0; j < 2; ++j) {
+      acc[j] = make_float4(0.f, 0.f, 0.f, 0.f);
+      const int quad = qa + j;
+      float4 v[kColMaxGrid / 32];
+#pragma unroll
+      for (int k = 0; k < kColMaxGrid / 32; ++k) {
+        const int cc = lane + 32 * k;
+        v[k] = (quad < q1 && cc < n)
+                   ? __ldcg(reinterpret_cast<const float4 *>(slab + static_cast<int64_t>(cc) * din) +
+                            quad)
+                   : make_float4(0.f, 0.f, 0.f, 0.f);
+      }
+#pragma unroll
+      for (int k = 0; k < kColMaxGrid / 32; ++k) {
+        acc[j].x += v[k].x;
+        acc[j].y += v[k].y;
+        acc[j].z += v[k].z;
+        acc[j].w += v[k].w;
+      }
+    }
+#pragma unroll
+    for (int j = 0; j < 2; ++j) {
+      const int quad = qa + j;
+      const float t[4] = {warp_sum(acc[j].x), warp_sum(acc[j].y), warp_sum(acc[j].z),
+                          warp_sum(acc[j].w)};
+      if (lane == 0 && quad < q1) {
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          const int rr = 4 * (quad - q0) + k;
+          const float o = cs.resid[rr] + t[k];
+          cs.resid[rr] = o;
+          if (out != nullptr) {
+            const int i = 4 * quad + k;
+            if (out_f32)
+              static_cast<float *>(out)[i] = o;
+            else
+              static_cast<uint16_t *>(out)[i] = float_to_bf16_rn(o);
+          }
+        }
       }
     }
   }
 }
 
+// Helper warp for layers [0, L): the layer-0 residual, then per layer l the owner's sums of
+// layer l - 1 (once every CTA has arrived), the shared scalar of layer l, and a meeting with the
+// consumers; after the last layer, the output.
+__device__ inline void cols_helper(const StackParams &p, ColSmem &cs, int *abort, int lane) {
+  const LayerShape &s = p.s;
+  const int n = gridDim.x;
+  int q0, q1;
+  col_owned_quads(s.din, blockIdx.x, n, &q0, &q1);
+  for (int t = lane; t < 4 * (q1 - q0); t += 32) {
+    const int i = 4 * q0 + t;
+    cs.resid[t] = p.resid0_f32 ? static_cast<const float *>(p.resid0)[i]
+                               : bf16_to_float(static_cast<const uint16_t *>(p.resid0)[i]);
+  }
+  const int64_t slab_pass = static_cast<int64_t>(n) * s.din;
+  for (int l = 0; l < p.L; ++l) {
+    [[maybe_unused]] unsigned long long *tlr = lane == 0 ? MOE_TL_ROW(p.tl, p.L, l) : nullptr;
+    if (l > 0) {
+      int ok = 1;
+      if (lane == 0) ok = wait_count(p.bar, static_cast<uint32_t>(l) * n, abort, p.err);
+      MOE_TL_AT(tlr, 52);
+      MOE_TL_AT(tlr, 58);
+      ok = __shfl_sync(0xffffffffu, ok, 0);
+      if (ok) col_reduce(p.slab + ((l - 1) & 1) * slab_pass, s.din, cs, nullptr, 1, lane);
+    }
+    const LayerPtrs &w = p.layers[l];
+    if (s.n_shared > 0) {
+      float scalar = 1.f;
+      if (w.gate_vec != nullptr) {
+        const uint16_t *x = p.x + static_cast<int64_t>(l) * s.din;
+        float dot = 0.f;
+        for (int c = lane; c < s.din; c += 32)
+          dot = fmaf(bf16_to_float(x[c]), bf16_to_float(w.gate_vec[c]), dot);
+        dot = warp_sum(dot);
+        scalar = 1.0f / (1.0f + expf(-dot));
+      }
+      if (lane == 0) cs.s_gate[l & 1] = scalar;
+    }
+    MOE_TL_AT(tlr, 15);
+    consumers_helper_sync();
+  }
+  int ok = 1;
+  if (lane == 0) ok = wait_count(p.bar, static_cast<uint32_t>(p.L) * n, abort, p.err);
+  ok = __shfl_sync(0xffffffffu, ok, 0);
+  if (ok) col_reduce(p.slab + ((p.L - 1) & 1) * slab_pass, s.din, cs, p.out, p.out_f32, lane);
+}
+
+// ------------------------------------------------------------------ the kernel
 // One token per layer (m = 1), layers [0, L): see the top of this file.
 template <int BR, int BD, int BSH>
-__global__ void __launch_bounds__(kThreads, 1) cols_kernel(const StackParams p) {
+__global__ void __launch_bounds__(kColThreads, 1) cols_kernel(const StackParams p) {
   extern __shared__ __align__(128) uint8_t ring[];
   __shared__ __align__(16) RingSmem rs;
-  __shared__ SmemA sma;
   __shared__ __align__(16) ColSmem cs;
-  __shared__ LayerPtrs wl;   // the consumers' copy of the current layer's pointers
-  __shared__ LayerPtrs wpr;  // the producers' copy
+  __shared__ LayerPtrs wpr;  // the producers' copy of the current layer's pointers
   __shared__ ColPtrs cpr;
   __shared__ int stop_pr;
   // the expert ids and scores of layers l and l + 1 (the producer may be a layer ahead)
@@ -275,25 +647,45 @@ __global__ void __launch_bounds__(kThreads, 1) cols_kernel(const StackParams p) 
   if (tid == 0) {
     mbar_init(&a_done, 1);
     int nbk = 0;
-    int64_t u0 = 0;
+    int64_t u0 = 0, u1 = 0;
     cs.np = col_pieces(s.top_k, s.dff, s.n_shared, s.dff_shared, p.cp.cb_r, p.cp.cb_s,
                        blockIdx.x, n, cs.pc, &nbk, &u0);
+    col_range(static_cast<int64_t>(s.top_k) * s.dff + static_cast<int64_t>(s.n_shared) * s.dff_shared,
+              blockIdx.x, n, &u0, &u1);
     cs.nbk = nbk;
     cs.u0 = static_cast<int>(u0);
+    cs.ncols = static_cast<int>(u1 - u0);
     if (cs.np < 0) {  // outside the plan (the host checks every CTA): do nothing
       cs.np = 0;
-      atomicOr(p.err, kDevErrTimeout);
+      atomicOr(p.err, kDevErrPlan);
+      rs.abort = 1;
+    }
+    cs.s_gate[0] = cs.s_gate[1] = 1.f;
+    int nck_r = 0;
+    cs.nck = col_chunks(s.top_k, s.dff, s.n_shared, s.dff_shared, p.plan.geo_r.R,
+                        p.plan.geo_s.R, blockIdx.x, n, cs.ck_seg, cs.ck_j, cs.ck_n, cs.ck_u,
+                        &nck_r);
+    cs.nck_r = nck_r;
+    if (cs.nck < 0) {  // outside the plan (the host checks every CTA): do nothing
+      cs.nck = cs.nck_r = 0;
+      atomicOr(p.err, kDevErrPlan);
       rs.abort = 1;
     }
   }
   __syncthreads();
   Ring r = make_ring(rs.full, rs.empty, ring, rs.desc, p.plan, &rs.abort, p.err);
 
+  if (warp == kColHelperWarp) {
+    cols_helper(p, cs, &rs.abort, lane);
+    return;
+  }
   if (warp >= kConsumerWarps) {
     const uint64_t pol = policy_evict_first();
     const int pl = tid - kConsumers;
     for (int l = 0; l < p.L; ++l) {
       producer_sync();  // every producer is done with the previous layer's copies
+      [[maybe_unused]] unsigned long long *tlr = pl == 0 ? MOE_TL_ROW(p.tl, p.L, l) : nullptr;
+      MOE_TL_AT(tlr, 0);
       if (pl == 0) {
         wpr = p.layers[l];
         cpr = p.cols[l];
@@ -304,6 +696,8 @@ __global__ void __launch_bounds__(kThreads, 1) cols_kernel(const StackParams p) 
           else          // every CTA has finished the previous layer before its ids are read
             wait_count(p.bar, static_cast<uint32_t>(l) * n, &rs.abort, p.err);
         }
+        MOE_TL_AT(tlr, 1);
+        MOE_TL_AT(tlr, 59);
         stop_pr = flag_abort(&rs.abort);
       }
       producer_sync();
@@ -311,38 +705,59 @@ __global__ void __launch_bounds__(kThreads, 1) cols_kernel(const StackParams p) 
       const int64_t ks = s.top_k;
       int *ids_l = ids2[l & 1];
       float *sc_l = sc2[l & 1];
-      producer_load_token(s, p.ids + l * ks, p.scores + l * ks, ids_l, sc_l, p.err, pl);
-      produce_a<BR, BSH>(s, wpr, p.plan.geo_r, p.plan.geo_s, ids_l, sc_l, rs.cnt, r, pl, pol);
-      produce_down_cols(s, p.cp, cpr, cs, ids_l, r, pl, pol);
+      producer_load_token(s, p.ids + l * ks, p.scores + l * ks, ids_l, sc_l, p.err, pl,
+                          p.ids_used ? p.ids_used + l * ks : nullptr);
+      MOE_TL_AT(tlr, 2);
+      if (pl == 0) {
+        MOE_TL_SET_HOOK_P(tlr);
+        MOE_TL_STAGE_BASE_P(r.used);
+        cols_produce_layer<BR, BSH>(s, p.plan, p.cp, cpr, cs, ids_l, sc_l, rs.cnt, r, pol);
+      }
+      __syncwarp();
+      MOE_TL_AT(tlr, 4);
     }
     ring_drain(r, pl);
     return;
   }
 
-  // the owned rows' residual (layer 0's input)
-  {
-    const int i0 = static_cast<int>(static_cast<int64_t>(s.din) * blockIdx.x / n);
-    const int i1 = static_cast<int>(static_cast<int64_t>(s.din) * (blockIdx.x + 1) / n);
-    for (int t = tid; t < i1 - i0; t += kConsumers)
-      cs.resid[t] = p.resid0_f32 ? static_cast<const float *>(p.resid0)[i0 + t]
-                                 : bf16_to_float(static_cast<const uint16_t *>(p.resid0)[i0 + t]);
-  }
-  const int64_t slab_pass = static_cast<int64_t>(n) * n * p.cp.ro;
+  // consumers
+  const int64_t slab_pass = static_cast<int64_t>(n) * s.din;
   const int nquads = s.din >> 2;
+  const bool two = s.din > 4 * kConsumers;  // a second row quad per thread
   for (int l = 0; l < p.L; ++l) {
-    if (tid == 0) wl = p.layers[l];
-    consumer_sync(kConsumers);
-    // the previous layer's output rows this CTA owns (the barrier has passed)
-    if (l > 0) col_reduce(p.slab + ((l - 1) & 1) * slab_pass, s.din, p.cp.ro, cs, nullptr, 1,
-                          warp, lane);
-    consume_a<BR, BSH, false>(s, wl, p.plan.geo_r, p.plan.geo_s,
-                              xsource_plain(p.x + static_cast<int64_t>(l) * s.din), rs.cnt,
-                              cs.act, r, sma, tid, cs.u0);
-    consumer_sync(kConsumers);  // activations complete; the ids were published by phase A
+    [[maybe_unused]] unsigned long long *tlr = tid == 0 ? MOE_TL_ROW(p.tl, p.L, l) : nullptr;
+    MOE_TL_AT(tlr, 5);
+    MOE_TL_AT(tlr, 56);
+    if (tid == 0) {
+      MOE_TL_SET_HOOK(tlr);
+      MOE_TL_STAGE_BASE(r.used);
+    }
+    cols_phase_a<BR, BSH>(s, p.plan.geo_r, p.plan.geo_s, p.x + static_cast<int64_t>(l) * s.din,
+                          rs.cnt, cs, r, warp, lane);
+    MOE_TL_AT(tlr, 9);
+    consumer_sync(kConsumers);  // every (gate, up) sum written; the ids were published by the
+                                // phase's first stage
+    MOE_TL_AT(tlr, 10);
     if (tid == 0) mbar_arrive(&a_done);
     const int *ids_l = ids2[l & 1];
-    col_planes<BD, BSH>(s, p.cp, cs, ids_l, warp, lane);
+    {
+      const int wprow = ((s.din >> 5) + 31) >> 5;
+      for (int t = tid; t < cs.ncols; t += kConsumers) {
+        float2 a = cs.red[t][0];
+        for (int h = 1; h < wprow; ++h) {
+          const float2 b = cs.red[t][h];
+          a.x += b.x;
+          a.y += b.y;
+        }
+        cs.act[t] = silu_f(a.x) * a.y;
+      }
+    }
+    MOE_TL_AT(tlr, 3);
+    consumers_helper_sync();  // activations complete; the helper's shared scalar is ready
+    MOE_TL_AT(tlr, 6);
+    col_planes<BD, BSH>(s, p.cp, cs, ids_l, sc2[l & 1], cs.s_gate[l & 1], warp, lane);
     consumer_sync(kConsumers);
+    MOE_TL_AT(tlr, 11);
     float part[2][4];
 #pragma unroll
     for (int a = 0; a < 2; ++a)
@@ -352,7 +767,6 @@ __global__ void __launch_bounds__(kThreads, 1) cols_kernel(const StackParams p) 
       const ColPiece q = cs.pc[qi];
       int e;
       if (!col_valid(s, q, ids_l, &e)) continue;
-      const bool two = s.din > 4 * kConsumers;  // a second row quad per thread
       if (q.seg < s.top_k) {
         if (two)
           consume_piece<BD, 2>(q, cs.us[qi], p.cp, s.din, cs.planes, r, lane, tid, part);
@@ -365,25 +779,25 @@ __global__ void __launch_bounds__(kThreads, 1) cols_kernel(const StackParams p) 
           consume_piece<BSH, 1>(q, cs.us[qi], p.cp, s.din, cs.planes, r, lane, tid, part);
       }
     }
-    // partials of all din rows into the slab, grouped by the row's owner CTA
-    float *sl = p.slab + (l & 1) * slab_pass;
+    MOE_TL_AT(tlr, 12);
+    // this CTA's partial output of all din rows: one contiguous vector of the slab pass
+    float *sl = p.slab + (l & 1) * slab_pass + static_cast<int64_t>(blockIdx.x) * s.din;
 #pragma unroll
     for (int a = 0; a < 2; ++a) {
       const int quad = tid + a * kConsumers;
-      if (quad < nquads) {
-#pragma unroll
-        for (int k = 0; k < 4; ++k) {
-          const int i = 4 * quad + k;
-          const int o = static_cast<int>((static_cast<int64_t>(i + 1) * n - 1) / s.din);
-          const int rr = i - static_cast<int>(static_cast<int64_t>(s.din) * o / n);
-          sl[(static_cast<int64_t>(o) * n + blockIdx.x) * p.cp.ro + rr] = part[a][k];
-        }
-      }
+      if (quad < nquads)
+        reinterpret_cast<float4 *>(sl)[quad] =
+            make_float4(part[a][0], part[a][1], part[a][2], part[a][3]);
     }
-    consumers_grid_barrier(p.bar, static_cast<uint32_t>(l + 1) * n, tid, &rs.abort, p.err);
+    MOE_TL_AT(tlr, 13);
+    consumer_sync(kConsumers);
+    // bar.sync orders the CTA's partials before this thread's release, which is cumulative; the
+    // consumers do not wait: the producer and the helper wait for the count
+    if (tid == 0) red_release_add(p.bar, 1u);
+    MOE_TL_AT(tlr, 14);
+    MOE_TL_AT(tlr, 57);
   }
-  col_reduce(p.slab + ((p.L - 1) & 1) * slab_pass, s.din, p.cp.ro, cs, p.out, p.out_f32, warp,
-             lane);
+  if (tid == 0) MOE_TL_SET_HOOK(nullptr);
 }
 
 // Down code widths of the column-split kernels: 4 or 8 bits.
@@ -397,7 +811,8 @@ __global__ void __launch_bounds__(kThreads, 1) cols_kernel(const StackParams p) 
 template <int BR>
 cudaError_t launch_cols_family(const StackParams &p, int grid, cudaStream_t stream) {
   MOE_COLS_BITS(p.cp.cb_r == 8 ? 4 : 8, BD, MOE_COLS_BITS(p.cp.cb_s == 8 ? 4 : 8, BSH,
-      return launch(cols_kernel<BR, BD, BSH>, p, grid, p.plan.smem, stream, false, true)));
+      return launch(cols_kernel<BR, BD, BSH>, p, grid, p.plan.smem, stream, false, true,
+                    kColThreads)));
   return cudaErrorInvalidValue;
 }
 
@@ -415,8 +830,8 @@ cudaError_t cols_occupancy_family(int bits_d, int bits_sh, size_t smem, int *per
   cudaError_t e = cudaSuccess;
   int nb = 0;
   MOE_COLS_BITS(bits_d, BD, MOE_COLS_BITS(bits_sh, BSH,
-      e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&nb, cols_kernel<BR, BD, BSH>, kThreads,
-                                                        smem)));
+      e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&nb, cols_kernel<BR, BD, BSH>,
+                                                        kColThreads, smem)));
   *per_sm = nb;
   return e;
 }

@@ -24,6 +24,8 @@ namespace moe {
 
 __device__ __forceinline__ void init_ring(uint64_t *full, uint64_t *empty, int nst, int *abort) {
   if (threadIdx.x == 0) {
+    MOE_TL_SET_HOOK(nullptr);  // timeline builds: no phase stamps unless a kernel asks for them
+    MOE_TL_SET_HOOK_P(nullptr);
     for (int s = 0; s < nst; ++s) {
       mbar_init(&full[s], 1);  // the producer's arrive.expect_tx; the bulk copies complete it
       mbar_init(&empty[s], kConsumerWarps);
@@ -58,7 +60,7 @@ __global__ void __launch_bounds__(kThreads, 1) gate_up_kernel(const GateUpParams
   const int tid = threadIdx.x, warp = tid >> 5;
   if (warp >= kConsumerWarps) {
     const int pl = tid - kConsumers;
-    producer_load_token(p.s, p.ids, p.scores, rs.ids, rs.scores, p.err, pl);
+    producer_load_token(p.s, p.ids, p.scores, rs.ids, rs.scores, p.err, pl, p.ids_used);
     produce_a<BR, BS>(p.s, p.w, p.plan.geo_r, p.plan.geo_s, rs.ids, rs.scores, rs.cnt, r, pl,
                       policy_evict_first());
     ring_drain(r, pl);
@@ -141,7 +143,7 @@ __global__ void __launch_bounds__(kThreads, 1) fused_kernel(const StackParams p)
           if (stop_pr) break;
           const int64_t tok = static_cast<int64_t>(l) * p.m + t;
           producer_load_token(s, p.ids + tok * ks, p.scores + tok * ks, rs.ids, rs.scores, p.err,
-                              pl);
+                              pl, p.ids_used ? p.ids_used + tok * ks : nullptr);
           produce_a<BR, BSH>(s, wpr, p.plan.geo_r, p.plan.geo_s, rs.ids, rs.scores, rs.cnt, r, pl,
                              pol);
           produce_b(s, wpr, p.plan.geo_b, rs.ids, r, pl, pol);
@@ -193,10 +195,10 @@ __global__ void __launch_bounds__(kThreads, 1) fused_kernel(const StackParams p)
 
 template <typename Kern, typename P>
 inline cudaError_t launch(Kern kern, const P &p, int grid, size_t smem, cudaStream_t stream,
-                          bool pdl, bool cooperative) {
+                          bool pdl, bool cooperative, int threads = kThreads) {
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(grid);
-  cfg.blockDim = dim3(kThreads);
+  cfg.blockDim = dim3(threads);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = stream;
   cudaLaunchAttribute attr[2];

@@ -374,7 +374,7 @@ template <int BITS, bool GATED>
 __device__ int consume_g_class(const LayerShape &s, const GroupSmem &gs, const GClass &c,
                                const GateUpGeom &g, const GOut &go, int count, int op_off,
                                const float *scores_s, float *outp, Ring &r, SmemA &sm,
-                               bool &waited, bool &ok, int tid) {
+                               bool &waited, bool &ok, int tid, bool fold = true) {
   constexpr int VEC = Fmt<BITS>::kVecs, C = Operand<BITS>::C;
   constexpr int RPT = GATED ? rows_per_thread_a<BITS>() : rows_per_thread_gb<BITS>();
   constexpr int V = GATED ? 2 * RPT : RPT;
@@ -409,13 +409,13 @@ __device__ int consume_g_class(const LayerShape &s, const GroupSmem &gs, const G
       if (c.shared) {
         m = q;
         col = go.col_shared + d.e * go.col_sh;
-        coef = GATED ? gs.sscal[m] : 1.f;
+        coef = GATED && fold ? gs.sscal[m] : 1.f;
       } else {
         const int o = gs.rt.offs[d.e] + q;
         m = gs.pm[o];
         const int k = gs.pk[o];
         col = k * go.col_pe;
-        coef = GATED ? scores_s[m * s.top_k + k] : 1.f;
+        coef = GATED && fold ? scores_s[m * s.top_k + k] : 1.f;
       }
       if (held + d.n > cap) {
         flush_g(sm, held, wpg, GATED, outp, tid, true);
@@ -466,7 +466,7 @@ template <int BR, int BS, bool GATED>
 __device__ void consume_g_phase(const LayerShape &s, const GroupSmem &gs, const GClass *cls,
                                 const GateUpGeom &gr, const GateUpGeom &gsh, const GOut &go,
                                 const int *op_off, const float *scores_s, float *outp, Ring &r,
-                                SmemA &sm, int tid) {
+                                SmemA &sm, int tid, bool fold = true) {
   const int lane = tid & 31;
   bool ok = warp_wait_full(r, lane), waited = true;
   const int nr = gs.cnt[GATED ? 0 : 2], ns = gs.cnt[GATED ? 1 : 3];
@@ -475,17 +475,22 @@ __device__ void consume_g_phase(const LayerShape &s, const GroupSmem &gs, const 
     return;
   }
   int held = consume_g_class<BR, GATED>(s, gs, cls[0], gr, go, nr, op_off[0], scores_s, outp, r,
-                                        sm, waited, ok, tid);
+                                        sm, waited, ok, tid, fold);
   if (held > 0) flush_g(sm, held, gr.tpr / 32, GATED, outp, tid, ns > 0);
   held = consume_g_class<BS, GATED>(s, gs, cls[1], gsh, go, ns, op_off[1], scores_s, outp, r, sm,
-                                    waited, ok, tid);
+                                    waited, ok, tid, fold);
   if (held > 0) flush_g(sm, held, gsh.tpr / 32, GATED, outp, tid, false);
 }
 
 // Tail of a grouped layer for the CTA's output rows: out = resid + (routed + shared), routed
 // summed over the valid slots in slot order.  y and the residual are complete (grid barrier).
+// pool: y holds the slots' and shared experts' outputs without their coefficients, and the tail
+// is the one of "Red Lite dev39 -- fused expert tail" (Change) as written:
+//   out = resid + (sum_k score_k * y_k + scalar * sum_s y_s).
 __device__ inline void tail_g(const LayerShape &s, const int *ids_s, int m, const float *y, int y_stride,
-                       const void *resid, int resid_f32, void *out, int out_f32, int tid) {
+                       const void *resid, int resid_f32, void *out, int out_f32, int tid,
+                       bool pool = false, const float *scores_s = nullptr,
+                       const float *sscal = nullptr) {
   int i0, i1;
   range_b(s, i0, i1);
   const int rows = i1 - i0;
@@ -495,14 +500,18 @@ __device__ inline void tail_g(const LayerShape &s, const int *ids_s, int m, cons
     float routed = 0.f, shared = 0.f;
     for (int k = 0; k < s.top_k; ++k) {
       const int e = ids_s[tok * s.top_k + k];
-      if (e >= 0 && e < s.n_experts) routed += yt[static_cast<int64_t>(k) * s.din];
+      if (e >= 0 && e < s.n_experts) {
+        const float yk = yt[static_cast<int64_t>(k) * s.din];
+        routed = pool ? fmaf(scores_s[tok * s.top_k + k], yk, routed) : routed + yk;
+      }
     }
     for (int sh = 0; sh < s.n_shared; ++sh)
       shared += yt[static_cast<int64_t>(s.top_k + sh) * s.din];
     const int64_t o = static_cast<int64_t>(tok) * s.din + i;
     const float rs = resid_f32 ? static_cast<const float *>(resid)[o]
                                : bf16_to_float(static_cast<const uint16_t *>(resid)[o]);
-    const float v = rs + (routed + shared);
+    const float v = pool ? rs + (s.n_shared > 0 ? fmaf(sscal[tok], shared, routed) : routed)
+                         : rs + (routed + shared);
     if (out_f32)
       static_cast<float *>(out)[o] = v;
     else
@@ -578,6 +587,7 @@ __device__ void fused_grouped(const StackParams &p, uint8_t *dyn, uint64_t *full
         gs.ids[q] = e;
         gs.scores[q] = scores[q];
         if (e < 0 || e >= s.n_experts) atomicOr(p.err, kDevErrBadId);
+        if (p.ids_used != nullptr && blockIdx.x == 0) p.ids_used[static_cast<int64_t>(l) * P + q] = e;
       }
       producer_sync();
       route_invert_warp(gs.ids, P, s.n_experts, gs.rt, pl);
@@ -616,7 +626,7 @@ __device__ void fused_grouped(const StackParams &p, uint8_t *dyn, uint64_t *full
     group_classes(s, wl, 0, ca, cb);  // the consumers use no row bases
     const GOut goa{p.act_stride, K * s.dff, s.dff, s.n_shared > 0 ? s.dff_shared : s.dff};
     consume_g_phase<BR, BSH, true>(s, gs, ca, p.gp.ga_r, p.gp.ga_s, goa, p.gp.op_off, gs.scores,
-                                   p.act, r, sm, tid);
+                                   p.act, r, sm, tid, !p.pool);
     consumers_grid_barrier(p.bar, (3u * l + 1u) * n, tid, abort, p.err);
     const GOut gob{y_stride, K * s.din, s.din, s.din};
     consume_g_phase<BD, BSH, false>(s, gs, cb, p.gp.gb_r, p.gp.gb_s, gob, p.gp.op_off + 2,
@@ -640,7 +650,8 @@ __device__ void fused_grouped(const StackParams &p, uint8_t *dyn, uint64_t *full
       out = l & 1 ? p.ping1 : p.ping0;
       out_f32 = 1;
     }
-    tail_g(s, gs.ids, m, p.y, y_stride, resid, resid_f32, out, out_f32, tid);
+    tail_g(s, gs.ids, m, p.y, y_stride, resid, resid_f32, out, out_f32, tid, p.pool != 0,
+           gs.scores, gs.sscal);
     if (l < p.L - 1) consumers_grid_barrier(p.bar, (3u * l + 3u) * n, tid, abort, p.err);
   }
 }

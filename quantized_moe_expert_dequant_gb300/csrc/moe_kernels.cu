@@ -157,6 +157,37 @@ __global__ void repack_down_kernel(const uint32_t *codes, const __half *scales,
   }
 }
 
+// Gate/up records: one thread per 16-byte word of a record's codes, then one per fp16 of its
+// scale/bias runs (and the padding, zeroed).
+__global__ void repack_gate_up_kernel(const uint4 *g_codes, const __half *g_scales,
+                                      const __half *g_biases, const uint4 *u_codes,
+                                      const __half *u_scales, const __half *u_biases,
+                                      int64_t records, int rb16, int G, int rec, uint8_t *out) {
+  const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
+  const int64_t nc = records * 2 * rb16;
+  for (int64_t x = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; x < nc;
+       x += stride) {
+    const int64_t r = x / (2 * rb16);
+    const int w = static_cast<int>(x - r * 2 * rb16);
+    const uint4 v = w < rb16 ? g_codes[r * rb16 + w] : u_codes[r * rb16 + (w - rb16)];
+    reinterpret_cast<uint4 *>(out + r * rec)[w] = v;
+  }
+  const int tail = (rec - 32 * rb16) / 2;  // fp16 slots after the codes
+  const int64_t ns = records * tail;
+  for (int64_t x = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; x < ns;
+       x += stride) {
+    const int64_t r = x / tail;
+    const int k = static_cast<int>(x - r * tail);
+    const int run = k / G, g = k - run * G;
+    __half v = __float2half(0.f);
+    if (run < 4) {
+      const __half *src = run == 0 ? g_scales : run == 1 ? g_biases : run == 2 ? u_scales : u_biases;
+      v = src[r * G + g];
+    }
+    reinterpret_cast<__half *>(out + r * rec + 32 * rb16)[k] = v;
+  }
+}
+
 // ================================================================== host side
 static int fmt_codes(int bits) { return bits == 4 ? 32 : bits == 8 ? 16 : 64; }
 static int align_up(int v, int a) { return (v + a - 1) / a * a; }
@@ -226,7 +257,7 @@ bool make_plan(const LayerShape &s, int bits_gu, int bits_d, int bits_sh, Plan *
   if (s.top_k > 0 && stage_a(plan->geo_r) > st) st = stage_a(plan->geo_r);
   if (s.n_shared > 0 && stage_a(plan->geo_s) > st) st = stage_a(plan->geo_s);
   int n = kRingBytes / st;
-  if (n > kMaxStages) n = kMaxStages;
+  if (n > kMaxRowStages) n = kMaxRowStages;
   if (n < 2) return false;
   plan->nst = n;
   plan->stage_bytes = st;
@@ -269,7 +300,7 @@ bool make_group_plan(const LayerShape &s, int bits_gu, int bits_d, int bits_sh, 
     }
   }
   int n = ring_bytes / st;
-  if (n > kMaxStages) n = kMaxStages;
+  if (n > kMaxRowStages) n = kMaxRowStages;
   if (n < 2) return false;
   gp->t_sub = t;
   gp->nst = n;
@@ -278,20 +309,43 @@ bool make_group_plan(const LayerShape &s, int bits_gu, int bits_d, int bits_sh, 
   return true;
 }
 
+// Phase-A geometry of the column split: R (gate, up) row pairs per stage, about 32 KB of codes,
+// each pair taken by one warp per 1024 columns (a lane owns 32 columns of both rows).
+static bool geom_cols_a(int din, int bits, GateUpGeom *g) {
+  if (bits != 4 && bits != 8) return false;
+  const int nk = din / 32, wpr = (nk + 31) / 32;
+  if (din < 64 || wpr > 4) return false;
+  g->bits = bits;
+  g->rb = col_record_bytes(din, bits);   // a stage holds R records
+  int R = 1;
+  while ((R * 2) * 2 * (din * bits / 8) <= 32 * 1024 && R * 2 * wpr <= kConsumerWarps) R *= 2;
+  g->R = R;
+  g->T = nk;
+  g->tpr = 32 * wpr;
+  g->groups = kConsumerWarps / (R * wpr);
+  g->sw = 0;
+  return true;
+}
+
 bool make_col_plan(const LayerShape &s, int bits_gu, int bits_d, int bits_sh, int grid,
                    int ring_bytes, ColPlan *cp, Plan *plan) {
   const bool sh = s.n_shared > 0;
-  if (grid < 1 || (bits_d != 4 && bits_d != 8) || (sh && bits_sh != 4 && bits_sh != 8))
+  if (grid < 1 || grid > kColMaxGrid || (bits_d != 4 && bits_d != 8) ||
+      (sh && bits_sh != 4 && bits_sh != 8))
     return false;
-  if (s.din > 4 * 2 * kConsumers || s.din % 4) return false;  // two row quads per thread
-  if (!geom_a(s.din, bits_gu, &plan->geo_r) || !geom_a(s.din, bits_sh, &plan->geo_s))
+  if (s.din > 4 * 2 * kConsumers || s.din % 64) return false;  // two row quads per thread
+  if (s.dff > 32767 || s.dff_shared > 32767) return false;    // chunk rows are 16-bit
+  if (!geom_cols_a(s.din, bits_gu, &plan->geo_r) || !geom_cols_a(s.din, bits_sh, &plan->geo_s))
     return false;
   cp->cb_r = 32 / bits_d;
   cp->cb_s = sh ? 32 / bits_sh : cp->cb_r;
   const int blk = s.din * 4;  // one column block of all din rows
   int sa = 0;
-  if (s.top_k > 0) sa = stage_a(plan->geo_r);
-  if (sh && stage_a(plan->geo_s) > sa) sa = stage_a(plan->geo_s);
+  if (s.top_k > 0) sa = align_up(plan->geo_r.R * plan->geo_r.rb, 128);
+  if (sh && align_up(plan->geo_s.R * plan->geo_s.rb, 128) > sa)
+    sa = align_up(plan->geo_s.R * plan->geo_s.rb, 128);
+  cp->rec_r = plan->geo_r.rb;
+  cp->rec_s = plan->geo_s.rb;
   int nbs = sa / blk - 1;
   nbs = nbs < 1 ? 1 : (nbs > 16 ? 16 : nbs);
   int st = align_up((nbs + 1) * blk, 128);
@@ -300,7 +354,7 @@ bool make_col_plan(const LayerShape &s, int bits_gu, int bits_d, int bits_sh, in
   if (n > kMaxStages) n = kMaxStages;
   if (n < 2) return false;
   cp->nbs = nbs;
-  cp->ro = align_up((s.din + grid - 1) / grid, 4);
+  cp->ro = 4 * ((s.din / 4 + grid - 1) / grid);   // the owner's row quads
   if (cp->ro > kMaxOwnRows) return false;
   // every CTA's pieces within the kernel's limits
   const int64_t U = (int64_t)s.top_k * s.dff + (int64_t)s.n_shared * s.dff_shared;
@@ -311,6 +365,11 @@ bool make_col_plan(const LayerShape &s, int bits_gu, int bits_d, int bits_sh, in
     int64_t u0 = 0;
     if (col_pieces(s.top_k, s.dff, s.n_shared, s.dff_shared, cp->cb_r, cp->cb_s, c, grid, pc,
                    &nbk, &u0) < 0)
+      return false;
+    short sg[kMaxColChunks], jj[kMaxColChunks], nn[kMaxColChunks], uu[kMaxColChunks];
+    int nrt = 0;
+    if (col_chunks(s.top_k, s.dff, s.n_shared, s.dff_shared, plan->geo_r.R, plan->geo_s.R, c,
+                   grid, sg, jj, nn, uu, &nrt) < 0)
       return false;
   }
   std::memset(&plan->geo_b, 0, sizeof plan->geo_b);
@@ -431,6 +490,23 @@ int cols_grid_limit(size_t smem, int bits_gu, int bits_d, int bits_sh) {
   return per_sm * sms;
 }
 #undef MOE_FAMILY_CALL
+
+cudaError_t launch_repack_gate_up(const uint8_t *g_codes, const __half *g_scales,
+                                  const __half *g_biases, const uint8_t *u_codes,
+                                  const __half *u_scales, const __half *u_biases, int experts,
+                                  int rows, int din, int bits, uint8_t *out, cudaStream_t stream) {
+  if (experts < 1 || rows < 1) return cudaSuccess;
+  const int rb = din * bits / 8, G = din / 64;
+  const int64_t records = static_cast<int64_t>(experts) * rows;
+  const int64_t n = records * (2 * rb / 16 > 4 * G ? 2 * rb / 16 : 4 * G);
+  int64_t grid = (n + 255) / 256;
+  grid = grid < 1 ? 1 : (grid > 8192 ? 8192 : grid);
+  repack_gate_up_kernel<<<static_cast<int>(grid), 256, 0, stream>>>(
+      reinterpret_cast<const uint4 *>(g_codes), g_scales, g_biases,
+      reinterpret_cast<const uint4 *>(u_codes), u_scales, u_biases, records, rb / 16, G,
+      col_record_bytes(din, bits), out);
+  return cudaGetLastError();
+}
 
 cudaError_t launch_repack_down(const uint8_t *codes, const __half *scales, const __half *biases,
                                int experts, int din, int dff, int bits, uint32_t *out_codes,

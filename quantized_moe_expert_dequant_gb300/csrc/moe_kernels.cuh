@@ -32,7 +32,8 @@ constexpr int kProducerWarps = 1;           // issues the weight stream (bulk co
 constexpr int kProducers = kProducerWarps * 32;
 constexpr int kThreads = kConsumers + kProducers;
 constexpr int kRingBytes = 208 * 1024;      // shared-memory ring of one CTA
-constexpr int kMaxStages = 8;
+constexpr int kMaxStages = 12;             // ring slots a kernel's shared state holds
+constexpr int kMaxRowStages = 8;           // ring slots the row-split plans use, at most
 constexpr int kMaxRowsB = 128;              // phase B: output rows one CTA owns, at most
 constexpr int kMaxActRegs = 32;             // phase B: a thread owns at most this many codes' worth
                                             // of steps (one step at 4 and 6 bits, two at 8 bits)
@@ -91,21 +92,35 @@ constexpr int kMaxColsCta = 256;     // activation columns one CTA owns, at most
 constexpr int kMaxColPieces = 16;    // (segment, group) pieces of one CTA's columns, at most
 constexpr int kMaxColBlocks = 64;    // down column blocks one CTA reads, at most
 constexpr int kMaxOwnRows = 32;      // output rows one CTA sums from the partials, at most
+constexpr int kColMaxGrid = 160;     // CTAs of a column-split launch, at most (the owner's sums
+                                     // read five partial vectors per lane)
 
 struct ColDownDev {
   const uint32_t *codes;   // [experts][dff / cb][din]
   const __half2 *sb;       // [experts][dff / 64][din]
 };
 
+// Gate/up rows of the column split as records, one per row pair j of each expert:
+//   [gate codes: rb][up codes: rb][gate scales: G][gate biases: G][up scales: G][up biases: G],
+// the four fp16 runs padded together to a multiple of 16 bytes (rec bytes per record), so that
+// the R row pairs of a stage are one contiguous bulk copy.
 struct ColPtrs {
   ColDownDev r, s;         // routed experts, shared experts
+  const uint8_t *gu_r;     // [experts][dff][rec_r] gate/up records of the routed experts
+  const uint8_t *gu_s;     // [n_shared][dff_shared][rec_s] those of the shared experts
 };
 
 struct ColPlan {
   int cb_r, cb_s;          // codes per 32-bit word of the routed / shared down projection
   int nbs;                 // column blocks per down stage, at most
-  int ro;                  // rows per owner in the partial-sum slab (padded)
+  int ro;                  // output rows one CTA owns, at most (4 * its row quads)
+  int rec_r, rec_s;        // bytes of one gate/up record, routed / shared
 };
+
+// Bytes of one gate/up record of a row of `din` codes at `bits`.
+__host__ __device__ inline int col_record_bytes(int din, int bits) {
+  return 2 * (din * bits / 8) + ((8 * (din / 64) + 15) / 16) * 16;
+}
 
 // One piece of a CTA's columns: the columns [j0, j1) of one segment (routed slot or shared expert)
 // that lie in one group of 64.
@@ -171,6 +186,43 @@ __host__ __device__ inline int col_pieces(int top_k, int dff, int n_shared, int 
   return np;
 }
 
+// The gate/up stages of CTA c out of n in the column split: its activation columns [u0, u1) cut
+// into chunks of at most R row pairs (R_s for the shared experts) that never cross an expert, in
+// column order.  Chunk i: segment seg[i] (routed slot, or top_k + shared expert), first row j[i]
+// inside the expert, rows cnt[i], flattened first column u[i].  Returns the chunk count and the
+// routed chunks in *n_routed, or -1 beyond kMaxColChunks.
+constexpr int kMaxColChunks = 96;
+__host__ __device__ inline int col_chunks(int top_k, int dff, int n_shared, int dff_shared, int R,
+                                          int R_s, int c, int n, short *seg, short *j, short *cnt,
+                                          short *u, int *n_routed) {
+  const int64_t Ur = static_cast<int64_t>(top_k) * dff;
+  const int64_t U = Ur + static_cast<int64_t>(n_shared) * dff_shared;
+  int64_t u0, u1;
+  col_range(U, c, n, &u0, &u1);
+  int nc = 0, nr = 0;
+  for (int64_t x = u0; x < u1;) {
+    const bool routed = x < Ur;
+    const int width = routed ? dff : dff_shared;
+    const int64_t rel = routed ? x : x - Ur;
+    const int sg = static_cast<int>(rel / width);
+    const int jj = static_cast<int>(rel - static_cast<int64_t>(sg) * width);
+    int take = width - jj;
+    const int lim = routed ? R : R_s;
+    if (take > lim) take = lim;
+    if (take > u1 - x) take = static_cast<int>(u1 - x);
+    if (nc == kMaxColChunks) return -1;
+    seg[nc] = static_cast<short>(routed ? sg : top_k + sg);
+    j[nc] = static_cast<short>(jj);
+    cnt[nc] = static_cast<short>(take);
+    u[nc] = static_cast<short>(x - u0);
+    nr += routed;
+    ++nc;
+    x += take;
+  }
+  *n_routed = nr;
+  return nc;
+}
+
 // Kernel A alone.
 struct GateUpParams {
   LayerShape s;
@@ -184,6 +236,7 @@ struct GateUpParams {
   const float *scores;      // [top_k]
   float *act;               // [top_k*dff + n_shared*dff_shared]
   int32_t *err;             // sticky error word
+  int32_t *ids_used;        // [top_k] or null: CTA 0 writes the ids it read
 };
 
 // Kernel B alone.
@@ -227,9 +280,14 @@ struct StackParams {
   // column-split mode (m = 1): repacked down projections per layer, plan, partial-sum slab
   const ColPtrs *cols;      // device array [L]
   ColPlan cp;
-  float *slab;              // [2][grid][grid][cp.ro]
+  float *slab;              // [2][grid][din]: each CTA's partial output vector, two passes
   int ahead;                // 1: every layer's ids are inputs known before the step: the weight
                             // stream runs on into the next layer (not the decode dependency)
+  unsigned long long *tl;   // timeline builds: [grid][L][kTlPoints] time stamps; else null
+  int32_t *ids_used;        // [L][m][top_k] or null: CTA 0 writes the ids its producer read
+  int pool;                 // grouped path: gate/up without the score (or shared scalar); the
+                            // tail forms resid + (sum_k score_k y_k + scalar * sum y_shared) from
+                            // the per-slot outputs y, which it keeps
 };
 
 // Host-side plan; false when the shape is outside what the kernels support.
@@ -239,13 +297,19 @@ bool make_group_plan(const LayerShape &s, int bits_gu, int bits_d, int bits_sh, 
                      GroupPlan *gp);
 
 // Column-split plan for a grid of `grid` CTAs (phase-A geometry and ring in *plan); false when
-// the shape is outside the column-split kernels (down codes of 4 or 8 bits, din <= 4096, and the
-// per-CTA limits above).
+// the shape is outside the column-split kernels (down codes of 4 or 8 bits, din <= 4096, at most
+// kColMaxGrid CTAs, and the per-CTA limits above).  A phase-A stage holds R (gate row, up row)
+// pairs, R a power of two with R * ceil(din / 2048) <= 16 (one warp per 2048 columns of a pair).
 bool make_col_plan(const LayerShape &s, int bits_gu, int bits_d, int bits_sh, int grid,
                    int ring_bytes, ColPlan *cp, Plan *plan);
 cudaError_t launch_cols(const StackParams &p, int grid, cudaStream_t stream);
 cudaError_t prepare_cols(int smem_optin, int bits_gu, int bits_d, int bits_sh, int *dyn_limit);
 int cols_grid_limit(size_t smem, int bits_gu, int bits_d, int bits_sh);
+// Writes the gate/up records (see ColPtrs) of `experts` experts of `rows` row pairs.
+cudaError_t launch_repack_gate_up(const uint8_t *g_codes, const __half *g_scales,
+                                  const __half *g_biases, const uint8_t *u_codes,
+                                  const __half *u_scales, const __half *u_biases, int experts,
+                                  int rows, int din, int bits, uint8_t *out, cudaStream_t stream);
 // Writes the column-block-major copy of `experts` down projections (rows din, cols dff, bits).
 cudaError_t launch_repack_down(const uint8_t *codes, const __half *scales, const __half *biases,
                                int experts, int din, int dff, int bits, uint32_t *out_codes,

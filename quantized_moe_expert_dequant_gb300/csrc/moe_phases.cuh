@@ -21,6 +21,7 @@
 #include "moe_common.cuh"
 #include "moe_kernels.cuh"
 #include "moe_tma.cuh"
+#include "moe_timeline.cuh"
 
 namespace moe {
 
@@ -297,8 +298,9 @@ __device__ __forceinline__ void set_timeout(int *abort, int32_t *err) {
 
 __device__ __forceinline__ bool ring_wait(uint64_t *bar, uint32_t parity, int *abort,
                                           int32_t *err, long long limit = kWaitCycles) {
+  // a completed phase is the common case: test it without the suspending wait's fixed cost
+  if (mbar_test_wait(bar, parity)) return true;
   if (flag_abort(abort)) return false;
-  if (mbar_try_wait(bar, parity)) return true;
   const long long t0 = clock64();
   while (!mbar_try_wait(bar, parity)) {
     if (flag_abort(abort)) return false;
@@ -387,17 +389,20 @@ __device__ __forceinline__ void consumers_grid_barrier(uint32_t *cnt, uint32_t t
 }
 
 // Producer side, at the start of a (layer, token): the expert ids and scores into shared memory
-// (lanes in parallel) and the error bit for ids outside [0, n_experts).  The caller has already
+// (lanes in parallel) and the error bit for ids outside [0, n_experts); with ids_used set, CTA 0
+// also writes the ids it read there (the route the kernel took, for the caller to check).  The caller has already
 // waited for whatever makes them complete; the producer_sync after the loads orders them before
 // the producer's first arrive on a stage, which publishes them to the consumers.
 __device__ __forceinline__ void producer_load_token(const LayerShape &s, const int32_t *ids,
                                                     const float *scores, int *ids_s,
-                                                    float *scores_s, int32_t *err, int lane) {
+                                                    float *scores_s, int32_t *err, int lane,
+                                                    int32_t *ids_used = nullptr) {
   for (int k = lane; k < s.top_k; k += kProducers) {
     const int e = ids[k];
     ids_s[k] = e;
     scores_s[k] = scores != nullptr ? scores[k] : 0.f;
     if (e < 0 || e >= s.n_experts) atomicOr(err, kDevErrBadId);
+    if (ids_used != nullptr && blockIdx.x == 0) ids_used[k] = e;  // what this kernel read
   }
   producer_sync();
 }

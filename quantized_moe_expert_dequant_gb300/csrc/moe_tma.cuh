@@ -12,6 +12,7 @@ namespace moe {
 constexpr long long kWaitCycles = 4000000000LL;  // about two seconds at GB300 clocks
 constexpr int kDevErrBadId = 1;
 constexpr int kDevErrTimeout = 2;
+constexpr int kDevErrPlan = 4;  // a kernel found its launch plan inconsistent with the shape
 
 __device__ __forceinline__ uint32_t smem_addr(const void *p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));
@@ -46,6 +47,19 @@ __device__ __forceinline__ void mbar_arrive(uint64_t *bar) {
   asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_addr(bar)) : "memory");
 }
 
+// Non-blocking: whether the phase with the given parity has completed.
+__device__ __forceinline__ bool mbar_test_wait(uint64_t *bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(smem_addr(bar)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
 // The thread may be suspended in hardware (up to the hint, in ns) until the phase completes,
 // instead of spinning on the barrier word.
 __device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity) {
@@ -62,7 +76,7 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity) {
 
 // Waits for the phase with the given parity to complete; false after kWaitCycles.
 __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity) {
-  if (mbar_try_wait(bar, parity)) return true;
+  if (mbar_test_wait(bar, parity)) return true;
   const long long t0 = clock64();
   while (!mbar_try_wait(bar, parity)) {
     if (clock64() - t0 > kWaitCycles) return false;
@@ -79,6 +93,14 @@ __device__ __forceinline__ void bulk_g2s(void *dst, const void *src, uint32_t by
       " [%0], [%1], %2, [%3], %4;" ::"r"(smem_addr(dst)),
       "l"(src), "r"(bytes), "r"(smem_addr(bar)), "l"(policy)
       : "memory");
+}
+
+// Bulk prefetch of [src, src + bytes) into L2 (no completion signal); src 16-byte aligned, bytes a
+// multiple of 16.
+__device__ __forceinline__ void bulk_prefetch_l2(const void *src, uint32_t bytes, uint64_t policy) {
+  asm volatile("cp.async.bulk.prefetch.L2.global.L2::cache_hint [%0], %1, %2;" ::"l"(src),
+               "r"(bytes), "l"(policy)
+               : "memory");
 }
 
 // 16-byte asynchronous copy global -> shared through the load path (LDGSTS), bypassing L1.  On

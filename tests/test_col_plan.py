@@ -24,7 +24,7 @@ def built():
 CASES = [ALL["qwen3_stack_8bit"], ALL["e512_stack"], ALL["qwen3_layer_4bit"],
          ALL["qwen15_layer_shared"],
          Shape("small", 256, 128, 8, 2, 8, 8, 8, n_shared=1, dff_shared=128, bits_shared=4),
-         Shape("ragged", 384, 192, 10, 3, 6, 6, 4),
+         Shape("ragged", 384, 192, 10, 3, 4, 4, 4),
          Shape("fewer columns than CTAs", 64, 64, 4, 2, 8, 8, 4),
          Shape("shared only", 256, 64, 1, 0, 8, 8, 8, n_shared=2, dff_shared=128, bits_shared=8)]
 
@@ -88,30 +88,40 @@ def test_plan_stages_fit_the_ring_and_the_slab_rows(built, shape):
     p = Bn.col_plan(shape, grid, RING)
     bsh = shape.bits_shared if shape.n_shared else shape.bits_down
     assert p["cb_r"] == 32 // shape.bits_down and p["cb_s"] == 32 // bsh
-    assert 2 <= p["stages"] <= 8 and p["stages"] * p["stage_bytes"] <= RING
+    assert 2 <= p["stages"] <= 12 and p["stages"] * p["stage_bytes"] <= RING
     assert p["stage_bytes"] % 128 == 0
     assert 1 <= p["nbs"] <= 16 and (p["nbs"] + 1) * shape.din * 4 <= p["stage_bytes"]
-    # a phase-A stage of each class present: its gate and up rows
+    # a phase-A stage of each class present: its gate and up rows; R pairs, R a power of two,
+    # one warp per 2048 columns of a pair, so the warps of a stage divide the 16 consumer warps
     classes = [(p["rows_a_r"], shape.bits_gate)] if shape.top_k else []
     classes += [(p["rows_a_s"], bsh)] if shape.n_shared else []
+    wpr = -(-shape.din // 1024)
     for rows, bits in classes:
         assert 2 * rows * shape.din * bits // 8 <= p["stage_bytes"]
-    # every output row has an owner CTA and a slot below ro in the owner's block of the slab
-    ro = p["ro"]
-    assert ro % 4 == 0 and ro <= 32 and ro >= -(-shape.din // grid)
-    for i in range(shape.din):
-        o = ((i + 1) * grid - 1) // shape.din
-        rr = i - shape.din * o // grid
-        assert shape.din * o // grid <= i < shape.din * (o + 1) // grid and 0 <= rr < ro
+        assert rows & (rows - 1) == 0 and 16 % (rows * wpr) == 0
+    # every output row quad has exactly one owner CTA, whose quads fit its ro rows
+    nq, ro = shape.din // 4, p["ro"]
+    assert ro % 4 == 0 and ro <= 32
+    owned = [0] * nq
+    for c in range(grid):
+        q0, q1 = nq * c // grid, nq * (c + 1) // grid
+        assert 4 * (q1 - q0) <= ro
+        for q in range(q0, q1):
+            owned[q] += 1
+    assert owned == [1] * nq
 
 
 def test_plan_refuses_what_the_kernel_does_not_take(built):
     six = Shape("6-bit down", 256, 128, 8, 2, 8, 8, 6)
+    six_gu = Shape("6-bit gate/up", 256, 128, 8, 2, 6, 6, 8)
     wide = Shape("din 8192", 8192, 128, 4, 2, 8, 8, 8)
-    for shape in (six, wide):
+    for shape in (six, six_gu, wide):
         with pytest.raises(Bn.MoeError) as e:
             Bn.col_plan(shape, 152, RING)
         assert e.value.rc == Bn.MOE_ERR_UNSUPPORTED
     with pytest.raises(Bn.MoeError) as e:     # a ring too small for two stages
         Bn.col_plan(ALL["qwen3_stack_8bit"], 152, 40 * 1024)
+    assert e.value.rc == Bn.MOE_ERR_UNSUPPORTED
+    with pytest.raises(Bn.MoeError) as e:     # more CTAs than the owner's sums read
+        Bn.col_plan(ALL["qwen3_stack_8bit"], 161, RING)
     assert e.value.rc == Bn.MOE_ERR_UNSUPPORTED

@@ -54,8 +54,8 @@ LAYERS = {
     "256x128 E8 K2 8/8/8 + gated shared 4-bit": Shape("c1", 256, 128, 8, 2, 8, 8, 8, n_shared=1,
                                                       dff_shared=128, bits_shared=4,
                                                       shared_gate=1, seed=41),
-    # 4-bit down under 6-bit gate/up, ragged widths
-    "384x192 E10 K3 6/6/4": Shape("c2", 384, 192, 10, 3, 6, 6, 4, seed=42),
+    # 4-bit down under 4-bit gate/up, ragged widths (din not a multiple of 1024: idle lanes)
+    "384x192 E10 K3 4/4/4": Shape("c2", 384, 192, 10, 3, 4, 4, 4, seed=42),
     # fewer columns than CTAs: most CTAs own nothing and contribute zero partials
     "64x64 E4 K2 8/8/4": Shape("c3", 64, 64, 4, 2, 8, 8, 4, seed=43),
     # din > 2048: two row quads per thread; two ungated 8-bit shared experts
@@ -183,6 +183,10 @@ def test_columns_mode_rejects_what_it_does_not_run():
     six = C.host_layer_device(Shape("c6", 128, 64, 4, 2, 4, 4, 6, seed=50))
     with pytest.raises(Bn.MoeError) as e:
         Bn.MoeDecode(six, kernel_mode=COLS)            # 6-bit down codes
+    assert e.value.rc == Bn.MOE_ERR_UNSUPPORTED
+    six_gu = C.host_layer_device(Shape("c6g", 128, 64, 4, 2, 6, 6, 8, seed=52))
+    with pytest.raises(Bn.MoeError) as e:
+        Bn.MoeDecode(six_gu, kernel_mode=COLS)         # 6-bit gate/up codes
     assert e.value.rc == Bn.MOE_ERR_UNSUPPORTED
     ok = C.host_layer_device(Shape("c7", 128, 64, 4, 2, 4, 4, 8, layers=2, seed=51))
     with pytest.raises(Bn.MoeError) as e:
