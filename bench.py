@@ -52,7 +52,8 @@ KERNEL_SOURCES = ["quantized_moe_expert_dequant_gb300/csrc/moe_cols.cuh",
                   "quantized_moe_expert_dequant_gb300/csrc/moe_kernels.cuh",
                   "quantized_moe_expert_dequant_gb300/csrc/moe_phases.cuh",
                   "quantized_moe_expert_dequant_gb300/csrc/moe_tma.cuh",
-                  "quantized_moe_expert_dequant_gb300/csrc/moe_common.cuh"]
+                  "quantized_moe_expert_dequant_gb300/csrc/moe_common.cuh",
+                  "quantized_moe_expert_dequant_gb300/csrc/moe_timeline.cuh"]
 
 
 # ---------------------------------------------------------------- algorithmic bytes
@@ -244,10 +245,37 @@ def measured_peaks():
         return None
 
 
+def code_only(text: str) -> str:
+    """C/C++/CUDA source without comments and with runs of whitespace collapsed, so that the
+    hash below changes with the code, not with its comments."""
+    import re
+    out, i, n = [], 0, len(text)
+    while i < n:
+        if text.startswith("//", i):
+            j = text.find("\n", i)
+            i = n if j < 0 else j
+        elif text.startswith("/*", i):
+            j = text.find("*/", i + 2)
+            i = n if j < 0 else j + 2
+            out.append(" ")
+        elif text[i] in "\"'":
+            q, j = text[i], i + 1
+            while j < n and text[j] != q:
+                j += 2 if text[j] == "\\" else 1
+            out.append(text[i:j + 1])
+            i = j + 1
+        else:
+            out.append(text[i])
+            i += 1
+    return re.sub(r"\s+", " ", "".join(out)).strip()
+
+
 def kernel_source_hash() -> str:
+    """Hash of the dominant kernels' code (comments and layout ignored): a DRAM-traffic record
+    in profiles/traffic.txt is used only while it matches."""
     h = hashlib.sha256()
     for f in KERNEL_SOURCES:
-        h.update(open(os.path.join(ROOT, f), "rb").read())
+        h.update(code_only(open(os.path.join(ROOT, f), encoding="utf-8").read()).encode())
     return h.hexdigest()[:16]
 
 
@@ -369,8 +397,7 @@ def run_ours(args, shape: Shape):
     chained = args.chain_norm
     kernels = args.kernels
     if kernels == "auto":   # the column split where it runs, else the row split
-        cols_ok = (m == 1 and not chained and shape.bits_down in (4, 8)
-                   and (shape.n_shared == 0 or shape.bits_shared in (4, 8)) and shape.din <= 4096)
+        cols_ok = (m == 1 and not chained and shape.bits_gate in (4, 8) and shape.din <= 4096)
         kernels = "columns" if cols_ok else "fused"
     mode = mode_of(kernels)
     norm = None

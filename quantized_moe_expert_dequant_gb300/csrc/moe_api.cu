@@ -137,8 +137,9 @@ int prepare(const moe_decode_config *c, Prepared &P) {
   if (cols_mode(c->kernel_mode)) {
     if (c->max_tokens != 1) return MOE_ERR_UNSUPPORTED;
     int lim = 0;
-    if (moe::prepare_cols(smem_optin, c->bits_gate, c->bits_down, P.bits_sh, &lim) !=
-        cudaSuccess) {
+    if (moe::prepare_cols(smem_optin, moe::col_gu_bits(c->bits_gate),
+                          moe::col_down_bits(c->bits_down), moe::col_down_bits(P.bits_sh),
+                          &lim) != cudaSuccess) {
       cudaGetLastError();
       return MOE_ERR_UNSUPPORTED;  // no column-split kernel for these code widths
     }
@@ -146,7 +147,9 @@ int prepare(const moe_decode_config *c, Prepared &P) {
     if (!moe::make_col_plan(P.shape, c->bits_gate, c->bits_down, P.bits_sh, sms, ring, &P.cplan,
                             &P.col_plan))
       return MOE_ERR_UNSUPPORTED;
-    const int per = moe::cols_grid_limit(P.col_plan.smem, c->bits_gate, c->bits_down, P.bits_sh);
+    const int per = moe::cols_grid_limit(P.col_plan.smem, moe::col_gu_bits(c->bits_gate),
+                                         moe::col_down_bits(c->bits_down),
+                                         moe::col_down_bits(P.bits_sh));
     if (per < sms) return MOE_ERR_UNSUPPORTED;  // one CTA per SM, all resident
     P.grid_cols = sms;
   }
@@ -299,7 +302,7 @@ struct ColWeights {
   moe::ColPtrs *dev = nullptr;  // device array [L]
 
   bool repack(int experts, int din, int dff, int bits, const moe_proj &p, moe::ColDownDev *out) {
-    const size_t words = (size_t)experts * (dff * bits / 32) * din;
+    const size_t words = (size_t)experts * (dff * moe::col_down_bits(bits) / 32) * din;
     const size_t pairs = (size_t)experts * (dff / 64) * din;
     void *c = nullptr, *b = nullptr;
     if (cudaMalloc(&c, words * 4) != cudaSuccess) return false;
@@ -317,7 +320,7 @@ struct ColWeights {
   bool records(int experts, int rows, int din, int bits, const moe_proj &g, const moe_proj &u,
                const uint8_t **out) {
     void *b = nullptr;
-    const size_t bytes = (size_t)experts * rows * moe::col_record_bytes(din, bits);
+    const size_t bytes = (size_t)experts * rows * moe::col_record_bytes(din, moe::col_gu_bits(bits));
     if (cudaMalloc(&b, bytes) != cudaSuccess) return false;
     bufs.push_back(b);
     *out = static_cast<const uint8_t *>(b);
@@ -968,6 +971,8 @@ extern "C" int moe_debug_col_pieces(int32_t top_k, int32_t dff, int32_t n_shared
   if (top_k + n_shared < 1 || (top_k > 0 && (dff <= 0 || dff % 64)) ||
       (n_shared > 0 && (dff_shared <= 0 || dff_shared % 64)))
     return MOE_ERR_INVALID_ARG;
+  bits_down = moe::col_down_bits(bits_down);     // 6-bit down codes are stored as bytes
+  bits_shared = moe::col_down_bits(bits_shared);
   if ((bits_down != 4 && bits_down != 8) || (n_shared > 0 && bits_shared != 4 && bits_shared != 8))
     return MOE_ERR_UNSUPPORTED;
   const int64_t U = (int64_t)top_k * dff + (int64_t)n_shared * dff_shared;

@@ -46,6 +46,22 @@ namespace moe {
 constexpr int kColHelperWarp = kConsumerWarps + kProducerWarps;
 constexpr int kColThreads = kThreads + 32;    // consumers, producer, helper
 constexpr int kColMaxWpr = 4;                 // warps per gate/up row pair (32 columns a lane)
+// After the first ring-full of a layer's stages, ask L2 for the rest of the layer's bytes.
+constexpr bool kColPrefetchOverflow = false;
+// Consumers test a stage's barrier from every lane (no broadcast from lane 0).
+constexpr bool kColLaneWait = true;
+
+// Consumer side: every lane tests the stage's full barrier until it completes (bounded; on the
+// rare long wait the common path below takes over).
+__device__ __forceinline__ bool cols_wait_full(Ring &r, int lane) {
+  if (kColLaneWait) {
+    for (int it = 0; it < 64; ++it) {
+      if (mbar_test_wait(&r.full[r.st], r.ph)) return true;
+      __nanosleep(32);
+    }
+  }
+  return warp_wait_full(r, lane);
+}
 
 // ------------------------------------------------------------------ one lane's operand
 // The lane's 32 values of x (half a group of 64 of a gate/up row) with ONE exponent, in the form
@@ -176,7 +192,6 @@ __device__ __forceinline__ void load_lane_x(LaneOp<BITS> &op, const uint16_t *x,
 
 // ------------------------------------------------------------------ shared state
 struct ColSmem {
-  float act[kMaxColsCta];                 // silu(gate) * up of the CTA's columns, index u - u0
   float2 red[kMaxColsCta][kColMaxWpr];    // (gate, up) sums of each column from each of the
                                           // warps that share its row pair
   uint32_t planes[kMaxColBlocks * 8];     // per block: byte planes (3 words at 8 bits, 6 at 4)
@@ -209,56 +224,80 @@ __device__ __forceinline__ void consumers_helper_sync() {
 
 // ------------------------------------------------------------------ gate/up
 // The stages of one class (routed slots or shared experts) of the CTA's gate/up rows.  A stage
-// holds up to R (gate row, up row) records (see ColPtrs); each pair is taken by wpr warps, each
-// lane of them owning 32 columns of both rows (columns 32 (32 h + lane) ...), so R * wpr warps
-// work on a stage, by turns when they are fewer than 16: with A = 16 / (R * wpr) warp sets, stage
-// i of the phase goes to set i mod A.  Every warp waits for and releases every stage.
-// The warp's (gate, up) sums go to red[u - u0][h]; the caller forms the activations.
+// holds up to R (gate row, up row) records (see ColPtrs); each pair is split among wpr lane sets of
+// 32 lanes, each lane owning 32 columns of both rows (columns 32 (32 h + lane) ...), which makes
+// T = R * wpr tasks (pair p, part h), task index p * wpr + h.  A warp takes two tasks of a stage,
+// t and t + W (W = T / 2 warps per stage, slot t), so W warps work on a stage, by turns: with
+// A = 16 / W warp sets, stage i of the phase goes to set i mod A and the sets overlap consecutive
+// stages.  Every warp waits for and releases every stage.  The tasks' (gate, up) sums go to
+// red[u - u0][h]; the caller forms the activations.
+template <int BITS>
+__device__ __forceinline__ void cols_a_task(const LaneOp<BITS> &xo, const uint8_t *rec, int koff,
+                                            int rbc, int G, int k, bool on, int rt,
+                                            float &gv, float &uv) {
+  constexpr int VEC = LaneOp<BITS>::VEC;
+  gv = uv = 0.f;
+  if (!on) return;
+  const uint8_t *rg = rec + koff;
+  const uint8_t *ws = rec + 2 * rbc + (k >> 1) * 2;
+  uint4 cg[VEC], cu[VEC];
+#pragma unroll
+  for (int j = 0; j < VEC; ++j) {
+    cg[j] = lds_u4(rg + 16 * ((j + rt) % VEC));
+    cu[j] = lds_u4(rg + rbc + 16 * ((j + rt) % VEC));
+  }
+  const float sg = lds_half(ws), bg = lds_half(ws + 2 * G);
+  const float su = lds_half(ws + 4 * G), bu = lds_half(ws + 6 * G);
+  gv = fmaf(sg, xo.dot(cg) * xo.unit, bg * xo.sum);
+  uv = fmaf(su, xo.dot(cu) * xo.unit, bu * xo.sum);
+}
+
 template <int BITS>
 __device__ int cols_a_class(const LayerShape &s, const GateUpGeom &g, int count, int i0,
                             const LaneOp<BITS> &xo, ColSmem &cs, Ring &r, bool &waited,
                             bool &ok, int warp, int lane) {
-  constexpr int VEC = LaneOp<BITS>::VEC;
   const int nk = s.din >> 5;                     // 32-column slots of a row
   const int wpr = (nk + 31) >> 5;
-  const int per = g.R * wpr;                     // warps working on one stage
-  const int A = kConsumerWarps / per;
-  const int slot = warp % per, turn = warp / per;
-  const int p = slot / wpr, h = slot - p * wpr;
+  const int T = g.R * wpr;                       // tasks of a full stage
+  const int W = (T + 1) >> 1;                    // warps working on one stage
+  const int A = kConsumerWarps / W;
+  const int slot = warp % W, turn = warp / W;
+  // the warp's two tasks: pair p and lane set h of each (the same h: W is a multiple of wpr)
+  const int t1 = slot, t2 = slot + W;
+  const int p1 = t1 / wpr, p2 = t2 / wpr, h = t1 - p1 * wpr;
   const int k = 32 * h + lane;                   // the lane's 32-column slot of the row
   const bool lane_on = k < nk;
   const int rt = LaneOp<BITS>::rot(lane);
-  const int lane_off = k * (4 * BITS);           // the lane's bytes inside a row
+  const int koff = k * (4 * BITS);               // the lane's bytes inside a row
   const int rbc = s.din * BITS / 8;              // code bytes of a row
   const int G = s.din / kGroup;
   int i = i0;
   for (int c = 0; c < count; ++c, ++i) {
     if (!waited) {
       if (warp == 0 && lane == 0) MOE_TL_STAGE_WAIT(r.used);
-      ok = warp_wait_full(r, lane);
+      ok = cols_wait_full(r, lane);
     }
     waited = false;
     if (warp == 0 && lane == 0) MOE_TL_STAGE_C(r.used);
     const StageDesc d = r.desc[r.st];
-    const bool mine = ok && turn < A && (A == 1 || (i % A) == turn) && p < d.n;
-    if (mine) {  // warp-uniform
-      float gv = 0.f, uv = 0.f;
-      if (lane_on) {
-        const uint8_t *rec = r.stage() + p * g.rb;   // the pair's record
-        const uint8_t *rg = rec + lane_off;
-        const uint8_t *ws = rec + 2 * rbc + (k >> 1) * 2;
-        uint4 cv[VEC];
-#pragma unroll
-        for (int j = 0; j < VEC; ++j) cv[j] = lds_u4(rg + 16 * ((j + rt) % VEC));
-        gv = fmaf(lds_half(ws), xo.dot(cv) * xo.unit, lds_half(ws + 2 * G) * xo.sum);
-#pragma unroll
-        for (int j = 0; j < VEC; ++j) cv[j] = lds_u4(rg + rbc + 16 * ((j + rt) % VEC));
-        uv = fmaf(lds_half(ws + 4 * G), xo.dot(cv) * xo.unit, lds_half(ws + 6 * G) * xo.sum);
-      }
+    const bool mine = ok && turn < A && (A == 1 || (i % A) == turn);
+    const bool on1 = mine && t1 < T && p1 < d.n, on2 = mine && t2 < T && p2 < d.n;
+    if (on1) {  // warp-uniform
+      float v[4];
+      const uint8_t *sb = r.stage();
+      cols_a_task<BITS>(xo, sb + p1 * g.rb, koff, rbc, G, k, lane_on, rt, v[0], v[1]);
+      cols_a_task<BITS>(xo, sb + p2 * g.rb, koff, rbc, G, k, lane_on && on2, rt, v[2], v[3]);
       warp_release(r, lane);
-      gv = warp_sum(gv);
-      uv = warp_sum(uv);
-      if (lane == 0) cs.red[d.u + p - cs.u0][h] = make_float2(gv, uv);
+      // lanes 0-7 hold the gate sum of task 1, 8-15 its up sum, 16-23 and 24-31 task 2's
+      const float val = warp_transpose_reduce<4>(v, lane);
+      const int which = lane >> 3;
+      if ((lane & 7) == 0 && (which < 2 || on2)) {
+        float2 *dst = &cs.red[d.u + (which < 2 ? p1 : p2) - cs.u0][h];
+        if (which & 1)
+          dst->y = val;
+        else
+          dst->x = val;
+      }
     } else {
       warp_release(r, lane);
     }
@@ -274,14 +313,14 @@ __device__ void cols_phase_a(const LayerShape &s, const GateUpGeom &gr, const Ga
                              const uint16_t *x, const int *cnt, ColSmem &cs, Ring &r, int warp,
                              int lane) {
   const int nk = s.din >> 5, wpr = (nk + 31) >> 5;
-  const int kr = 32 * ((warp % (gr.R * wpr)) % wpr) + lane;
+  const int kr = 32 * ((warp % ((gr.R * wpr + 1) >> 1)) % wpr) + lane;
   LaneOp<BR> xr;
   load_lane_x<BR>(xr, x, kr, kr < nk, lane);
   if (warp == 0 && lane == 0) {
     MOE_TL_HOOK(7);
     MOE_TL_STAGE_WAIT(r.used);
   }
-  bool ok = warp_wait_full(r, lane), waited = true;
+  bool ok = cols_wait_full(r, lane), waited = true;
   if (warp == 0 && lane == 0) MOE_TL_HOOK(8);
   const int nr = cnt[0], ns = cnt[1];
   if (nr + ns == 0) {  // an empty stage
@@ -290,7 +329,7 @@ __device__ void cols_phase_a(const LayerShape &s, const GateUpGeom &gr, const Ga
   }
   int i = cols_a_class<BR>(s, gr, nr, 0, xr, cs, r, waited, ok, warp, lane);
   if (ns > 0) {
-    const int ks = 32 * ((warp % (gs.R * wpr)) % wpr) + lane;
+    const int ks = 32 * ((warp % ((gs.R * wpr + 1) >> 1)) % wpr) + lane;
     LaneOp<BSH> xs;
     load_lane_x<BSH>(xs, x, ks, ks < nk, lane);
     cols_a_class<BSH>(s, gs, ns, i, xs, cs, r, waited, ok, warp, lane);
@@ -308,6 +347,44 @@ __device__ __forceinline__ bool ring_claim_lane(Ring &r) {
   return r.used < r.nst || ring_wait(&r.empty[r.st], r.ph ^ 1u, r.abort, r.err);
 }
 
+// L2 prefetch of the layer's stages from index `from` on (the same walk as the copies).
+__device__ inline void cols_prefetch_from(const LayerShape &s, const Plan &plan, const ColPlan &cp,
+                                          const ColPtrs &cw, const ColSmem &cs, const int *ids,
+                                          int from, uint64_t pol) {
+  int i = 0;
+  for (int c = 0; c < cs.nck; ++c) {
+    const bool routed = c < cs.nck_r;
+    const int sg = cs.ck_seg[c];
+    const int e = routed ? ids[sg] : sg - s.top_k;
+    if (routed && (e < 0 || e >= s.n_experts)) continue;
+    if (i++ < from) continue;
+    const GateUpGeom &g = routed ? plan.geo_r : plan.geo_s;
+    const uint8_t *recs = routed ? cw.gu_r : cw.gu_s;
+    const int rows_pe = routed ? s.dff : s.dff_shared;
+    bulk_prefetch_l2(recs + (static_cast<int64_t>(e) * rows_pe + cs.ck_j[c]) * g.rb,
+                     static_cast<uint32_t>(cs.ck_n[c]) * g.rb, pol);
+  }
+  const uint32_t blk_bytes = static_cast<uint32_t>(s.din) * 4u;
+  for (int qi = 0; qi < cs.np; ++qi) {
+    const ColPiece q = cs.pc[qi];
+    int e;
+    if (!col_valid(s, q, ids, &e)) continue;
+    const bool routed = q.seg < s.top_k;
+    const ColDownDev &d = routed ? cw.r : cw.s;
+    const int width = routed ? s.dff : s.dff_shared;
+    const int nblk = width / (routed ? cp.cb_r : cp.cb_s);
+    const int G = width / kGroup;
+    for (int bo = 0; bo < q.nb; bo += cp.nbs) {
+      const int nk = (q.nb - bo) < cp.nbs ? (q.nb - bo) : cp.nbs;
+      if (i++ < from) continue;
+      bulk_prefetch_l2(d.codes + (static_cast<int64_t>(e) * nblk + q.blk0 + bo) * s.din,
+                       static_cast<uint32_t>(nk) * blk_bytes, pol);
+      if (bo + nk == q.nb)
+        bulk_prefetch_l2(d.sb + (static_cast<int64_t>(e) * G + q.grp) * s.din, blk_bytes, pol);
+    }
+  }
+}
+
 template <int BR, int BSH>
 __device__ bool cols_produce_layer(const LayerShape &s, const Plan &plan, const ColPlan &cp,
                                    const ColPtrs &cw, const ColSmem &cs, const int *ids,
@@ -320,11 +397,14 @@ __device__ bool cols_produce_layer(const LayerShape &s, const Plan &plan, const 
   const int ns = cs.nck - cs.nck_r;
   cnt[0] = nr;
   cnt[1] = ns;
+  int issued = 0;
   for (int i = 0; i < cs.nck; ++i) {
     const bool routed = i < cs.nck_r;
     const int sg = cs.ck_seg[i];
     const int e = routed ? ids[sg] : sg - s.top_k;
     if (routed && (e < 0 || e >= s.n_experts)) continue;
+    if (kColPrefetchOverflow && issued++ == r.nst)
+      cols_prefetch_from(s, plan, cp, cw, cs, ids, r.nst, pol);
     if (!ring_claim_lane(r)) return false;
     const GateUpGeom &g = routed ? plan.geo_r : plan.geo_s;
     const uint8_t *recs = routed ? cw.gu_r : cw.gu_s;
@@ -356,6 +436,8 @@ __device__ bool cols_produce_layer(const LayerShape &s, const Plan &plan, const 
     for (int bo = 0; bo < q.nb; bo += cp.nbs) {
       const int nk = (q.nb - bo) < cp.nbs ? (q.nb - bo) : cp.nbs;
       const bool ends = bo + nk == q.nb;
+      if (kColPrefetchOverflow && issued++ == r.nst)
+        cols_prefetch_from(s, plan, cp, cw, cs, ids, r.nst, pol);
       if (!ring_claim_lane(r)) return false;
       const uint32_t code_bytes = static_cast<uint32_t>(nk) * blk_bytes;
       uint8_t *sb = r.stage();
@@ -372,13 +454,16 @@ __device__ bool cols_produce_layer(const LayerShape &s, const Plan &plan, const 
   return true;
 }
 
-// Consumers: byte planes of every block of every valid piece, from the local activations times
-// the piece's coefficient (the routed slot's score, or the shared scalar).
-// Warp w handles pieces w, w + 16, ...; lane b the piece's block b.
+// Consumers: the activations of every valid piece and their byte planes, one warp per piece
+// (pieces w, w + 16, ...): lane c holds columns c and c + 32 of the piece, forms
+// act = coef * silu(gate) * up from the warps' (gate, up) sums (coef: the routed slot's score, or
+// the shared scalar), and the piece's fixed-point exponent and activation sum come from warp
+// reductions; lane b then gathers the fixed-point values of the piece's column block b with
+// shuffles and writes its planes.
 template <int BD, int BSD>
 __device__ inline void col_planes(const LayerShape &s, const ColPlan &cp, ColSmem &cs,
                                   const int *ids, const float *scores, float shared_coef,
-                                  int warp, int lane) {
+                                  int wprow, int warp, int lane) {
   for (int qi = warp; qi < cs.np; qi += kConsumerWarps) {
     const ColPiece q = cs.pc[qi];
     int e;
@@ -388,24 +473,40 @@ __device__ inline void col_planes(const LayerShape &s, const ColPlan &cp, ColSme
     const int cb = routed ? cp.cb_r : cp.cb_s;
     const float coef = routed ? scores[q.seg] : shared_coef;
     const int n = q.j1 - q.j0;  // at most 64
-    const float v0 = lane < n ? coef * cs.act[q.a0 + lane] : 0.f;
-    const float v1 = lane + 32 < n ? coef * cs.act[q.a0 + lane + 32] : 0.f;
-    const float mx = warp_max(fmaxf(fabsf(v0), fabsf(v1)));
-    const float sm = warp_sum(v0 + v1);
+    float v[2];
+#pragma unroll
+    for (int t = 0; t < 2; ++t) {
+      const int c = lane + 32 * t;
+      v[t] = 0.f;
+      if (c < n) {
+        float2 a = cs.red[q.a0 + c][0];
+        for (int h = 1; h < wprow; ++h) {
+          const float2 b = cs.red[q.a0 + c][h];
+          a.x += b.x;
+          a.y += b.y;
+        }
+        v[t] = coef * (silu_f(a.x) * a.y);
+      }
+    }
+    const float mx = warp_max(fmaxf(fabsf(v[0]), fabsf(v[1])));
+    const float sm = warp_sum(v[0] + v[1]);
     const int E = fixed_exponent(mx);
     const float sc = pow2f(22 - E);
+    const int f0 = __float2int_rn(v[0] * sc), f1 = __float2int_rn(v[1] * sc);
     if (lane == 0) cs.us[qi] = make_float2(pow2f(bits == 8 ? E - 22 : E - 26), sm);
-    for (int b = lane; b < q.nb; b += 32) {
-      const int c0 = (q.blk0 + b) * cb;  // first column of the block, expert coordinates
-      int f[8];
+    // block b covers piece columns rel = (blk0 + b) * cb - j0 + k, k < cb
+    const int rel0 = (q.blk0 + lane) * cb - q.j0;
+    int f[8];
 #pragma unroll
-      for (int k = 0; k < 8; ++k) {
-        const int c = c0 + k;
-        f[k] = (k < cb && c >= q.j0 && c < q.j1)
-                   ? __float2int_rn(coef * cs.act[q.a0 + c - q.j0] * sc)
-                   : 0;
-      }
-      uint32_t *pl = cs.planes + (q.pb + b) * 8;
+    for (int k = 0; k < 8; ++k) {
+      const int rel = rel0 + k;
+      const int src = rel & 31;
+      const int g0 = __shfl_sync(0xffffffffu, f0, src);
+      const int g1 = __shfl_sync(0xffffffffu, f1, src);
+      f[k] = (k < cb && rel >= 0 && rel < n) ? (rel >= 32 ? g1 : g0) : 0;
+    }
+    if (lane < q.nb) {
+      uint32_t *pl = cs.planes + (q.pb + lane) * 8;
       if (bits == 8) {
         byte_planes(f[0], f[1], f[2], f[3], pl[0], pl[1], pl[2]);
         pl[3] = pl[4] = pl[5] = pl[6] = pl[7] = 0u;
@@ -439,7 +540,7 @@ __device__ __forceinline__ void consume_piece(const ColPiece &q, float2 us, cons
     const int nk = (q.nb - bo) < cp.nbs ? (q.nb - bo) : cp.nbs;
     const bool ends = bo + nk == q.nb;
     if (tid == 0) MOE_TL_STAGE_WAIT(r.used);
-    const bool ok = warp_wait_full(r, lane);
+    const bool ok = cols_wait_full(r, lane);
     if (tid == 0) MOE_TL_STAGE_C(r.used);
     const uint8_t *sb = r.stage();
     if (ok) {
@@ -452,6 +553,7 @@ __device__ __forceinline__ void consume_piece(const ColPiece &q, float2 us, cons
           for (int k = 0; k < 4; ++k)
 #pragma unroll
             for (int z = 0; z < NPL; ++z) al[k][z] = 0u;
+#pragma unroll 4
           for (int b = 0; b < nk; ++b) {
             const uint4 pa = *reinterpret_cast<const uint4 *>(planes + (q.pb + bo + b) * 8);
             const uint4 pb = *reinterpret_cast<const uint4 *>(planes + (q.pb + bo + b) * 8 + 4);
@@ -740,22 +842,11 @@ __global__ void __launch_bounds__(kColThreads, 1) cols_kernel(const StackParams 
     MOE_TL_AT(tlr, 10);
     if (tid == 0) mbar_arrive(&a_done);
     const int *ids_l = ids2[l & 1];
-    {
-      const int wprow = ((s.din >> 5) + 31) >> 5;
-      for (int t = tid; t < cs.ncols; t += kConsumers) {
-        float2 a = cs.red[t][0];
-        for (int h = 1; h < wprow; ++h) {
-          const float2 b = cs.red[t][h];
-          a.x += b.x;
-          a.y += b.y;
-        }
-        cs.act[t] = silu_f(a.x) * a.y;
-      }
-    }
     MOE_TL_AT(tlr, 3);
-    consumers_helper_sync();  // activations complete; the helper's shared scalar is ready
+    consumers_helper_sync();  // the helper's shared scalar is ready
     MOE_TL_AT(tlr, 6);
-    col_planes<BD, BSH>(s, p.cp, cs, ids_l, sc2[l & 1], cs.s_gate[l & 1], warp, lane);
+    col_planes<BD, BSH>(s, p.cp, cs, ids_l, sc2[l & 1], cs.s_gate[l & 1],
+                        ((s.din >> 5) + 31) >> 5, warp, lane);
     consumer_sync(kConsumers);
     MOE_TL_AT(tlr, 11);
     float part[2][4];

@@ -163,6 +163,7 @@ __global__ void repack_gate_up_kernel(const uint4 *g_codes, const __half *g_scal
                                       const __half *g_biases, const uint4 *u_codes,
                                       const __half *u_scales, const __half *u_biases,
                                       int64_t records, int rb16, int G, int rec, uint8_t *out) {
+  const int codes_bytes = rec - ((8 * G + 15) / 16) * 16;  // the two code rows
   const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
   const int64_t nc = records * 2 * rb16;
   for (int64_t x = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; x < nc;
@@ -172,7 +173,7 @@ __global__ void repack_gate_up_kernel(const uint4 *g_codes, const __half *g_scal
     const uint4 v = w < rb16 ? g_codes[r * rb16 + w] : u_codes[r * rb16 + (w - rb16)];
     reinterpret_cast<uint4 *>(out + r * rec)[w] = v;
   }
-  const int tail = (rec - 32 * rb16) / 2;  // fp16 slots after the codes
+  const int tail = (rec - codes_bytes) / 2;  // fp16 slots after the codes
   const int64_t ns = records * tail;
   for (int64_t x = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; x < ns;
        x += stride) {
@@ -184,7 +185,61 @@ __global__ void repack_gate_up_kernel(const uint4 *g_codes, const __half *g_scal
       const __half *src = run == 0 ? g_scales : run == 1 ? g_biases : run == 2 ? u_scales : u_biases;
       v = src[r * G + g];
     }
-    reinterpret_cast<__half *>(out + r * rec + 32 * rb16)[k] = v;
+    reinterpret_cast<__half *>(out + r * rec + codes_bytes)[k] = v;
+  }
+}
+
+// Column-block-major copy of 6-bit down projections, widened to bytes: word (jb, i) holds codes
+// 4 jb .. 4 jb + 3 of row i, one per byte (the canonical row packs 16 codes in 3 words, LSB first).
+__global__ void repack_down6_kernel(const uint32_t *codes, int experts, int din, int dff,
+                                    uint32_t *out_codes) {
+  const int words = dff * 6 / 32;  // canonical words per row
+  const int nblk = dff / 4;
+  const int64_t nc = static_cast<int64_t>(experts) * nblk * din;
+  const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
+  for (int64_t x = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; x < nc;
+       x += stride) {
+    const int64_t i = x % din, t = x / din;
+    const int64_t jb = t % nblk, e = t / nblk;
+    const uint32_t *row = codes + (e * din + i) * words;
+    uint32_t w = 0;
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      const int64_t bit = (jb * 4 + k) * 6;
+      const int wi = static_cast<int>(bit >> 5), sh = static_cast<int>(bit & 31);
+      uint64_t v = row[wi];
+      if (sh + 6 > 32) v |= static_cast<uint64_t>(row[wi + 1]) << 32;
+      w |= static_cast<uint32_t>((v >> sh) & 63u) << (8 * k);
+    }
+    out_codes[x] = w;
+  }
+}
+
+// Gate/up records of 6-bit rows, codes widened to bytes (the scale/bias runs are written by
+// repack_gate_up_kernel with no code words): one thread per byte-quad of a record's codes.
+__global__ void repack_gate_up6_kernel(const uint32_t *g_codes, const uint32_t *u_codes,
+                                       int64_t records, int din, int rec, uint8_t *out) {
+  const int words = din * 6 / 32;  // canonical words per row
+  const int quads = din / 4;       // 32-bit words of a widened row
+  const int64_t n = records * 2 * quads;
+  const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
+  for (int64_t x = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; x < n;
+       x += stride) {
+    const int64_t r = x / (2 * quads);
+    const int q = static_cast<int>(x - r * 2 * quads);
+    const bool up = q >= quads;
+    const int qq = up ? q - quads : q;
+    const uint32_t *row = (up ? u_codes : g_codes) + r * words;
+    uint32_t w = 0;
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      const int bit = (qq * 4 + k) * 6;
+      const int wi = bit >> 5, sh = bit & 31;
+      uint64_t v = row[wi];
+      if (sh + 6 > 32) v |= static_cast<uint64_t>(row[wi + 1]) << 32;
+      w |= static_cast<uint32_t>((v >> sh) & 63u) << (8 * k);
+    }
+    reinterpret_cast<uint32_t *>(out + r * rec)[q] = w;
   }
 }
 
@@ -319,6 +374,7 @@ static bool geom_cols_a(int din, int bits, GateUpGeom *g) {
   g->rb = col_record_bytes(din, bits);   // a stage holds R records
   int R = 1;
   while ((R * 2) * 2 * (din * bits / 8) <= 32 * 1024 && R * 2 * wpr <= kConsumerWarps) R *= 2;
+  if (R < 2) return false;  // a warp takes two tasks of the same lane set: R even
   g->R = R;
   g->T = nk;
   g->tpr = 32 * wpr;
@@ -330,12 +386,16 @@ static bool geom_cols_a(int din, int bits, GateUpGeom *g) {
 bool make_col_plan(const LayerShape &s, int bits_gu, int bits_d, int bits_sh, int grid,
                    int ring_bytes, ColPlan *cp, Plan *plan) {
   const bool sh = s.n_shared > 0;
+  bits_gu = col_gu_bits(bits_gu);   // 6-bit codes are stored widened to bytes
+  const int bits_sh_gu = col_gu_bits(bits_sh);
+  bits_d = col_down_bits(bits_d);
+  bits_sh = col_down_bits(bits_sh);
   if (grid < 1 || grid > kColMaxGrid || (bits_d != 4 && bits_d != 8) ||
       (sh && bits_sh != 4 && bits_sh != 8))
     return false;
   if (s.din > 4 * 2 * kConsumers || s.din % 64) return false;  // two row quads per thread
   if (s.dff > 32767 || s.dff_shared > 32767) return false;    // chunk rows are 16-bit
-  if (!geom_cols_a(s.din, bits_gu, &plan->geo_r) || !geom_cols_a(s.din, bits_sh, &plan->geo_s))
+  if (!geom_cols_a(s.din, bits_gu, &plan->geo_r) || !geom_cols_a(s.din, bits_sh_gu, &plan->geo_s))
     return false;
   cp->cb_r = 32 / bits_d;
   cp->cb_s = sh ? 32 / bits_sh : cp->cb_r;
@@ -496,15 +556,22 @@ cudaError_t launch_repack_gate_up(const uint8_t *g_codes, const __half *g_scales
                                   const __half *u_scales, const __half *u_biases, int experts,
                                   int rows, int din, int bits, uint8_t *out, cudaStream_t stream) {
   if (experts < 1 || rows < 1) return cudaSuccess;
-  const int rb = din * bits / 8, G = din / 64;
+  const int wb = col_gu_bits(bits);               // stored width
+  const int rb = din * wb / 8, G = din / 64;
+  const int rec = col_record_bytes(din, wb);
   const int64_t records = static_cast<int64_t>(experts) * rows;
   const int64_t n = records * (2 * rb / 16 > 4 * G ? 2 * rb / 16 : 4 * G);
   int64_t grid = (n + 255) / 256;
   grid = grid < 1 ? 1 : (grid > 8192 ? 8192 : grid);
+  // codes as they are (4, 8 bits), the scale/bias runs and the padding
   repack_gate_up_kernel<<<static_cast<int>(grid), 256, 0, stream>>>(
       reinterpret_cast<const uint4 *>(g_codes), g_scales, g_biases,
-      reinterpret_cast<const uint4 *>(u_codes), u_scales, u_biases, records, rb / 16, G,
-      col_record_bytes(din, bits), out);
+      reinterpret_cast<const uint4 *>(u_codes), u_scales, u_biases, records,
+      wb == bits ? rb / 16 : 0, G, rec, out);
+  if (wb != bits)  // 6-bit rows: the codes widened to bytes
+    repack_gate_up6_kernel<<<static_cast<int>(grid), 256, 0, stream>>>(
+        reinterpret_cast<const uint32_t *>(g_codes), reinterpret_cast<const uint32_t *>(u_codes),
+        records, din, rec, out);
   return cudaGetLastError();
 }
 
@@ -516,9 +583,13 @@ cudaError_t launch_repack_down(const uint8_t *codes, const __half *scales, const
   const int64_t n = static_cast<int64_t>(experts) * din * (words > groups ? words : groups);
   int64_t grid = (n + 255) / 256;
   grid = grid < 1 ? 1 : (grid > 4096 ? 4096 : grid);
+  // the scale/bias pairs (and, below 6 bits, the codes as they are)
   repack_down_kernel<<<static_cast<int>(grid), 256, 0, stream>>>(
-      reinterpret_cast<const uint32_t *>(codes), scales, biases, experts, din, words, groups,
-      out_codes, out_sb);
+      reinterpret_cast<const uint32_t *>(codes), scales, biases, experts, din,
+      bits == 6 ? 0 : words, groups, out_codes, out_sb);
+  if (bits == 6)
+    repack_down6_kernel<<<static_cast<int>(grid), 256, 0, stream>>>(
+        reinterpret_cast<const uint32_t *>(codes), experts, din, dff, out_codes);
   return cudaGetLastError();
 }
 

@@ -86,8 +86,14 @@ struct GroupPlan {
 // activations locally and multiplies them into the matching columns of the down projections, so
 // the down weights are read in a column-block-major copy made at create time:
 //   codes  [experts][dff / cb][din] 32-bit words; word (jb, i) holds the cb = 32 / bits codes of
-//          row i, columns jb * cb .. jb * cb + cb - 1, exactly as in the canonical row (LSB first)
+//          row i, columns jb * cb .. jb * cb + cb - 1, exactly as in the canonical row (LSB first);
+//          6-bit codes are widened to one byte each (cb = 4, the 8-bit layout: exact, codes < 64)
 //   sb     [experts][dff / 64][din] (scale, bias) pairs of row i, group g
+
+// Code width of a projection as the column split stores and reads it: 6-bit codes are widened to
+// one byte each (exact: codes < 64), so its kernels take 4- and 8-bit codes only.
+__host__ __device__ inline int col_down_bits(int bits) { return bits == 6 ? 8 : bits; }
+__host__ __device__ inline int col_gu_bits(int bits) { return bits == 6 ? 8 : bits; }
 constexpr int kMaxColsCta = 256;     // activation columns one CTA owns, at most
 constexpr int kMaxColPieces = 16;    // (segment, group) pieces of one CTA's columns, at most
 constexpr int kMaxColBlocks = 64;    // down column blocks one CTA reads, at most
@@ -102,6 +108,7 @@ struct ColDownDev {
 
 // Gate/up rows of the column split as records, one per row pair j of each expert:
 //   [gate codes: rb][up codes: rb][gate scales: G][gate biases: G][up scales: G][up biases: G],
+// (6-bit codes stored as bytes, col_gu_bits)
 // the four fp16 runs padded together to a multiple of 16 bytes (rec bytes per record), so that
 // the R row pairs of a stage are one contiguous bulk copy.
 struct ColPtrs {

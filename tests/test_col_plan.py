@@ -25,6 +25,9 @@ CASES = [ALL["qwen3_stack_8bit"], ALL["e512_stack"], ALL["qwen3_layer_4bit"],
          ALL["qwen15_layer_shared"],
          Shape("small", 256, 128, 8, 2, 8, 8, 8, n_shared=1, dff_shared=128, bits_shared=4),
          Shape("ragged", 384, 192, 10, 3, 4, 4, 4),
+         Shape("6-bit down", 256, 128, 8, 2, 8, 8, 6, n_shared=1, dff_shared=128, bits_shared=6),
+         Shape("6-bit gate/up", 256, 128, 8, 2, 6, 6, 8),
+         ALL["dots_stack_mixed"],
          Shape("fewer columns than CTAs", 64, 64, 4, 2, 8, 8, 4),
          Shape("shared only", 256, 64, 1, 0, 8, 8, 8, n_shared=2, dff_shared=128, bits_shared=8)]
 
@@ -51,7 +54,7 @@ def test_pieces_tile_the_columns_once(built, shape, grid):
         for seg, j0, j1, a0, blk0, nb, pb, grp in pieces:
             routed = seg < K
             width, bits = (dff, shape.bits_down) if routed else (dsh, bsh)
-            cb = 32 // bits
+            cb = 32 // (8 if bits == 6 else bits)   # 6-bit codes are stored as bytes
             base = seg * dff if routed else K * dff + (seg - K) * dsh
             assert 0 <= seg < K + nsh
             assert base + j0 == u0 + a0 == nxt          # contiguous, in column order
@@ -72,7 +75,7 @@ def test_bad_arguments_are_rejected(built):
         Bn.col_pieces(8, 768, 0, 0, 8, 8, 152, 152)     # cta outside the grid
     assert e.value.rc == Bn.MOE_ERR_INVALID_ARG
     with pytest.raises(Bn.MoeError) as e:
-        Bn.col_pieces(8, 768, 0, 0, 6, 6, 0, 152)       # 6-bit down codes: not this kernel
+        Bn.col_pieces(8, 768, 0, 0, 5, 5, 0, 152)       # 5-bit codes: no such format
     assert e.value.rc == Bn.MOE_ERR_UNSUPPORTED
     with pytest.raises(Bn.MoeError) as e:
         Bn.col_pieces(8, 100, 0, 0, 8, 8, 0, 152)       # width not a multiple of 64
@@ -87,7 +90,8 @@ def test_plan_stages_fit_the_ring_and_the_slab_rows(built, shape):
     grid = 152
     p = Bn.col_plan(shape, grid, RING)
     bsh = shape.bits_shared if shape.n_shared else shape.bits_down
-    assert p["cb_r"] == 32 // shape.bits_down and p["cb_s"] == 32 // bsh
+    wide = lambda b: 8 if b == 6 else b                # 6-bit down codes are stored as bytes
+    assert p["cb_r"] == 32 // wide(shape.bits_down) and p["cb_s"] == 32 // wide(bsh)
     assert 2 <= p["stages"] <= 12 and p["stages"] * p["stage_bytes"] <= RING
     assert p["stage_bytes"] % 128 == 0
     assert 1 <= p["nbs"] <= 16 and (p["nbs"] + 1) * shape.din * 4 <= p["stage_bytes"]
@@ -97,7 +101,7 @@ def test_plan_stages_fit_the_ring_and_the_slab_rows(built, shape):
     classes += [(p["rows_a_s"], bsh)] if shape.n_shared else []
     wpr = -(-shape.din // 1024)
     for rows, bits in classes:
-        assert 2 * rows * shape.din * bits // 8 <= p["stage_bytes"]
+        assert 2 * rows * shape.din * wide(bits) // 8 <= p["stage_bytes"]
         assert rows & (rows - 1) == 0 and 16 % (rows * wpr) == 0
     # every output row quad has exactly one owner CTA, whose quads fit its ro rows
     nq, ro = shape.din // 4, p["ro"]
@@ -112,10 +116,8 @@ def test_plan_stages_fit_the_ring_and_the_slab_rows(built, shape):
 
 
 def test_plan_refuses_what_the_kernel_does_not_take(built):
-    six = Shape("6-bit down", 256, 128, 8, 2, 8, 8, 6)
-    six_gu = Shape("6-bit gate/up", 256, 128, 8, 2, 6, 6, 8)
     wide = Shape("din 8192", 8192, 128, 4, 2, 8, 8, 8)
-    for shape in (six, six_gu, wide):
+    for shape in (wide,):
         with pytest.raises(Bn.MoeError) as e:
             Bn.col_plan(shape, 152, RING)
         assert e.value.rc == Bn.MOE_ERR_UNSUPPORTED

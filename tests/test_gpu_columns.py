@@ -56,6 +56,8 @@ LAYERS = {
                                                       shared_gate=1, seed=41),
     # 4-bit down under 4-bit gate/up, ragged widths (din not a multiple of 1024: idle lanes)
     "384x192 E10 K3 4/4/4": Shape("c2", 384, 192, 10, 3, 4, 4, 4, seed=42),
+    # 6-bit gate/up (stored as bytes in the records), 4-bit down
+    "384x192 E10 K3 6/6/4": Shape("c2b", 384, 192, 10, 3, 6, 6, 4, seed=55),
     # fewer columns than CTAs: most CTAs own nothing and contribute zero partials
     "64x64 E4 K2 8/8/4": Shape("c3", 64, 64, 4, 2, 8, 8, 4, seed=43),
     # din > 2048: two row quads per thread; two ungated 8-bit shared experts
@@ -64,15 +66,23 @@ LAYERS = {
     # shared experts only
     "256 shared only 8-bit": Shape("c5", 256, 64, 1, 0, 8, 8, 8, n_shared=2, dff_shared=128,
                                    bits_shared=8, shared_gate=1, seed=45),
+    # 6-bit down codes (widened to bytes in the column-block copy), 8-bit shared expert
+    "512x192 E6 K2 8/8/6 + shared 6-bit": Shape("c8", 512, 192, 6, 2, 8, 8, 6, n_shared=1,
+                                               dff_shared=128, bits_shared=6, seed=53),
     "qwen3-30b-a3b layer (full size)": QWEN3_30B_A3B_4BIT_LAYER,
     "qwen1.5-moe-a2.7b layer (full size)": QWEN15_MOE_A27B_LAYER,
+    # dots.llm1-like layer: din 4096, 4-bit gate/up, 6-bit down, two ungated 4-bit shared experts
+    "dots-like layer 4/4/6 (full size)": Shape("dots-like layer", 4096, 1408, 128, 6, 4, 4, 6,
+                                                n_shared=2, dff_shared=1408, bits_shared=4,
+                                                seed=54),
 }
 
 
 @pytest.mark.parametrize("name", list(LAYERS))
 def test_columns_layer_matches_oracle_on_every_row(name):
     shape = LAYERS[name]
-    layer = C.host_layer_device(shape)
+    layer = (C.host_layer_device(shape) if shape.layer_weight_bytes() < 1 << 30
+             else Bn.synth_layer_device(shape, 0))
     x, r, ids, sc = C.token_inputs(shape)
     out, err = run_layer(layer, x, r, ids, sc)
     assert err == 0
@@ -180,13 +190,9 @@ def test_columns_full_size_stack(name):
 
 
 def test_columns_mode_rejects_what_it_does_not_run():
-    six = C.host_layer_device(Shape("c6", 128, 64, 4, 2, 4, 4, 6, seed=50))
+    wide = C.host_layer_device(Shape("c6w", 8192, 64, 2, 1, 4, 4, 8, seed=52))
     with pytest.raises(Bn.MoeError) as e:
-        Bn.MoeDecode(six, kernel_mode=COLS)            # 6-bit down codes
-    assert e.value.rc == Bn.MOE_ERR_UNSUPPORTED
-    six_gu = C.host_layer_device(Shape("c6g", 128, 64, 4, 2, 6, 6, 8, seed=52))
-    with pytest.raises(Bn.MoeError) as e:
-        Bn.MoeDecode(six_gu, kernel_mode=COLS)         # 6-bit gate/up codes
+        Bn.MoeDecode(wide, kernel_mode=COLS)           # din above 4096
     assert e.value.rc == Bn.MOE_ERR_UNSUPPORTED
     ok = C.host_layer_device(Shape("c7", 128, 64, 4, 2, 4, 4, 8, layers=2, seed=51))
     with pytest.raises(Bn.MoeError) as e:
