@@ -369,7 +369,8 @@ def run_reference(args, shape: Shape):
 def mode_of(kernels: str) -> int:
     from quantized_moe_expert_dequant_gb300 import binding as Bn
     return {"fused": Bn.KERNELS_FUSED, "separate": Bn.KERNELS_SEPARATE,
-            "columns": Bn.KERNELS_COLUMNS, "columns-ahead": Bn.KERNELS_COLUMNS_AHEAD}[kernels]
+            "columns": Bn.KERNELS_COLUMNS, "columns-ahead": Bn.KERNELS_COLUMNS_AHEAD,
+            "mma": Bn.KERNELS_MMA}[kernels]
 
 
 def run_ours(args, shape: Shape):
@@ -555,9 +556,12 @@ def run_ours(args, shape: Shape):
     ach_b = mean_b / (ms_b * 1e-3) / 1e9
     one_launch = (Bn.KERNELS_FUSED, Bn.KERNELS_COLUMNS, Bn.KERNELS_COLUMNS_AHEAD)
     dominant = {Bn.KERNELS_FUSED: "fused_kernel", Bn.KERNELS_COLUMNS: "cols_kernel",
-                Bn.KERNELS_COLUMNS_AHEAD: "cols_kernel"}.get(mode, "gate_up_kernel")
-    if mode in one_launch:
-        # one launch per step: the step's bytes over the step's device time
+                Bn.KERNELS_COLUMNS_AHEAD: "cols_kernel",
+                Bn.KERNELS_MMA: "mma path (route, gate_up_mma, down_mma, tail per layer)"
+                }.get(mode, "gate_up_kernel")
+    if mode in one_launch or mode == Bn.KERNELS_MMA:
+        # the step's bytes over the step's device time (one launch per step, or the tensor-core
+        # path's four launches per layer taken together)
         ach, per_launch_bytes, per_launch_us = (step_bytes / (ms_per_step * 1e-3) / 1e9,
                                                 step_bytes, ms_per_step * 1e3)
     else:
@@ -608,7 +612,8 @@ def run_ours(args, shape: Shape):
         "cpu_baseline": cpu,
         "e2e": {"value": world * m * e2e_steps / e2e_s * (L if args.single_layer else 1),
                 "unit": unit, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
-        "gpu_launches": args.steps if mode in one_launch else args.steps * L * m * 2,
+        "gpu_launches": (args.steps if mode in one_launch else
+                         args.steps * L * 4 if mode == Bn.KERNELS_MMA else args.steps * L * m * 2),
         "clocks": clocks,
         "samples": sample_stats(samp_a),
     }
@@ -846,7 +851,8 @@ def main(argv=None):
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", choices=sorted(ALL), default=DEFAULT_WORKLOAD)
     ap.add_argument("--tokens", type=int, default=1)
-    ap.add_argument("--kernels", choices=["auto", "fused", "separate", "columns", "columns-ahead"],
+    ap.add_argument("--kernels", choices=["auto", "fused", "separate", "columns", "columns-ahead",
+                                          "mma"],
                     default="auto",
                     help="one persistent kernel per step (row split, two device-wide barriers "
                          "per layer), kernel A and kernel B per layer, one persistent kernel "
@@ -859,7 +865,7 @@ def main(argv=None):
     ap.add_argument("--samples", type=int, default=10,
                     help="timed samples after the K steps (at least 10), each of at least 5 "
                          "replays and about 100 ms")
-    ap.add_argument("--ab", choices=["fused", "separate", "columns", "columns-ahead"],
+    ap.add_argument("--ab", choices=["fused", "separate", "columns", "columns-ahead", "mma"],
                     default=None,
                     help="also time this kernel mode, its samples alternating with the main "
                          "mode's (A/B on the same box and weights)")

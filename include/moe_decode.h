@@ -69,7 +69,7 @@ typedef struct moe_decode_config {
   int32_t resid_dtype;     /* MOE_DTYPE_BF16 or MOE_DTYPE_F32 */
   int32_t out_dtype;       /* MOE_DTYPE_F32 (default) or MOE_DTYPE_BF16 (rounded to nearest) */
   int32_t kernel_mode;     /* MOE_KERNELS_FUSED (default), _SEPARATE, _COLUMNS, _COLUMNS_AHEAD,
-                              _POOL */
+                              _POOL, _MMA */
 } moe_decode_config;
 
 /* How a layer is launched.  FUSED: one cooperative persistent kernel per forward (or per stack
@@ -103,12 +103,23 @@ typedef struct moe_decode_config {
  * exactly the page's association.  moe_decode_routes copies the per-slot outputs out.  It is the
  * unfused counterpart of the other modes, which fold the score or the scalar into the activation
  * and sum routed and shared terms in one accumulation; results agree within the parity bound. */
+/* MMA: the batch form on tensor cores, for a few to a few dozen tokens.  The m tokens' slots are
+ * grouped by expert (distinct ids ascending, pairs in (token, slot) order); each selected expert's
+ * gate/up and down rows are read once for all the tokens that name it, in tiles of 16 rows x 8
+ * (token, slot) pairs on mma.sync bf16 instructions (codes enter exactly as bf16 integers, 8-bit
+ * codes as two nibble tiles; x exactly; the fp32 activation as a bf16 high part plus a bf16
+ * remainder; fp32 accumulation; the group scale and bias applied per 64 codes).  Four launches
+ * per layer: route and shared scalars, gate/up, down, tail (out = resid + the valid slots in slot
+ * order + the shared experts).  Requires max_tokens <= 64, max_tokens * top_k <= 256,
+ * n_experts <= 1024; the chained stack and moe_stack_step_parts (one phase) do not take it.
+ * Deterministic; equal to the other modes within the parity bound. */
 enum {
   MOE_KERNELS_FUSED = 0,
   MOE_KERNELS_SEPARATE = 1,
   MOE_KERNELS_COLUMNS = 2,
   MOE_KERNELS_COLUMNS_AHEAD = 3,
-  MOE_KERNELS_POOL = 4
+  MOE_KERNELS_POOL = 4,
+  MOE_KERNELS_MMA = 5
 };
 
 /*

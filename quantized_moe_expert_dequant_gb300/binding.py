@@ -24,6 +24,7 @@ MOE_OK, MOE_ERR_INVALID_ARG, MOE_ERR_UNSUPPORTED, MOE_ERR_CUDA, MOE_ERR_OOM, MOE
 DTYPE_BF16, DTYPE_F32 = 0, 1
 PART_GATE_UP, PART_DOWN = 1, 2
 KERNELS_FUSED, KERNELS_SEPARATE, KERNELS_COLUMNS, KERNELS_COLUMNS_AHEAD, KERNELS_POOL = 0, 1, 2, 3, 4
+KERNELS_MMA = 5
 NOALLOC_MAX_ACT_FLOATS = 65536
 _STATUS = {0: "MOE_OK", -1: "MOE_ERR_INVALID_ARG", -2: "MOE_ERR_UNSUPPORTED", -3: "MOE_ERR_CUDA",
            -4: "MOE_ERR_OOM", -5: "MOE_ERR_BAD_ID", -6: "MOE_ERR_TIMEOUT",

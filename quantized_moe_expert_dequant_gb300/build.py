@@ -25,7 +25,7 @@ LIB = os.path.join(PKG, "libmoe_decode.so")
 LIB_TIMELINE = os.path.join(PKG, "libmoe_decode_timeline.so")
 SOURCES = ["moe_kernels_g4.cu", "moe_kernels_g6.cu", "moe_kernels_g8.cu", "moe_grouped_g4.cu",
            "moe_grouped_g6.cu", "moe_grouped_g8.cu", "moe_cols_g4.cu", "moe_cols_g6.cu",
-           "moe_cols_g8.cu", "moe_kernels.cu",
+           "moe_cols_g8.cu", "moe_kernels.cu", "moe_mma.cu",
            "moe_api.cu", "moe_pack.cpp", "synth.cu", "gemv.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 

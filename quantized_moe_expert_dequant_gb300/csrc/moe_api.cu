@@ -8,6 +8,7 @@
 
 #include "moe_decode.h"
 #include "moe_kernels.cuh"
+#include "moe_mma.cuh"
 #include "moe_timeline.cuh"
 
 namespace {
@@ -42,7 +43,8 @@ int validate_config(const moe_decode_config *c) {
     return MOE_ERR_INVALID_ARG;
   if (c->out_dtype != MOE_DTYPE_BF16 && c->out_dtype != MOE_DTYPE_F32) return MOE_ERR_INVALID_ARG;
   if (c->kernel_mode != MOE_KERNELS_FUSED && c->kernel_mode != MOE_KERNELS_SEPARATE &&
-      c->kernel_mode != MOE_KERNELS_POOL && !cols_mode(c->kernel_mode))
+      c->kernel_mode != MOE_KERNELS_POOL && c->kernel_mode != MOE_KERNELS_MMA &&
+      !cols_mode(c->kernel_mode))
     return MOE_ERR_INVALID_ARG;
   // int32 indexing of the activation vector and of one expert's rows
   const int64_t act = (int64_t)c->top_k * c->dff + (int64_t)c->n_shared * c->dff_shared;
@@ -127,6 +129,11 @@ int prepare(const moe_decode_config *c, Prepared &P) {
                                       c->max_tokens > 1 ? c->max_tokens : 2, &P.gplan) &&
                  P.gplan.smem <= (size_t)dyn_limit;
   if (pool && !P.grouped_ok) return MOE_ERR_UNSUPPORTED;
+  // the tensor-core batch kernels group at most kMaxPairs slots of kMaxGroupTokens tokens
+  if (c->kernel_mode == MOE_KERNELS_MMA &&
+      (c->max_tokens > moe::kMaxGroupTokens || c->max_tokens * c->top_k > moe::kMaxPairs ||
+       c->n_experts > moe::kMaxGroupExperts))
+    return MOE_ERR_UNSUPPORTED;
   P.grid_sep = sms;
   const int lim = moe::fused_grid_limit(P.plan, c->bits_gate, c->bits_down, P.bits_sh);
   P.grid_fused = lim < sms ? lim : sms;
@@ -392,8 +399,11 @@ struct Workspace {
   moe::LayerPtrs *layers = nullptr;
   float *slab = nullptr;  // column-split mode: [2][grid][din] partial outputs
   int32_t *ids_used = nullptr;  // handles: [max_tokens][top_k] ids the last forward's kernels read
+  int32_t *route = nullptr;     // tensor-core batch mode: the batch's route (kMmaRouteInts)
+  float *sscal = nullptr;       // tensor-core batch mode: [max_tokens] shared scalars
 
-  // Grouped forwards keep every token's activations and per-slot partial outputs at once.
+  // Grouped forwards (and the tensor-core batch mode) keep every token's activations and
+  // per-slot partial outputs at once.
   bool alloc(const moe_decode_config &c, int n_layers, bool grouped, size_t nslab = 0) {
     const size_t na = act_floats(c) * (grouped ? c.max_tokens : 1);
     const size_t ny = grouped ? (size_t)c.max_tokens * (c.top_k + c.n_shared) * c.din : 1;
@@ -405,7 +415,9 @@ struct Workspace {
               cudaMalloc(&layers, sizeof(moe::LayerPtrs) * n_layers) == cudaSuccess &&
               (nslab == 0 || cudaMalloc(&slab, nslab * sizeof(float)) == cudaSuccess) &&
               cudaMalloc(&ids_used, (size_t)c.max_tokens * (c.top_k > 0 ? c.top_k : 1) *
-                                        sizeof(int32_t)) == cudaSuccess;
+                                        sizeof(int32_t)) == cudaSuccess &&
+              cudaMalloc(&route, moe::kMmaRouteInts * sizeof(int32_t)) == cudaSuccess &&
+              cudaMalloc(&sscal, (size_t)c.max_tokens * sizeof(float)) == cudaSuccess;
     if (!ok) cudaGetLastError();
     return ok;
   }
@@ -417,8 +429,36 @@ struct Workspace {
     cudaFree(layers);
     cudaFree(slab);
     cudaFree(ids_used);
+    cudaFree(route);
+    cudaFree(sscal);
   }
 };
+
+// Tensor-core batch kernels (moe_mma.cu) for the m tokens of one layer.
+cudaError_t enqueue_mma(const Prepared &P, const moe::LayerPtrs &w, const Workspace &ws,
+                        const void *x, int m, const int32_t *ids, const float *scores,
+                        const void *resid, int resid_dtype, void *out, int out_dtype,
+                        cudaStream_t stream, int32_t *ids_used = nullptr) {
+  moe::MmaParams p;
+  p.s = P.shape;
+  p.w = w;
+  p.m = m;
+  p.x = static_cast<const uint16_t *>(x);
+  p.ids = ids;
+  p.scores = scores;
+  p.resid = resid;
+  p.out = out;
+  p.resid_f32 = resid_dtype == MOE_DTYPE_F32;
+  p.out_f32 = out_dtype == MOE_DTYPE_F32;
+  p.route = ws.route;
+  p.sscal = ws.sscal;
+  p.act = ws.act;
+  p.act_stride = static_cast<int>(act_floats(P.cfg));
+  p.y = ws.y;
+  p.err = ws.err;
+  p.ids_used = ids_used;
+  return moe::launch_mma_layer(p, P.cfg.bits_gate, P.cfg.bits_down, P.bits_sh, stream);
+}
 
 }  // namespace
 
@@ -447,7 +487,8 @@ extern "C" int moe_decode_create(const moe_decode_config *cfg, const moe_layer_w
     return rc;
   }
   h->w = layer_ptrs(*cfg, *weights);
-  if (!h->ws.alloc(*cfg, 1, h->P.grouped_ok, slab_floats(h->P))) {
+  if (!h->ws.alloc(*cfg, 1, h->P.grouped_ok || cfg->kernel_mode == MOE_KERNELS_MMA,
+                   slab_floats(h->P))) {
     h->ws.release();
     delete h;
     return MOE_ERR_OOM;
@@ -488,6 +529,9 @@ extern "C" int moe_decode_forward(moe_decode_t *h, const void *x, int32_t m, con
   if (cols_mode(c.kernel_mode))
     e = enqueue_cols(h->P, h->ws.layers, h->cw.dev, 1, h->ws.slab, h->ws.err, h->ws.bar, x, ids,
                      scores, resid, c.resid_dtype, out, c.out_dtype, st, nullptr, used);
+  else if (c.kernel_mode == MOE_KERNELS_MMA)
+    e = enqueue_mma(h->P, h->w, h->ws, x, m, ids, scores, resid, c.resid_dtype, out, c.out_dtype,
+                    st, used);
   else if (c.kernel_mode == MOE_KERNELS_FUSED || c.kernel_mode == MOE_KERNELS_POOL)
     e = enqueue_fused(h->P, h->ws.layers, 1, h->ws.act, h->ws.y, h->ws.err, h->ws.bar, nullptr,
                       nullptr, x, m, ids, scores, resid, c.resid_dtype, out, c.out_dtype, st,
@@ -688,7 +732,8 @@ int stack_create(const moe_decode_config *cfg, int32_t n_layers, const moe_layer
   int rc = validate_config(cfg);
   if (rc != MOE_OK) return rc;
   if (cfg->out_dtype != MOE_DTYPE_F32) return MOE_ERR_INVALID_ARG;
-  if (norm_weight && cols_mode(cfg->kernel_mode)) return MOE_ERR_UNSUPPORTED;
+  if (norm_weight && (cols_mode(cfg->kernel_mode) || cfg->kernel_mode == MOE_KERNELS_MMA))
+    return MOE_ERR_UNSUPPORTED;
   for (int l = 0; l < n_layers; ++l) {
     rc = validate_weights(cfg, &layers[l]);
     if (rc != MOE_OK) return rc;
@@ -708,7 +753,8 @@ int stack_create(const moe_decode_config *cfg, int32_t n_layers, const moe_layer
   s->layers.resize(n_layers);
   for (int l = 0; l < n_layers; ++l) s->layers[l] = layer_ptrs(*cfg, layers[l]);
   const size_t M = cfg->max_tokens, din = cfg->din, K = cfg->top_k;
-  bool ok = s->ws.alloc(*cfg, n_layers, s->P.grouped_ok, slab_floats(s->P)) &&
+  bool ok = s->ws.alloc(*cfg, n_layers, s->P.grouped_ok || cfg->kernel_mode == MOE_KERNELS_MMA,
+                        slab_floats(s->P)) &&
             cudaMalloc(&s->ping[0], M * din * sizeof(float)) == cudaSuccess &&
             cudaMalloc(&s->ping[1], M * din * sizeof(float)) == cudaSuccess &&
             cudaMalloc(&s->x_dev, (size_t)n_layers * M * din * 2) == cudaSuccess &&
@@ -776,6 +822,19 @@ cudaError_t enqueue_stack(moe_stack *s, const void *x, int m, const int32_t *ids
                          s->ping[0], s->ping[1], x, m, ids, scores, resid0, c.resid_dtype, out,
                          MOE_DTYPE_F32, st, s->norm_w, s->norm_eps);
   const size_t din = c.din, K = c.top_k;
+  if (c.kernel_mode == MOE_KERNELS_MMA) {
+    for (int l = 0; l < L; ++l) {
+      const void *xl = static_cast<const uint16_t *>(x) + (size_t)l * m * din;
+      const int32_t *il = ids ? ids + (size_t)l * m * K : nullptr;
+      const float *sl = scores ? scores + (size_t)l * m * K : nullptr;
+      const void *rl = l == 0 ? resid0 : s->ping[(l - 1) & 1];
+      void *ol = l == L - 1 ? out : s->ping[l & 1];
+      cudaError_t e = enqueue_mma(s->P, s->layers[l], s->ws, xl, m, il, sl, rl,
+                                  l == 0 ? c.resid_dtype : MOE_DTYPE_F32, ol, MOE_DTYPE_F32, st);
+      if (e != cudaSuccess) return e;
+    }
+    return cudaSuccess;
+  }
   for (int l = 0; l < L; ++l) {
     NormIn norm;
     if (s->norm_w && l > 0) {
@@ -824,7 +883,8 @@ extern "C" int moe_stack_step_parts(moe_stack_t *s, int32_t parts, const void *x
                                     void *out, void *stream) {
   if (!s || !x || !resid0 || !out) return MOE_ERR_INVALID_ARG;
   if (parts < 1 || parts > (MOE_PART_GATE_UP | MOE_PART_DOWN)) return MOE_ERR_INVALID_ARG;
-  if (cols_mode(s->P.cfg.kernel_mode) && parts != (MOE_PART_GATE_UP | MOE_PART_DOWN))
+  if ((cols_mode(s->P.cfg.kernel_mode) || s->P.cfg.kernel_mode == MOE_KERNELS_MMA) &&
+      parts != (MOE_PART_GATE_UP | MOE_PART_DOWN))
     return MOE_ERR_UNSUPPORTED;
   if (m < 1 || m > s->P.cfg.max_tokens) return MOE_ERR_INVALID_ARG;
   if (s->P.cfg.top_k > 0 && (!ids || !scores)) return MOE_ERR_INVALID_ARG;

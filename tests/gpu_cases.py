@@ -1,7 +1,11 @@
 """Shared builders for the GPU tests: seeded problems, the oracle's expectation, and the parity bar.
 
 Parity bar (fp32-accumulated output): max|gpu - oracle| <= 1e-3 * rms(oracle) + 1e-6 and relative
-L2 error <= 1e-4.  A bf16 output is compared with the oracle rounded to bf16, within one bf16 ulp.
+L2 error <= 1e-4.  A bf16 output must be the bf16 rounding of a value that meets that bar: every
+element within one bf16 ulp of the oracle rounded to bf16, or within the fp32 bar's absolute
+allowance of the oracle plus half a bf16 ulp of the element (near zero one bf16 ulp is finer than
+the fp32 sums' own rounding, so the first test alone would hold a bf16 output to more than the
+fp32 one).
 """
 from __future__ import annotations
 
@@ -12,6 +16,7 @@ from oracle import oracle as O
 from quantized_moe_expert_dequant_gb300 import binding as Bn
 from quantized_moe_expert_dequant_gb300 import synth
 from quantized_moe_expert_dequant_gb300.workloads import Shape
+from tests.oracle_jobs import OracleLayer, oracle_tokens  # noqa: F401  (re-exported)
 
 ATOL_RMS, ATOL_ABS, REL_L2 = 1e-3, 1e-6, 1e-4
 
@@ -54,35 +59,6 @@ def token_inputs(shape: Shape, layer: int = 0, m: int = 1, step: int = 0):
     return x, r, ids, sc
 
 
-class OracleLayer:
-    """The oracle's view of one synthetic layer: experts regenerated on the host on demand."""
-
-    def __init__(self, shape: Shape, layer: int = 0):
-        self.shape, self.layer = shape, layer
-        self._cache = {}
-
-    def packed(self, proj, e, rows, cols, bits):
-        key = (proj, e)
-        if key not in self._cache:
-            c, s, b = synth.expert_proj(self.shape.seed, self.layer, proj, e, rows, cols, bits)
-            self._cache[key] = O.Packed(c, s, b, bits)
-        return self._cache[key]
-
-    def token(self, x_bits, resid, ids, scores, rows=None):
-        sh = self.shape
-        valid = [(int(e), float(w)) for e, w in zip(ids, scores) if 0 <= int(e) < sh.n_experts]
-        g = [self.packed(synth.GATE, e, sh.dff, sh.din, sh.bits_gate) for e, _ in valid]
-        u = [self.packed(synth.UP, e, sh.dff, sh.din, sh.bits_up) for e, _ in valid]
-        d = [self.packed(synth.DOWN, e, sh.din, sh.dff, sh.bits_down) for e, _ in valid]
-        n, w, b = sh.n_shared, sh.dff_shared, sh.bits_shared
-        sg = [self.packed(synth.SH_GATE, i, w, sh.din, b) for i in range(n)]
-        su = [self.packed(synth.SH_UP, i, w, sh.din, b) for i in range(n)]
-        sd = [self.packed(synth.SH_DOWN, i, sh.din, w, b) for i in range(n)]
-        gv = synth.gate_vector(sh.seed, self.layer, sh.din) if (n and sh.shared_gate) else None
-        sc = np.array([w_ for _, w_ in valid], dtype=np.float32)
-        return O.moe_token(x_bits, resid, sc, g, u, d, sg, su, sd, gate_vec_bf16=gv, rows=rows)
-
-
 def parity(gpu, ref) -> tuple[float, float, float]:
     gpu = np.asarray(gpu, dtype=np.float64).reshape(-1)
     ref = np.asarray(ref, dtype=np.float64).reshape(-1)
@@ -104,7 +80,14 @@ def assert_parity_bf16(gpu_bf16: torch.Tensor, ref: np.ndarray, what=""):
     r = synth.bf16_bits_to_f32(synth.f32_to_bf16_bits(ref.astype(np.float32))).astype(np.float64)
     _, e = np.frexp(r)
     ulp = np.ldexp(1.0, e - 8)  # |r| in [2^(e-1), 2^e): bf16 spacing 2^(e-8)
-    assert np.all(np.abs(g - r) <= ulp), f"{what}: bf16 output beyond one ulp"
+    _, eg = np.frexp(g)
+    half_g = np.ldexp(1.0, eg - 9)
+    ref64 = np.asarray(ref, dtype=np.float64).reshape(-1)
+    allow = ATOL_RMS * float(np.sqrt(np.mean(ref64 ** 2))) + ATOL_ABS
+    ok = (np.abs(g - r) <= ulp) | (np.abs(g - ref64) <= allow + half_g)
+    bad = np.nonzero(~ok)[0]
+    assert bad.size == 0, (f"{what}: bf16 output off at {bad[:4].tolist()}: "
+                           f"{g[bad[:4]].tolist()} vs {ref64[bad[:4]].tolist()}")
 
 
 def oracle_stack(shape: Shape, x, ids, sc, resid0, m: int = 1, rows=None, norm=None,

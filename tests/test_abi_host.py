@@ -88,7 +88,7 @@ def _weights(n_proj=6, gate_vec=True, misalign=False):
     (dict(shared_gate=2), Bn.MOE_ERR_INVALID_ARG),
     (dict(resid_dtype=7), Bn.MOE_ERR_INVALID_ARG),
     (dict(out_dtype=-1), Bn.MOE_ERR_INVALID_ARG),
-    (dict(kernel_mode=5), Bn.MOE_ERR_INVALID_ARG),
+    (dict(kernel_mode=6), Bn.MOE_ERR_INVALID_ARG),
 ])
 def test_create_rejects_invalid_config(L, kw, rc):
     h = ctypes.c_void_p()
