@@ -434,14 +434,119 @@ struct Workspace {
   }
 };
 
-// Tensor-core batch kernels (moe_mma.cu) for the m tokens of one layer.
-cudaError_t enqueue_mma(const Prepared &P, const moe::LayerPtrs &w, const Workspace &ws,
-                        const void *x, int m, const int32_t *ids, const float *scores,
-                        const void *resid, int resid_dtype, void *out, int out_dtype,
-                        cudaStream_t stream, int32_t *ids_used = nullptr) {
+// The tensor-core batch mode's own state: each layer's tile-group copy (moe_mma.cuh) and the
+// batch workspace, owned by a handle or a stack.
+struct MmaState {
+  std::vector<void *> bufs;
+  std::vector<moe::MmaLayerDev> layers;
+  int32_t *nc = nullptr;
+  float *xsum = nullptr, *xinv = nullptr, *ainv = nullptr, *asum = nullptr;
+  __half *x16 = nullptr, *a16 = nullptr;
+  float2 *gu_part = nullptr;
+  float *y_part = nullptr;
+  float *zero = nullptr;
+
+  template <class T>
+  bool grab(T **p, size_t bytes) {
+    void *b = nullptr;
+    if (cudaMalloc(&b, bytes > 0 ? bytes : 16) != cudaSuccess) return false;
+    bufs.push_back(b);
+    *p = static_cast<T *>(b);
+    return true;
+  }
+  // MOE_OK, MOE_ERR_OOM or MOE_ERR_CUDA.
+  int build(const moe_decode_config &c, const moe_layer_weights *w, int L) {
+    if (cudaDeviceSynchronize() != cudaSuccess) return MOE_ERR_CUDA;
+    const size_t M = c.max_tokens, gx = c.din / 64, act = act_floats(c), ga = act / 64;
+    const size_t ny = c.top_k + c.n_shared;
+    bool ok = grab(&nc, 2 * sizeof(int32_t)) && grab(&xsum, M * gx * 4) &&
+              grab(&xinv, M * gx * 4) && grab(&x16, M * gx * 128 * 2) &&
+              grab(&gu_part, (size_t)moe::kMmaMaxChunks * M * act * 8) &&
+              grab(&a16, M * ga * 128 * 2) && grab(&ainv, M * ga * 4) &&
+              grab(&asum, M * ga * 4) &&
+              grab(&y_part, (size_t)moe::kMmaMaxChunks * M * ny * c.din * 4) &&
+              grab(&zero, 256) && cudaMemset(zero, 0, 256) == cudaSuccess;
+    if (!ok) {
+      cudaGetLastError();
+      return MOE_ERR_OOM;
+    }
+    const int bsh = c.n_shared > 0 ? c.bits_shared : c.bits_down;
+    layers.resize(L);
+    for (int l = 0; l < L; ++l) {
+      moe::MmaLayerDev d{};
+      const moe_layer_weights &x = w[l];
+      uint8_t *b = nullptr;
+      if (c.top_k > 0) {
+        if (!grab(&b, (size_t)c.n_experts * (c.dff / 16) * (c.din / 64) *
+                          moe::mma_gu_block(c.bits_gate)))
+          return MOE_ERR_OOM;
+        d.gu_r = b;
+        if (moe::launch_repack_mma_gu(
+                static_cast<const uint8_t *>(x.gate.codes), static_cast<const __half *>(x.gate.scales),
+                static_cast<const __half *>(x.gate.biases), static_cast<const uint8_t *>(x.up.codes),
+                static_cast<const __half *>(x.up.scales), static_cast<const __half *>(x.up.biases),
+                c.n_experts, c.dff, c.din, c.bits_gate, b, nullptr) != cudaSuccess)
+          return MOE_ERR_CUDA;
+        if (!grab(&b, (size_t)c.n_experts * (c.din / 16) * (c.dff / 64) *
+                          moe::mma_dn_block(c.bits_down)))
+          return MOE_ERR_OOM;
+        d.dn_r = b;
+        if (moe::launch_repack_mma_down(static_cast<const uint8_t *>(x.down.codes),
+                                        static_cast<const __half *>(x.down.scales),
+                                        static_cast<const __half *>(x.down.biases), c.n_experts,
+                                        c.din, c.dff, c.bits_down, b, nullptr) != cudaSuccess)
+          return MOE_ERR_CUDA;
+      }
+      if (c.n_shared > 0) {
+        if (!grab(&b, (size_t)c.n_shared * (c.dff_shared / 16) * (c.din / 64) *
+                          moe::mma_gu_block(bsh)))
+          return MOE_ERR_OOM;
+        d.gu_s = b;
+        if (moe::launch_repack_mma_gu(
+                static_cast<const uint8_t *>(x.sh_gate.codes),
+                static_cast<const __half *>(x.sh_gate.scales),
+                static_cast<const __half *>(x.sh_gate.biases),
+                static_cast<const uint8_t *>(x.sh_up.codes),
+                static_cast<const __half *>(x.sh_up.scales),
+                static_cast<const __half *>(x.sh_up.biases), c.n_shared, c.dff_shared, c.din, bsh,
+                b, nullptr) != cudaSuccess)
+          return MOE_ERR_CUDA;
+        if (!grab(&b, (size_t)c.n_shared * (c.din / 16) * (c.dff_shared / 64) *
+                          moe::mma_dn_block(bsh)))
+          return MOE_ERR_OOM;
+        d.dn_s = b;
+        if (moe::launch_repack_mma_down(static_cast<const uint8_t *>(x.sh_down.codes),
+                                        static_cast<const __half *>(x.sh_down.scales),
+                                        static_cast<const __half *>(x.sh_down.biases), c.n_shared,
+                                        c.din, c.dff_shared, bsh, b, nullptr) != cudaSuccess)
+          return MOE_ERR_CUDA;
+      }
+      layers[l] = d;
+    }
+    return cudaDeviceSynchronize() == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
+  }
+  void release() {
+    for (void *b : bufs) cudaFree(b);
+    bufs.clear();
+    layers.clear();
+  }
+};
+
+// Tensor-core batch kernels (moe_mma.cu) for the m tokens of layer l.
+cudaError_t enqueue_mma(const Prepared &P, const moe::LayerPtrs &w, const MmaState &ms, int l,
+                        const Workspace &ws, const void *x, int m, const int32_t *ids,
+                        const float *scores, const void *resid, int resid_dtype, void *out,
+                        int out_dtype, cudaStream_t stream, int32_t *ids_used = nullptr) {
+  const moe_decode_config &c = P.cfg;
   moe::MmaParams p;
+  std::memset(&p, 0, sizeof p);
   p.s = P.shape;
   p.w = w;
+  p.t = ms.layers[l];
+  p.bits_r = c.bits_gate;
+  p.bits_s = P.bits_sh;
+  p.bits_dr = c.bits_down;
+  p.bits_ds = P.bits_sh;
   p.m = m;
   p.x = static_cast<const uint16_t *>(x);
   p.ids = ids;
@@ -450,14 +555,22 @@ cudaError_t enqueue_mma(const Prepared &P, const moe::LayerPtrs &w, const Worksp
   p.out = out;
   p.resid_f32 = resid_dtype == MOE_DTYPE_F32;
   p.out_f32 = out_dtype == MOE_DTYPE_F32;
+  p.act_stride = static_cast<int>(act_floats(c));
   p.route = ws.route;
+  p.nc = ms.nc;
   p.sscal = ws.sscal;
-  p.act = ws.act;
-  p.act_stride = static_cast<int>(act_floats(P.cfg));
-  p.y = ws.y;
+  p.xsum = ms.xsum;
+  p.xinv = ms.xinv;
+  p.x16 = ms.x16;
+  p.gu_part = ms.gu_part;
+  p.a16 = ms.a16;
+  p.ainv = ms.ainv;
+  p.asum = ms.asum;
+  p.y_part = ms.y_part;
+  p.zero = ms.zero;
   p.err = ws.err;
   p.ids_used = ids_used;
-  return moe::launch_mma_layer(p, P.cfg.bits_gate, P.cfg.bits_down, P.bits_sh, stream);
+  return moe::launch_mma_layer(p, stream);
 }
 
 }  // namespace
@@ -468,6 +581,7 @@ struct moe_decode {
   moe::LayerPtrs w;
   Workspace ws;
   ColWeights cw;
+  MmaState mma;
   int last_m = 0;  // tokens of the last forward (moe_decode_routes)
 };
 
@@ -487,8 +601,7 @@ extern "C" int moe_decode_create(const moe_decode_config *cfg, const moe_layer_w
     return rc;
   }
   h->w = layer_ptrs(*cfg, *weights);
-  if (!h->ws.alloc(*cfg, 1, h->P.grouped_ok || cfg->kernel_mode == MOE_KERNELS_MMA,
-                   slab_floats(h->P))) {
+  if (!h->ws.alloc(*cfg, 1, h->P.grouped_ok, slab_floats(h->P))) {
     h->ws.release();
     delete h;
     return MOE_ERR_OOM;
@@ -497,6 +610,15 @@ extern "C" int moe_decode_create(const moe_decode_config *cfg, const moe_layer_w
     rc = h->cw.build(*cfg, weights, 1);
     if (rc != MOE_OK) {
       h->cw.release();
+      h->ws.release();
+      delete h;
+      return rc;
+    }
+  }
+  if (cfg->kernel_mode == MOE_KERNELS_MMA) {
+    rc = h->mma.build(*cfg, weights, 1);
+    if (rc != MOE_OK) {
+      h->mma.release();
       h->ws.release();
       delete h;
       return rc;
@@ -530,8 +652,8 @@ extern "C" int moe_decode_forward(moe_decode_t *h, const void *x, int32_t m, con
     e = enqueue_cols(h->P, h->ws.layers, h->cw.dev, 1, h->ws.slab, h->ws.err, h->ws.bar, x, ids,
                      scores, resid, c.resid_dtype, out, c.out_dtype, st, nullptr, used);
   else if (c.kernel_mode == MOE_KERNELS_MMA)
-    e = enqueue_mma(h->P, h->w, h->ws, x, m, ids, scores, resid, c.resid_dtype, out, c.out_dtype,
-                    st, used);
+    e = enqueue_mma(h->P, h->w, h->mma, 0, h->ws, x, m, ids, scores, resid, c.resid_dtype, out,
+                    c.out_dtype, st, used);
   else if (c.kernel_mode == MOE_KERNELS_FUSED || c.kernel_mode == MOE_KERNELS_POOL)
     e = enqueue_fused(h->P, h->ws.layers, 1, h->ws.act, h->ws.y, h->ws.err, h->ws.bar, nullptr,
                       nullptr, x, m, ids, scores, resid, c.resid_dtype, out, c.out_dtype, st,
@@ -573,6 +695,7 @@ extern "C" int moe_decode_get_error(moe_decode_t *h, int32_t *device_error) {
 extern "C" void moe_decode_destroy(moe_decode_t *h) {
   if (!h) return;
   h->cw.release();
+  h->mma.release();
   h->ws.release();
   delete h;
 }
@@ -692,6 +815,7 @@ struct moe_stack {
   std::vector<moe::LayerPtrs> layers;
   Workspace ws;
   ColWeights cw;
+  MmaState mma;
   float *ping[2] = {nullptr, nullptr};
   cudaStream_t cap = nullptr;
   std::vector<GraphEntry> graphs;
@@ -711,6 +835,7 @@ extern "C" void moe_stack_destroy(moe_stack_t *s) {
   for (auto &g : s->graphs) cudaGraphExecDestroy(g.exec);
   if (s->cap) cudaStreamDestroy(s->cap);
   s->cw.release();
+  s->mma.release();
   s->ws.release();
   cudaFree(s->ping[0]);
   cudaFree(s->ping[1]);
@@ -753,8 +878,7 @@ int stack_create(const moe_decode_config *cfg, int32_t n_layers, const moe_layer
   s->layers.resize(n_layers);
   for (int l = 0; l < n_layers; ++l) s->layers[l] = layer_ptrs(*cfg, layers[l]);
   const size_t M = cfg->max_tokens, din = cfg->din, K = cfg->top_k;
-  bool ok = s->ws.alloc(*cfg, n_layers, s->P.grouped_ok || cfg->kernel_mode == MOE_KERNELS_MMA,
-                        slab_floats(s->P)) &&
+  bool ok = s->ws.alloc(*cfg, n_layers, s->P.grouped_ok, slab_floats(s->P)) &&
             cudaMalloc(&s->ping[0], M * din * sizeof(float)) == cudaSuccess &&
             cudaMalloc(&s->ping[1], M * din * sizeof(float)) == cudaSuccess &&
             cudaMalloc(&s->x_dev, (size_t)n_layers * M * din * 2) == cudaSuccess &&
@@ -773,6 +897,13 @@ int stack_create(const moe_decode_config *cfg, int32_t n_layers, const moe_layer
       cudaStreamCreateWithFlags(&s->cap, cudaStreamNonBlocking) != cudaSuccess) {
     moe_stack_destroy(s);
     return MOE_ERR_CUDA;
+  }
+  if (cfg->kernel_mode == MOE_KERNELS_MMA) {
+    rc = s->mma.build(*cfg, layers, n_layers);
+    if (rc != MOE_OK) {
+      moe_stack_destroy(s);
+      return rc;
+    }
   }
   if (cols_mode(cfg->kernel_mode)) {
     rc = s->cw.build(*cfg, layers, n_layers);
@@ -829,7 +960,7 @@ cudaError_t enqueue_stack(moe_stack *s, const void *x, int m, const int32_t *ids
       const float *sl = scores ? scores + (size_t)l * m * K : nullptr;
       const void *rl = l == 0 ? resid0 : s->ping[(l - 1) & 1];
       void *ol = l == L - 1 ? out : s->ping[l & 1];
-      cudaError_t e = enqueue_mma(s->P, s->layers[l], s->ws, xl, m, il, sl, rl,
+      cudaError_t e = enqueue_mma(s->P, s->layers[l], s->mma, l, s->ws, xl, m, il, sl, rl,
                                   l == 0 ? c.resid_dtype : MOE_DTYPE_F32, ol, MOE_DTYPE_F32, st);
       if (e != cudaSuccess) return e;
     }
