@@ -397,9 +397,11 @@ def run_ours(args, shape: Shape):
     layers = [Bn.synth_layer_device(shape, l) for l in range(L)]
     chained = args.chain_norm
     kernels = args.kernels
-    if kernels == "auto":   # the column split where it runs, else the row split
+    if kernels == "auto":   # one token: the column split; a batch: the tensor-core tiles
         cols_ok = (m == 1 and not chained and shape.bits_gate in (4, 8) and shape.din <= 4096)
-        kernels = "columns" if cols_ok else "fused"
+        mma_ok = (m > 1 and not chained and m <= 64 and m * shape.top_k <= 256
+                  and shape.n_experts <= 1024)
+        kernels = "columns" if cols_ok else "mma" if mma_ok else "fused"
     mode = mode_of(kernels)
     norm = None
     if chained and L > 1:
@@ -645,7 +647,8 @@ TL_POINTS = {0: "producer: layer top", 1: "producer: barrier seen", 2: "producer
              11: "consumers: planes built", 12: "consumers: down stages consumed",
              13: "consumers: partials written", 14: "consumers: arrived",
              15: "helper: owner's sums and shared scalar done",
-             52: "helper: previous layer's arrivals complete"}
+             52: "helper: previous layer's arrivals complete",
+             53: "producer: stage counts published", 54: "producer: first ring slot claimed"}
 
 
 def timeline_summary(tl: np.ndarray) -> dict:
@@ -854,13 +857,16 @@ def main(argv=None):
     ap.add_argument("--kernels", choices=["auto", "fused", "separate", "columns", "columns-ahead",
                                           "mma"],
                     default="auto",
-                    help="one persistent kernel per step (row split, two device-wide barriers "
-                         "per layer), kernel A and kernel B per layer, one persistent kernel "
-                         "per step with the column split (one barrier per layer), or auto: the "
-                         "column split where it runs (1 token, 4/8-bit down codes, no folded "
-                         "norm), else the row split.  columns-ahead: the column split with every "
-                         "layer's ids treated as inputs known before the step (the weight stream "
-                         "runs on into the next layer; not the decode dependency)")
+                    help="fused: one persistent kernel per step (row split, two device-wide "
+                         "barriers per layer); separate: kernel A and kernel B per layer; "
+                         "columns: one persistent kernel per step with the column split (one "
+                         "barrier per layer); mma: the tensor-core batch kernels (five launches "
+                         "per layer); auto: the column split for one token where it runs (no "
+                         "folded norm, din <= 4096), the tensor-core kernels for batches of up to "
+                         "64 tokens and 256 slots, else the row split.  columns-ahead: the column "
+                         "split with every layer's ids treated as inputs known before the step "
+                         "(the weight stream runs on into the next layer; not the decode "
+                         "dependency)")
     ap.add_argument("--input-sets", type=int, default=4)
     ap.add_argument("--samples", type=int, default=10,
                     help="timed samples after the K steps (at least 10), each of at least 5 "

@@ -397,6 +397,7 @@ __device__ bool cols_produce_layer(const LayerShape &s, const Plan &plan, const 
   const int ns = cs.nck - cs.nck_r;
   cnt[0] = nr;
   cnt[1] = ns;
+  MOE_TL_AT(::moe::tl_hook_row_p(), 53);
   int issued = 0;
   for (int i = 0; i < cs.nck; ++i) {
     const bool routed = i < cs.nck_r;
@@ -406,6 +407,7 @@ __device__ bool cols_produce_layer(const LayerShape &s, const Plan &plan, const 
     if (kColPrefetchOverflow && issued++ == r.nst)
       cols_prefetch_from(s, plan, cp, cw, cs, ids, r.nst, pol);
     if (!ring_claim_lane(r)) return false;
+    if (i == 0) MOE_TL_AT(::moe::tl_hook_row_p(), 54);
     const GateUpGeom &g = routed ? plan.geo_r : plan.geo_s;
     const uint8_t *recs = routed ? cw.gu_r : cw.gu_s;
     const int rows_pe = routed ? s.dff : s.dff_shared;

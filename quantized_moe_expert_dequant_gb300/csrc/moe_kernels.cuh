@@ -194,11 +194,12 @@ __host__ __device__ inline int col_pieces(int top_k, int dff, int n_shared, int 
 }
 
 // The gate/up stages of CTA c out of n in the column split: its activation columns [u0, u1) cut
-// into chunks of at most R row pairs (R_s for the shared experts) that never cross an expert, in
-// column order.  Chunk i: segment seg[i] (routed slot, or top_k + shared expert), first row j[i]
+// into chunks of at most R row pairs (R_s for the shared experts; kColFirstRows for the first)
+// that never cross an expert, in column order.  Chunk i: segment seg[i] (routed slot, or top_k + shared expert), first row j[i]
 // inside the expert, rows cnt[i], flattened first column u[i].  Returns the chunk count and the
 // routed chunks in *n_routed, or -1 beyond kMaxColChunks.
 constexpr int kMaxColChunks = 96;
+constexpr int kColFirstRows = 2;  // row pairs of a CTA's first gate/up stage of a layer
 __host__ __device__ inline int col_chunks(int top_k, int dff, int n_shared, int dff_shared, int R,
                                           int R_s, int c, int n, short *seg, short *j, short *cnt,
                                           short *u, int *n_routed) {
@@ -214,7 +215,8 @@ __host__ __device__ inline int col_chunks(int top_k, int dff, int n_shared, int 
     const int sg = static_cast<int>(rel / width);
     const int jj = static_cast<int>(rel - static_cast<int64_t>(sg) * width);
     int take = width - jj;
-    const int lim = routed ? R : R_s;
+    // the CTA's first chunk is short, so that the first copy of a layer lands early
+    const int lim = nc == 0 ? min(routed ? R : R_s, kColFirstRows) : (routed ? R : R_s);
     if (take > lim) take = lim;
     if (take > u1 - x) take = static_cast<int>(u1 - x);
     if (nc == kMaxColChunks) return -1;
