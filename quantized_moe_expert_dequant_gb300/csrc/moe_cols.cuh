@@ -46,8 +46,9 @@ namespace moe {
 constexpr int kColHelperWarp = kConsumerWarps + kProducerWarps;
 constexpr int kColThreads = kThreads + 32;    // consumers, producer, helper
 constexpr int kColMaxWpr = 4;                 // warps per gate/up row pair (32 columns a lane)
-// After the first ring-full of a layer's stages, ask L2 for the rest of the layer's bytes.
-constexpr bool kColPrefetchOverflow = false;
+// After the first ring-full of a layer's stages, ask L2 for the rest of the layer's bytes (their
+// requests no longer wait for free ring slots).
+constexpr bool kColPrefetchOverflow = true;
 // Consumers test a stage's barrier from every lane (no broadcast from lane 0).
 constexpr bool kColLaneWait = true;
 

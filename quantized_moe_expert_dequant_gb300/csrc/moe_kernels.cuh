@@ -199,7 +199,7 @@ __host__ __device__ inline int col_pieces(int top_k, int dff, int n_shared, int 
 // inside the expert, rows cnt[i], flattened first column u[i].  Returns the chunk count and the
 // routed chunks in *n_routed, or -1 beyond kMaxColChunks.
 constexpr int kMaxColChunks = 96;
-constexpr int kColFirstRows = 2;  // row pairs of a CTA's first gate/up stage of a layer
+constexpr int kColFirstRows = 4;  // row pairs of a CTA's first gate/up stage of a layer
 __host__ __device__ inline int col_chunks(int top_k, int dff, int n_shared, int dff_shared, int R,
                                           int R_s, int c, int n, short *seg, short *j, short *cnt,
                                           short *u, int *n_routed) {
