@@ -705,15 +705,27 @@ __global__ void __launch_bounds__(kThreads) mma_prep_kernel(const MmaParams p) {
   const int Gx = s.din / kGroup;
   const bool need16 = (s.top_k > 0 && p.bits_r == 8) || (s.n_shared > 0 && p.bits_s == 8);
   const uint16_t *xt = p.x + static_cast<int64_t>(t) * s.din;
-  for (int gi = warp; gi < Gx; gi += kWarps) {
-    const uint32_t two = *reinterpret_cast<const uint32_t *>(xt + gi * kGroup + 2 * lane);
-    const float v0 = __uint_as_float(two << 16), v1 = __uint_as_float(two & 0xffff0000u);
-    const int64_t ix = static_cast<int64_t>(t) * Gx + gi;
-    if (need16) {
-      pack_group(v0, v1, p.x16 + ix * 128, p.xinv + ix, p.xsum + ix, lane);
-    } else {
-      const float sum = warp_sum(v0 + v1);
-      if (lane == 0) p.xsum[ix] = sum;
+  // a warp's groups kPrepBatch at a time: every load issued before the first reduction
+  constexpr int kPrepBatch = 8;
+  for (int g0 = warp; g0 < Gx; g0 += kWarps * kPrepBatch) {
+    uint32_t two[kPrepBatch];
+#pragma unroll
+    for (int b = 0; b < kPrepBatch; ++b) {
+      const int gi = g0 + b * kWarps;
+      two[b] = gi < Gx ? *reinterpret_cast<const uint32_t *>(xt + gi * kGroup + 2 * lane) : 0u;
+    }
+#pragma unroll
+    for (int b = 0; b < kPrepBatch; ++b) {
+      const int gi = g0 + b * kWarps;
+      if (gi >= Gx) break;
+      const float v0 = __uint_as_float(two[b] << 16), v1 = __uint_as_float(two[b] & 0xffff0000u);
+      const int64_t ix = static_cast<int64_t>(t) * Gx + gi;
+      if (need16) {
+        pack_group(v0, v1, p.x16 + ix * 128, p.xinv + ix, p.xsum + ix, lane);
+      } else {
+        const float sum = warp_sum(v0 + v1);
+        if (lane == 0) p.xsum[ix] = sum;
+      }
     }
   }
   if (s.n_shared > 0) {
@@ -781,15 +793,29 @@ __global__ void mma_tail_kernel(const MmaParams p) {
     const int t = static_cast<int>(x / s.din);
     const int i = static_cast<int>(x - static_cast<int64_t>(t) * s.din);
     const float *yt = p.y_part + static_cast<int64_t>(t) * ny * s.din + i;
+    // eight slots at a time: every load issued first (a dropped slot's value is read, not used)
     float sum = 0.f;
-    for (int k = 0; k < ny; ++k) {
-      if (k < s.top_k) {
-        const int e = p.ids[t * s.top_k + k];
-        if (e < 0 || e >= s.n_experts) continue;
+    for (int k0 = 0; k0 < ny; k0 += 8) {
+      float yv[8];
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        float yk = 0.f;
+        if (k0 + j < ny)
+          for (int c = 0; c < nc; ++c)
+            yk += yt[c * cstride + static_cast<int64_t>(k0 + j) * s.din];
+        yv[j] = yk;
       }
-      float yk = 0.f;
-      for (int c = 0; c < nc; ++c) yk += yt[c * cstride + static_cast<int64_t>(k) * s.din];
-      sum += yk;
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        const int k = k0 + j;
+        if (k >= ny) break;
+        bool valid = true;
+        if (k < s.top_k) {
+          const int e = p.ids[t * s.top_k + k];
+          valid = e >= 0 && e < s.n_experts;
+        }
+        if (valid) sum += yv[j];
+      }
     }
     const float r = p.resid_f32 ? static_cast<const float *>(p.resid)[x]
                                 : bf16_to_float(static_cast<const uint16_t *>(p.resid)[x]);
