@@ -370,7 +370,7 @@ def mode_of(kernels: str) -> int:
     from quantized_moe_expert_dequant_gb300 import binding as Bn
     return {"fused": Bn.KERNELS_FUSED, "separate": Bn.KERNELS_SEPARATE,
             "columns": Bn.KERNELS_COLUMNS, "columns-ahead": Bn.KERNELS_COLUMNS_AHEAD,
-            "mma": Bn.KERNELS_MMA}[kernels]
+            "mma": Bn.KERNELS_MMA, "pool": Bn.KERNELS_POOL}[kernels]
 
 
 def run_ours(args, shape: Shape):
@@ -556,8 +556,10 @@ def run_ours(args, shape: Shape):
     peak_note = "of measured" if peaks else "of fallback"
     ach_a = mean_a / (ms_a * 1e-3) / 1e9
     ach_b = mean_b / (ms_b * 1e-3) / 1e9
-    one_launch = (Bn.KERNELS_FUSED, Bn.KERNELS_COLUMNS, Bn.KERNELS_COLUMNS_AHEAD)
-    dominant = {Bn.KERNELS_FUSED: "fused_kernel", Bn.KERNELS_COLUMNS: "cols_kernel",
+    one_launch = (Bn.KERNELS_FUSED, Bn.KERNELS_COLUMNS, Bn.KERNELS_COLUMNS_AHEAD,
+                  Bn.KERNELS_POOL)
+    dominant = {Bn.KERNELS_FUSED: "fused_kernel", Bn.KERNELS_POOL: "fused_kernel",
+                Bn.KERNELS_COLUMNS: "cols_kernel",
                 Bn.KERNELS_COLUMNS_AHEAD: "cols_kernel",
                 Bn.KERNELS_MMA: "mma path (route, gate_up_mma, down_mma, tail per layer)"
                 }.get(mode, "gate_up_kernel")
@@ -855,13 +857,14 @@ def main(argv=None):
     ap.add_argument("--workload", choices=sorted(ALL), default=DEFAULT_WORKLOAD)
     ap.add_argument("--tokens", type=int, default=1)
     ap.add_argument("--kernels", choices=["auto", "fused", "separate", "columns", "columns-ahead",
-                                          "mma"],
+                                          "mma", "pool"],
                     default="auto",
                     help="fused: one persistent kernel per step (row split, two device-wide "
                          "barriers per layer); separate: kernel A and kernel B per layer; "
                          "columns: one persistent kernel per step with the column split (one "
                          "barrier per layer); mma: the tensor-core batch kernels (five launches "
-                         "per layer); auto: the column split for one token where it runs (no "
+                         "per layer); pool: the row split with each slot's output kept apart and "
+                         "the page's tail association; auto: the column split for one token where it runs (no "
                          "folded norm, din <= 4096), the tensor-core kernels for batches of up to "
                          "64 tokens and 256 slots, else the row split.  columns-ahead: the column "
                          "split with every layer's ids treated as inputs known before the step "
@@ -871,7 +874,7 @@ def main(argv=None):
     ap.add_argument("--samples", type=int, default=10,
                     help="timed samples after the K steps (at least 10), each of at least 5 "
                          "replays and about 100 ms")
-    ap.add_argument("--ab", choices=["fused", "separate", "columns", "columns-ahead", "mma"],
+    ap.add_argument("--ab", choices=["fused", "separate", "columns", "columns-ahead", "mma", "pool"],
                     default=None,
                     help="also time this kernel mode, its samples alternating with the main "
                          "mode's (A/B on the same box and weights)")

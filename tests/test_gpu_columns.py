@@ -153,7 +153,7 @@ def test_columns_small_stack_equals_chain_and_oracle(shape):
     ahead.close()
 
 
-@pytest.mark.parametrize("name", ["qwen3_stack_8bit", "e512_stack"])
+@pytest.mark.parametrize("name", ["qwen3_stack_8bit", "e512_stack", "dots_stack_mixed"])
 def test_columns_full_size_stack(name):
     shape = ALL[name]
     free, _ = torch.cuda.mem_get_info()

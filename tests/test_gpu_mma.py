@@ -9,6 +9,7 @@ import torch
 from quantized_moe_expert_dequant_gb300 import binding as Bn
 from quantized_moe_expert_dequant_gb300.workloads import ALL, Shape
 from tests import gpu_cases as C
+from tests.test_gpu_stack import check_contributions, run_chain, stack_inputs
 
 pytestmark = pytest.mark.gpu
 
@@ -178,3 +179,35 @@ def test_limits():
     with pytest.raises(Bn.MoeError) as e:        # the chained stack reads RMSNorm of the output
         Bn.MoeStack([layer, layer], max_tokens=2, kernel_mode=Bn.KERNELS_MMA, norm_weight=norm)
     assert e.value.rc == Bn.MOE_ERR_UNSUPPORTED
+
+
+@pytest.mark.parametrize("name,m", [("qwen3_stack_8bit", 8), ("dots_stack_mixed", 32)])
+def test_full_size_stack(name, m):
+    """The full stack in the bench's launch configuration (one graph per step, five launches per
+    layer): byte-identical to the same layers run one forward each, and each checked layer's block
+    term out_l - out_{l-1} against the oracle on sampled rows of three tokens."""
+    shape = ALL[name]
+    free, _ = torch.cuda.mem_get_info()
+    need = shape.layer_weight_bytes() * shape.layers * 2.1   # plus the tile-group copies
+    assert free > need, f"needs {need / 1e9:.1f} GB of device memory"
+    try:
+        layers = [Bn.synth_layer_device(shape, l) for l in range(shape.layers)]
+        x, ids, sc, resid0 = stack_inputs(shape, m=m, step=5)
+        stack = Bn.MoeStack(layers, max_tokens=m, kernel_mode=Bn.KERNELS_MMA)
+        out = torch.empty((m, shape.din), dtype=torch.float32, device="cuda")
+        stack.step(C.dev(x, torch.bfloat16), C.dev(ids, torch.int32), C.dev(sc, torch.float32),
+                   C.dev(resid0, torch.bfloat16), out)
+        torch.cuda.synchronize()
+        assert stack.get_error() == 0
+        stack.close()
+        outs = run_chain(layers, x, ids, sc, resid0, m, mode=Bn.KERNELS_MMA)
+        assert torch.equal(out.view(torch.int32), outs[-1].view(torch.int32))
+        rng = np.random.default_rng(11)
+        rows = np.unique(np.concatenate([[0, shape.din - 1],
+                                         rng.choice(shape.din, 62, replace=False)]))
+        L = shape.layers
+        check_contributions(shape, x, ids, sc, resid0, outs, [0, 1, L // 2, L - 1], rows,
+                            tokens=(0, m // 2, m - 1))
+    finally:
+        layers = None
+        torch.cuda.empty_cache()

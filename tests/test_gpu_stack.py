@@ -53,7 +53,7 @@ def check_layers(shape, x, ids, sc, resid0, outs, rows, tokens=(0,)):
             C.assert_parity(got, ref[l][t], f"{shape.name}: layer {l} token {t}")
 
 
-def check_contributions(shape, x, ids, sc, resid0, outs, layers_to_check, rows):
+def check_contributions(shape, x, ids, sc, resid0, outs, layers_to_check, rows, tokens=(0,)):
     """Layers of a full-size stack, on sampled rows, through a property that holds at any size:
     a layer adds its block term to its residual, so out_l - out_{l-1} is the oracle's block output
     with a zero residual on the same seeded inputs (layer 0: out_0 - resid0).  The fp32 sum in the
@@ -61,11 +61,13 @@ def check_contributions(shape, x, ids, sc, resid0, outs, layers_to_check, rows):
     zero = np.zeros(shape.din, np.float32)
     for l in layers_to_check:
         ora = C.OracleLayer(shape, l)
-        got = outs[l][0].cpu().numpy().astype(np.float64)
-        prev = (synth.bf16_bits_to_f32(resid0[0]) if l == 0
-                else outs[l - 1][0].cpu().numpy()).astype(np.float64)
-        ref = ora.token(x[l][0], zero, ids[l][0], sc[l][0], rows=rows)
-        C.assert_parity((got - prev)[rows], ref, f"{shape.name}: layer {l} block term")
+        for t in tokens:
+            got = outs[l][t].cpu().numpy().astype(np.float64)
+            prev = (synth.bf16_bits_to_f32(resid0[t]) if l == 0
+                    else outs[l - 1][t].cpu().numpy()).astype(np.float64)
+            ref = ora.token(x[l][t], zero, ids[l][t], sc[l][t], rows=rows)
+            C.assert_parity((got - prev)[rows], ref,
+                            f"{shape.name}: layer {l} token {t} block term")
 
 
 def test_small_stack_graph_equals_chain_and_oracle():
