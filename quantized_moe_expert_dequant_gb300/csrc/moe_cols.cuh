@@ -46,9 +46,6 @@ namespace moe {
 constexpr int kColHelperWarp = kConsumerWarps + kProducerWarps;
 constexpr int kColThreads = kThreads + 32;    // consumers, producer, helper
 constexpr int kColMaxWpr = 4;                 // warps per gate/up row pair (32 columns a lane)
-// After the first ring-full of a layer's stages, ask L2 for the rest of the layer's bytes (their
-// requests no longer wait for free ring slots).
-constexpr bool kColPrefetchOverflow = true;
 // Consumers test a stage's barrier from every lane (no broadcast from lane 0).
 constexpr bool kColLaneWait = true;
 
@@ -217,6 +214,58 @@ __device__ __forceinline__ bool col_valid(const LayerShape &s, const ColPiece &q
   return e >= 0 && e < s.n_experts;
 }
 
+// The down stream of a layer in stages of C = cp.nbs + 1 slots of one column block (din 32-bit
+// words): every valid piece's code blocks, then its (scale, bias) record, in piece order.  Packed
+// (cp.pack): every slot filled, a piece may continue in the next stage and its record may open the
+// next one.  Else a stage holds up to cp.nbs blocks of one piece, and the record rides in the
+// piece's last stage.
+struct DownWalk {
+  int qi;     // the current piece (cs.np: none left)
+  int done;   // its code blocks already placed
+};
+
+__device__ __forceinline__ int next_valid_piece(const LayerShape &s, const ColSmem &cs,
+                                                const int *ids, int from) {
+  for (int i = from; i < cs.np; ++i) {
+    int e;
+    if (col_valid(s, cs.pc[i], ids, &e)) return i;
+  }
+  return cs.np;
+}
+
+// One stage from w: seg(qi, piece, expert, b0, nk, slot) for each run of nk code blocks of a piece
+// (b0: the run's first block inside the piece) and seg(qi, piece, expert, -1, 0, slot) for a
+// piece's record; w moves past the stage.  The producer and the consumers walk the same stages.
+template <class Seg>
+__device__ __forceinline__ void col_down_stage(const LayerShape &s, const ColPlan &cp,
+                                               const ColSmem &cs, const int *ids, DownWalk &w,
+                                               Seg seg) {
+  const int C = cp.nbs + 1;
+  int k = 0;
+  while (k < C && w.qi < cs.np) {
+    const ColPiece q = cs.pc[w.qi];
+    int e;
+    col_valid(s, q, ids, &e);
+    const int room = cp.pack ? C - k : cp.nbs;
+    const int nk = min(q.nb - w.done, room);
+    if (nk > 0) {
+      seg(w.qi, q, e, w.done, nk, k);
+      k += nk;
+      w.done += nk;
+    }
+    if (w.done < q.nb) {
+      if (!cp.pack) break;
+      continue;           // packed: the stage is full
+    }
+    if (k == C) break;    // the record opens the next stage
+    seg(w.qi, q, e, -1, 0, k);
+    ++k;
+    w.qi = next_valid_piece(s, cs, ids, w.qi + 1);
+    w.done = 0;
+    if (!cp.pack) break;
+  }
+}
+
 // Named barrier 3: the consumer warps and the helper warp, once per layer (the helper's shared
 // scalar is ready and its reads of the older slab pass are done).
 __device__ __forceinline__ void consumers_helper_sync() {
@@ -339,6 +388,23 @@ __device__ void cols_phase_a(const LayerShape &s, const GateUpGeom &gr, const Ga
 
 // ------------------------------------------------------------------ down
 // ------------------------------------------------------------------ the producer's layer
+// The source of one segment of a down stage: nk code blocks of a piece from block b0, or
+// (nk == 0) the piece's (scale, bias) record.
+__device__ __forceinline__ const uint8_t *col_down_src(const LayerShape &s, const ColPlan &cp,
+                                                       const ColPtrs &cw, const ColPiece &q, int e,
+                                                       int b0, int nk) {
+  const bool routed = q.seg < s.top_k;
+  const ColDownDev &d = routed ? cw.r : cw.s;
+  const int width = routed ? s.dff : s.dff_shared;
+  if (nk > 0) {
+    const int nblk = width / (routed ? cp.cb_r : cp.cb_s);
+    return reinterpret_cast<const uint8_t *>(
+        d.codes + (static_cast<int64_t>(e) * nblk + q.blk0 + b0) * s.din);
+  }
+  return reinterpret_cast<const uint8_t *>(
+      d.sb + (static_cast<int64_t>(e) * (width / kGroup) + q.grp) * s.din);
+}
+
 // Lane 0 of the producer warp streams one layer, in the order the consumers take the stages: the
 // CTA's gate/up chunks (routed, then shared; one empty stage when it has none), each ONE bulk copy
 // of consecutive records (see ColPtrs), then the down column blocks of every valid piece (at most
@@ -364,6 +430,19 @@ __device__ inline void cols_prefetch_from(const LayerShape &s, const Plan &plan,
     const int rows_pe = routed ? s.dff : s.dff_shared;
     bulk_prefetch_l2(recs + (static_cast<int64_t>(e) * rows_pe + cs.ck_j[c]) * g.rb,
                      static_cast<uint32_t>(cs.ck_n[c]) * g.rb, pol);
+  }
+  if (cp.pack) {
+    const uint32_t blk_bytes = static_cast<uint32_t>(s.din) * 4u;
+    DownWalk w{next_valid_piece(s, cs, ids, 0), 0};
+    while (w.qi < cs.np) {
+      const bool want = i++ >= from;
+      col_down_stage(s, cp, cs, ids, w, [&](int, const ColPiece &q, int e, int b0, int nk, int) {
+        if (want)
+          bulk_prefetch_l2(col_down_src(s, cp, cw, q, e, b0, nk),
+                           static_cast<uint32_t>(nk > 0 ? nk : 1) * blk_bytes, pol);
+      });
+    }
+    return;
   }
   const uint32_t blk_bytes = static_cast<uint32_t>(s.din) * 4u;
   for (int qi = 0; qi < cs.np; ++qi) {
@@ -405,7 +484,7 @@ __device__ bool cols_produce_layer(const LayerShape &s, const Plan &plan, const 
     const int sg = cs.ck_seg[i];
     const int e = routed ? ids[sg] : sg - s.top_k;
     if (routed && (e < 0 || e >= s.n_experts)) continue;
-    if (kColPrefetchOverflow && issued++ == r.nst)
+    if (cp.prefetch && issued++ == r.nst)
       cols_prefetch_from(s, plan, cp, cw, cs, ids, r.nst, pol);
     if (!ring_claim_lane(r)) return false;
     if (i == 0) MOE_TL_AT(::moe::tl_hook_row_p(), 54);
@@ -426,6 +505,30 @@ __device__ bool cols_produce_layer(const LayerShape &s, const Plan &plan, const 
     mbar_arrive_expect_tx(&r.full[r.st], 0);
     r.advance();
   }
+  if (cp.pack) {
+    const uint32_t blk_bytes = static_cast<uint32_t>(s.din) * 4u;
+    DownWalk w{next_valid_piece(s, cs, ids, 0), 0};
+    while (w.qi < cs.np) {
+      if (cp.prefetch && issued++ == r.nst)
+        cols_prefetch_from(s, plan, cp, cw, cs, ids, r.nst, pol);
+      if (!ring_claim_lane(r)) return false;
+      DownWalk probe = w;  // the stage's bytes first: the barrier expects them before the copies
+      uint32_t total = 0;
+      col_down_stage(s, cp, cs, ids, probe, [&](int, const ColPiece &, int, int, int nk, int) {
+        total += static_cast<uint32_t>(nk > 0 ? nk : 1) * blk_bytes;
+      });
+      uint8_t *st = r.stage();
+      mbar_arrive_expect_tx(&r.full[r.st], total);
+      col_down_stage(s, cp, cs, ids, w, [&](int, const ColPiece &q, int e, int b0, int nk, int slot) {
+        const uint8_t *src = col_down_src(s, cp, cw, q, e, b0, nk);
+        bulk_g2s(st + static_cast<uint32_t>(slot) * blk_bytes, src,
+                 static_cast<uint32_t>(nk > 0 ? nk : 1) * blk_bytes, &r.full[r.st], pol);
+      });
+      MOE_TL_STAGE_P(r.used);
+      r.advance();
+    }
+    return true;
+  }
   const uint32_t blk_bytes = static_cast<uint32_t>(s.din) * 4u;
   for (int qi = 0; qi < cs.np; ++qi) {
     const ColPiece q = cs.pc[qi];
@@ -439,7 +542,7 @@ __device__ bool cols_produce_layer(const LayerShape &s, const Plan &plan, const 
     for (int bo = 0; bo < q.nb; bo += cp.nbs) {
       const int nk = (q.nb - bo) < cp.nbs ? (q.nb - bo) : cp.nbs;
       const bool ends = bo + nk == q.nb;
-      if (kColPrefetchOverflow && issued++ == r.nst)
+      if (cp.prefetch && issued++ == r.nst)
         cols_prefetch_from(s, plan, cp, cw, cs, ids, r.nst, pol);
       if (!ring_claim_lane(r)) return false;
       const uint32_t code_bytes = static_cast<uint32_t>(nk) * blk_bytes;
@@ -616,6 +719,126 @@ __device__ __forceinline__ void consume_piece(const ColPiece &q, float2 us, cons
         }
       }
     }
+    warp_release(r, lane);
+  }
+}
+
+// Consumers: down blocks of one piece inside a stage.  Thread t owns the row quads t and (QPT = 2)
+// t + 512 (rows 4 quad .. 4 quad + 3).  Its sums over the run of nk blocks are exact integers (one
+// quad at a time); they join the piece's per-row fp32 sums dsum at the run's end (at most 64
+// columns a piece keeps m * 256 + l below 2^31).  pl: the planes of the run's first block.
+template <int BITS, int QPT>
+__device__ __forceinline__ void down_blocks(const uint8_t *base, const uint32_t *pl, int nk,
+                                            uint32_t blk_bytes, int nquads, int tid,
+                                            float (&dsum)[QPT][4]) {
+  constexpr int NPL = BITS == 8 ? 3 : 6;
+#pragma unroll
+  for (int a = 0; a < QPT; ++a) {
+    const int quad = tid + a * kConsumers;
+    if (quad < nquads) {
+      uint32_t al[4][NPL];  // l and m planes (unsigned) and h planes (two's complement)
+#pragma unroll
+      for (int k = 0; k < 4; ++k)
+#pragma unroll
+        for (int z = 0; z < NPL; ++z) al[k][z] = 0u;
+#pragma unroll 4
+      for (int b = 0; b < nk; ++b) {
+        const uint4 pa = *reinterpret_cast<const uint4 *>(pl + b * 8);
+        const uint4 pb = *reinterpret_cast<const uint4 *>(pl + b * 8 + 4);
+        const uint4 w4 = lds_u4(base + static_cast<uint32_t>(b) * blk_bytes + quad * 16);
+        const uint32_t w[4] = {w4.x, w4.y, w4.z, w4.w};
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          if constexpr (BITS == 8) {
+            al[k][0] = dp4a_uu(w[k], pa.x, al[k][0]);
+            al[k][1] = dp4a_uu(w[k], pa.y, al[k][1]);
+            al[k][2] = static_cast<uint32_t>(dp4a_us(w[k], pa.z, static_cast<int>(al[k][2])));
+          } else {
+            const uint32_t lo = w[k] & 0x0f0f0f0fu, hi = w[k] & 0xf0f0f0f0u;
+            al[k][0] = dp4a_uu(lo, pa.x, al[k][0]);
+            al[k][1] = dp4a_uu(lo, pa.y, al[k][1]);
+            al[k][2] = static_cast<uint32_t>(dp4a_us(lo, pa.z, static_cast<int>(al[k][2])));
+            al[k][3] = dp4a_uu(hi, pa.w, al[k][3]);
+            al[k][4] = dp4a_uu(hi, pb.x, al[k][4]);
+            al[k][5] = static_cast<uint32_t>(dp4a_us(hi, pb.y, static_cast<int>(al[k][5])));
+          }
+        }
+      }
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        uint32_t l, m;
+        int h;
+        if constexpr (BITS == 8) {
+          l = al[k][0];
+          m = al[k][1];
+          h = static_cast<int>(al[k][2]);
+        } else {
+          // the even sums scaled by 16 join the odd ones (read as 16 q)
+          l = al[k][0] * 16u + al[k][3];
+          m = al[k][1] * 16u + al[k][4];
+          h = static_cast<int>(al[k][2]) * 16 + static_cast<int>(al[k][5]);
+        }
+        dsum[a][k] += fmaf(static_cast<float>(h), 65536.f, static_cast<float>(m * 256u + l));
+      }
+    }
+  }
+}
+
+// A piece's (scale, bias) record (one half2 per row, at `base`): the group's scale and bias applied
+// to the piece's sums into part[][]; the sums restart at zero for the next piece.
+template <int QPT>
+__device__ __forceinline__ void down_record(const uint8_t *base, float2 us, int nquads, int tid,
+                                            float (&dsum)[QPT][4], float (&part)[2][4]) {
+#pragma unroll
+  for (int a = 0; a < QPT; ++a) {
+    const int quad = tid + a * kConsumers;
+    if (quad < nquads) {
+      const uint4 h4 = lds_u4(base + quad * 16);
+      const uint32_t hw[4] = {h4.x, h4.y, h4.z, h4.w};
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        const __half2 sbh = *reinterpret_cast<const __half2 *>(&hw[k]);
+        const float sc = __low2float(sbh), bi = __high2float(sbh);
+        part[a][k] += fmaf(sc, dsum[a][k] * us.x, bi * us.y);
+      }
+    }
+#pragma unroll
+    for (int k = 0; k < 4; ++k) dsum[a][k] = 0.f;
+  }
+}
+
+// Consumers: every down stage of the layer, walked like the producer packed them.
+template <int BD, int BSD, int QPT>
+__device__ void consume_down(const LayerShape &s, const ColPlan &cp, const ColSmem &cs,
+                             const int *ids, const uint32_t *planes, Ring &r, int lane, int tid,
+                             float (&part)[2][4]) {
+  const int nquads = s.din >> 2;
+  const uint32_t blk_bytes = static_cast<uint32_t>(s.din) * 4u;
+  float dsum[QPT][4];
+#pragma unroll
+  for (int a = 0; a < QPT; ++a)
+#pragma unroll
+    for (int k = 0; k < 4; ++k) dsum[a][k] = 0.f;
+  DownWalk w{next_valid_piece(s, cs, ids, 0), 0};
+  while (w.qi < cs.np) {
+    if (tid == 0) MOE_TL_STAGE_WAIT(r.used);
+    const bool ok = cols_wait_full(r, lane);
+    if (tid == 0) MOE_TL_STAGE_C(r.used);
+    const uint8_t *st = r.stage();
+    col_down_stage(s, cp, cs, ids, w,
+                   [&](int qi, const ColPiece &q, int, int b0, int nk, int slot) {
+                     if (!ok) return;
+                     const uint8_t *base = st + static_cast<uint32_t>(slot) * blk_bytes;
+                     if (nk > 0) {
+                       const uint32_t *pl = planes + (q.pb + b0) * 8;
+                       if (q.seg < s.top_k)
+                         down_blocks<BD, QPT>(base, pl, nk, blk_bytes, nquads, tid, dsum);
+                       else
+                         down_blocks<BSD, QPT>(base, pl, nk, blk_bytes, nquads, tid, dsum);
+                     } else {
+                       down_record<QPT>(base, cs.us[qi], nquads, tid, dsum, part);
+                     }
+                   });
     warp_release(r, lane);
   }
 }
@@ -857,20 +1080,27 @@ __global__ void __launch_bounds__(kColThreads, 1) cols_kernel(const StackParams 
     for (int a = 0; a < 2; ++a)
 #pragma unroll
       for (int k = 0; k < 4; ++k) part[a][k] = 0.f;
-    for (int qi = 0; qi < cs.np; ++qi) {
-      const ColPiece q = cs.pc[qi];
-      int e;
-      if (!col_valid(s, q, ids_l, &e)) continue;
-      if (q.seg < s.top_k) {
-        if (two)
-          consume_piece<BD, 2>(q, cs.us[qi], p.cp, s.din, cs.planes, r, lane, tid, part);
-        else
-          consume_piece<BD, 1>(q, cs.us[qi], p.cp, s.din, cs.planes, r, lane, tid, part);
-      } else {
-        if (two)
-          consume_piece<BSH, 2>(q, cs.us[qi], p.cp, s.din, cs.planes, r, lane, tid, part);
-        else
-          consume_piece<BSH, 1>(q, cs.us[qi], p.cp, s.din, cs.planes, r, lane, tid, part);
+    if (p.cp.pack) {
+      if (two)
+        consume_down<BD, BSH, 2>(s, p.cp, cs, ids_l, cs.planes, r, lane, tid, part);
+      else
+        consume_down<BD, BSH, 1>(s, p.cp, cs, ids_l, cs.planes, r, lane, tid, part);
+    } else {
+      for (int qi = 0; qi < cs.np; ++qi) {
+        const ColPiece q = cs.pc[qi];
+        int e;
+        if (!col_valid(s, q, ids_l, &e)) continue;
+        if (q.seg < s.top_k) {
+          if (two)
+            consume_piece<BD, 2>(q, cs.us[qi], p.cp, s.din, cs.planes, r, lane, tid, part);
+          else
+            consume_piece<BD, 1>(q, cs.us[qi], p.cp, s.din, cs.planes, r, lane, tid, part);
+        } else {
+          if (two)
+            consume_piece<BSH, 2>(q, cs.us[qi], p.cp, s.din, cs.planes, r, lane, tid, part);
+          else
+            consume_piece<BSH, 1>(q, cs.us[qi], p.cp, s.din, cs.planes, r, lane, tid, part);
+        }
       }
     }
     MOE_TL_AT(tlr, 12);

@@ -2,6 +2,7 @@
 // to the kernels of moe_fused.cuh (instantiated per gate/up code width in moe_kernels_g4.cu,
 // moe_kernels_g6.cu and moe_kernels_g8.cu); plus the small kernels (debug unpack, router, bounded
 // waits, debug route inversion).
+#include <algorithm>
 #include <cstring>
 
 #include "moe_grouped.cuh"
@@ -419,19 +420,32 @@ bool make_col_plan(const LayerShape &s, int bits_gu, int bits_d, int bits_sh, in
   // every CTA's pieces within the kernel's limits
   const int64_t U = (int64_t)s.top_k * s.dff + (int64_t)s.n_shared * s.dff_shared;
   if ((U + grid - 1) / grid > kMaxColsCta) return false;
+  int max_stages = 0;
   for (int c = 0; c < grid; ++c) {
     ColPiece pc[kMaxColPieces];
     int nbk = 0;
     int64_t u0 = 0;
-    if (col_pieces(s.top_k, s.dff, s.n_shared, s.dff_shared, cp->cb_r, cp->cb_s, c, grid, pc,
-                   &nbk, &u0) < 0)
-      return false;
+    const int np = col_pieces(s.top_k, s.dff, s.n_shared, s.dff_shared, cp->cb_r, cp->cb_s, c,
+                              grid, pc, &nbk, &u0);
+    if (np < 0) return false;
     short sg[kMaxColChunks], jj[kMaxColChunks], nn[kMaxColChunks], uu[kMaxColChunks];
     int nrt = 0;
-    if (col_chunks(s.top_k, s.dff, s.n_shared, s.dff_shared, plan->geo_r.R, plan->geo_s.R, c,
-                   grid, sg, jj, nn, uu, &nrt) < 0)
-      return false;
+    const int nck = col_chunks(s.top_k, s.dff, s.n_shared, s.dff_shared, plan->geo_r.R,
+                               plan->geo_s.R, c, grid, sg, jj, nn, uu, &nrt);
+    if (nck < 0) return false;
+    // the CTA's stages of a layer (unpacked) when every slot names a valid expert
+    int down = 0;
+    for (int i = 0; i < np; ++i) down += (pc[i].nb + nbs - 1) / nbs;
+    max_stages = std::max(max_stages, nck + down);
   }
+  // The prefetches queue on the bulk-copy engine ahead of the ring's next copies: worth it only
+  // for a short overflow (measured: qwen3 8-bit, 10-11 stages on a 6-slot ring, +1%; dots-like,
+  // 20-30 stages, -17%).
+  cp->prefetch = max_stages <= 2 * n;
+  // Packing pays where a piece's record would otherwise take a stage of its own next to one or
+  // two blocks and nothing is prefetched (measured, prefetch off: dots-like stack, 2-slot stages,
+  // +11%; qwen3 8-bit, 4-slot stages, -3%; with the prefetch on, packing measured slower).
+  cp->pack = nbs <= 2 && !cp->prefetch;
   std::memset(&plan->geo_b, 0, sizeof plan->geo_b);
   plan->nst = n;
   plan->stage_bytes = st;

@@ -122,6 +122,10 @@ struct ColPlan {
   int nbs;                 // column blocks per down stage, at most
   int ro;                  // output rows one CTA owns, at most (4 * its row quads)
   int rec_r, rec_s;        // bytes of one gate/up record, routed / shared
+  int pack;                // down stages filled across pieces (stages of at most 2 blocks, no
+                           // prefetch)
+  int prefetch;            // ask L2 for the stages beyond the first ring-full (when they are at
+                           // most one more ring-full)
 };
 
 // Bytes of one gate/up record of a row of `din` codes at `bits`.
