@@ -345,35 +345,40 @@ int moe_router_topk(const float *logits, int32_t m, int32_t n_experts, int32_t t
  * wait runs forever. */
 int moe_debug_wait_timeout(int32_t kind, int32_t *scratch, int32_t *device_error, void *stream);
 
-/* The column split's cut of one CTA's activation columns into pieces, exactly as the
+/* The column split's cut of a CTA's activation columns [u0, u1) into pieces, exactly as the
  * MOE_KERNELS_COLUMNS kernel computes it on the device (host only, no CUDA call: a debug export so
  * that the decomposition can be checked on a machine without a GPU).  The activation columns are
  * the flattened routed-then-shared rows of the gate/up projections (top_k * dff routed, then
- * n_shared * dff_shared); CTA `cta` of `grid` owns [U * cta / grid, U * (cta + 1) / grid), cut at
- * every segment (routed slot or shared expert) and every group of 64 columns.
+ * n_shared * dff_shared); the plan gives each CTA its range (moe_debug_col_plan's bounds), and the
+ * range is cut at every segment (routed slot or shared expert) and every group of 64 columns.
  *   bits_down, bits_shared  4 or 8: the down projection's code width (32 / bits codes per word)
- *   out   int32 host, room for 2 + 8 * max_pieces values: u0 (the CTA's first column), the piece
- *         count, then per piece seg (slot, or top_k + shared index), j0, j1 (columns inside the
- *         expert), a0 (index of j0 in the CTA's range), blk0 (first 32-bit column block), nb
- *         (blocks), pb (index of the first block in the CTA's block list), grp (j0 / 64)
- * Returns the piece count (>= 0), MOE_ERR_UNSUPPORTED when the CTA owns more columns, pieces or
+ *   out   int32 host, room for 8 * max_pieces values: per piece seg (slot, or top_k + shared
+ *         index), j0, j1 (columns inside the expert), a0 (index of j0 in the CTA's range), blk0
+ *         (first 32-bit column block), nb (blocks), pb (index of the first block in the CTA's
+ *         block list), grp (j0 / 64)
+ * Returns the piece count (>= 0), MOE_ERR_UNSUPPORTED when the range holds more columns, pieces or
  * blocks than the kernel holds (or more pieces than max_pieces), MOE_ERR_INVALID_ARG for bad
- * arguments.  No
- * counterpart on the pages: the split by columns is this implementation's. */
+ * arguments (a range outside [0, U]).  No counterpart on the pages: the split by columns is this
+ * implementation's. */
 int moe_debug_col_pieces(int32_t top_k, int32_t dff, int32_t n_shared, int32_t dff_shared,
-                         int32_t bits_down, int32_t bits_shared, int32_t cta, int32_t grid,
+                         int32_t bits_down, int32_t bits_shared, int32_t u0, int32_t u1,
                          int32_t *out, int32_t max_pieces);
 
 /* The column split's launch plan for a config on a grid of `grid` CTAs with `ring_bytes` of
  * dynamic shared memory, exactly as moe_decode_create makes it (host only, no CUDA call: a debug
- * export for checks without a GPU).  cfg's kernel_mode is ignored.  out (int32 host, 8 values)
+ * export for checks without a GPU).  cfg's kernel_mode is ignored.  out (int32 host, 10 values)
  * receives: stages in the ring, bytes per stage, column blocks per down stage (nbs), rows per
  * owner in the partial-sum slab (ro), the routed and the shared down projection's codes per
- * 32-bit word, the gate/up rows per routed and per shared phase-A stage.  Returns MOE_OK, or
- * MOE_ERR_UNSUPPORTED when the column split does not take the config (or the grid),
- * MOE_ERR_INVALID_ARG for an invalid config.  No counterpart on the pages. */
+ * 32-bit word, the gate/up rows per routed and per shared phase-A stage, whether down stages are
+ * packed across pieces, whether the stages past the first ring-full are prefetched into L2.
+ * bounds (int32 host, grid + 1 values, or NULL) receives the CTAs' column ranges: CTA c owns the
+ * activation columns [bounds[c], bounds[c + 1]), bounds[0] = 0 and bounds[grid] = U.  An
+ * unpacked plan starts from the even split (U c / grid) and moves each inner boundary at most 16
+ * columns so that the CTA with the most stages has as few as possible, then the fewest bytes,
+ * then the total bytes are least; a packed plan keeps the even split.  Returns MOE_OK, or MOE_ERR_UNSUPPORTED when the column split does not take the config
+ * (or the grid), MOE_ERR_INVALID_ARG for an invalid config.  No counterpart on the pages. */
 int moe_debug_col_plan(const moe_decode_config *cfg, int32_t grid, int32_t ring_bytes,
-                       int32_t *out);
+                       int32_t *out, int32_t *bounds);
 
 #ifdef __cplusplus
 }

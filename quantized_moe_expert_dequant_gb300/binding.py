@@ -121,7 +121,7 @@ def lib() -> ctypes.CDLL:
                 "moe_debug_wait_timeout": [i32, vp, vp, vp],
                 "moe_router_topk": [vp, i32, i32, i32, vp, vp, vp],
                 "moe_debug_col_pieces": [i32, i32, i32, i32, i32, i32, i32, i32, vp, i32],
-                "moe_debug_col_plan": [ctypes.POINTER(Config), i32, i32, vp],
+                "moe_debug_col_plan": [ctypes.POINTER(Config), i32, i32, vp, vp],
             }
             if _timeline:
                 sig["moe_stack_timeline"] = [vp, vp, i64, ctypes.POINTER(i32)]
@@ -443,27 +443,31 @@ def router_topk(logits: torch.Tensor, top_k: int, stream=None):
 
 
 def col_pieces(top_k: int, dff: int, n_shared: int, dff_shared: int, bits_down: int,
-               bits_shared: int, cta: int, grid: int, max_pieces: int = 64):
-    """The column split's pieces of one CTA (host only): (u0, [(seg, j0, j1, a0, blk0, nb, pb,
-    grp), ...])."""
+               bits_shared: int, u0: int, u1: int, max_pieces: int = 64):
+    """The column split's pieces of the activation columns [u0, u1) (host only):
+    [(seg, j0, j1, a0, blk0, nb, pb, grp), ...]."""
     import numpy as np
-    out = np.zeros(2 + 8 * max_pieces, dtype=np.int32)
-    rc = lib().moe_debug_col_pieces(top_k, dff, n_shared, dff_shared, bits_down, bits_shared, cta,
-                                    grid, out.ctypes.data, max_pieces)
+    out = np.zeros(8 * max_pieces, dtype=np.int32)
+    rc = lib().moe_debug_col_pieces(top_k, dff, n_shared, dff_shared, bits_down, bits_shared, u0,
+                                    u1, out.ctypes.data, max_pieces)
     check("moe_debug_col_pieces", min(rc, 0))
-    n = int(out[1])
-    return int(out[0]), [tuple(int(v) for v in out[2 + 8 * q:10 + 8 * q]) for q in range(n)]
+    return [tuple(int(v) for v in out[8 * q:8 + 8 * q]) for q in range(rc)]
 
 
 def col_plan(shape, grid: int, ring_bytes: int) -> dict:
-    """The column split's launch plan for a workload shape (host only)."""
+    """The column split's launch plan for a workload shape (host only); "bounds": the CTAs'
+    column ranges, CTA c owning [bounds[c], bounds[c + 1])."""
     import numpy as np
     cfg = config(shape, 1, DTYPE_BF16, DTYPE_F32, KERNELS_COLUMNS)
-    out = np.zeros(8, dtype=np.int32)
+    out = np.zeros(10, dtype=np.int32)
+    bounds = np.zeros(grid + 1, dtype=np.int32)
     check("moe_debug_col_plan", lib().moe_debug_col_plan(ctypes.byref(cfg), grid, ring_bytes,
-                                                         out.ctypes.data))
-    keys = ("stages", "stage_bytes", "nbs", "ro", "cb_r", "cb_s", "rows_a_r", "rows_a_s")
-    return dict(zip(keys, (int(v) for v in out)))
+                                                         out.ctypes.data, bounds.ctypes.data))
+    keys = ("stages", "stage_bytes", "nbs", "ro", "cb_r", "cb_s", "rows_a_r", "rows_a_s", "pack",
+            "prefetch")
+    plan = dict(zip(keys, (int(v) for v in out)))
+    plan["bounds"] = [int(v) for v in bounds]
+    return plan
 
 
 # ---------------------------------------------------------------- dense bf16 decode GEMV

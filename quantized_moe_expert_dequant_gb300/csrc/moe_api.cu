@@ -1156,8 +1156,8 @@ extern "C" int moe_router_topk(const float *logits, int32_t m, int32_t n_experts
 // ====================================================================== column-split plan (host)
 extern "C" int moe_debug_col_pieces(int32_t top_k, int32_t dff, int32_t n_shared,
                                     int32_t dff_shared, int32_t bits_down, int32_t bits_shared,
-                                    int32_t cta, int32_t grid, int32_t *out, int32_t max_pieces) {
-  if (!out || grid < 1 || cta < 0 || cta >= grid || top_k < 0 || n_shared < 0 || max_pieces < 0)
+                                    int32_t u0, int32_t u1, int32_t *out, int32_t max_pieces) {
+  if (!out || u0 < 0 || u1 < u0 || top_k < 0 || n_shared < 0 || max_pieces < 0)
     return MOE_ERR_INVALID_ARG;
   if (top_k + n_shared < 1 || (top_k > 0 && (dff <= 0 || dff % 64)) ||
       (n_shared > 0 && (dff_shared <= 0 || dff_shared % 64)))
@@ -1168,28 +1168,23 @@ extern "C" int moe_debug_col_pieces(int32_t top_k, int32_t dff, int32_t n_shared
     return MOE_ERR_UNSUPPORTED;
   const int64_t U = (int64_t)top_k * dff + (int64_t)n_shared * dff_shared;
   if (U > (1 << 24)) return MOE_ERR_UNSUPPORTED;
+  if (u1 > U) return MOE_ERR_INVALID_ARG;
+  if (u1 - u0 > moe::kMaxColsCta) return MOE_ERR_UNSUPPORTED;  // beyond the kernel's buffers
   moe::ColPiece pc[moe::kMaxColPieces];
   int nbk = 0;
-  int64_t u0 = 0;
-  int64_t u0c, u1c;  // the kernel's plan also rejects CTAs with more columns than it holds
-  moe::col_range(U, cta, grid, &u0c, &u1c);
-  if (u1c - u0c > moe::kMaxColsCta) return MOE_ERR_UNSUPPORTED;
   const int cb_r = 32 / bits_down, cb_s = n_shared > 0 ? 32 / bits_shared : cb_r;
-  const int np = moe::col_pieces(top_k, dff, n_shared, dff_shared, cb_r, cb_s, cta, grid, pc,
-                                 &nbk, &u0);
+  const int np = moe::col_pieces(top_k, dff, n_shared, dff_shared, cb_r, cb_s, u0, u1, pc, &nbk);
   if (np < 0 || np > max_pieces) return MOE_ERR_UNSUPPORTED;
-  out[0] = static_cast<int32_t>(u0);
-  out[1] = np;
   for (int q = 0; q < np; ++q) {
     const int32_t v[8] = {pc[q].seg, pc[q].j0, pc[q].j1, pc[q].a0,
                           pc[q].blk0, pc[q].nb, pc[q].pb, pc[q].grp};
-    std::memcpy(out + 2 + 8 * q, v, sizeof v);
+    std::memcpy(out + 8 * q, v, sizeof v);
   }
   return np;
 }
 
 extern "C" int moe_debug_col_plan(const moe_decode_config *cfg, int32_t grid, int32_t ring_bytes,
-                                  int32_t *out) {
+                                  int32_t *out, int32_t *bounds) {
   if (!out || grid < 1 || ring_bytes < 1) return MOE_ERR_INVALID_ARG;
   const int rc = validate_config(cfg);
   if (rc != MOE_OK) return rc;
@@ -1203,8 +1198,9 @@ extern "C" int moe_debug_col_plan(const moe_decode_config *cfg, int32_t grid, in
   if (!moe::make_col_plan(shape, cfg->bits_gate, cfg->bits_down, bits_sh, grid, ring_bytes, &cp,
                           &plan))
     return MOE_ERR_UNSUPPORTED;
-  const int32_t v[8] = {plan.nst, plan.stage_bytes, cp.nbs, cp.ro,
-                        cp.cb_r, cp.cb_s, plan.geo_r.R, plan.geo_s.R};
+  const int32_t v[10] = {plan.nst, plan.stage_bytes, cp.nbs, cp.ro, cp.cb_r,
+                         cp.cb_s, plan.geo_r.R, plan.geo_s.R, cp.pack, cp.prefetch};
   std::memcpy(out, v, sizeof v);
+  if (bounds) std::memcpy(bounds, cp.bounds, sizeof(int32_t) * (grid + 1));
   return MOE_OK;
 }

@@ -975,11 +975,9 @@ __global__ void __launch_bounds__(kColThreads, 1) cols_kernel(const StackParams 
   if (tid == 0) {
     mbar_init(&a_done, 1);
     int nbk = 0;
-    int64_t u0 = 0, u1 = 0;
-    cs.np = col_pieces(s.top_k, s.dff, s.n_shared, s.dff_shared, p.cp.cb_r, p.cp.cb_s,
-                       blockIdx.x, n, cs.pc, &nbk, &u0);
-    col_range(static_cast<int64_t>(s.top_k) * s.dff + static_cast<int64_t>(s.n_shared) * s.dff_shared,
-              blockIdx.x, n, &u0, &u1);
+    const int64_t u0 = p.cp.bounds[blockIdx.x], u1 = p.cp.bounds[blockIdx.x + 1];
+    cs.np = col_pieces(s.top_k, s.dff, s.n_shared, s.dff_shared, p.cp.cb_r, p.cp.cb_s, u0, u1,
+                       cs.pc, &nbk);
     cs.nbk = nbk;
     cs.u0 = static_cast<int>(u0);
     cs.ncols = static_cast<int>(u1 - u0);
@@ -991,8 +989,7 @@ __global__ void __launch_bounds__(kColThreads, 1) cols_kernel(const StackParams 
     cs.s_gate[0] = cs.s_gate[1] = 1.f;
     int nck_r = 0;
     cs.nck = col_chunks(s.top_k, s.dff, s.n_shared, s.dff_shared, p.plan.geo_r.R,
-                        p.plan.geo_s.R, blockIdx.x, n, cs.ck_seg, cs.ck_j, cs.ck_n, cs.ck_u,
-                        &nck_r);
+                        p.plan.geo_s.R, u0, u1, cs.ck_seg, cs.ck_j, cs.ck_n, cs.ck_u, &nck_r);
     cs.nck_r = nck_r;
     if (cs.nck < 0) {  // outside the plan (the host checks every CTA): do nothing
       cs.nck = cs.nck_r = 0;

@@ -3,7 +3,9 @@
 // moe_kernels_g6.cu and moe_kernels_g8.cu); plus the small kernels (debug unpack, router, bounded
 // waits, debug route inversion).
 #include <algorithm>
+#include <cstdint>
 #include <cstring>
+#include <vector>
 
 #include "moe_grouped.cuh"
 
@@ -384,6 +386,107 @@ static bool geom_cols_a(int din, int bits, GateUpGeom *g) {
   return true;
 }
 
+// What the columns [u0, u1) cost the CTA that owns them in one layer when every slot names a valid
+// expert: its stages (gate/up chunks, then down stages: unpacked, or packed when `pack`) in the
+// high bits, its bytes in the low 40.  -1 when the range breaks a per-CTA limit.
+static int64_t col_cost(const LayerShape &s, const ColPlan &cp, const Plan &plan, int64_t u0,
+                        int64_t u1, bool pack) {
+  if (u1 < u0 || u1 - u0 > kMaxColsCta) return -1;
+  ColPiece pc[kMaxColPieces];
+  int nbk = 0;
+  const int np = col_pieces(s.top_k, s.dff, s.n_shared, s.dff_shared, cp.cb_r, cp.cb_s, u0, u1,
+                            pc, &nbk);
+  if (np < 0) return -1;
+  short sg[kMaxColChunks], jj[kMaxColChunks], nn[kMaxColChunks], uu[kMaxColChunks];
+  int nrt = 0;
+  const int nck = col_chunks(s.top_k, s.dff, s.n_shared, s.dff_shared, plan.geo_r.R,
+                             plan.geo_s.R, u0, u1, sg, jj, nn, uu, &nrt);
+  if (nck < 0) return -1;
+  int down = 0;
+  if (pack) {
+    down = (nbk + np + cp.nbs) / (cp.nbs + 1);  // every slot of a stage filled
+  } else {
+    for (int i = 0; i < np; ++i) down += (pc[i].nb + cp.nbs - 1) / cp.nbs;
+  }
+  int64_t bytes = static_cast<int64_t>(nbk + np) * s.din * 4;  // code blocks and records
+  for (int i = 0; i < nck; ++i) bytes += static_cast<int64_t>(nn[i]) * (i < nrt ? cp.rec_r : cp.rec_s);
+  return (static_cast<int64_t>(nck + down) << 40) | bytes;
+}
+
+// The CTAs' column ranges of an unpacked plan (cp->bounds): starting from the even split, each
+// inner boundary moves at most kColSlack columns so that the costliest CTA (stages first, then
+// bytes) costs as little as possible, and among those splits the total bytes (blocks read by two
+// CTAs, records of cut groups) are least.  A layer waits for its slowest CTA, and a CTA whose
+// columns end a few columns into a new group carries one more down stage than its neighbours: the
+// even split of the qwen3 8-bit shape (768 columns a slot over 19 CTAs) gives 4 CTAs of every 19
+// five down stages, this one none.  false when no split within the slack keeps every CTA inside
+// the limits.
+constexpr int kColSlack = 16;
+static bool col_balance(const LayerShape &s, ColPlan *cp, const Plan &plan, int grid) {
+  const int64_t U = static_cast<int64_t>(s.top_k) * s.dff +
+                    static_cast<int64_t>(s.n_shared) * s.dff_shared;
+  const int D = static_cast<int>(std::min<int64_t>(kColSlack, U / grid / 2));
+  const int W = 2 * D + 1;
+  const int64_t kInf = INT64_MAX;
+  // boundary c sits at U c / grid + (i - D), window slot i; boundaries 0 and grid are fixed
+  auto pos = [&](int c, int i) -> int64_t {
+    const int64_t v = U * c / grid + (i - D);
+    return (c == 0 || c == grid || v < 0 || v > U) ? -1 : v;
+  };
+  auto slot_ok = [&](int c, int i) {
+    return (c == 0 || c == grid) ? i == D : pos(c, i) >= 0;
+  };
+  auto at = [&](int c, int i) -> int64_t { return (c == 0) ? 0 : (c == grid ? U : pos(c, i)); };
+  std::vector<int64_t> cost(static_cast<size_t>(grid) * W * W, -1);
+  for (int c = 0; c < grid; ++c)
+    for (int i = 0; i < W; ++i) {
+      if (!slot_ok(c, i)) continue;
+      for (int j = 0; j < W; ++j)
+        if (slot_ok(c + 1, j) && at(c + 1, j) >= at(c, i))
+          cost[(static_cast<size_t>(c) * W + i) * W + j] =
+              col_cost(s, *cp, plan, at(c, i), at(c + 1, j), false);
+    }
+  // pass 1: the least possible cost of the costliest CTA
+  std::vector<int64_t> best(static_cast<size_t>(grid + 1) * W, kInf);
+  best[static_cast<size_t>(grid) * W + D] = 0;
+  for (int c = grid - 1; c >= 0; --c)
+    for (int i = 0; i < W; ++i)
+      for (int j = 0; j < W; ++j) {
+        const int64_t k = cost[(static_cast<size_t>(c) * W + i) * W + j];
+        const int64_t rest = best[static_cast<size_t>(c + 1) * W + j];
+        if (k < 0 || rest == kInf) continue;
+        int64_t &b = best[static_cast<size_t>(c) * W + i];
+        b = std::min(b, std::max(k, rest));
+      }
+  const int64_t M = best[D];
+  if (M == kInf) return false;
+  // pass 2: within that bound, the least total bytes
+  const int64_t mask = (int64_t{1} << 40) - 1;
+  std::vector<int64_t> sum(static_cast<size_t>(grid + 1) * W, kInf);
+  std::vector<int> next(static_cast<size_t>(grid) * W, -1);
+  sum[static_cast<size_t>(grid) * W + D] = 0;
+  for (int c = grid - 1; c >= 0; --c)
+    for (int i = 0; i < W; ++i)
+      for (int j = 0; j < W; ++j) {
+        const int64_t k = cost[(static_cast<size_t>(c) * W + i) * W + j];
+        const int64_t rest = sum[static_cast<size_t>(c + 1) * W + j];
+        if (k < 0 || k > M || rest == kInf) continue;
+        const int64_t v = rest + (k & mask);
+        if (v < sum[static_cast<size_t>(c) * W + i]) {
+          sum[static_cast<size_t>(c) * W + i] = v;
+          next[static_cast<size_t>(c) * W + i] = j;
+        }
+      }
+  if (sum[D] == kInf) return false;
+  int i = D;
+  for (int c = 0; c < grid; ++c) {
+    cp->bounds[c] = static_cast<int32_t>(at(c, i));
+    i = next[static_cast<size_t>(c) * W + i];
+  }
+  cp->bounds[grid] = static_cast<int32_t>(U);
+  return true;
+}
+
 bool make_col_plan(const LayerShape &s, int bits_gu, int bits_d, int bits_sh, int grid,
                    int ring_bytes, ColPlan *cp, Plan *plan) {
   const bool sh = s.n_shared > 0;
@@ -417,27 +520,15 @@ bool make_col_plan(const LayerShape &s, int bits_gu, int bits_d, int bits_sh, in
   cp->nbs = nbs;
   cp->ro = 4 * ((s.din / 4 + grid - 1) / grid);   // the owner's row quads
   if (cp->ro > kMaxOwnRows) return false;
-  // every CTA's pieces within the kernel's limits
   const int64_t U = (int64_t)s.top_k * s.dff + (int64_t)s.n_shared * s.dff_shared;
-  if ((U + grid - 1) / grid > kMaxColsCta) return false;
+  if ((U + grid - 1) / grid > kMaxColsCta || U > (int64_t{1} << 30)) return false;
+  // the column ranges, balanced for the unpacked stages; the stages of the costliest CTA decide
+  // the prefetch and the packing
+  if (!col_balance(s, cp, *plan, grid)) return false;
   int max_stages = 0;
-  for (int c = 0; c < grid; ++c) {
-    ColPiece pc[kMaxColPieces];
-    int nbk = 0;
-    int64_t u0 = 0;
-    const int np = col_pieces(s.top_k, s.dff, s.n_shared, s.dff_shared, cp->cb_r, cp->cb_s, c,
-                              grid, pc, &nbk, &u0);
-    if (np < 0) return false;
-    short sg[kMaxColChunks], jj[kMaxColChunks], nn[kMaxColChunks], uu[kMaxColChunks];
-    int nrt = 0;
-    const int nck = col_chunks(s.top_k, s.dff, s.n_shared, s.dff_shared, plan->geo_r.R,
-                               plan->geo_s.R, c, grid, sg, jj, nn, uu, &nrt);
-    if (nck < 0) return false;
-    // the CTA's stages of a layer (unpacked) when every slot names a valid expert
-    int down = 0;
-    for (int i = 0; i < np; ++i) down += (pc[i].nb + nbs - 1) / nbs;
-    max_stages = std::max(max_stages, nck + down);
-  }
+  for (int c = 0; c < grid; ++c)
+    max_stages = std::max(max_stages, static_cast<int>(
+                              col_cost(s, *cp, *plan, cp->bounds[c], cp->bounds[c + 1], false) >> 40));
   // The prefetches queue on the bulk-copy engine ahead of the ring's next copies: worth it only
   // for a short overflow (measured: qwen3 8-bit, 10-11 stages on a 6-slot ring, +1%; dots-like,
   // 20-30 stages, -17%).
@@ -446,6 +537,14 @@ bool make_col_plan(const LayerShape &s, int bits_gu, int bits_d, int bits_sh, in
   // two blocks and nothing is prefetched (measured, prefetch off: dots-like stack, 2-slot stages,
   // +11%; qwen3 8-bit, 4-slot stages, -3%; with the prefetch on, packing measured slower).
   cp->pack = nbs <= 2 && !cp->prefetch;
+  // A packed plan keeps the even split (measured, dots-like stack: 619.7 tok/s even, 615.4 with
+  // the unpacked balance, 606.0 with a split weighted for the packed stages, which lowered its
+  // costliest CTA from 30 stages to 29; the unpacked plans gained 0.6-4.6% from the balance).
+  if (cp->pack) {
+    for (int c = 0; c <= grid; ++c) cp->bounds[c] = static_cast<int32_t>(U * c / grid);
+    for (int c = 0; c < grid; ++c)
+      if (col_cost(s, *cp, *plan, cp->bounds[c], cp->bounds[c + 1], true) < 0) return false;
+  }
   std::memset(&plan->geo_b, 0, sizeof plan->geo_b);
   plan->nst = n;
   plan->stage_bytes = st;

@@ -126,6 +126,7 @@ struct ColPlan {
                            // prefetch)
   int prefetch;            // ask L2 for the stages beyond the first ring-full (when they are at
                            // most one more ring-full)
+  int32_t bounds[kColMaxGrid + 1];  // CTA c owns the activation columns [bounds[c], bounds[c+1])
 };
 
 // Bytes of one gate/up record of a row of `din` codes at `bits`.
@@ -145,22 +146,19 @@ struct ColPiece {
   int grp;      // group: j0 / 64
 };
 
-// The activation columns [u0, u1) of CTA c out of n (balanced split of U columns).
+// The even split of U activation columns over n CTAs: CTA c's columns [u0, u1).  The plan starts
+// from it and moves each boundary a few columns (ColPlan::bounds).
 __host__ __device__ inline void col_range(int64_t U, int c, int n, int64_t *u0, int64_t *u1) {
   *u0 = U * c / n;
   *u1 = U * (c + 1) / n;
 }
 
-// Cuts CTA c's columns into pieces; returns the piece count (-1 when more than kMaxColPieces or
-// the blocks exceed kMaxColBlocks) and the block count in *nblocks.
+// Cuts the activation columns [u0, u1) into pieces; returns the piece count (-1 when more than
+// kMaxColPieces or the blocks exceed kMaxColBlocks) and the block count in *nblocks.
 __host__ __device__ inline int col_pieces(int top_k, int dff, int n_shared, int dff_shared,
-                                          int cb_r, int cb_s, int c, int n, ColPiece *pc,
-                                          int *nblocks, int64_t *u0_out) {
+                                          int cb_r, int cb_s, int64_t u0, int64_t u1,
+                                          ColPiece *pc, int *nblocks) {
   const int64_t Ur = static_cast<int64_t>(top_k) * dff;
-  const int64_t U = Ur + static_cast<int64_t>(n_shared) * dff_shared;
-  int64_t u0, u1;
-  col_range(U, c, n, &u0, &u1);
-  *u0_out = u0;
   int np = 0, nbk = 0;
   for (int64_t u = u0; u < u1;) {
     int seg, j, width, cb;
@@ -197,20 +195,17 @@ __host__ __device__ inline int col_pieces(int top_k, int dff, int n_shared, int 
   return np;
 }
 
-// The gate/up stages of CTA c out of n in the column split: its activation columns [u0, u1) cut
-// into chunks of at most R row pairs (R_s for the shared experts; kColFirstRows for the first)
-// that never cross an expert, in column order.  Chunk i: segment seg[i] (routed slot, or top_k + shared expert), first row j[i]
-// inside the expert, rows cnt[i], flattened first column u[i].  Returns the chunk count and the
-// routed chunks in *n_routed, or -1 beyond kMaxColChunks.
+// The gate/up stages of a CTA of the column split: its activation columns [u0, u1) cut into
+// chunks of at most R row pairs (R_s for the shared experts; kColFirstRows for the first) that
+// never cross an expert, in column order.  Chunk i: segment seg[i] (routed slot, or top_k +
+// shared expert), first row j[i] inside the expert, rows cnt[i], first column u[i] relative to
+// u0.  Returns the chunk count and the routed chunks in *n_routed, or -1 beyond kMaxColChunks.
 constexpr int kMaxColChunks = 96;
 constexpr int kColFirstRows = 4;  // row pairs of a CTA's first gate/up stage of a layer
 __host__ __device__ inline int col_chunks(int top_k, int dff, int n_shared, int dff_shared, int R,
-                                          int R_s, int c, int n, short *seg, short *j, short *cnt,
-                                          short *u, int *n_routed) {
+                                          int R_s, int64_t u0, int64_t u1, short *seg, short *j,
+                                          short *cnt, short *u, int *n_routed) {
   const int64_t Ur = static_cast<int64_t>(top_k) * dff;
-  const int64_t U = Ur + static_cast<int64_t>(n_shared) * dff_shared;
-  int64_t u0, u1;
-  col_range(U, c, n, &u0, &u1);
   int nc = 0, nr = 0;
   for (int64_t x = u0; x < u1;) {
     const bool routed = x < Ur;

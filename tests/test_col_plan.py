@@ -1,12 +1,16 @@
 """The column split's decomposition of the activation columns and its launch plan, on the host
 (no GPU).
 
-moe_debug_col_pieces returns, for one CTA, the pieces the MOE_KERNELS_COLUMNS kernel computes on
-the device (the same function).  Over all CTAs of a grid the pieces must tile the activation
-index space exactly once, in order, each piece inside one segment and one group of 64 columns,
-with column blocks that cover its columns and stay inside the expert, and a block list that the
-kernel's per-CTA buffers hold.
+moe_debug_col_pieces returns, for one column range, the pieces the MOE_KERNELS_COLUMNS kernel
+computes on the device (the same function).  Over all CTAs of a grid the pieces must tile the
+activation index space exactly once, in order, each piece inside one segment and one group of 64
+columns, with column blocks that cover its columns and stay inside the expert, and a block list
+that the kernel's per-CTA buffers hold.  The plan's column ranges (moe_debug_col_plan's bounds)
+must cover the columns once, stay within 16 columns of the even split (a packed plan: equal it),
+and never leave a CTA with more stages than the even split's costliest one.
 """
+import math
+
 import pytest
 
 from quantized_moe_expert_dequant_gb300 import binding as Bn
@@ -32,23 +36,15 @@ CASES = [ALL["qwen3_stack_8bit"], ALL["e512_stack"], ALL["qwen3_layer_4bit"],
          Shape("shared only", 256, 64, 1, 0, 8, 8, 8, n_shared=2, dff_shared=128, bits_shared=8)]
 
 
-@pytest.mark.parametrize("grid", [152, 148, 7, 1])
-@pytest.mark.parametrize("shape", CASES, ids=lambda s: s.name)
-def test_pieces_tile_the_columns_once(built, shape, grid):
+def check_pieces(shape, bounds):
+    """Every range's pieces: contiguous, inside one segment and group, blocks covering them."""
     K, dff, nsh, dsh = shape.top_k, shape.dff, shape.n_shared, shape.dff_shared
     bsh = shape.bits_shared if nsh else shape.bits_down
     U = K * dff + nsh * dsh
-    if -(-U // grid) > MAX_COLS:
-        c = max(range(grid), key=lambda c: U * (c + 1) // grid - U * c // grid)
-        with pytest.raises(Bn.MoeError) as e:   # beyond the kernel's per-CTA buffers
-            Bn.col_pieces(K, dff, nsh, dsh, shape.bits_down, bsh, c, grid)
-        assert e.value.rc == Bn.MOE_ERR_UNSUPPORTED
-        return
     nxt = 0
-    for c in range(grid):
-        u0, pieces = Bn.col_pieces(K, dff, nsh, dsh, shape.bits_down, bsh, c, grid)
-        assert u0 == U * c // grid == nxt
-        u1 = U * (c + 1) // grid
+    for u0, u1 in zip(bounds[:-1], bounds[1:]):
+        pieces = Bn.col_pieces(K, dff, nsh, dsh, shape.bits_down, bsh, u0, u1)
+        assert u0 == nxt
         assert u1 - u0 <= MAX_COLS and len(pieces) <= MAX_PIECES
         nblocks = 0
         for seg, j0, j1, a0, blk0, nb, pb, grp in pieces:
@@ -70,15 +66,97 @@ def test_pieces_tile_the_columns_once(built, shape, grid):
     assert nxt == U
 
 
+@pytest.mark.parametrize("grid", [152, 148, 7, 1])
+@pytest.mark.parametrize("shape", CASES, ids=lambda s: s.name)
+def test_pieces_tile_the_columns_once(built, shape, grid):
+    """The even split of the columns over `grid` CTAs, cut into pieces range by range."""
+    K, dff, nsh, dsh = shape.top_k, shape.dff, shape.n_shared, shape.dff_shared
+    bsh = shape.bits_shared if nsh else shape.bits_down
+    U = K * dff + nsh * dsh
+    bounds = [U * c // grid for c in range(grid + 1)]
+    if -(-U // grid) > MAX_COLS:
+        c = max(range(grid), key=lambda c: bounds[c + 1] - bounds[c])
+        with pytest.raises(Bn.MoeError) as e:   # beyond the kernel's per-CTA buffers
+            Bn.col_pieces(K, dff, nsh, dsh, shape.bits_down, bsh, bounds[c], bounds[c + 1])
+        assert e.value.rc == Bn.MOE_ERR_UNSUPPORTED
+        return
+    check_pieces(shape, bounds)
+
+
+def cta_stages(shape, plan, u0, u1, pack):
+    """A CTA's stages in a layer when every slot names a valid expert: gate/up chunks of at most R
+    row pairs (4 for the CTA's first), never across an expert, then its down stages."""
+    K, dff, nsh, dsh = shape.top_k, shape.dff, shape.n_shared, shape.dff_shared
+    bsh = shape.bits_shared if nsh else shape.bits_down
+    chunks, x = 0, u0
+    while x < u1:
+        routed = x < K * dff
+        width = dff if routed else dsh
+        rel = x if routed else x - K * dff
+        R = plan["rows_a_r"] if routed else plan["rows_a_s"]
+        take = min(width - rel % width, min(R, 4) if chunks == 0 else R, u1 - x)
+        chunks += 1
+        x += take
+    pieces = Bn.col_pieces(K, dff, nsh, dsh, shape.bits_down, bsh, u0, u1)
+    nbs = plan["nbs"]
+    if pack:
+        down = -(-(sum(p[5] for p in pieces) + len(pieces)) // (nbs + 1))
+    else:
+        down = sum(-(-p[5] // nbs) for p in pieces)
+    return chunks, down
+
+
+@pytest.mark.parametrize("grid", [152, 148])
+@pytest.mark.parametrize("shape", CASES, ids=lambda s: s.name)
+def test_plan_bounds_balance_the_stages(built, shape, grid):
+    U = shape.top_k * shape.dff + shape.n_shared * shape.dff_shared
+    plan = Bn.col_plan(shape, grid, RING)
+    b = plan["bounds"]
+    assert len(b) == grid + 1 and b[0] == 0 and b[-1] == U
+    assert all(b[c] <= b[c + 1] for c in range(grid))
+    check_pieces(shape, b)
+    even = [U * c // grid for c in range(grid + 1)]
+    if plan["pack"]:                           # a packed plan keeps the even split
+        assert b == even
+    else:                                      # boundaries within 16 columns of the even split
+        assert all(abs(b[c] - even[c]) <= 16 for c in range(grid + 1))
+    cost = lambda bb: max(sum(cta_stages(shape, plan, bb[c], bb[c + 1], plan["pack"]))
+                          for c in range(grid))
+    assert cost(b) <= cost(even)
+    # prefetch when the stages past the first ring-full fit one more; pack only without it
+    unpacked = max(sum(cta_stages(shape, plan, b[c], b[c + 1], False)) for c in range(grid))
+    assert plan["prefetch"] == (unpacked <= 2 * plan["stages"])
+    assert plan["pack"] == (plan["nbs"] <= 2 and not plan["prefetch"])
+
+
+def test_plan_bounds_qwen3_8bit(built):
+    """The qwen3 8-bit stack (8 slots of 768 columns, 19 CTAs a slot, 3 blocks of 4 columns a down
+    stage): the even split gives 4 CTAs of every 19 five down stages (40 columns ending a few
+    columns into a new group of 64); the plan gives every CTA 4, and 6 gate/up chunks."""
+    shape = ALL["qwen3_stack_8bit"]
+    plan = Bn.col_plan(shape, 152, RING)
+    assert plan["nbs"] == 3 and not plan["pack"] and plan["prefetch"]
+    b = plan["bounds"]
+    even = [6144 * c // 152 for c in range(153)]
+    ev = [cta_stages(shape, plan, even[c], even[c + 1], False)[1] for c in range(152)]
+    assert sorted(set(ev)) == [4, 5] and ev.count(5) == 32
+    st = [cta_stages(shape, plan, b[c], b[c + 1], False) for c in range(152)]
+    assert all(d == 4 for _, d in st) and all(g == 6 for g, _ in st)
+    assert all(38 <= b[c + 1] - b[c] <= 42 for c in range(152))
+
+
 def test_bad_arguments_are_rejected(built):
     with pytest.raises(Bn.MoeError) as e:
-        Bn.col_pieces(8, 768, 0, 0, 8, 8, 152, 152)     # cta outside the grid
+        Bn.col_pieces(8, 768, 0, 0, 8, 8, 6100, 6145)   # range past the columns
     assert e.value.rc == Bn.MOE_ERR_INVALID_ARG
     with pytest.raises(Bn.MoeError) as e:
-        Bn.col_pieces(8, 768, 0, 0, 5, 5, 0, 152)       # 5-bit codes: no such format
+        Bn.col_pieces(8, 768, 0, 0, 8, 8, 40, 39)       # range backwards
+    assert e.value.rc == Bn.MOE_ERR_INVALID_ARG
+    with pytest.raises(Bn.MoeError) as e:
+        Bn.col_pieces(8, 768, 0, 0, 5, 5, 0, 40)        # 5-bit codes: no such format
     assert e.value.rc == Bn.MOE_ERR_UNSUPPORTED
     with pytest.raises(Bn.MoeError) as e:
-        Bn.col_pieces(8, 100, 0, 0, 8, 8, 0, 152)       # width not a multiple of 64
+        Bn.col_pieces(8, 100, 0, 0, 8, 8, 0, 40)        # width not a multiple of 64
     assert e.value.rc == Bn.MOE_ERR_INVALID_ARG
 
 
