@@ -572,30 +572,43 @@ __device__ inline void col_planes(const LayerShape &s, const ColPlan &cp, ColSme
                                   int wprow, int warp, int lane) {
   for (int qi = warp; qi < cs.np; qi += kConsumerWarps) {
     const ColPiece q = cs.pc[qi];
-    int e;
-    if (!col_valid(s, q, ids, &e)) continue;
     const bool routed = q.seg < s.top_k;
-    const int bits = routed ? BD : BSD;
-    const int cb = routed ? cp.cb_r : cp.cb_s;
+    // every load of the piece at once (the slot's id and score, the parked sums): the step is
+    // a chain of latencies, so the loads share one round trip
+    const int e = routed ? ids[q.seg] : 0;
     const float coef = routed ? scores[q.seg] : shared_coef;
     const int n = q.j1 - q.j0;  // at most 64
+    float2 a[2][kColMaxWpr];
+#pragma unroll
+    for (int t = 0; t < 2; ++t)
+#pragma unroll
+      for (int h = 0; h < kColMaxWpr; ++h)
+        a[t][h] = lane + 32 * t < n && h < wprow ? cs.red[q.a0 + lane + 32 * t][h]
+                                                 : make_float2(0.f, 0.f);
+    if (routed && (e < 0 || e >= s.n_experts)) continue;  // the slot names no valid expert
+    const int bits = routed ? BD : BSD;
+    const int cb = routed ? cp.cb_r : cp.cb_s;
     float v[2];
 #pragma unroll
     for (int t = 0; t < 2; ++t) {
-      const int c = lane + 32 * t;
-      v[t] = 0.f;
-      if (c < n) {
-        float2 a = cs.red[q.a0 + c][0];
-        for (int h = 1; h < wprow; ++h) {
-          const float2 b = cs.red[q.a0 + c][h];
-          a.x += b.x;
-          a.y += b.y;
+      float2 g = a[t][0];
+#pragma unroll
+      for (int h = 1; h < kColMaxWpr; ++h) {
+        if (h < wprow) {
+          g.x += a[t][h].x;
+          g.y += a[t][h].y;
         }
-        v[t] = coef * (silu_f(a.x) * a.y);
       }
+      v[t] = lane + 32 * t < n ? coef * (silu_f(g.x) * g.y) : 0.f;
     }
-    const float mx = warp_max(fmaxf(fabsf(v[0]), fabsf(v[1])));
-    const float sm = warp_sum(v[0] + v[1]);
+    // the piece's largest magnitude and sum: two butterflies, interleaved (the same order as
+    // warp_max and warp_sum)
+    float mx = fmaxf(fabsf(v[0]), fabsf(v[1])), sm = v[0] + v[1];
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+      mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+      sm += __shfl_xor_sync(0xffffffffu, sm, o);
+    }
     const int E = fixed_exponent(mx);
     const float sc = pow2f(22 - E);
     const int f0 = __float2int_rn(v[0] * sc), f1 = __float2int_rn(v[1] * sc);
