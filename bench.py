@@ -279,8 +279,10 @@ def kernel_source_hash() -> str:
     return h.hexdigest()[:16]
 
 
-def profiled_traffic(kernel: str, workload: str):
-    """dram bytes per launch from the committed ncu summary, if taken on the current source."""
+def profiled_traffic(kernel: str, workload: str, layers: int):
+    """dram bytes per launch of `layers` layers from the committed ncu summary, if taken on the
+    current source: the record's bytes per launch of its own layer count, scaled by the layers
+    (the kernel's traffic is per layer)."""
     path = os.path.join(ROOT, "profiles", "traffic.txt")
     if not os.path.exists(path):
         return None
@@ -288,7 +290,9 @@ def profiled_traffic(kernel: str, workload: str):
     for line in open(path):
         kv = dict(p.split("=", 1) for p in line.split() if "=" in p)
         if kv.get("kernel") == kernel and kv.get("workload") == workload and kv.get("src") == src:
-            return float(kv["dram_bytes_per_launch"])
+            per = float(kv["dram_bytes_per_launch"])
+            rec_layers = int(kv.get("layers", layers))
+            return per * layers / rec_layers
     return None
 
 
@@ -571,7 +575,7 @@ def run_ours(args, shape: Shape):
     else:
         ach, per_launch_bytes, per_launch_us = ach_a, mean_a, ms_a * 1e3
     traffic = (None if mode == Bn.KERNELS_COLUMNS_AHEAD else
-               profiled_traffic(dominant, args.workload + ("_chained" if chained else "")))
+               profiled_traffic(dominant, args.workload + ("_chained" if chained else ""), L))
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
