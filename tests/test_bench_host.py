@@ -1,5 +1,6 @@
 """Host-side pieces of bench.py (no GPU): the kernel-source hash that keys the DRAM-traffic record,
-and the timeline summary's arithmetic on a synthetic stamp array."""
+the record's scaling to the layers a run launches, and the timeline summary's arithmetic on a
+synthetic stamp array."""
 import numpy as np
 
 import bench
@@ -41,3 +42,19 @@ def test_timeline_summary_on_synthetic_stamps():
                - 2.0) < 1e-6
     assert [st["stage"] for st in s["stages"]] == list(range(12))
     assert abs(s["stages"][3]["full_us"] - 3.5) < 1e-6 and abs(s["stages"][3]["issued_us"] - 1.75) < 1e-6
+
+
+def test_profiled_traffic_scales_by_layers(tmp_path, monkeypatch):
+    """A record of bytes per launch of its own layer count gives a run of other layers the same
+    bytes per layer; a record on other sources, or of another kernel or workload, gives none."""
+    (tmp_path / "profiles").mkdir()
+    src = bench.kernel_source_hash()
+    (tmp_path / "profiles" / "traffic.txt").write_text(
+        f"kernel=cols_kernel workload=w layers=48 src={src} dram_bytes_per_launch=4800\n"
+        f"kernel=cols_kernel workload=old layers=48 src=0000000000000000 dram_bytes_per_launch=1\n")
+    monkeypatch.setattr(bench, "ROOT", str(tmp_path))
+    monkeypatch.setattr(bench, "kernel_source_hash", lambda: src)
+    assert bench.profiled_traffic("cols_kernel", "w", 48) == 4800
+    assert bench.profiled_traffic("cols_kernel", "w", 6) == 600
+    assert bench.profiled_traffic("cols_kernel", "old", 48) is None
+    assert bench.profiled_traffic("fused_kernel", "w", 48) is None
