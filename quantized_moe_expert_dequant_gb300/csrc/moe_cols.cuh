@@ -468,11 +468,15 @@ __device__ inline void cols_prefetch_from(const LayerShape &s, const Plan &plan,
 template <int BR, int BSH>
 __device__ bool cols_produce_layer(const LayerShape &s, const Plan &plan, const ColPlan &cp,
                                    const ColPtrs &cw, const ColSmem &cs, const int *ids,
-                                   const float *scores, int *cnt, Ring &r, uint64_t pol) {
-  int nr = 0;
-  for (int i = 0; i < cs.nck_r; ++i) {
-    const int e = ids[cs.ck_seg[i]];
-    nr += e >= 0 && e < s.n_experts;
+                                   const float *scores, bool all_valid, int *cnt, Ring &r,
+                                   uint64_t pol) {
+  int nr = cs.nck_r;  // every slot names a valid expert: all routed chunks
+  if (!all_valid) {
+    nr = 0;
+    for (int i = 0; i < cs.nck_r; ++i) {
+      const int e = ids[cs.ck_seg[i]];
+      nr += e >= 0 && e < s.n_experts;
+    }
   }
   const int ns = cs.nck - cs.nck_r;
   cnt[0] = nr;
@@ -976,6 +980,7 @@ __global__ void __launch_bounds__(kColThreads, 1) cols_kernel(const StackParams 
   __shared__ LayerPtrs wpr;  // the producers' copy of the current layer's pointers
   __shared__ ColPtrs cpr;
   __shared__ int stop_pr;
+  __shared__ int all_valid_pr;  // every slot of the producer's current layer names a valid expert
   // the expert ids and scores of layers l and l + 1 (the producer may be a layer ahead)
   __shared__ int ids2[2][kMaxTopK];
   __shared__ float sc2[2][kMaxTopK];
@@ -1044,12 +1049,13 @@ __global__ void __launch_bounds__(kColThreads, 1) cols_kernel(const StackParams 
       int *ids_l = ids2[l & 1];
       float *sc_l = sc2[l & 1];
       producer_load_token(s, p.ids + l * ks, p.scores + l * ks, ids_l, sc_l, p.err, pl,
-                          p.ids_used ? p.ids_used + l * ks : nullptr);
+                          p.ids_used ? p.ids_used + l * ks : nullptr, &all_valid_pr);
       MOE_TL_AT(tlr, 2);
       if (pl == 0) {
         MOE_TL_SET_HOOK_P(tlr);
         MOE_TL_STAGE_BASE_P(r.used);
-        cols_produce_layer<BR, BSH>(s, p.plan, p.cp, cpr, cs, ids_l, sc_l, rs.cnt, r, pol);
+        cols_produce_layer<BR, BSH>(s, p.plan, p.cp, cpr, cs, ids_l, sc_l, all_valid_pr != 0,
+                                    rs.cnt, r, pol);
       }
       __syncwarp();
       MOE_TL_AT(tlr, 4);

@@ -396,13 +396,23 @@ __device__ __forceinline__ void consumers_grid_barrier(uint32_t *cnt, uint32_t t
 __device__ __forceinline__ void producer_load_token(const LayerShape &s, const int32_t *ids,
                                                     const float *scores, int *ids_s,
                                                     float *scores_s, int32_t *err, int lane,
-                                                    int32_t *ids_used = nullptr) {
+                                                    int32_t *ids_used = nullptr,
+                                                    int *all_valid = nullptr) {
+  int bad = 0;
   for (int k = lane; k < s.top_k; k += kProducers) {
+    // both loads before either store: one round trip
     const int e = ids[k];
+    const float sc = scores != nullptr ? scores[k] : 0.f;
     ids_s[k] = e;
-    scores_s[k] = scores != nullptr ? scores[k] : 0.f;
-    if (e < 0 || e >= s.n_experts) atomicOr(err, kDevErrBadId);
+    scores_s[k] = sc;
+    const bool b = e < 0 || e >= s.n_experts;
+    bad |= b;
+    if (b) atomicOr(err, kDevErrBadId);
     if (ids_used != nullptr && blockIdx.x == 0) ids_used[k] = e;  // what this kernel read
+  }
+  if (all_valid != nullptr) {  // the whole warp calls this
+    const unsigned any = __ballot_sync(0xffffffffu, bad);
+    if (lane == 0) *all_valid = any == 0u;
   }
   producer_sync();
 }
