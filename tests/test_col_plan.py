@@ -205,3 +205,31 @@ def test_plan_refuses_what_the_kernel_does_not_take(built):
     with pytest.raises(Bn.MoeError) as e:     # more CTAs than the owner's sums read
         Bn.col_plan(ALL["qwen3_stack_8bit"], 161, RING)
     assert e.value.rc == Bn.MOE_ERR_UNSUPPORTED
+
+
+@pytest.mark.parametrize("top_k,dff,grid", [(2, 192, 5), (1, 320, 6)])
+def test_plan_bounds_are_optimal_on_small_grids(built, top_k, dff, grid):
+    """An exhaustive search (memoised over (CTA, boundary)) of every placement of the inner
+    boundaries within 16 columns of the even split: the plan's costliest CTA has the fewest stages
+    any placement gives, here one fewer than the even split's."""
+    import functools
+    shape = Shape("small grid", 128, dff, 4, top_k, 8, 8, 8, seed=5)
+    U = top_k * dff
+    plan = Bn.col_plan(shape, grid, RING)
+    assert not plan["pack"]
+    even = [U * c // grid for c in range(grid + 1)]
+    D = min(16, U // grid // 2)
+
+    @functools.lru_cache(maxsize=None)
+    def stages(u0, u1):
+        return sum(cta_stages(shape, plan, u0, u1, False))
+
+    @functools.lru_cache(maxsize=None)
+    def fewest(c, u0):     # the least max-stages of CTAs c.. when CTA c starts at u0
+        if c == grid - 1:
+            return stages(u0, U)
+        lo, hi = max(u0, even[c + 1] - D), min(U, even[c + 1] + D)
+        return min(max(stages(u0, u1), fewest(c + 1, u1)) for u1 in range(lo, hi + 1))
+
+    cost = lambda b: max(stages(b[c], b[c + 1]) for c in range(grid))
+    assert cost(plan["bounds"]) == fewest(0, 0) == cost(even) - 1
